@@ -1,0 +1,59 @@
+"""Plant plausible mistakes in a copy of the oracle (on the CPU) and check that a pin catches each."""
+import importlib.util
+import os
+
+import numpy as np
+import pytest
+
+from tests import pins
+
+ORACLE_SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "hq_oracle.py")
+
+
+def _mutant(old, new):
+    src = open(ORACLE_SRC).read()
+    assert old in src, old
+    spec = importlib.util.spec_from_loader("oracle_mutant", loader=None)
+    mod = importlib.util.module_from_spec(spec)
+    exec(compile(src.replace(old, new, 1), "oracle_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+MUTATIONS = {
+    "nibble_order_swapped": ("out[..., 0::2] = p & 0xF", "out[..., 0::2] = p >> 4\n    out[..., 1::2] = p & 0xF\n    return out\n    out[..., 0::2] = p & 0xF"),
+    "zero_point_dropped": ("(decode_int(q, 4, False) - zq)", "(decode_int(q, 4, False))"),
+    "zero_point_sign": ("(decode_int(q, 4, False) - zq)", "(decode_int(q, 4, False) + zq)"),
+    "weight_transposed": ("@ np.asarray(wdeq, dtype=np.float64).T", "@ np.asarray(wdeq, dtype=np.float64).T[::-1]"),
+    "e2m1_subnormal": ("m * 0.5, np.ldexp", "m * 0.75, np.ldexp"),
+    "e2m1_bias": ("(e - 1).astype(np.int32)", "(e - 2).astype(np.int32)"),
+    "e4m3_bias": ("(e - 7).astype(np.int32)", "(e - 8).astype(np.int32)"),
+    "e4m3_subnormal": ("np.ldexp(m / 8.0, -6)", "np.ldexp(m / 8.0, -7)"),
+    "e8m0_bias": ("(b - 127).astype(np.int32)", "(b - 128).astype(np.int32)"),
+    "int4_unsigned_as_signed": ("c = np.where(c >= (1 << (bits - 1)), c - (1 << bits), c)", "c = np.where(c > (1 << (bits - 1)), c - (1 << bits), c)"),
+    "nvfp4_global_dropped": ("return decode_e2m1(q) * sb * g\n    if wfmt", "return decode_e2m1(q) * sb\n    if wfmt"),
+    "act_token_scale_dropped": ("return decode_e4m3(data) * s", "return decode_e4m3(data)"),
+    "act_nvfp4_block": ("np.repeat(decode_ue4m3(scale), 16, axis=-1)", "np.repeat(decode_ue4m3(scale), 32, axis=-1)"),
+    "group_index": ("np.repeat(s, group, axis=-1)[..., :k]\n    if wfmt == \"uint4_zp\"", "np.tile(s, group)[..., :k]\n    if wfmt == \"uint4_zp\""),
+    "bias_dropped": ("y = y + decode_bf16(bias).reshape(1, -1)", "y = y"),
+    "topk_weight_dropped": ("v = v * float(np.asarray(topk_weights)[t, j])", "v = v"),
+    "moe_slot_order": ("t, j = divmod(int(r), k)", "j, t = divmod(int(r), T)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name):
+    mod = _mutant(*MUTATIONS[name])
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin(mod)
+        except (AssertionError, ValueError, IndexError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught the planted mistake {name}"
+
+
+def test_unmutated_copy_passes():
+    mod = _mutant("import numpy as np", "import numpy as np")
+    for pin in pins.ALL_PINS:
+        pin(mod)

@@ -1,0 +1,131 @@
+"""Quantization recipes that turn the synthetic fp32 draws into the GEMM's inputs.
+
+These are the input recipes of the benchmark workloads (they encode; nothing
+here decodes or multiplies).  Each rule is the plainest reading of the format's
+public definition:
+
+* grouped INT4: scale = absmax / 7 rounded to bf16, codes rint(w / scale)
+  clamped to [-7, 7] (the value set of a zero-exponent e0m3 float);
+* grouped UINT4 with zero point: scale = (max - min) / 15 in bf16, zero =
+  clamp(rint(-min / scale), 0, 15), code = clamp(rint(w / scale) + zero, 0, 15);
+* NVFP4: fp32 tensor scale g = amax / (6 * 448), e4m3 block-16 scale
+  e4m3(amax_b / (6 g)) saturated at 448, e2m1 codes of x / (sb * g);
+* MXFP4 (OCP Microscaling v1.0 section 6.3): e8m0 block-32 scale
+  2**(floor(log2 amax_b) - 2), e2m1 codes of x / scale, saturating;
+* FP8 per token: s_t = absmax_t / 448, e4m3(a / s_t) saturated.
+
+Rounding is to nearest, ties to even, everywhere.  All functions take torch
+tensors on any device and return tensors on the same device.  Codes are packed
+two per byte, low nibble = even k.
+"""
+import torch
+
+E4M3_MAX = 448.0
+E2M1_MAX = 6.0
+
+
+def pack_nibbles(codes):
+    """[..., K] uint8 codes in 0..15 -> [..., K/2] bytes, low nibble = even k."""
+    c = codes.to(torch.uint8)
+    return (c[..., 0::2] | (c[..., 1::2] << 4)).contiguous()
+
+
+def _rint(x):
+    return torch.round(x)  # round half to even
+
+
+def quant_int4_sym(w, group):
+    """w fp32 [..., N, K] -> (packed codes uint8 [..., N, K/2], scales bf16 [..., N, K/group])."""
+    *lead, n, k = w.shape
+    wg = w.reshape(*lead, n, k // group, group)
+    s = (wg.abs().amax(dim=-1) / 7.0).to(torch.bfloat16)
+    sf = s.float().unsqueeze(-1)
+    q = torch.where(sf > 0, _rint(wg / torch.where(sf > 0, sf, torch.ones_like(sf))), torch.zeros_like(wg))
+    q = q.clamp(-7, 7).to(torch.int16)
+    codes = (q & 0xF).to(torch.uint8).reshape(*lead, n, k)
+    return pack_nibbles(codes), s.contiguous()
+
+
+def quant_uint4_zp(w, group):
+    """w fp32 [..., N, K] -> (packed codes, scales bf16 [..., N, K/g], zeros uint8 [..., N, K/g])."""
+    *lead, n, k = w.shape
+    wg = w.reshape(*lead, n, k // group, group)
+    lo = wg.amin(dim=-1)
+    hi = wg.amax(dim=-1)
+    s = ((hi - lo) / 15.0).to(torch.bfloat16)
+    sf = s.float()
+    safe = torch.where(sf > 0, sf, torch.ones_like(sf))
+    z = torch.where(sf > 0, _rint(-lo / safe), torch.zeros_like(sf)).clamp(0, 15)
+    q = torch.where(sf.unsqueeze(-1) > 0, _rint(wg / safe.unsqueeze(-1)) + z.unsqueeze(-1), torch.zeros_like(wg))
+    q = q.clamp(0, 15).to(torch.uint8).reshape(*lead, n, k)
+    return pack_nibbles(q), s.contiguous(), z.to(torch.uint8).contiguous()
+
+
+def e2m1_encode(v):
+    """fp32 -> e2m1 code (uint8, 0..15): nearest on {0,.5,1,1.5,2,3,4,6}, ties to even, saturating.
+
+    Zero magnitudes get code 0 (positive zero).
+    """
+    a = v.abs()
+    # magnitude code m: thresholds between neighbours, tie goes to the even mantissa
+    m = torch.zeros_like(a, dtype=torch.uint8)
+    m = torch.where(a > 0.25, torch.full_like(m, 1), m)
+    m = torch.where(a >= 0.75, torch.full_like(m, 2), m)
+    m = torch.where(a > 1.25, torch.full_like(m, 3), m)
+    m = torch.where(a >= 1.75, torch.full_like(m, 4), m)
+    m = torch.where(a > 2.5, torch.full_like(m, 5), m)
+    m = torch.where(a >= 3.5, torch.full_like(m, 6), m)
+    m = torch.where(a > 5.0, torch.full_like(m, 7), m)
+    sign = ((v < 0) & (m > 0)).to(torch.uint8) << 3
+    return m | sign
+
+
+def e4m3_encode(v):
+    """fp32 -> e4m3fn byte, RNE, saturating at +-448."""
+    return v.clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def _e4m3_value(b):
+    return b.view(torch.float8_e4m3fn).to(torch.float32)
+
+
+def quant_nvfp4(x, block=16, global_amax=None):
+    """x fp32 [..., R, K] -> (packed e2m1 [..., R, K/2], ue4m3 scales [..., R, K/16], g fp32 scalar tensor).
+
+    g is the per-tensor decode multiplier amax / (6 * 448); value = e2m1 * sb * g.
+    """
+    *lead, r, k = x.shape
+    amax = x.abs().amax() if global_amax is None else global_amax
+    g = (amax.to(torch.float32) / (E2M1_MAX * E4M3_MAX)).reshape(())
+    xb = x.reshape(*lead, r, k // block, block)
+    amax_b = xb.abs().amax(dim=-1)
+    safe_g = torch.where(g > 0, g, torch.ones_like(g))
+    sb = e4m3_encode(amax_b / (E2M1_MAX * safe_g))
+    sbf = _e4m3_value(sb) * safe_g
+    den = torch.where(sbf > 0, sbf, torch.ones_like(sbf)).unsqueeze(-1)
+    q = e2m1_encode(xb / den)
+    q = torch.where(sbf.unsqueeze(-1) > 0, q, torch.zeros_like(q)).reshape(*lead, r, k)
+    return pack_nibbles(q), sb.contiguous(), g
+
+
+def quant_mxfp4(w, block=32):
+    """w fp32 [..., N, K] -> (packed e2m1 [..., N, K/2], e8m0 scales uint8 [..., N, K/32])."""
+    *lead, n, k = w.shape
+    wb = w.reshape(*lead, n, k // block, block)
+    amax = wb.abs().amax(dim=-1)
+    _, ex = torch.frexp(amax)  # amax = m * 2**ex, m in [0.5, 1): floor(log2 amax) = ex - 1
+    e = (ex.to(torch.int32) - 1 - 2 + 127).clamp(0, 254)
+    e = torch.where(amax > 0, e, torch.full_like(e, 127))
+    scale = torch.ldexp(torch.ones_like(amax), (e - 127).to(torch.float32))
+    q = e2m1_encode(wb / scale.unsqueeze(-1))
+    q = torch.where(amax.unsqueeze(-1) > 0, q, torch.zeros_like(q)).reshape(*lead, n, k)
+    return pack_nibbles(q), e.to(torch.uint8).contiguous()
+
+
+def quant_e4m3_per_token(a):
+    """a fp32 [T, K] -> (e4m3 bytes [T, K], per-token fp32 scale [T] = absmax / 448)."""
+    s = a.abs().amax(dim=-1) / E4M3_MAX
+    safe = torch.where(s > 0, s, torch.ones_like(s))
+    q = e4m3_encode(a / safe.unsqueeze(-1))
+    q = torch.where(s.unsqueeze(-1) > 0, q, torch.zeros_like(q))
+    return q.contiguous(), s.to(torch.float32).contiguous()
