@@ -1,0 +1,428 @@
+"""Benchmark of the fused-dequantization quantized GEMM on GB300.
+
+Default workload: dense W4A16 with UINT4 codes + zero points (group 128),
+K=4096, N=14336, swept over M in {1, 16, 64, 256, 1024, 4096, 8192}.  One step
+is one call per M (the whole hot path: repacked weights are resident, every
+call decodes, multiplies and runs the epilogue).  Each call is timed alone with
+CUDA events on its stream after an L2 flush (a write of 2x the L2 size outside
+the event window), as in the microbenchmark protocol of the Humming
+announcement ("Results: kernel microbenchmarks": cold L2, warmed, independent
+samples).
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.  `--config` selects another
+workload (nvfp4, moe_w4a16, moe_mxfp4, w4a16_sym) for ad-hoc measurement.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from workload import configs as W  # noqa: E402
+
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# dense tensor-core peaks relative to bf16 (nominal 2.25 / 4.5 / 13.5 PFLOP/s)
+DTYPE_RATIO = {"bf16": 1.0, "fp8": 2.0, "fp4": 6.0}
+PATH_DTYPE = {"int4_sym": "bf16", "uint4_zp": "bf16", "nvfp4": "fp4", "mxfp4": "fp8"}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+def env_rank():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ workload
+def make_calls(cfg_name, seed, device):
+    """Inputs resident on the device for every size of the sweep: [(size, call, info)]."""
+    import quantized_gemm_dequant_gb300 as hq
+    c = W.CONFIGS[cfg_name]
+    calls = []
+    if c["kind"] == "dense":
+        base = W.make_dense(cfg_name, 1, seed=seed, device=device)
+        fmt, packed = hq.pack_inputs(base, device)
+        wbytes = W.weight_bytes(c["wfmt"], c["N"], c["K"], c["G"])
+        for M in c["sizes"]:
+            a = W.quantize_acts(c["afmt"], W.acts_fp32(seed, M, c["K"], outliers=c["afmt"] == "nvfp4", device=device))
+            ws = hq.make_workspace(fmt, M, 1, device)
+            out = torch.empty((M, c["N"]), dtype=torch.bfloat16, device=device)
+            info = dict(M=M, flops=W.dense_flops(M, c["N"], c["K"]), weight_bytes=wbytes,
+                        total_bytes=wbytes + W.act_bytes(c["afmt"], M, c["K"]) + 2 * M * c["N"],
+                        h2d=sum(t.numel() * t.element_size() for t in a.values()), d2h=2 * M * c["N"])
+
+            def call(a=a, ws=ws, out=out, M=M, stream=None):
+                return hq.gemm(fmt, a, packed, M, out=out, workspace=ws, stream=stream)
+
+            calls.append((M, call, info, a, out, ws))
+        return fmt, packed, calls
+    E, k = c["E"], c["topk"]
+    base = W.make_moe(cfg_name, 1, seed=seed, device=device)
+    fmt, packed = hq.pack_inputs(base, device)
+    del base
+    per_expert = W.weight_bytes(c["wfmt"], c["N"], c["K"], c["G"])
+    for T in c["sizes"]:
+        a = W.quantize_acts(c["afmt"], W.acts_fp32(seed, T, c["K"], device=device))
+        ids, tw = W.zipf_route(seed, T, E, k, device=device)
+        hit = int(torch.unique(ids).numel())
+        ws = hq.make_workspace(fmt, T, k, device)
+        out = torch.empty((T * k, c["N"]), dtype=torch.bfloat16, device=device)
+        info = dict(M=T, flops=2.0 * T * k * c["N"] * c["K"], weight_bytes=per_expert * hit, experts_hit=hit,
+                    total_bytes=per_expert * hit + W.act_bytes(c["afmt"], T, c["K"]) + 2 * T * k * c["N"] + 8 * T * k,
+                    h2d=sum(t.numel() * t.element_size() for t in a.values()) + 8 * T * k, d2h=2 * T * k * c["N"])
+
+        def call(a=a, ids=ids, tw=tw, ws=ws, out=out, stream=None):
+            return hq.moe_gemm(fmt, a, packed, ids, tw, out=out, workspace=ws, stream=stream)
+
+        calls.append((T, call, info, dict(a, ids=ids, tw=tw), out, ws))
+    return fmt, packed, calls
+
+
+def roofline_of(info, t_s, pk, dt):
+    tc = pk["bf16_tflops"] * DTYPE_RATIO[dt] * 1e12
+    t_hbm = info["total_bytes"] / (pk["hbm_gbs"] * 1e9)
+    t_tc = info["flops"] / tc
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    return bound, max(t_hbm, t_tc) / t_s
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args):
+    rank, world, local = env_rank()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    pk, pk_src = peaks()
+    c = W.CONFIGS[args.config]
+    dt = PATH_DTYPE[c["wfmt"]]
+    fmt, packed, calls = make_calls(args.config, args.seed, dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def one_step(times):
+        for i, (M, call, info, _, _, _) in enumerate(calls):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call(stream=stream)
+            e1.record(stream)
+            times[i].append((e0, e1))
+
+    warm = [[] for _ in calls]
+    for _ in range(args.warmup):
+        one_step(warm)
+    barrier()
+    times = [[] for _ in calls]
+    clk = ClockSampler(local)
+    clk.start()
+    barrier()
+    t_wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_step(times)
+    barrier()
+    t_wall = time.perf_counter() - t_wall0
+    clocks = clk.stop()
+    per_call_ms = [[a.elapsed_time(b) for a, b in ts] for ts in times]
+    step_ms = sum(sum(x) for x in per_call_ms) / args.steps
+    # device status must be clean after the run
+    import quantized_gemm_dequant_gb300 as hq
+    for (_, _, _, _, _, ws) in calls:
+        st = hq.last_device_status(ws)
+        if st != 0:
+            raise RuntimeError(f"device status {hq.status_string(st)} after the timed run")
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([step_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        step_ms = float(tt.item())
+    flops_step = sum(info["flops"] for (_, _, info, _, _, _) in calls)
+    value = world * flops_step / (step_ms * 1e-3) / 1e12
+
+    sweep, by_kernel = [], {}
+    for (M, _, info, _, _, _), ms in zip(calls, per_call_ms):
+        t = statistics.median(ms) * 1e-3
+        bound, frac = roofline_of(info, t, pk, dt)
+        e = dict(M=M, us=round(t * 1e6, 2), tflops=round(info["flops"] / t / 1e12, 3),
+                 weight_gbs=round(info["weight_bytes"] / t / 1e9, 1), total_gbs=round(info["total_bytes"] / t / 1e9, 1),
+                 bound=bound, roofline_frac=round(frac, 4))
+        if "experts_hit" in info:
+            e["experts_hit"] = info["experts_hit"]
+        sweep.append(e)
+        key = kernel_name(args.config, M)
+        k = by_kernel.setdefault(key, dict(flops=0.0, bytes=0.0, t=0.0, n=0))
+        k["flops"] += info["flops"] * len(ms)
+        k["bytes"] += info["total_bytes"] * len(ms)
+        k["t"] += sum(ms) * 1e-3
+        k["n"] += len(ms)
+    dom = max(by_kernel, key=lambda k: by_kernel[k]["t"])
+    d = by_kernel[dom]
+    tc_peak = pk["bf16_tflops"] * DTYPE_RATIO[dt]
+    t_launch = d["t"] / d["n"]
+    if d["flops"] / (tc_peak * 1e12) >= d["bytes"] / (pk["hbm_gbs"] * 1e9):
+        ach = d["flops"] / d["n"] / t_launch / 1e12
+        roof = dict(bound="tensor", achieved=round(ach, 2), peak=tc_peak, unit="TFLOP/s", frac=round(ach / tc_peak, 4))
+    else:
+        ach = d["bytes"] / d["n"] / t_launch / 1e9
+        roof = dict(bound="hbm", achieved=round(ach, 1), peak=pk["hbm_gbs"], unit="GB/s", frac=round(ach / pk["hbm_gbs"], 4))
+    roof.update(kernel=dom, launches_per_step=d["n"] // args.steps, peak_source=f"{pk_src} ({dt} "
+                f"{'burst bf16 x nominal ratio' if dt != 'bf16' else 'burst'})", traffic=traffic_of(dom, args.config))
+
+    e2e = measure_e2e(args, calls, stream, dev) if not args.no_e2e else None
+    cpu = cpu_baseline_line(args) if (rank == 0 and not args.no_cpu) else None
+    line = {
+        "metric": "quantized GEMM TFLOP/s and weight GB/s vs M; % of HBM / tensor-core roofline",
+        "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": dt, "data": "synthetic (seeded Philox draws, quantized by the workload recipe)",
+        "config": {"workload": workload_name(args.config), "sizes": c["sizes"],
+                   "l2": "flushed before every call (write of max(2xL2, 256 MB), outside the event window)",
+                   "timing": "CUDA events around each call on its stream; step = sum over the sweep",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roof, "sweep": sweep, "gpu_launches": gpu_launches(args.config, calls) * args.steps,
+        "clocks": clocks, "wall_s_timed": round(t_wall, 3), "e2e": e2e, "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def kernel_name(cfg, M):
+    c = W.CONFIGS[cfg]
+    path = {"int4_sym": 0, "uint4_zp": 0, "nvfp4": 1, "mxfp4": 2}[c["wfmt"]]
+    if c["kind"] == "dense":
+        bt = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128 if M <= 128 else 256
+    else:
+        avg = -(-M * c["topk"] // c["E"])
+        bt = 16 if avg <= 16 else 32 if avg <= 32 else 64 if avg <= 64 else 128
+    return f"hq::hq_gemm_kernel<{path}, {bt}>"
+
+
+def gpu_launches(cfg, calls):
+    # dense: one GEMM kernel per call; MoE: routing kernel + GEMM kernel (+ a memset of the expert counts)
+    return len(calls) * (1 if W.CONFIGS[cfg]["kind"] == "dense" else 2)
+
+
+def traffic_of(kernel, cfg):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if one matches this build."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(cfg, {}).get(kernel)
+        return e.get("dram_bytes_per_launch") if e else None
+    except Exception:
+        return None
+
+
+def workload_name(cfg):
+    c = W.CONFIGS[cfg]
+    if c["kind"] == "dense":
+        return (f"dense {c['wfmt']} x {c['afmt']} (group {c['G']}), K={c['K']}, N={c['N']}, "
+                f"M in {c['sizes']}")
+    return (f"MoE {c['wfmt']} x {c['afmt']}, E={c['E']}, top-{c['topk']}, K={c['K']}, N={c['N']}, "
+            f"T in {c['sizes']}, Zipf(1.1) routing")
+
+
+def measure_e2e(args, calls, stream, dev):
+    """Same sweep through the C ABI with pinned host buffers: H2D of the inputs, the call, D2H of C."""
+    hosts = []
+    for (M, call, info, a, out, ws) in calls:
+        ha = {k: v.detach().cpu().pin_memory() for k, v in a.items()}
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hosts.append((ha, hout))
+
+    def one(times):
+        for (M, call, info, a, out, ws), (ha, hout) in zip(calls, hosts):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for k, v in ha.items():
+                a[k].copy_(v, non_blocking=True)
+            call(stream=stream)
+            hout.copy_(out, non_blocking=True)
+            e1.record(stream)
+            times.append((e0, e1))
+
+    for _ in range(max(1, args.warmup)):
+        one([])
+    torch.cuda.synchronize(dev)
+    ts = []
+    for _ in range(args.steps):
+        one(ts)
+    torch.cuda.synchronize(dev)
+    ms = sum(a.elapsed_time(b) for a, b in ts) / args.steps
+    flops = sum(info["flops"] for (_, _, info, _, _, _) in calls)
+    return {"value": round(flops / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(sum(info["h2d"] for (_, _, info, _, _, _) in calls)),
+            "d2h_bytes_per_step": int(sum(info["d2h"] for (_, _, info, _, _, _) in calls)),
+            "ms_per_step": round(ms, 4), "note": "weights packed once and resident; per call: H2D of the "
+            "activations (pinned), the C-ABI call, D2H of C; no L2 flush"}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_step(cfg_name, seed, state):
+    """One bounded sample of the workload through the CPU oracle: for each size of the sweep,
+    decode the weights and compute min(M, 2) output rows in fp64.  Returns (flops, seconds)."""
+    import numpy as np
+    import oracle
+    from tests import ref_helpers as R
+    c = W.CONFIGS[cfg_name]
+    if "inp" not in state:
+        if c["kind"] == "dense":
+            state["inp"] = W.make_dense(cfg_name, 2, seed=seed)
+        else:
+            state["inp"] = W.make_moe(cfg_name, 2, seed=seed, experts_subset=None) if c["E"] <= 128 else None
+    inp = state["inp"]
+    flops, t0 = 0.0, time.perf_counter()
+    for M in c["sizes"]:
+        rows = min(M, 2)
+        if c["kind"] == "dense":
+            y = oracle.gemm(R.acts_of(inp, list(range(rows))), R.weights_of(inp))
+            flops += 2.0 * rows * c["N"] * c["K"]
+        else:
+            if inp is None:  # too large for the host: one expert stands for the sample
+                one = W.make_moe(cfg_name, 2, seed=seed, experts_subset=[0])
+                y = oracle.gemm(R.acts_of(one, list(range(rows))), R.weights_of(one, 0))
+            else:
+                y = oracle.gemm(R.acts_of(inp, list(range(rows))), R.weights_of(inp, 0))
+            flops += 2.0 * rows * c["N"] * c["K"]
+        assert np.all(np.isfinite(y))
+    return flops, time.perf_counter() - t0
+
+
+def cpu_cores():
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(v):
+            return int(os.environ[v])
+    return os.cpu_count()
+
+
+def cpu_baseline_line(args):
+    state = {}
+    flops, s = oracle_step(args.config, args.seed, state)
+    return {"value": round(flops / s / 1e12, 9), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": "one pass of the sweep with min(M, 2) output rows per size: full weight decode to fp64 "
+                      "plus the fp64 matmul of those rows (numpy)", "seconds": round(s, 2)}
+
+
+def run_reference(args):
+    rank, world, _ = env_rank()
+    if rank != 0:
+        return
+    state = {}
+    for _ in range(args.warmup):
+        oracle_step(args.config, args.seed, state)
+    flops = secs = 0.0
+    for _ in range(args.steps):
+        f, s = oracle_step(args.config, args.seed, state)
+        flops += f
+        secs += s
+    value = flops / secs / 1e12
+    c = W.CONFIGS[args.config]
+    line = {
+        "metric": "quantized GEMM TFLOP/s and weight GB/s vs M; % of HBM / tensor-core roofline",
+        "impl": "reference", "value": round(value, 9), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name(args.config), "sizes": c["sizes"]},
+        "cpu_baseline": {"value": round(value, 9), "unit": "TFLOP/s", "kind": "oracle", "cores": cpu_cores(),
+                         "sample": "per step: each size of the sweep, weight decode + fp64 matmul of min(M, 2) rows"},
+        "e2e": {"value": round(value, 9), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="w4a16_asym", choices=list(W.CONFIGS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup) if args.impl == "ours" else args.warmup
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,162 @@
+/* hq.h -- C ABI of the GB300 (sm_103a) fused-dequantization quantized GEMM library.
+ *
+ * The operation is the one the Humming announcement describes for its kernel
+ * library: low-bit weights in a unified "standard format" ("A unified
+ * quantization representation"), repacked into a kernel layout ("Tuning and JIT
+ * compilation per workload", preprocessing paragraph), multiplied by BF16, FP8
+ * or FP4 activations with dequantization and scaling inside the kernel and the
+ * scales, top-k weights and bias applied in the output stage ("Shared CUDA
+ * components across formats and architectures"), for dense GEMMs and for MoE
+ * GEMMs whose tokens are spread over experts ("Results: kernel
+ * microbenchmarks", WnA16 paragraph on the Indexed and Grouped MoE paths).
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers, 16-byte aligned, owned by the
+ *    caller.  The library never allocates or frees device memory.
+ *  - Calls are asynchronous on `stream`; they return after enqueueing work.
+ *    Argument errors are detected on the host and returned synchronously
+ *    before anything is enqueued.  Errors found by a kernel (a bounded wait
+ *    that timed out, a routing id out of range) are recorded in the status
+ *    word at the start of the workspace; read it with hq_last_device_status.
+ *  - No C++ exception crosses this interface.  No global mutable state is
+ *    kept, so calls on different streams with different workspaces may run
+ *    concurrently.
+ *  - Weights W are [N, K] per expert ("out, in", as for a linear layer);
+ *    the product is C[m, n] = sum_k A[m, k] * Wdeq[n, k].
+ *  - 4-bit codes are stored two per byte, the low nibble holding the even k.
+ */
+#ifndef HQ_H_
+#define HQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define HQ_API __attribute__((visibility("default")))
+#else
+#define HQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st* hq_stream_t;
+
+typedef enum {
+  HQ_OK = 0,
+  HQ_ERR_INVALID_ARG = 1, /* null pointer, bad size, inconsistent descriptor */
+  HQ_ERR_UNSUPPORTED = 2, /* a format combination this library does not implement */
+  HQ_ERR_ALIGNMENT = 3,   /* a pointer not 16-byte aligned, or K not a multiple of the tile */
+  HQ_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch error, no device) */
+  HQ_ERR_TIMEOUT = 5,     /* device: a pipeline wait exceeded its time limit; the output is undefined */
+  HQ_ERR_BAD_ROUTING = 6, /* device: a top-k expert id outside [0, E) or repeated within a token */
+  HQ_ERR_WORKSPACE = 7    /* workspace missing or smaller than hq_workspace_bytes() */
+} hq_status_t;
+
+/* Weight numeric formats (the "standard format" parameters). */
+enum {
+  HQ_W_INT4_SYM = 1, /* q in [-7, 7] two's complement nibbles (the e0m3 value set), bf16 scale per group */
+  HQ_W_UINT4_ZP = 2, /* q, z in [0, 15], value (q - z) * s, bf16 scale and uint4 zero per group */
+  HQ_W_NVFP4 = 3,    /* e2m1 codes, ue4m3 scale per 16 K, fp32 global scale per expert */
+  HQ_W_MXFP4 = 4     /* e2m1 codes, e8m0 scale per 32 K (OCP Microscaling) */
+};
+/* Scale data types. */
+enum { HQ_S_BF16 = 1, HQ_S_UE4M3 = 2, HQ_S_UE8M0 = 3 };
+/* Activation formats. */
+enum {
+  HQ_A_BF16 = 1,       /* bf16 [M, K] */
+  HQ_A_E4M3_TOKEN = 2, /* e4m3 [M, K] bytes + fp32 scale per row (token) */
+  HQ_A_NVFP4 = 3       /* e2m1 [M, K/2] packed + ue4m3 [M, K/16] + fp32 global scale [1] */
+};
+
+/* The unified quantization description ("standard format").  Supported
+ * combinations:
+ *   INT4_SYM, group 128, BF16 scales,  no zero, no global, act BF16
+ *   UINT4_ZP, group 128, BF16 scales,  zero,    no global, act BF16
+ *   NVFP4,    group 16,  UE4M3 scales, no zero, global,    act NVFP4
+ *   MXFP4,    group 32,  UE8M0 scales, no zero, no global, act E4M3_TOKEN
+ * Anything else returns HQ_ERR_UNSUPPORTED. */
+typedef struct {
+  int32_t weight_type;      /* HQ_W_* */
+  int32_t group_size;       /* K elements per scale */
+  int32_t scale_type;       /* HQ_S_* */
+  int32_t has_zero;         /* 1 for UINT4_ZP */
+  int32_t has_global_scale; /* 1 for NVFP4 */
+  int32_t act_type;         /* HQ_A_* */
+  int64_t N;                /* output features per expert, >= 1 */
+  int64_t K;                /* input features, multiple of 256 */
+  int64_t num_experts;      /* 1 for a dense layer */
+} hq_format_t;
+
+/* Activation operand.  data: see HQ_A_*; scale: fp32 [M] for E4M3_TOKEN,
+ * ue4m3 [M, K/16] for NVFP4, NULL for BF16; global_scale: fp32 [1] for NVFP4. */
+typedef struct {
+  const void* data;
+  const void* scale;
+  const float* global_scale;
+} hq_act_t;
+
+/* Bytes of the packed (kernel-layout) weight buffer for `fmt` (all experts).
+ * Returns 0 for an invalid or unsupported descriptor. */
+HQ_API size_t hq_packed_bytes(const hq_format_t* fmt);
+
+/* Repack standard-format weights into the kernel layout (preprocessing: validate,
+ * pad N to the 128-row tile, reorder codes, scales and zeros into tile order).
+ *   codes        uint8 [E][N][K/2]
+ *   scales       [E][N][K/group] of scale_type (bf16 as 16-bit patterns, ue4m3/e8m0 bytes)
+ *   zeros        uint8 [E][N][K/group], values 0..15 (UINT4_ZP), else NULL
+ *   global_scale fp32 [E] (NVFP4), else NULL
+ *   packed       hq_packed_bytes(fmt) bytes, written entirely (padding zeroed)
+ * Runs one kernel on `stream`.  Bit-exact and invertible by hq_unpack_weights. */
+HQ_API hq_status_t hq_pack_weights(const hq_format_t* fmt, const uint8_t* codes, const void* scales, const uint8_t* zeros,
+                            const float* global_scale, void* packed, hq_stream_t stream);
+
+/* Inverse of hq_pack_weights: writes the standard-format tensors back (same
+ * shapes; zeros / global_scale may be NULL when the format has none). */
+HQ_API hq_status_t hq_unpack_weights(const hq_format_t* fmt, const void* packed, uint8_t* codes, void* scales,
+                              uint8_t* zeros, float* global_scale, hq_stream_t stream);
+
+/* Workspace bytes for a call with M rows (dense) or T tokens with `topk`
+ * experts each (MoE; pass topk = 1 for dense).  The workspace holds the
+ * device status word, split-K partial sums and tile counters, and the MoE
+ * routing tables.  It must be zeroed once with hq_workspace_init before its
+ * first use; calls leave it reusable.  One workspace serves one stream at a time. */
+HQ_API size_t hq_workspace_bytes(const hq_format_t* fmt, int64_t M_or_T, int32_t topk);
+
+/* Zero `bytes` of workspace on `stream` (cudaMemsetAsync). */
+HQ_API hq_status_t hq_workspace_init(void* workspace, size_t bytes, hq_stream_t stream);
+
+/* Dense quantized GEMM: C[M, N] (bf16, row-major) = A . Wdeq^T (+ bias[n]).
+ *   A       activation operand, M rows of K
+ *   packedW hq_pack_weights output with num_experts == 1
+ *   bias    bf16 [N] or NULL
+ * Output scaling: NVFP4 multiplies by A.global_scale * W global scale,
+ * E4M3_TOKEN by the row's token scale.  M may be 0 (no work).  Accumulation is
+ * fp32; C is rounded to nearest-even bf16. */
+HQ_API hq_status_t hq_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* packedW, const void* bias, void* C,
+                    int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes, hq_stream_t stream);
+
+/* MoE grouped GEMM over E = fmt->num_experts experts.
+ *   A            T token rows of K
+ *   topk_ids     int32 [T, topk], distinct expert ids per token in [0, E)
+ *   topk_weights fp32 [T, topk] or NULL (NULL = weight 1)
+ *   C            bf16 [T * topk, N]: row t*topk + j = topk_weights[t, j] * (A[t] . Wdeq[topk_ids[t, j]]^T)
+ * A row whose id is out of range is left unwritten and HQ_ERR_BAD_ROUTING is
+ * recorded in the workspace status. */
+HQ_API hq_status_t hq_moe_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* packedW, const int32_t* topk_ids,
+                        const float* topk_weights, int64_t T, int32_t topk, void* C, void* workspace, size_t ws_bytes,
+                        hq_stream_t stream);
+
+/* Copy the device status word out of `workspace` (synchronizes `stream`) and
+ * clear it.  *status_out receives HQ_OK or the first device-detected error. */
+HQ_API hq_status_t hq_last_device_status(void* workspace, int32_t* status_out, hq_stream_t stream);
+
+/* Static description of a status code. */
+HQ_API const char* hq_status_string(hq_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HQ_H_ */

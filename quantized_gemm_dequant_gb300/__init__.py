@@ -1,0 +1,187 @@
+"""Python binding of libhq (GB300 fused-dequantization quantized GEMM).
+
+Argument marshalling only: every step of the computation runs in the library's
+CUDA kernels.  torch provides device memory and the current stream.  Importing
+this package fails loudly if libhq.so has not been built (run
+`python -c "import __graft_entry__ as g; g.build()"` or
+`python quantized_gemm_dequant_gb300/build.py`).
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libhq.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libhq.so not found at {LIB_PATH}: build the CUDA library first "
+                      "(quantized_gemm_dequant_gb300/build.py)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+# ----------------------------------------------------------------- C types
+HQ_OK, HQ_ERR_INVALID_ARG, HQ_ERR_UNSUPPORTED, HQ_ERR_ALIGNMENT, HQ_ERR_CUDA, HQ_ERR_TIMEOUT, \
+    HQ_ERR_BAD_ROUTING, HQ_ERR_WORKSPACE = range(8)
+HQ_W_INT4_SYM, HQ_W_UINT4_ZP, HQ_W_NVFP4, HQ_W_MXFP4 = 1, 2, 3, 4
+HQ_S_BF16, HQ_S_UE4M3, HQ_S_UE8M0 = 1, 2, 3
+HQ_A_BF16, HQ_A_E4M3_TOKEN, HQ_A_NVFP4 = 1, 2, 3
+
+EXPORTS = ["hq_packed_bytes", "hq_pack_weights", "hq_unpack_weights", "hq_workspace_bytes", "hq_workspace_init",
+           "hq_gemm", "hq_moe_gemm", "hq_last_device_status", "hq_status_string"]
+
+
+class Format(ctypes.Structure):
+    _fields_ = [("weight_type", ctypes.c_int32), ("group_size", ctypes.c_int32), ("scale_type", ctypes.c_int32),
+                ("has_zero", ctypes.c_int32), ("has_global_scale", ctypes.c_int32), ("act_type", ctypes.c_int32),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("num_experts", ctypes.c_int64)]
+
+
+class Act(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("global_scale", ctypes.c_void_p)]
+
+
+_vp, _i64, _i32, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+_F = ctypes.POINTER(Format)
+_A = ctypes.POINTER(Act)
+_lib.hq_packed_bytes.argtypes = [_F]
+_lib.hq_packed_bytes.restype = _sz
+_lib.hq_pack_weights.argtypes = [_F, _vp, _vp, _vp, _vp, _vp, _vp]
+_lib.hq_pack_weights.restype = ctypes.c_int
+_lib.hq_unpack_weights.argtypes = [_F, _vp, _vp, _vp, _vp, _vp, _vp]
+_lib.hq_unpack_weights.restype = ctypes.c_int
+_lib.hq_workspace_bytes.argtypes = [_F, _i64, _i32]
+_lib.hq_workspace_bytes.restype = _sz
+_lib.hq_workspace_init.argtypes = [_vp, _sz, _vp]
+_lib.hq_workspace_init.restype = ctypes.c_int
+_lib.hq_gemm.argtypes = [_F, _A, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _vp]
+_lib.hq_gemm.restype = ctypes.c_int
+_lib.hq_moe_gemm.argtypes = [_F, _A, _vp, _vp, _vp, _i64, _i32, _vp, _vp, _sz, _vp]
+_lib.hq_moe_gemm.restype = ctypes.c_int
+_lib.hq_last_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32), _vp]
+_lib.hq_last_device_status.restype = ctypes.c_int
+_lib.hq_status_string.argtypes = [ctypes.c_int]
+_lib.hq_status_string.restype = ctypes.c_char_p
+
+_WEIGHT = {"int4_sym": (HQ_W_INT4_SYM, 128, HQ_S_BF16, 0, 0, HQ_A_BF16),
+           "uint4_zp": (HQ_W_UINT4_ZP, 128, HQ_S_BF16, 1, 0, HQ_A_BF16),
+           "nvfp4": (HQ_W_NVFP4, 16, HQ_S_UE4M3, 0, 1, HQ_A_NVFP4),
+           "mxfp4": (HQ_W_MXFP4, 32, HQ_S_UE8M0, 0, 0, HQ_A_E4M3_TOKEN)}
+
+
+class HQError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} (status {code})")
+
+
+def status_string(code):
+    return _lib.hq_status_string(int(code)).decode()
+
+
+def _check(code, where):
+    if code != HQ_OK:
+        raise HQError(code, where)
+
+
+def make_format(wfmt, N, K, num_experts=1, **override):
+    """The standard-format descriptor of one of the supported weight formats."""
+    wt, g, st, hz, hg, at = _WEIGHT[wfmt]
+    f = Format(wt, g, st, hz, hg, at, int(N), int(K), int(num_experts))
+    for k, v in override.items():
+        setattr(f, k, v)
+    return f
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def packed_bytes(fmt):
+    return int(_lib.hq_packed_bytes(ctypes.byref(fmt)))
+
+
+def pack_weights(fmt, codes, scales, zeros=None, global_scale=None, out=None, stream=None):
+    """Repack standard-format weight tensors (on the GPU) into the kernel layout; returns a uint8 tensor."""
+    nb = packed_bytes(fmt)
+    if nb == 0:
+        raise HQError(HQ_ERR_UNSUPPORTED, "hq_packed_bytes")
+    if out is None:
+        out = torch.empty(nb, dtype=torch.uint8, device=codes.device)
+    _check(_lib.hq_pack_weights(ctypes.byref(fmt), _ptr(codes), _ptr(scales), _ptr(zeros), _ptr(global_scale),
+                                _ptr(out), _stream(stream)), "hq_pack_weights")
+    return out
+
+
+def unpack_weights(fmt, packed, codes, scales, zeros=None, global_scale=None, stream=None):
+    _check(_lib.hq_unpack_weights(ctypes.byref(fmt), _ptr(packed), _ptr(codes), _ptr(scales), _ptr(zeros),
+                                  _ptr(global_scale), _stream(stream)), "hq_unpack_weights")
+
+
+def workspace_bytes(fmt, rows, topk=1):
+    return int(_lib.hq_workspace_bytes(ctypes.byref(fmt), int(rows), int(topk)))
+
+
+def make_workspace(fmt, rows, topk=1, device="cuda", stream=None):
+    """Allocate (through torch) and zero a workspace for calls with `rows` rows / tokens."""
+    nb = workspace_bytes(fmt, rows, topk)
+    if nb == 0:
+        raise HQError(HQ_ERR_INVALID_ARG, "hq_workspace_bytes")
+    ws = torch.empty(nb, dtype=torch.uint8, device=device)
+    _check(_lib.hq_workspace_init(_ptr(ws), nb, _stream(stream)), "hq_workspace_init")
+    return ws
+
+
+def _act(a):
+    return Act(a["data"].data_ptr(), a["scale"].data_ptr() if a.get("scale") is not None else None,
+               a["gscale"].data_ptr() if a.get("gscale") is not None else None)
+
+
+def gemm(fmt, act, packed, M, bias=None, out=None, workspace=None, stream=None):
+    """C[M, N] bf16 = A . Wdeq^T (+ bias).  `act` is {'data', 'scale'?, 'gscale'?} of device tensors."""
+    dev = act["data"].device
+    if out is None:
+        out = torch.empty((M, fmt.N), dtype=torch.bfloat16, device=dev)
+    if workspace is None:
+        workspace = make_workspace(fmt, M, 1, dev, stream)
+    A = _act(act)
+    _check(_lib.hq_gemm(ctypes.byref(fmt), ctypes.byref(A), _ptr(packed), _ptr(bias), _ptr(out), int(M), fmt.N,
+                        fmt.K, _ptr(workspace), workspace.numel(), _stream(stream)), "hq_gemm")
+    return out
+
+
+def moe_gemm(fmt, act, packed, topk_ids, topk_weights=None, out=None, workspace=None, stream=None):
+    """C[T*topk, N] bf16, row t*topk+j = topk_w[t,j] * (A[t] . Wdeq[ids[t,j]]^T)."""
+    T, k = topk_ids.shape
+    dev = act["data"].device
+    if out is None:
+        out = torch.empty((T * k, fmt.N), dtype=torch.bfloat16, device=dev)
+    if workspace is None:
+        workspace = make_workspace(fmt, T, k, dev, stream)
+    A = _act(act)
+    _check(_lib.hq_moe_gemm(ctypes.byref(fmt), ctypes.byref(A), _ptr(packed), _ptr(topk_ids), _ptr(topk_weights),
+                            int(T), int(k), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "hq_moe_gemm")
+    return out
+
+
+def last_device_status(workspace, stream=None):
+    v = ctypes.c_int32(0)
+    _check(_lib.hq_last_device_status(_ptr(workspace), ctypes.byref(v), _stream(stream)), "hq_last_device_status")
+    return int(v.value)
+
+
+def pack_inputs(inputs, device="cuda", stream=None):
+    """Pack the weights of a workload dict (see the workload package) onto `device`; returns (fmt, packed)."""
+    w = inputs["w"]
+    E = inputs.get("E", 1)
+    fmt = make_format(inputs["wfmt"], inputs["N"], inputs["K"], E)
+    t = {k: v.to(device).contiguous() for k, v in w.items()}
+    scales = t["scales"].view(torch.uint8) if t["scales"].dtype == torch.bfloat16 else t["scales"]
+    packed = pack_weights(fmt, t["codes"], scales, t.get("zeros"), t.get("gscale"), stream=stream)
+    return fmt, packed

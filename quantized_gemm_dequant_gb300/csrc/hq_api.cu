@@ -1,0 +1,328 @@
+// C ABI: argument validation, launch planning and kernel launches.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/hq.h"
+#include "hq_gemm_kernel.cuh"
+#include "hq_layout.h"
+
+namespace hq {
+cudaError_t launch_pack(int dir, int wt, int64_t N, int64_t K, int64_t E, const void* codes, const void* scales,
+                        const void* zeros, const float* gscale, void* packed, cudaStream_t stream);
+cudaError_t launch_route(const int32_t* ids, int64_t rows, int E, int cap, int* counts, int* region, int* status,
+                         cudaStream_t stream);
+cudaError_t launch_gemm_int4(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_nvfp4(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_mxfp4(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
+
+namespace {
+
+constexpr int64_t kMaxExperts = 512;
+constexpr int64_t kMaxRows = (int64_t)1 << 30;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validate the descriptor against the supported combinations.
+hq_status_t check_format(const hq_format_t* f) {
+  if (!f) return HQ_ERR_INVALID_ARG;
+  if (f->N < 1 || f->K < 1 || f->num_experts < 1 || f->num_experts > kMaxExperts) return HQ_ERR_INVALID_ARG;
+  if (f->N > kMaxRows || f->K > kMaxRows) return HQ_ERR_INVALID_ARG;
+  switch (f->weight_type) {
+    case HQ_W_INT4_SYM:
+      if (f->group_size != 128 || f->scale_type != HQ_S_BF16 || f->has_zero || f->has_global_scale ||
+          f->act_type != HQ_A_BF16)
+        return HQ_ERR_UNSUPPORTED;
+      if (f->K % 128) return HQ_ERR_ALIGNMENT;
+      break;
+    case HQ_W_UINT4_ZP:
+      if (f->group_size != 128 || f->scale_type != HQ_S_BF16 || !f->has_zero || f->has_global_scale ||
+          f->act_type != HQ_A_BF16)
+        return HQ_ERR_UNSUPPORTED;
+      if (f->K % 128) return HQ_ERR_ALIGNMENT;
+      break;
+    case HQ_W_NVFP4:
+      if (f->group_size != 16 || f->scale_type != HQ_S_UE4M3 || f->has_zero || !f->has_global_scale ||
+          f->act_type != HQ_A_NVFP4)
+        return HQ_ERR_UNSUPPORTED;
+      if (f->K % 256) return HQ_ERR_ALIGNMENT;
+      break;
+    case HQ_W_MXFP4:
+      if (f->group_size != 32 || f->scale_type != HQ_S_UE8M0 || f->has_zero || f->has_global_scale ||
+          f->act_type != HQ_A_E4M3_TOKEN)
+        return HQ_ERR_UNSUPPORTED;
+      if (f->K % 128) return HQ_ERR_ALIGNMENT;
+      break;
+    default:
+      return HQ_ERR_UNSUPPORTED;
+  }
+  return HQ_OK;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Launch plan of one call; also fixes the workspace layout.
+struct Plan {
+  int path = 0;
+  int bt = 16;
+  int sk = 0;
+  int grid = 1;
+  int64_t n_tiles = 0, kst = 0, m_tiles = 0;
+  int64_t max_tiles = 0;   // upper bound of tiles (split-K counters)
+  int64_t region_cap = 0;  // MoE rows per expert
+  size_t off_counts = 0, off_counters = 0, off_region = 0, off_partials = 0, ws_bytes = 0;
+};
+
+int pick_bt_dense(int64_t M) {
+  if (M <= 16) return 16;
+  if (M <= 32) return 32;
+  if (M <= 64) return 64;
+  if (M <= 128) return 128;
+  return 256;
+}
+int pick_bt_moe(int64_t rows, int64_t E) {
+  const int64_t avg = (rows + E - 1) / E;
+  if (avg <= 16) return 16;
+  if (avg <= 32) return 32;
+  if (avg <= 64) return 64;
+  return 128;
+}
+
+Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int sms) {
+  Plan p;
+  const PackGeom g = pack_geom(f->weight_type, f->N, f->K, f->num_experts);
+  p.path = g.path;
+  p.n_tiles = g.n_tiles;
+  p.kst = g.k_stages;
+  if (sms < 1) sms = 1;
+  size_t off = 256;  // status word
+  if (!moe) {
+    p.bt = pick_bt_dense(M_or_T);
+    p.m_tiles = (M_or_T + p.bt - 1) / p.bt;
+    p.max_tiles = p.m_tiles * p.n_tiles;
+    p.sk = (p.max_tiles < 2 * (int64_t)sms && p.kst > 1) ? 1 : 0;
+    const int64_t W = p.max_tiles * (p.sk ? p.kst : 1);
+    p.grid = (int)(W < sms ? (W < 1 ? 1 : W) : sms);
+  } else {
+    const int64_t rows = M_or_T * topk;
+    const int64_t E = f->num_experts;
+    p.bt = pick_bt_moe(rows, E);
+    p.region_cap = M_or_T;
+    const int64_t active = rows < E ? rows : E;
+    p.max_tiles = p.n_tiles * (active + (rows + p.bt - 1) / p.bt);
+    const int64_t est_tiles = p.n_tiles * active;
+    p.sk = (est_tiles < 2 * (int64_t)sms && p.kst > 1) ? 1 : 0;
+    const int64_t W = p.max_tiles * (p.sk ? p.kst : 1);
+    p.grid = (int)(W < sms ? (W < 1 ? 1 : W) : sms);
+    p.off_counts = off;
+    off = align256(off + sizeof(int) * (size_t)E);
+  }
+  p.off_counters = off;
+  off = align256(off + sizeof(int) * (size_t)(p.max_tiles > 0 ? p.max_tiles : 1));
+  if (moe) {
+    p.off_region = off;
+    off = align256(off + sizeof(int) * (size_t)(f->num_experts * (p.region_cap > 0 ? p.region_cap : 1)));
+  }
+  if (p.sk) {
+    p.off_partials = off;
+    off = align256(off + sizeof(float) * (size_t)2 * p.grid * p.bt * TILE_N);
+  }
+  p.ws_bytes = off;
+  return p;
+}
+
+cudaError_t launch_path(const Plan& p, const GemmArgs& a, cudaStream_t s) {
+  if (p.path == PATH_INT4) return launch_gemm_int4(a, p.bt, p.grid, s);
+  if (p.path == PATH_NVFP4) return launch_gemm_nvfp4(a, p.bt, p.grid, s);
+  return launch_gemm_mxfp4(a, p.bt, p.grid, s);
+}
+
+hq_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? HQ_OK : HQ_ERR_CUDA; }
+
+}  // namespace
+}  // namespace hq
+
+using namespace hq;
+
+extern "C" {
+
+size_t hq_packed_bytes(const hq_format_t* fmt) {
+  if (check_format(fmt) != HQ_OK) return 0;
+  return (size_t)pack_geom(fmt->weight_type, fmt->N, fmt->K, fmt->num_experts).total_bytes;
+}
+
+hq_status_t hq_pack_weights(const hq_format_t* fmt, const uint8_t* codes, const void* scales, const uint8_t* zeros,
+                            const float* global_scale, void* packed, hq_stream_t stream) {
+  hq_status_t st = check_format(fmt);
+  if (st != HQ_OK) return st;
+  if (!codes || !scales || !packed) return HQ_ERR_INVALID_ARG;
+  if (fmt->has_zero && !zeros) return HQ_ERR_INVALID_ARG;
+  if (fmt->has_global_scale && !global_scale) return HQ_ERR_INVALID_ARG;
+  if (!aligned16(packed)) return HQ_ERR_ALIGNMENT;
+  return cuda_status(launch_pack(0, fmt->weight_type, fmt->N, fmt->K, fmt->num_experts, codes, scales, zeros,
+                                 global_scale, packed, (cudaStream_t)stream));
+}
+
+hq_status_t hq_unpack_weights(const hq_format_t* fmt, const void* packed, uint8_t* codes, void* scales,
+                              uint8_t* zeros, float* global_scale, hq_stream_t stream) {
+  hq_status_t st = check_format(fmt);
+  if (st != HQ_OK) return st;
+  if (!codes || !scales || !packed) return HQ_ERR_INVALID_ARG;
+  if (fmt->has_zero && !zeros) return HQ_ERR_INVALID_ARG;
+  if (!aligned16(packed)) return HQ_ERR_ALIGNMENT;
+  return cuda_status(launch_pack(1, fmt->weight_type, fmt->N, fmt->K, fmt->num_experts, codes, scales, zeros,
+                                 global_scale, const_cast<void*>(packed), (cudaStream_t)stream));
+}
+
+size_t hq_workspace_bytes(const hq_format_t* fmt, int64_t M_or_T, int32_t topk) {
+  if (check_format(fmt) != HQ_OK || M_or_T < 0 || topk < 1) return 0;
+  const int sms = num_sms();
+  if (fmt->num_experts > 1 || topk > 1) return make_plan(fmt, M_or_T, topk, true, sms).ws_bytes;
+  // one expert with top-1 serves both hq_gemm and hq_moe_gemm: cover both plans
+  const size_t d = make_plan(fmt, M_or_T, 1, false, sms).ws_bytes;
+  const size_t m = make_plan(fmt, M_or_T, 1, true, sms).ws_bytes;
+  return d > m ? d : m;
+}
+
+hq_status_t hq_workspace_init(void* workspace, size_t bytes, hq_stream_t stream) {
+  if (!workspace || bytes == 0) return HQ_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(workspace, 0, bytes, (cudaStream_t)stream));
+}
+
+hq_status_t hq_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* packedW, const void* bias, void* C,
+                    int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes, hq_stream_t stream) {
+  hq_status_t st = check_format(fmt);
+  if (st != HQ_OK) return st;
+  if (fmt->num_experts != 1 || N != fmt->N || K != fmt->K || M < 0 || M > kMaxRows) return HQ_ERR_INVALID_ARG;
+  if (M == 0) return HQ_OK;
+  if (!A || !A->data || !packedW || !C) return HQ_ERR_INVALID_ARG;
+  if (fmt->act_type == HQ_A_E4M3_TOKEN && !A->scale) return HQ_ERR_INVALID_ARG;
+  if (fmt->act_type == HQ_A_NVFP4 && (!A->scale || !A->global_scale)) return HQ_ERR_INVALID_ARG;
+  if (!aligned16(A->data) || !aligned16(packedW) || (A->scale && fmt->act_type == HQ_A_NVFP4 && !aligned16(A->scale)))
+    return HQ_ERR_ALIGNMENT;
+  const int sms = num_sms();
+  if (sms < 1) return HQ_ERR_CUDA;
+  const Plan p = make_plan(fmt, M, 1, false, sms);
+  if (!workspace || ws_bytes < p.ws_bytes) return HQ_ERR_WORKSPACE;
+  const PackGeom g = pack_geom(fmt->weight_type, N, K, 1);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  GemmArgs a{};
+  a.w = static_cast<const uint8_t*>(packedW);
+  a.w_expert_bytes = g.expert_bytes;
+  a.w_blk = g.blk_bytes;
+  a.w_gscale = g.gscale_off >= 0 ? reinterpret_cast<const float*>(a.w + g.gscale_off) : nullptr;
+  a.a = static_cast<const uint8_t*>(A->data);
+  a.a_sf = fmt->act_type == HQ_A_NVFP4 ? static_cast<const uint8_t*>(A->scale) : nullptr;
+  a.a_scale = fmt->act_type == HQ_A_NVFP4 ? A->global_scale
+                                            : (fmt->act_type == HQ_A_E4M3_TOKEN ? static_cast<const float*>(A->scale)
+                                                                                 : nullptr);
+  a.bias = static_cast<const uint16_t*>(bias);
+  a.c = static_cast<uint16_t*>(C);
+  a.M = (int)M;
+  a.N = (int)N;
+  a.K = (int)K;
+  a.n_tiles = (int)p.n_tiles;
+  a.kst = (int)p.kst;
+  a.zp = fmt->has_zero;
+  a.moe = 0;
+  a.E = 1;
+  a.topk = 1;
+  a.m_tiles = (int)p.m_tiles;
+  a.sk = p.sk;
+  a.status = reinterpret_cast<int*>(ws);
+  a.counters = reinterpret_cast<int*>(ws + p.off_counters);
+  a.partials = p.sk ? reinterpret_cast<float*>(ws + p.off_partials) : nullptr;
+  return cuda_status(launch_path(p, a, (cudaStream_t)stream));
+}
+
+hq_status_t hq_moe_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* packedW, const int32_t* topk_ids,
+                        const float* topk_weights, int64_t T, int32_t topk, void* C, void* workspace, size_t ws_bytes,
+                        hq_stream_t stream) {
+  hq_status_t st = check_format(fmt);
+  if (st != HQ_OK) return st;
+  if (T < 0 || topk < 1 || T * topk > kMaxRows) return HQ_ERR_INVALID_ARG;
+  if (T == 0) return HQ_OK;
+  if (!A || !A->data || !packedW || !C || !topk_ids) return HQ_ERR_INVALID_ARG;
+  if (fmt->act_type == HQ_A_E4M3_TOKEN && !A->scale) return HQ_ERR_INVALID_ARG;
+  if (fmt->act_type == HQ_A_NVFP4 && (!A->scale || !A->global_scale)) return HQ_ERR_INVALID_ARG;
+  if (!aligned16(A->data) || !aligned16(packedW)) return HQ_ERR_ALIGNMENT;
+  const int sms = num_sms();
+  if (sms < 1) return HQ_ERR_CUDA;
+  const Plan p = make_plan(fmt, T, topk, true, sms);
+  if (!workspace || ws_bytes < p.ws_bytes) return HQ_ERR_WORKSPACE;
+  const int64_t E = fmt->num_experts;
+  const PackGeom g = pack_geom(fmt->weight_type, fmt->N, fmt->K, E);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(ws);
+  int* counts = reinterpret_cast<int*>(ws + p.off_counts);
+  int* region = reinterpret_cast<int*>(ws + p.off_region);
+  cudaError_t err =
+      launch_route(topk_ids, T * topk, (int)E, (int)p.region_cap, counts, region, status, (cudaStream_t)stream);
+  if (err != cudaSuccess) return HQ_ERR_CUDA;
+  GemmArgs a{};
+  a.w = static_cast<const uint8_t*>(packedW);
+  a.w_expert_bytes = g.expert_bytes;
+  a.w_blk = g.blk_bytes;
+  a.w_gscale = g.gscale_off >= 0 ? reinterpret_cast<const float*>(a.w + g.gscale_off) : nullptr;
+  a.a = static_cast<const uint8_t*>(A->data);
+  a.a_sf = fmt->act_type == HQ_A_NVFP4 ? static_cast<const uint8_t*>(A->scale) : nullptr;
+  a.a_scale = fmt->act_type == HQ_A_NVFP4 ? A->global_scale
+                                            : (fmt->act_type == HQ_A_E4M3_TOKEN ? static_cast<const float*>(A->scale)
+                                                                                 : nullptr);
+  a.bias = nullptr;
+  a.c = static_cast<uint16_t*>(C);
+  a.M = (int)T;
+  a.N = (int)fmt->N;
+  a.K = (int)fmt->K;
+  a.n_tiles = (int)p.n_tiles;
+  a.kst = (int)p.kst;
+  a.zp = fmt->has_zero;
+  a.moe = 1;
+  a.E = (int)E;
+  a.topk = topk;
+  a.topk_w = topk_weights;
+  a.counts = counts;
+  a.region = region;
+  a.region_cap = (int)p.region_cap;
+  a.m_tiles = 0;
+  a.sk = p.sk;
+  a.status = status;
+  a.counters = reinterpret_cast<int*>(ws + p.off_counters);
+  a.partials = p.sk ? reinterpret_cast<float*>(ws + p.off_partials) : nullptr;
+  return cuda_status(launch_path(p, a, (cudaStream_t)stream));
+}
+
+hq_status_t hq_last_device_status(void* workspace, int32_t* status_out, hq_stream_t stream) {
+  if (!workspace || !status_out) return HQ_ERR_INVALID_ARG;
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(v), (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return HQ_ERR_CUDA;
+  *status_out = v;
+  return HQ_OK;
+}
+
+const char* hq_status_string(hq_status_t s) {
+  switch (s) {
+    case HQ_OK: return "ok";
+    case HQ_ERR_INVALID_ARG: return "invalid argument";
+    case HQ_ERR_UNSUPPORTED: return "unsupported format combination";
+    case HQ_ERR_ALIGNMENT: return "misaligned pointer or K not a multiple of the K tile";
+    case HQ_ERR_CUDA: return "CUDA runtime error";
+    case HQ_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case HQ_ERR_BAD_ROUTING: return "top-k expert id out of range or rows per expert over capacity";
+    case HQ_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

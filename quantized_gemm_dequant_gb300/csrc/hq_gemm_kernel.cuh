@@ -1,0 +1,708 @@
+// Persistent warp-specialised quantized GEMM for sm_103a (dense and MoE).
+//
+// Orientation: the weight tile is the UMMA "A" operand (M = 128 weight rows)
+// and the token tile is "B" (N = BT tokens), so D[n, m] sits in tensor memory
+// with one weight row per lane.  Small token counts then still fill the
+// 128-row MMA.
+//
+// Warp roles (352 threads):
+//   warps 0-7  INT4 path: decode the stage's 4-bit codes into bf16 A tiles in
+//              tensor memory (warp w: lane quarter w%4, K half w/4).
+//              FP4 paths: warps 0-3 copy block scales into tensor memory,
+//              MXFP4 warps 4-7 expand packed e2m1 into the MMA's 16-byte
+//              padded layout.  All 8: epilogue (tensor memory -> scales ->
+//              bf16 store, or split-K partial + last-arriver reduction).
+//   warps 8-9  producers: one bulk copy per weight stage block, cp.async
+//              gather of the activation rows (dense rows or routed MoE rows)
+//              into the 128-byte-swizzled K-major layout.
+//   warp 10    MMA issuer (one thread): tcgen05.mma kind::f16 with A from
+//              tensor memory (INT4), kind::mxf4nvf4 scale_vec::4X (NVFP4),
+//              kind::mxf8f6f4 scale_vec::1X with e2m1 x e4m3 (MXFP4).
+//
+// Work is split into pieces (tile, K-stage range).  With few tiles the K
+// stages of all tiles are dealt out evenly to the CTAs (Stream-K); tiles cut
+// between CTAs are finished by the last CTA to arrive, which sums the partial
+// sums in a fixed order.  No CTA ever waits for another.
+#pragma once
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "hq_layout.h"
+#include "hq_ptx.cuh"
+
+namespace hq {
+
+constexpr int NUM_THREADS = 352;
+constexpr int PRODUCER_WARP0 = 8;
+constexpr int MMA_WARP = 10;
+constexpr int NUM_EPI_THREADS = 256;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
+constexpr int ERR_TIMEOUT = 5;
+constexpr int ERR_BAD_ROUTING = 6;
+
+struct GemmArgs {
+  const uint8_t* w;        // packed weights, all experts
+  int64_t w_expert_bytes;  // bytes per expert
+  int w_blk;               // bytes per packed stage block (<= Cfg::W_BLK)
+  const float* w_gscale;   // NVFP4 per-expert global scales, else null
+  const uint8_t* a;        // activation data
+  const uint8_t* a_sf;     // NVFP4 activation block scales [rows][K/16]
+  const float* a_scale;    // E4M3: per-token [rows]; NVFP4: global [1]
+  const uint16_t* bias;    // bf16 [N] or null
+  uint16_t* c;             // bf16 output
+  int M;                   // dense rows / MoE tokens
+  int N, K;
+  int n_tiles, kst;  // 128-row tiles along N, stage blocks along K
+  int zp;            // INT4 path: zero points present
+  int moe, E, topk;
+  const float* topk_w;  // MoE [T*topk] or null
+  const int* counts;    // MoE [E] routed rows per expert
+  const int* region;    // MoE [E][region_cap] flat (t*topk + j) rows per expert
+  int region_cap;
+  int m_tiles;  // dense: token tiles
+  int sk;       // 1: Stream-K split over K stages
+  int* status;
+  int* counters;
+  float* partials;
+};
+
+template <int PATH, int BT>
+struct Cfg {
+  static constexpr int KSTAGE = PATH == PATH_NVFP4 ? 256 : 128;
+  static constexpr int W_BLK = PATH == PATH_INT4 ? 8576 : (PATH == PATH_NVFP4 ? 18432 : 8704);
+  static constexpr int W_REGION = ((W_BLK + 1023) / 1024) * 1024;
+  // activation row bytes per stage: bf16 128 K = 256 B; fp4 256 K = 128 B; e4m3 128 K = 128 B
+  static constexpr int ACT_ROW = PATH == PATH_INT4 ? 256 : 128;
+  static constexpr int ACT_BYTES = BT * ACT_ROW;
+  static constexpr int ACT_REGION = ((ACT_BYTES + 1023) / 1024) * 1024;
+  static constexpr int SF_ROWS = BT < 32 ? 32 : BT;
+  static constexpr int ACT_SF_REGION = PATH == PATH_NVFP4 ? ((SF_ROWS * 16 + 1023) / 1024) * 1024 : 0;
+  static constexpr int EXP_REGION = PATH == PATH_MXFP4 ? 16384 : 0;
+  static constexpr int STAGE_BYTES = W_REGION + ACT_REGION + ACT_SF_REGION + EXP_REGION;
+  static constexpr int SMEM_BUDGET = 200 * 1024;
+  static constexpr int S_RAW = SMEM_BUDGET / STAGE_BYTES;
+  static constexpr int STAGES = S_RAW > 8 ? 8 : S_RAW;
+  static constexpr int CB = BT < 32 ? 1 : BT / 32;  // scale-factor columns per MMA step for B
+  static constexpr int SFB_STEP = CB < 4 ? 4 : CB;  // column stride per MMA step (kept 4-aligned)
+  static constexpr int SF_STAGE_COLS = PATH == PATH_NVFP4 ? 16 + 4 * SFB_STEP : 4;
+  static constexpr int NA = 4;  // INT4: tensor-memory A slots of 64 columns
+  static constexpr int CH = ACT_ROW / 16;  // 16-byte chunks per activation row per stage
+  static constexpr int SMEM_RAW = STAGES * STAGE_BYTES + 1024 /*align*/ + 4096 /*barriers, MoE prefix*/;
+  // at least 120 KB so that one CTA (and one 512-column tensor-memory allocation) owns each SM
+  static constexpr int SMEM_BYTES = SMEM_RAW < 120 * 1024 ? 120 * 1024 : SMEM_RAW;
+  static_assert(STAGES >= 2, "stage ring too small");
+  static_assert(PATH != PATH_NVFP4 || 256 + STAGES * SF_STAGE_COLS <= 512, "tensor memory");
+  static_assert(PATH != PATH_MXFP4 || 256 + 4 * 8 + SFB_STEP <= 512, "tensor memory");
+};
+
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint16_t f32_to_bf16(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+template <int X>
+__device__ __forceinline__ void tmem_st_x(uint32_t taddr, const uint32_t* r);
+template <>
+__device__ __forceinline__ void tmem_st_x<1>(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r[0]) : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_st_x<2>(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(r[0]), "r"(r[1])
+               : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_st_x<4>(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_st_x<8>(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_st_x<16>(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// ----------------------------------------------------------------- work pieces
+struct Piece {
+  int tile;     // tile index (token tile major, N tile minor)
+  int g0, g1;   // K-stage range
+  bool full;    // covers all K stages of the tile
+  int slot;     // Stream-K partial slot (2*cta + {0 first piece, 1 last piece})
+};
+
+struct Sched {
+  int tiles, kst, P, cta, sk;
+  int64_t W;  // total stage iterations
+  __device__ int64_t start(int c) const { return (int64_t)c * W / P; }
+  // largest CTA whose range starts at or before iteration it
+  __device__ int cta_of(int64_t it) const { return (int)(((it + 1) * P - 1) / W); }
+};
+
+// Enumerate this CTA's pieces in order; f(piece) is called for each.
+template <typename F>
+__device__ __forceinline__ void for_each_piece(const Sched& s, F&& f) {
+  if (!s.sk) {
+    for (int t = s.cta; t < s.tiles; t += s.P) f(Piece{t, 0, s.kst, true, 0});
+    return;
+  }
+  const int64_t it0 = s.start(s.cta), it1 = s.start(s.cta + 1);
+  int64_t it = it0;
+  bool first = true;
+  while (it < it1) {
+    const int t = (int)(it / s.kst);
+    const int g0 = (int)(it % s.kst);
+    const int64_t left = it1 - it;
+    const int g1 = (int)((int64_t)g0 + left < s.kst ? g0 + left : s.kst);
+    const bool full = (g0 == 0 && g1 == s.kst);
+    f(Piece{t, g0, g1, full, 2 * s.cta + (first ? 0 : 1)});
+    it += g1 - g0;
+    first = false;
+  }
+}
+
+// ----------------------------------------------------------------- shared state
+template <int PATH, int BT>
+struct Smem {
+  using C = Cfg<PATH, BT>;
+  uint64_t full[C::STAGES];
+  uint64_t empty[C::STAGES];
+  uint64_t ready[C::STAGES];  // FP4 paths: scales in tensor memory (+ expanded A for MXFP4)
+  uint64_t afull[C::NA];
+  uint64_t aempty[C::NA];
+  uint64_t dfull;
+  uint64_t dempty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int fix_last;
+  int tile_prefix_total;
+};
+
+// Map a global token-tile index to (expert, local token tile) for MoE via the
+// per-expert tile prefix held in shared memory.
+__device__ __forceinline__ void moe_locate(const int* prefix, int E, int mt, int& e, int& lm) {
+  int lo = 0, hi = E;  // find e with prefix[e] <= mt < prefix[e+1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid] <= mt) lo = mid;
+    else hi = mid;
+  }
+  e = lo;
+  lm = mt - prefix[lo];
+}
+
+template <int PATH, int BT>
+__global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const GemmArgs args) {
+  using C = Cfg<PATH, BT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem<PATH, BT>& sh = *reinterpret_cast<Smem<PATH, BT>*>(smem + C::STAGES * C::STAGE_BYTES);
+  int* prefix = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + 1024);  // MoE: E + 1 ints (E <= 512)
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  // ---------------------------------------------------------------- setup
+  if (warp == 0) {
+    tmem_alloc(&sh.tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (tid == 32) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&sh.full[s], 1 + 64);
+      mbar_init(&sh.empty[s], (PATH == PATH_INT4 ? 8 : (PATH == PATH_NVFP4 ? 4 : 8)) + 1);
+      mbar_init(&sh.ready[s], PATH == PATH_MXFP4 ? 8 : 4);
+    }
+    for (int a = 0; a < C::NA; ++a) {
+      mbar_init(&sh.afull[a], 8);
+      mbar_init(&sh.aempty[a], 1);
+    }
+    mbar_init(&sh.dfull, 1);
+    mbar_init(&sh.dempty, 8);
+    mbar_init(&sh.drain, 1);
+    sh.abort_flag = 0;
+    fence_mbar_init();
+  }
+  // MoE: tile prefix over experts (E <= 512 enforced on the host)
+  int total_tiles;
+  if (args.moe) {
+    for (int e = tid; e < args.E; e += NUM_THREADS) {
+      int cnt = args.counts[e];
+      cnt = cnt < 0 ? 0 : (cnt > args.region_cap ? args.region_cap : cnt);
+      prefix[e + 1] = (cnt + BT - 1) / BT;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // inclusive scan of prefix[1..E] by one warp: each lane owns a contiguous run
+      const int per = (args.E + 31) / 32;
+      const int b0 = 1 + lane * per;
+      int run = 0;
+      for (int i = 0; i < per; ++i)
+        if (b0 + i <= args.E) run += prefix[b0 + i];
+      int incl = run;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      int acc = incl - run;
+      for (int i = 0; i < per; ++i)
+        if (b0 + i <= args.E) {
+          acc += prefix[b0 + i];
+          prefix[b0 + i] = acc;
+        }
+      if (lane == 0) prefix[0] = 0;
+      if (lane == 31) sh.tile_prefix_total = incl;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+  total_tiles = args.moe ? sh.tile_prefix_total * args.n_tiles : args.m_tiles * args.n_tiles;
+
+  Sched sched;
+  sched.tiles = total_tiles;
+  sched.kst = args.kst;
+  sched.W = (int64_t)total_tiles * args.kst;
+  sched.P = (int)((int64_t)gridDim.x < sched.W ? gridDim.x : sched.W);
+  sched.cta = blockIdx.x;
+  sched.sk = args.sk;
+  if (!args.sk) sched.P = gridDim.x;
+  const bool active = (int)blockIdx.x < sched.P && total_tiles > 0;
+  volatile int* abort_flag = &sh.abort_flag;
+
+  auto fail = [&](int code) {
+    *abort_flag = 1;
+    atomicCAS(args.status, 0, code);
+  };
+
+  // Row bookkeeping for a tile: token tile (dense) or (expert, local tile) (MoE).
+  auto tile_rows = [&](int tile, int& e, int& row0, int& nrows) {
+    const int mt = tile / args.n_tiles;
+    if (args.moe) {
+      int lm;
+      moe_locate(prefix, args.E, mt, e, lm);
+      int cnt = args.counts[e];
+      cnt = cnt > args.region_cap ? args.region_cap : cnt;
+      row0 = lm * BT;
+      nrows = cnt - row0 < BT ? cnt - row0 : BT;
+    } else {
+      e = 0;
+      row0 = mt * BT;
+      nrows = args.M - row0 < BT ? args.M - row0 : BT;
+    }
+  };
+
+  if (active && warp >= PRODUCER_WARP0 && warp < MMA_WARP) {
+    // ============================================================ producers
+    const int pt = tid - PRODUCER_WARP0 * 32;  // 0..63
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    int armed[C::STAGES];  // bulk copies issued per stage (thread pt == 0)
+#pragma unroll
+    for (int s = 0; s < C::STAGES; ++s) armed[s] = 0;
+    for_each_piece(sched, [&](const Piece& pc) {
+      if (!ok) return;
+      int e, row0, nrows;
+      tile_rows(pc.tile, e, row0, nrows);
+      const int nt = pc.tile % args.n_tiles;
+      const uint8_t* wblk = args.w + e * args.w_expert_bytes + ((int64_t)nt * args.kst) * args.w_blk;
+      for (int g = pc.g0; g < pc.g1; ++g) {
+        if (!mbar_wait(&sh.empty[stage], phase ^ 1, abort_flag, WAIT_LIMIT_NS)) {
+          fail(ERR_TIMEOUT);
+          ok = false;
+          return;
+        }
+        uint8_t* sbase = smem + stage * C::STAGE_BYTES;
+        if (pt == 0) {
+          mbar_arrive_expect_tx(&sh.full[stage], (uint32_t)args.w_blk);
+          bulk_g2s(sbase, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk, &sh.full[stage]);
+          ++armed[stage];
+        }
+        uint8_t* act = sbase + C::W_REGION;
+        for (int idx = pt; idx < BT * C::CH; idx += 64) {
+          const int i = idx / C::CH, ch = idx % C::CH;
+          int src = -1;
+          if (i < nrows) src = args.moe ? args.region[e * args.region_cap + row0 + i] / args.topk : row0 + i;
+          const int atom = ch >> 3, cc = ch & 7;
+          uint8_t* dst = act + atom * (BT * 128) + (i >> 3) * 1024 + (i & 7) * 128 + ((cc ^ (i & 7)) << 4);
+          const uint8_t* s;
+          if (PATH == PATH_INT4)
+            s = args.a + ((int64_t)(src < 0 ? 0 : src) * args.K + (int64_t)g * 128) * 2 + ch * 16;
+          else if (PATH == PATH_NVFP4)
+            s = args.a + (int64_t)(src < 0 ? 0 : src) * (args.K / 2) + (int64_t)g * 128 + ch * 16;
+          else
+            s = args.a + (int64_t)(src < 0 ? 0 : src) * args.K + (int64_t)g * 128 + ch * 16;
+          cp_async_16(dst, s, src < 0 ? 0u : 16u);
+        }
+        if (PATH == PATH_NVFP4) {
+          uint8_t* asf = act + C::ACT_REGION;
+          for (int i = pt; i < C::SF_ROWS; i += 64) {
+            int src = -1;
+            if (i < nrows) src = args.moe ? args.region[e * args.region_cap + row0 + i] / args.topk : row0 + i;
+            const uint8_t* s = args.a_sf + (int64_t)(src < 0 ? 0 : src) * (args.K / 16) + (int64_t)g * 16;
+            cp_async_16(asf + i * 16, s, src < 0 ? 0u : 16u);
+          }
+        }
+        cp_async_mbar_arrive_noinc(&sh.full[stage]);
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    });
+    cp_async_wait_all();
+    if (!ok && pt == 0) {
+      // aborted: let this CTA's bulk copies land before shared memory is released
+      int never = 0;
+      for (int s = 0; s < C::STAGES; ++s)
+        if (armed[s] > 0) mbar_wait(&sh.full[s], (uint32_t)((armed[s] - 1) & 1), &never, 200000000ull);
+    }
+  } else if (active && warp == MMA_WARP) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      int stage = 0, aslot = 0;
+      uint32_t phase = 0, aphase = 0;
+      int pidx = 0;
+      bool ok = true;
+      for_each_piece(sched, [&](const Piece& pc) {
+        if (!ok) return;
+        if (!mbar_wait(&sh.dempty, (pidx & 1) ^ 1, abort_flag, WAIT_LIMIT_NS)) {
+          fail(ERR_TIMEOUT);
+          ok = false;
+          return;
+        }
+        tc_fence_after();
+        for (int g = pc.g0; g < pc.g1; ++g) {
+          if (!mbar_wait(&sh.full[stage], phase, abort_flag, WAIT_LIMIT_NS)) {
+            fail(ERR_TIMEOUT);
+            ok = false;
+            return;
+          }
+          if (PATH == PATH_INT4) {
+            if (!mbar_wait(&sh.afull[aslot], aphase, abort_flag, WAIT_LIMIT_NS)) {
+              fail(ERR_TIMEOUT);
+              ok = false;
+              return;
+            }
+          } else {
+            if (!mbar_wait(&sh.ready[stage], phase, abort_flag, WAIT_LIMIT_NS)) {
+              fail(ERR_TIMEOUT);
+              ok = false;
+              return;
+            }
+          }
+          tc_fence_after();
+          fence_proxy_async_smem();
+          uint8_t* sbase = smem + stage * C::STAGE_BYTES;
+          const uint32_t act = smem_u32(sbase + C::W_REGION);
+          if (PATH == PATH_INT4) {
+            constexpr uint32_t idesc = idesc_bf16(128, BT);
+            const uint32_t a_t = tmem + 256 + aslot * 64;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint64_t bd = smem_desc(act + (i >> 2) * (BT * 128) + (i & 3) * 32, 16, 1024, 2);
+              umma_bf16_ts(tmem, a_t + i * 8, bd, idesc, (g > pc.g0 || i > 0) ? 1u : 0u);
+            }
+            umma_commit(&sh.aempty[aslot]);
+            if (++aslot == C::NA) {
+              aslot = 0;
+              aphase ^= 1;
+            }
+          } else if (PATH == PATH_NVFP4) {
+            constexpr uint32_t idesc = idesc_block_scaled(128, BT < 32 ? BT : BT, 1, 1, 0, 0, 0);
+            const uint32_t wa = smem_u32(sbase);
+            const uint32_t sf = tmem + 256 + stage * C::SF_STAGE_COLS;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const uint64_t ad = smem_desc(wa + t * 32, 16, 1024, 2);
+              const uint64_t bd = smem_desc(act + t * 32, 16, 1024, 2);
+              umma_nvf4_ss(tmem, ad, bd, idesc, sf + 4 * t, sf + 16 + t * C::SFB_STEP,
+                           (g > pc.g0 || t > 0) ? 1u : 0u);
+            }
+          } else {
+            const uint32_t xa = smem_u32(sbase + C::W_REGION + C::ACT_REGION);
+            const uint32_t sfa = tmem + 256 + stage * 4;
+            const uint32_t sfb = tmem + 256 + 4 * 8;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t idesc = idesc_block_scaled(128, BT, 5, 0, 1, i, 0);
+              const uint64_t ad = smem_desc(xa + i * 32, 16, 1024, 2);
+              const uint64_t bd = smem_desc(act + i * 32, 16, 1024, 2);
+              umma_mxf8_ss(tmem, ad, bd, idesc, sfa, sfb, (g > pc.g0 || i > 0) ? 1u : 0u);
+            }
+          }
+          umma_commit(&sh.empty[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        umma_commit(&sh.dfull);
+        ++pidx;
+      });
+      if (!ok) {
+        // aborted: wait for issued MMAs before tensor memory is released
+        int never = 0;
+        umma_commit(&sh.drain);
+        mbar_wait(&sh.drain, 0, &never, 200000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (active && warp < 8) {
+    // ============================================================ decode / scales / epilogue
+    const int q = warp & 3;   // tensor-memory lane quarter
+    const int h = warp >> 2;  // K half (INT4) / column half (epilogue)
+    const int r = q * 32 + lane;  // weight row within the tile
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    int stage = 0, aslot = 0;
+    uint32_t phase = 0, aphase = 0;
+    int pidx = 0;
+    bool ok = true;
+    if (PATH == PATH_MXFP4 && warp < 4) {
+      // unit activation block scales (2^0) for every MMA, written once
+      uint32_t ones[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ones[j] = 0x7F7F7F7Fu;
+      tmem_st_x<8>(tmem + lane_base + 256 + 4 * 8, ones);
+      tmem_wait_st();
+    }
+    for_each_piece(sched, [&](const Piece& pc) {
+      if (!ok) return;
+      int e, row0, nrows;
+      tile_rows(pc.tile, e, row0, nrows);
+      const int nt = pc.tile % args.n_tiles;
+      // ---------------------------------------------------- mainloop role
+      const bool in_mainloop = !(PATH == PATH_NVFP4 && warp >= 4);
+      for (int g = pc.g0; in_mainloop && g < pc.g1; ++g) {
+        if (!mbar_wait(&sh.full[stage], phase, abort_flag, WAIT_LIMIT_NS)) {
+          fail(ERR_TIMEOUT);
+          ok = false;
+          return;
+        }
+        uint8_t* sbase = smem + stage * C::STAGE_BYTES;
+        if (PATH == PATH_INT4) {
+          const uint32_t s16 = reinterpret_cast<const uint16_t*>(sbase + 8192)[r];
+          const uint32_t ss = s16 | (s16 << 16);
+          const uint32_t z = args.zp ? (uint32_t)sbase[8448 + r] : 8u;
+          const uint32_t zz = (0x4300u + z) * 0x00010001u;
+          uint4 raw[2];
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj)
+            raw[jj] = *reinterpret_cast<const uint4*>(sbase + ((2 * h + jj) * 128 + r) * 16);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.empty[stage]);
+          if (!mbar_wait(&sh.aempty[aslot], aphase ^ 1, abort_flag, WAIT_LIMIT_NS)) {
+            fail(ERR_TIMEOUT);
+            ok = false;
+            return;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            uint32_t out[16];
+            const uint32_t wv[4] = {raw[jj].x, raw[jj].y, raw[jj].z, raw[jj].w};
+#pragma unroll
+            for (int w4 = 0; w4 < 4; ++w4) {
+#pragma unroll
+              for (int p = 0; p < 4; ++p) {
+                const uint32_t x = lop3_and_or(wv[w4] >> (4 * p), 0x000F000Fu, 0x43004300u);
+                out[w4 * 4 + p] = bf16x2_mul(bf16x2_sub(x, zz), ss);
+              }
+            }
+            tmem_st_x<16>(tmem + lane_base + 256 + aslot * 64 + (2 * h + jj) * 16, out);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.afull[aslot]);
+          if (++aslot == C::NA) {
+            aslot = 0;
+            aphase ^= 1;
+          }
+        } else {
+          if (warp < 4) {
+            // scale factors -> tensor memory (replicated in every lane quarter)
+            if (PATH == PATH_NVFP4) {
+              const uint32_t* wsf = reinterpret_cast<const uint32_t*>(sbase + 16384);
+              uint32_t v[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] = wsf[j * 32 + lane];
+              const uint32_t sf = tmem + lane_base + 256 + stage * C::SF_STAGE_COLS;
+              tmem_st_x<16>(sf, v);
+              const uint8_t* asf = sbase + C::W_REGION + C::ACT_REGION;
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                uint32_t b[C::CB];
+#pragma unroll
+                for (int cc = 0; cc < C::CB; ++cc)
+                  b[cc] = *reinterpret_cast<const uint32_t*>(asf + (cc * 32 + lane) * 16 + t * 4);
+                tmem_st_x<C::CB>(sf + 16 + t * C::SFB_STEP, b);
+              }
+            } else {
+              const uint32_t* wsf = reinterpret_cast<const uint32_t*>(sbase + 8192);
+              uint32_t v[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) v[j] = wsf[j * 32 + lane];
+              tmem_st_x<4>(tmem + lane_base + 256 + stage * 4, v);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+          } else if (PATH == PATH_MXFP4) {
+            // expand packed e2m1 (8 bytes per 16 K) into the padded 16-byte chunks
+            const uint8_t* raw = sbase;
+            uint8_t* xt = sbase + C::W_REGION + C::ACT_REGION;
+            const int t128 = tid - 128;
+#pragma unroll 4
+            for (int p = t128; p < 1024; p += 128) {
+              const uint2 v = *reinterpret_cast<const uint2*>(raw + p * 8);
+              const int rr = p >> 3, cc = p & 7;
+              *reinterpret_cast<uint4*>(xt + (rr >> 3) * 1024 + (rr & 7) * 128 + ((cc ^ (rr & 7)) << 4)) =
+                  make_uint4(v.x, v.y, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0 && (PATH == PATH_MXFP4 || warp < 4)) {
+            mbar_arrive(&sh.ready[stage]);
+            mbar_arrive(&sh.empty[stage]);
+          }
+        }
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      // ---------------------------------------------------- epilogue
+      if (!mbar_wait(&sh.dfull, pidx & 1, abort_flag, WAIT_LIMIT_NS)) {
+        fail(ERR_TIMEOUT);
+        ok = false;
+        return;
+      }
+      tc_fence_after();
+      constexpr int HC = BT / 2;  // columns per warp
+      constexpr int CHUNK = HC < 16 ? HC : 16;
+      const int col0 = h * HC;
+      const int n = nt * TILE_N + r;
+      float post = 1.0f;
+      if (PATH == PATH_NVFP4) post = args.a_scale[0] * args.w_gscale[e];
+      const float bias_v = (args.bias && n < args.N) ? bf16_to_f32(args.bias[n]) : 0.0f;
+      float* part = args.partials + ((int64_t)pc.slot * BT) * TILE_N;
+#pragma unroll 1
+      for (int cb = 0; cb < HC; cb += CHUNK) {
+        uint32_t v[CHUNK];
+        if (CHUNK == 16) {
+          tmem_ld16(tmem + lane_base + col0 + cb, *reinterpret_cast<uint32_t(*)[16]>(v));
+        } else {
+          tmem_ld8(tmem + lane_base + col0 + cb, *reinterpret_cast<uint32_t(*)[8]>(v));
+        }
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < CHUNK; ++j) {
+          const int col = col0 + cb + j;
+          const float acc = __uint_as_float(v[j]);
+          if (!pc.full) {
+            part[col * TILE_N + r] = acc;
+          } else if (col < nrows && n < args.N) {
+            int orow, tok;
+            float f = post;
+            if (args.moe) {
+              orow = args.region[e * args.region_cap + row0 + col];
+              tok = orow / args.topk;
+              if (args.topk_w) f *= args.topk_w[orow];
+            } else {
+              orow = row0 + col;
+              tok = orow;
+            }
+            if (PATH == PATH_MXFP4) f *= args.a_scale[tok];
+            args.c[(int64_t)orow * args.N + n] = f32_to_bf16(acc * f + bias_v);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.dempty);
+      if (!pc.full) {
+        // ---------------------------------------------- Stream-K fix-up (last arriver sums)
+        __threadfence();
+        named_bar_sync(1, NUM_EPI_THREADS);
+        if (tid == 0) {
+          const int64_t first_it = (int64_t)pc.tile * sched.kst;
+          const int c_first = sched.cta_of(first_it);
+          const int c_last = sched.cta_of(first_it + sched.kst - 1);
+          const int nctr = c_last - c_first + 1;
+          const int old = atomicAdd(&args.counters[pc.tile], 1);
+          sh.fix_last = (old == nctr - 1) ? 1 : 0;
+          if (old == nctr - 1) args.counters[pc.tile] = 0;
+        }
+        named_bar_sync(1, NUM_EPI_THREADS);
+        if (sh.fix_last) {
+          __threadfence();
+          const int64_t first_it = (int64_t)pc.tile * sched.kst;
+          const int c_first = sched.cta_of(first_it);
+          const int c_last = sched.cta_of(first_it + sched.kst - 1);
+          for (int j = 0; j < HC; ++j) {
+            const int col = col0 + j;
+            float acc = 0.0f;
+            for (int c = c_first; c <= c_last; ++c) {
+              const int slot = (c == c_first && sched.start(c) < first_it) ? 2 * c + 1 : 2 * c;
+              acc += __ldcg(args.partials + ((int64_t)slot * BT + col) * TILE_N + r);
+            }
+            if (col < nrows && n < args.N) {
+              int orow, tok;
+              float f = post;
+              if (args.moe) {
+                orow = args.region[e * args.region_cap + row0 + col];
+                tok = orow / args.topk;
+                if (args.topk_w) f *= args.topk_w[orow];
+              } else {
+                orow = row0 + col;
+                tok = orow;
+              }
+              if (PATH == PATH_MXFP4) f *= args.a_scale[tok];
+              args.c[(int64_t)orow * args.N + n] = f32_to_bf16(acc * f + bias_v);
+            }
+          }
+        }
+      }
+      ++pidx;
+    });
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace hq

@@ -1,0 +1,137 @@
+// Repack (and its inverse) between the standard format and the kernel layout.
+// One thread per (expert, N tile, K stage, row); see hq_layout.h for the layout.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "hq_layout.h"
+
+namespace hq {
+
+__constant__ int kNibblePerm[8] = {0, 2, 4, 6, 1, 3, 5, 7};
+
+struct PackArgs {
+  int wt;
+  int64_t N, K, E;
+  int64_t n_tiles, k_stages;
+  int blk_bytes;
+  int64_t gscale_off;
+};
+
+__device__ __forceinline__ uint32_t get_nibble(const uint8_t* row, int64_t k) {
+  uint8_t b = row[k >> 1];
+  return (k & 1) ? (b >> 4) : (b & 0xF);
+}
+
+// dir = 0: pack (standard -> kernel layout); dir = 1: unpack.
+template <int DIR>
+__global__ void pack_kernel(PackArgs p, uint8_t* codes, uint8_t* scales, uint8_t* zeros, float* gscale,
+                            uint8_t* packed) {
+  const int64_t total = p.E * p.n_tiles * p.k_stages * TILE_N;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(idx % TILE_N);
+    int64_t t = idx / TILE_N;
+    const int64_t ks = t % p.k_stages;
+    t /= p.k_stages;
+    const int64_t nt = t % p.n_tiles;
+    const int64_t e = t / p.n_tiles;
+    const int64_t n = nt * TILE_N + r;
+    const bool valid = n < p.N;
+    uint8_t* blk = packed + ((e * p.n_tiles + nt) * p.k_stages + ks) * (int64_t)p.blk_bytes;
+    const int64_t rowc = (e * p.N + n) * (p.K / 2);  // byte offset of the row in codes
+    if (p.wt == WK_INT4_SYM || p.wt == WK_UINT4_ZP) {
+      const int G = 128;
+      const int64_t ng = p.K / G;
+      const uint32_t xr = (p.wt == WK_INT4_SYM) ? 8u : 0u;
+      for (int j = 0; j < 4; ++j) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(blk + (j * 128 + r) * 16);
+        for (int w = 0; w < 4; ++w) {
+          const int64_t k0 = ks * 128 + 32 * j + 8 * w;
+          if (DIR == 0) {
+            uint32_t word = 0;
+            if (valid)
+              for (int i = 0; i < 8; ++i) word |= ((get_nibble(codes + rowc, k0 + kNibblePerm[i]) ^ xr) & 0xF) << (4 * i);
+            dst[w] = word;
+          } else if (valid) {
+            const uint32_t word = dst[w];
+            for (int i = 0; i < 8; ++i) {
+              const int64_t k = k0 + kNibblePerm[i];
+              const uint32_t v = ((word >> (4 * i)) & 0xF) ^ xr;
+              uint8_t* b = codes + rowc + (k >> 1);
+              *b = (k & 1) ? (uint8_t)((*b & 0x0F) | (v << 4)) : (uint8_t)((*b & 0xF0) | v);
+            }
+          }
+        }
+      }
+      uint16_t* sdst = reinterpret_cast<uint16_t*>(blk + 8192) + r;
+      uint16_t* ssrc = reinterpret_cast<uint16_t*>(scales) + (e * p.N + n) * ng + ks;
+      if (DIR == 0) *sdst = valid ? *ssrc : (uint16_t)0;
+      else if (valid) *ssrc = *sdst;
+      if (p.wt == WK_UINT4_ZP) {
+        uint8_t* zdst = blk + 8448 + r;
+        uint8_t* zsrc = zeros + (e * p.N + n) * ng + ks;
+        if (DIR == 0) *zdst = valid ? (uint8_t)(*zsrc & 0xF) : (uint8_t)0;
+        else if (valid) *zsrc = *zdst;
+      }
+    } else if (p.wt == WK_NVFP4) {
+      for (int kb = 0; kb < 128; ++kb) {
+        const int c = kb >> 4;
+        uint8_t* d = blk + (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4) + (kb & 15);
+        uint8_t* s = codes + rowc + ks * 128 + kb;
+        if (DIR == 0) *d = valid ? *s : (uint8_t)0;
+        else if (valid) *s = *d;
+      }
+      const int l = r & 31, cq = r >> 5;
+      const int64_t nb = p.K / 16;
+      for (int tt = 0; tt < 4; ++tt) {
+        uint8_t* d = blk + 16384 + ((tt * 4 + cq) * 32 + l) * 4;
+        uint8_t* s = scales + (e * p.N + n) * nb + ks * 16 + tt * 4;
+        for (int b = 0; b < 4; ++b) {
+          if (DIR == 0) d[b] = valid ? s[b] : (uint8_t)0;
+          else if (valid) s[b] = d[b];
+        }
+      }
+      if (r == 0 && nt == 0 && ks == 0) {
+        float* g = reinterpret_cast<float*>(packed + p.gscale_off) + e;
+        if (DIR == 0) *g = gscale[e];
+        else if (gscale) gscale[e] = *g;
+      }
+    } else {  // MXFP4
+      for (int c = 0; c < 8; ++c) {
+        uint8_t* d = blk + (r * 8 + c) * 8;
+        uint8_t* s = codes + rowc + ks * 64 + c * 8;
+        for (int b = 0; b < 8; ++b) {
+          if (DIR == 0) d[b] = valid ? s[b] : (uint8_t)0;
+          else if (valid) s[b] = d[b];
+        }
+      }
+      const int l = r & 31, cq = r >> 5;
+      const int64_t nb = p.K / 32;
+      uint8_t* d = blk + 8192 + (cq * 32 + l) * 4;
+      uint8_t* s = scales + (e * p.N + n) * nb + ks * 4;
+      for (int b = 0; b < 4; ++b) {
+        if (DIR == 0) d[b] = valid ? s[b] : (uint8_t)0;
+        else if (valid) s[b] = d[b];
+      }
+    }
+  }
+}
+
+cudaError_t launch_pack(int dir, int wt, int64_t N, int64_t K, int64_t E, const void* codes, const void* scales,
+                        const void* zeros, const float* gscale, void* packed, cudaStream_t stream) {
+  const PackGeom g = pack_geom(wt, N, K, E);
+  PackArgs p{wt, N, K, E, g.n_tiles, g.k_stages, g.blk_bytes, g.gscale_off};
+  const int64_t total = E * g.n_tiles * g.k_stages * TILE_N;
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  if (blocks > 65535 * 16) blocks = 65535 * 16;
+  if (dir == 0)
+    pack_kernel<0><<<(unsigned)blocks, threads, 0, stream>>>(p, (uint8_t*)codes, (uint8_t*)scales, (uint8_t*)zeros,
+                                                           (float*)gscale, (uint8_t*)packed);
+  else
+    pack_kernel<1><<<(unsigned)blocks, threads, 0, stream>>>(p, (uint8_t*)codes, (uint8_t*)scales, (uint8_t*)zeros,
+                                                           (float*)gscale, (uint8_t*)packed);
+  return cudaGetLastError();
+}
+
+}  // namespace hq
