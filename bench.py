@@ -416,7 +416,10 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--sizes", default=None, help="comma list overriding the sweep (profiling)")
     args = ap.parse_args()
+    if args.sizes:
+        W.CONFIGS[args.config] = dict(W.CONFIGS[args.config], sizes=[int(x) for x in args.sizes.split(",")])
     args.warmup = max(3, args.warmup) if args.impl == "ours" else args.warmup
     if args.impl == "reference":
         run_reference(args)

@@ -1,4 +1,6 @@
 // C ABI: argument validation, launch planning and kernel launches.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -146,6 +148,46 @@ cudaError_t launch_path(const Plan& p, const GemmArgs& a, cudaStream_t s) {
 
 hq_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? HQ_OK : HQ_ERR_CUDA; }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link needed).
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// 2-D row-major tensor [rows][inner] of bf16 or bytes; box of box_rows x box_inner elements.
+bool encode_2d(CUtensorMap* m, const void* base, bool bf16, uint64_t inner, uint64_t rows, uint32_t box_inner,
+               uint32_t box_rows, bool swizzle128) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
+  if (!enc || !base) return false;
+  const uint64_t esize = bf16 ? 2 : 1;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * esize};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Activation tensor maps: dense rows as one box of BT rows per stage; MoE rows one at a time (gather4).
+bool act_maps(GemmArgs& a, const hq_format_t* f, const hq_act_t* A, int64_t rows, int bt, bool moe) {
+  const uint32_t box_rows = moe ? 1u : (uint32_t)bt;
+  const uint64_t K = (uint64_t)f->K;
+  if (f->act_type == HQ_A_BF16) return encode_2d(&a.tmap_a, A->data, true, K, rows, 64, box_rows, true);
+  if (f->act_type == HQ_A_E4M3_TOKEN) return encode_2d(&a.tmap_a, A->data, false, K, rows, 128, box_rows, true);
+  return encode_2d(&a.tmap_a, A->data, false, K / 2, rows, 128, box_rows, true) &&
+         encode_2d(&a.tmap_sf, A->scale, false, K / 16, rows, 16, box_rows, false);
+}
+
 }  // namespace
 }  // namespace hq
 
@@ -218,8 +260,7 @@ hq_status_t hq_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* packe
   a.w_expert_bytes = g.expert_bytes;
   a.w_blk = g.blk_bytes;
   a.w_gscale = g.gscale_off >= 0 ? reinterpret_cast<const float*>(a.w + g.gscale_off) : nullptr;
-  a.a = static_cast<const uint8_t*>(A->data);
-  a.a_sf = fmt->act_type == HQ_A_NVFP4 ? static_cast<const uint8_t*>(A->scale) : nullptr;
+  if (!act_maps(a, fmt, A, M, p.bt, false)) return HQ_ERR_INVALID_ARG;
   a.a_scale = fmt->act_type == HQ_A_NVFP4 ? A->global_scale
                                             : (fmt->act_type == HQ_A_E4M3_TOKEN ? static_cast<const float*>(A->scale)
                                                                                  : nullptr);
@@ -252,7 +293,8 @@ hq_status_t hq_moe_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* p
   if (!A || !A->data || !packedW || !C || !topk_ids) return HQ_ERR_INVALID_ARG;
   if (fmt->act_type == HQ_A_E4M3_TOKEN && !A->scale) return HQ_ERR_INVALID_ARG;
   if (fmt->act_type == HQ_A_NVFP4 && (!A->scale || !A->global_scale)) return HQ_ERR_INVALID_ARG;
-  if (!aligned16(A->data) || !aligned16(packedW)) return HQ_ERR_ALIGNMENT;
+  if (!aligned16(A->data) || !aligned16(packedW) || (fmt->act_type == HQ_A_NVFP4 && !aligned16(A->scale)))
+    return HQ_ERR_ALIGNMENT;
   const int sms = num_sms();
   if (sms < 1) return HQ_ERR_CUDA;
   const Plan p = make_plan(fmt, T, topk, true, sms);
@@ -263,16 +305,15 @@ hq_status_t hq_moe_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* p
   int* status = reinterpret_cast<int*>(ws);
   int* counts = reinterpret_cast<int*>(ws + p.off_counts);
   int* region = reinterpret_cast<int*>(ws + p.off_region);
+  GemmArgs a{};
+  if (!act_maps(a, fmt, A, T, p.bt, true)) return HQ_ERR_INVALID_ARG;
   cudaError_t err =
       launch_route(topk_ids, T * topk, (int)E, (int)p.region_cap, counts, region, status, (cudaStream_t)stream);
   if (err != cudaSuccess) return HQ_ERR_CUDA;
-  GemmArgs a{};
   a.w = static_cast<const uint8_t*>(packedW);
   a.w_expert_bytes = g.expert_bytes;
   a.w_blk = g.blk_bytes;
   a.w_gscale = g.gscale_off >= 0 ? reinterpret_cast<const float*>(a.w + g.gscale_off) : nullptr;
-  a.a = static_cast<const uint8_t*>(A->data);
-  a.a_sf = fmt->act_type == HQ_A_NVFP4 ? static_cast<const uint8_t*>(A->scale) : nullptr;
   a.a_scale = fmt->act_type == HQ_A_NVFP4 ? A->global_scale
                                             : (fmt->act_type == HQ_A_E4M3_TOKEN ? static_cast<const float*>(A->scale)
                                                                                  : nullptr);

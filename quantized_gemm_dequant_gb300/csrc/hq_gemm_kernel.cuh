@@ -5,25 +5,32 @@
 // with one weight row per lane.  Small token counts then still fill the
 // 128-row MMA.
 //
+// Two independent shared-memory rings feed the MMA:
+//   weight ring      one stage block per 128 K (256 K for NVFP4), one bulk copy each
+//   activation ring  one 128-byte-wide K-major tile per stage (64 K of bf16,
+//                    128 K of e4m3, 256 K of e2m1), loaded by TMA: a 2-D box for
+//                    dense rows, tile::gather4 of the routed rows for MoE
+//
 // Warp roles (352 threads):
-//   warps 0-7  INT4 path: decode the stage's 4-bit codes into bf16 A tiles in
-//              tensor memory (warp w: lane quarter w%4, K half w/4).
-//              FP4 paths: warps 0-3 copy block scales into tensor memory,
+//   warps 0-7  INT4 path: decode the weight block's 4-bit codes into bf16 A
+//              tiles in tensor memory (warp w: lane quarter w%4, K half w/4).
+//              FP4 paths: warps 0-3 copy block scales into tensor memory;
 //              MXFP4 warps 4-7 expand packed e2m1 into the MMA's 16-byte
 //              padded layout.  All 8: epilogue (tensor memory -> scales ->
-//              bf16 store, or split-K partial + last-arriver reduction).
-//   warps 8-9  producers: one bulk copy per weight stage block, cp.async
-//              gather of the activation rows (dense rows or routed MoE rows)
-//              into the 128-byte-swizzled K-major layout.
+//              bf16 store, or a split-K partial + last-arriver reduction).
+//   warp 8     weight producer (one thread): bulk copies.
+//   warp 9     activation producer: TMA loads (one thread issues; the warp
+//              reads the routed-row table for MoE).
 //   warp 10    MMA issuer (one thread): tcgen05.mma kind::f16 with A from
 //              tensor memory (INT4), kind::mxf4nvf4 scale_vec::4X (NVFP4),
 //              kind::mxf8f6f4 scale_vec::1X with e2m1 x e4m3 (MXFP4).
 //
-// Work is split into pieces (tile, K-stage range).  With few tiles the K
-// stages of all tiles are dealt out evenly to the CTAs (Stream-K); tiles cut
-// between CTAs are finished by the last CTA to arrive, which sums the partial
-// sums in a fixed order.  No CTA ever waits for another.
+// Work is split into pieces (tile, range of weight blocks along K).  With few
+// tiles the K blocks of all tiles are dealt out evenly to the CTAs
+// (Stream-K); tiles cut between CTAs are finished by the last CTA to arrive,
+// which sums the partial sums in a fixed order.  No CTA waits for another.
 #pragma once
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -33,7 +40,8 @@
 namespace hq {
 
 constexpr int NUM_THREADS = 352;
-constexpr int PRODUCER_WARP0 = 8;
+constexpr int WPROD_WARP = 8;
+constexpr int APROD_WARP = 9;
 constexpr int MMA_WARP = 10;
 constexpr int NUM_EPI_THREADS = 256;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
@@ -41,18 +49,18 @@ constexpr int ERR_TIMEOUT = 5;
 constexpr int ERR_BAD_ROUTING = 6;
 
 struct GemmArgs {
+  CUtensorMap tmap_a;   // activation data: dense 2-D box of BT rows, MoE one-row boxes for gather4
+  CUtensorMap tmap_sf;  // NVFP4 activation block scales (same row structure)
   const uint8_t* w;        // packed weights, all experts
   int64_t w_expert_bytes;  // bytes per expert
-  int w_blk;               // bytes per packed stage block (<= Cfg::W_BLK)
+  int w_blk;               // bytes per packed weight block (<= Cfg::W_BLK)
   const float* w_gscale;   // NVFP4 per-expert global scales, else null
-  const uint8_t* a;        // activation data
-  const uint8_t* a_sf;     // NVFP4 activation block scales [rows][K/16]
   const float* a_scale;    // E4M3: per-token [rows]; NVFP4: global [1]
   const uint16_t* bias;    // bf16 [N] or null
   uint16_t* c;             // bf16 output
   int M;                   // dense rows / MoE tokens
   int N, K;
-  int n_tiles, kst;  // 128-row tiles along N, stage blocks along K
+  int n_tiles, kst;  // 128-row tiles along N, weight blocks along K
   int zp;            // INT4 path: zero points present
   int moe, E, topk;
   const float* topk_w;  // MoE [T*topk] or null
@@ -60,7 +68,7 @@ struct GemmArgs {
   const int* region;    // MoE [E][region_cap] flat (t*topk + j) rows per expert
   int region_cap;
   int m_tiles;  // dense: token tiles
-  int sk;       // 1: Stream-K split over K stages
+  int sk;       // 1: Stream-K split over K blocks
   int* status;
   int* counters;
   float* partials;
@@ -68,31 +76,36 @@ struct GemmArgs {
 
 template <int PATH, int BT>
 struct Cfg {
-  static constexpr int KSTAGE = PATH == PATH_NVFP4 ? 256 : 128;
+  static constexpr int KSTAGE = PATH == PATH_NVFP4 ? 256 : 128;  // K per weight block
   static constexpr int W_BLK = PATH == PATH_INT4 ? 8576 : (PATH == PATH_NVFP4 ? 18432 : 8704);
   static constexpr int W_REGION = ((W_BLK + 1023) / 1024) * 1024;
-  // activation row bytes per stage: bf16 128 K = 256 B; fp4 256 K = 128 B; e4m3 128 K = 128 B
-  static constexpr int ACT_ROW = PATH == PATH_INT4 ? 256 : 128;
-  static constexpr int ACT_BYTES = BT * ACT_ROW;
+  static constexpr int X_REGION = PATH == PATH_MXFP4 ? 16384 : 0;  // expanded e2m1 A tile per weight stage
+  static constexpr int SUB = PATH == PATH_INT4 ? 2 : 1;             // activation stages per weight block
+  static constexpr int ACT_BYTES = BT * 128;
   static constexpr int ACT_REGION = ((ACT_BYTES + 1023) / 1024) * 1024;
   static constexpr int SF_ROWS = BT < 32 ? 32 : BT;
-  static constexpr int ACT_SF_REGION = PATH == PATH_NVFP4 ? ((SF_ROWS * 16 + 1023) / 1024) * 1024 : 0;
-  static constexpr int EXP_REGION = PATH == PATH_MXFP4 ? 16384 : 0;
-  static constexpr int STAGE_BYTES = W_REGION + ACT_REGION + ACT_SF_REGION + EXP_REGION;
-  static constexpr int SMEM_BUDGET = 200 * 1024;
-  static constexpr int S_RAW = SMEM_BUDGET / STAGE_BYTES;
-  static constexpr int STAGES = S_RAW > 8 ? 8 : S_RAW;
+  // NVFP4 activation scales: dense rows are 16 bytes apart; MoE rows come in gather4 groups of four,
+  // each group in its own 128-byte slot (row j at (j/4)*128 + (j%4)*16)
+  static constexpr int ASF_REGION = PATH == PATH_NVFP4 ? ((SF_ROWS * 32 + 1023) / 1024) * 1024 : 0;
+  static constexpr int A_STAGE = ACT_REGION + ASF_REGION;
+  static constexpr int W_STAGE = W_REGION + X_REGION;
+  static constexpr int RING_BUDGET = 216 * 1024;
+  static constexpr int SW = PATH == PATH_INT4 ? (BT <= 64 ? 12 : 4)
+                                              : (PATH == PATH_NVFP4 ? (BT <= 64 ? 8 : 4) : (BT <= 64 ? 6 : 3));
+  static constexpr int SA_FIT = (RING_BUDGET - SW * W_STAGE) / A_STAGE;
+  static constexpr int SA = SA_FIT > 16 ? 16 : SA_FIT;
   static constexpr int CB = BT < 32 ? 1 : BT / 32;  // scale-factor columns per MMA step for B
   static constexpr int SFB_STEP = CB < 4 ? 4 : CB;  // column stride per MMA step (kept 4-aligned)
   static constexpr int SF_STAGE_COLS = PATH == PATH_NVFP4 ? 16 + 4 * SFB_STEP : 4;
   static constexpr int NA = 4;  // INT4: tensor-memory A slots of 64 columns
-  static constexpr int CH = ACT_ROW / 16;  // 16-byte chunks per activation row per stage
-  static constexpr int SMEM_RAW = STAGES * STAGE_BYTES + 1024 /*align*/ + 4096 /*barriers, MoE prefix*/;
+  static constexpr int RING_BYTES = SW * W_STAGE + SA * A_STAGE;
+  static constexpr int SMEM_RAW = RING_BYTES + 1024 /*align*/ + 5120 /*barriers, MoE tables*/;
   // at least 120 KB so that one CTA (and one 512-column tensor-memory allocation) owns each SM
   static constexpr int SMEM_BYTES = SMEM_RAW < 120 * 1024 ? 120 * 1024 : SMEM_RAW;
-  static_assert(STAGES >= 2, "stage ring too small");
-  static_assert(PATH != PATH_NVFP4 || 256 + STAGES * SF_STAGE_COLS <= 512, "tensor memory");
-  static_assert(PATH != PATH_MXFP4 || 256 + 4 * 8 + SFB_STEP <= 512, "tensor memory");
+  static_assert(SA >= 2, "activation ring too small");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+  static_assert(PATH != PATH_NVFP4 || 256 + SW * SF_STAGE_COLS <= 512, "tensor memory");
+  static_assert(PATH != PATH_MXFP4 || 256 + 4 * SW + 8 <= 512, "tensor memory");
 };
 
 __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
@@ -109,10 +122,6 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float x) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
-
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 
 template <int X>
 __device__ __forceinline__ void tmem_st_x(uint32_t taddr, const uint32_t* r);
@@ -149,21 +158,20 @@ __device__ __forceinline__ void tmem_st_x<16>(uint32_t taddr, const uint32_t* r)
 
 // ----------------------------------------------------------------- work pieces
 struct Piece {
-  int tile;     // tile index (token tile major, N tile minor)
-  int g0, g1;   // K-stage range
-  bool full;    // covers all K stages of the tile
-  int slot;     // Stream-K partial slot (2*cta + {0 first piece, 1 last piece})
+  int tile;    // tile index (token tile major, N tile minor)
+  int g0, g1;  // weight-block range along K
+  bool full;   // covers all K blocks of the tile
+  int slot;    // Stream-K partial slot (2*cta + {0 first piece, 1 last piece})
 };
 
 struct Sched {
   int tiles, kst, P, cta, sk;
-  int64_t W;  // total stage iterations
+  int64_t W;  // total block iterations
   __device__ int64_t start(int c) const { return (int64_t)c * W / P; }
   // largest CTA whose range starts at or before iteration it
   __device__ int cta_of(int64_t it) const { return (int)(((it + 1) * P - 1) / W); }
 };
 
-// Enumerate this CTA's pieces in order; f(piece) is called for each.
 template <typename F>
 __device__ __forceinline__ void for_each_piece(const Sched& s, F&& f) {
   if (!s.sk) {
@@ -178,8 +186,7 @@ __device__ __forceinline__ void for_each_piece(const Sched& s, F&& f) {
     const int g0 = (int)(it % s.kst);
     const int64_t left = it1 - it;
     const int g1 = (int)((int64_t)g0 + left < s.kst ? g0 + left : s.kst);
-    const bool full = (g0 == 0 && g1 == s.kst);
-    f(Piece{t, g0, g1, full, 2 * s.cta + (first ? 0 : 1)});
+    f(Piece{t, g0, g1, g0 == 0 && g1 == s.kst, 2 * s.cta + (first ? 0 : 1)});
     it += g1 - g0;
     first = false;
   }
@@ -189,10 +196,12 @@ __device__ __forceinline__ void for_each_piece(const Sched& s, F&& f) {
 template <int PATH, int BT>
 struct Smem {
   using C = Cfg<PATH, BT>;
-  uint64_t full[C::STAGES];
-  uint64_t empty[C::STAGES];
-  uint64_t ready[C::STAGES];  // FP4 paths: scales in tensor memory (+ expanded A for MXFP4)
-  uint64_t afull[C::NA];
+  uint64_t w_full[C::SW];
+  uint64_t w_empty[C::SW];
+  uint64_t ready[C::SW];  // FP4 paths: scales in tensor memory (+ expanded A for MXFP4)
+  uint64_t a_full[C::SA];
+  uint64_t a_empty[C::SA];
+  uint64_t afull[C::NA];  // INT4: decoded A slot written
   uint64_t aempty[C::NA];
   uint64_t dfull;
   uint64_t dempty;
@@ -201,6 +210,7 @@ struct Smem {
   int abort_flag;
   int fix_last;
   int tile_prefix_total;
+  int rows_tok[256];  // MoE: token index of each row of the activation producer's current tile
 };
 
 // Map a global token-tile index to (expert, local token tile) for MoE via the
@@ -217,12 +227,15 @@ __device__ __forceinline__ void moe_locate(const int* prefix, int E, int mt, int
 }
 
 template <int PATH, int BT>
-__global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const GemmArgs args) {
+__global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_constant__ GemmArgs args) {
   using C = Cfg<PATH, BT>;
+  static_assert(sizeof(Smem<PATH, BT>) <= 2048, "shared state");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Smem<PATH, BT>& sh = *reinterpret_cast<Smem<PATH, BT>*>(smem + C::STAGES * C::STAGE_BYTES);
-  int* prefix = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + 1024);  // MoE: E + 1 ints (E <= 512)
+  uint8_t* wring = smem;                       // SW x W_STAGE
+  uint8_t* aring = smem + C::SW * C::W_STAGE;  // SA x A_STAGE
+  Smem<PATH, BT>& sh = *reinterpret_cast<Smem<PATH, BT>*>(smem + C::RING_BYTES);
+  int* prefix = reinterpret_cast<int*>(smem + C::RING_BYTES + 2048);  // MoE: E + 1 ints (E <= 512)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -233,10 +246,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const GemmArgs 
     tmem_relinquish();
   }
   if (tid == 32) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&sh.full[s], 1 + 64);
-      mbar_init(&sh.empty[s], (PATH == PATH_INT4 ? 8 : (PATH == PATH_NVFP4 ? 4 : 8)) + 1);
+    for (int s = 0; s < C::SW; ++s) {
+      mbar_init(&sh.w_full[s], 1);
+      mbar_init(&sh.w_empty[s], PATH == PATH_INT4 ? 8 : (PATH == PATH_NVFP4 ? 4 + 1 : 8 + 1));
       mbar_init(&sh.ready[s], PATH == PATH_MXFP4 ? 8 : 4);
+    }
+    for (int s = 0; s < C::SA; ++s) {
+      mbar_init(&sh.a_full[s], 1);
+      mbar_init(&sh.a_empty[s], PATH == PATH_NVFP4 ? 4 + 1 : 1);
     }
     for (int a = 0; a < C::NA; ++a) {
       mbar_init(&sh.afull[a], 8);
@@ -248,8 +265,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const GemmArgs 
     sh.abort_flag = 0;
     fence_mbar_init();
   }
+  if (tid == APROD_WARP * 32) {
+    prefetch_tmap(&args.tmap_a);
+    if (PATH == PATH_NVFP4) prefetch_tmap(&args.tmap_sf);
+  }
   // MoE: tile prefix over experts (E <= 512 enforced on the host)
-  int total_tiles;
   if (args.moe) {
     for (int e = tid; e < args.E; e += NUM_THREADS) {
       int cnt = args.counts[e];
@@ -258,7 +278,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const GemmArgs 
     }
     __syncthreads();
     if (warp == 0) {
-      // inclusive scan of prefix[1..E] by one warp: each lane owns a contiguous run
       const int per = (args.E + 31) / 32;
       const int b0 = 1 + lane * per;
       int run = 0;
@@ -284,16 +303,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const GemmArgs 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
-  total_tiles = args.moe ? sh.tile_prefix_total * args.n_tiles : args.m_tiles * args.n_tiles;
+  const int total_tiles = args.moe ? sh.tile_prefix_total * args.n_tiles : args.m_tiles * args.n_tiles;
 
   Sched sched;
   sched.tiles = total_tiles;
   sched.kst = args.kst;
   sched.W = (int64_t)total_tiles * args.kst;
-  sched.P = (int)((int64_t)gridDim.x < sched.W ? gridDim.x : sched.W);
+  sched.P = args.sk ? (int)((int64_t)gridDim.x < sched.W ? gridDim.x : sched.W) : (int)gridDim.x;
   sched.cta = blockIdx.x;
   sched.sk = args.sk;
-  if (!args.sk) sched.P = gridDim.x;
   const bool active = (int)blockIdx.x < sched.P && total_tiles > 0;
   volatile int* abort_flag = &sh.abort_flag;
 
@@ -302,7 +320,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const GemmArgs 
     atomicCAS(args.status, 0, code);
   };
 
-  // Row bookkeeping for a tile: token tile (dense) or (expert, local tile) (MoE).
+  // Row bookkeeping of a tile: token tile (dense) or (expert, local tile) (MoE).
   auto tile_rows = [&](int tile, int& e, int& row0, int& nrows) {
     const int mt = tile / args.n_tiles;
     if (args.moe) {
@@ -319,150 +337,188 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const GemmArgs 
     }
   };
 
-  if (active && warp >= PRODUCER_WARP0 && warp < MMA_WARP) {
-    // ============================================================ producers
-    const int pt = tid - PRODUCER_WARP0 * 32;  // 0..63
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    int armed[C::STAGES];  // bulk copies issued per stage (thread pt == 0)
-#pragma unroll
-    for (int s = 0; s < C::STAGES; ++s) armed[s] = 0;
-    for_each_piece(sched, [&](const Piece& pc) {
-      if (!ok) return;
-      int e, row0, nrows;
-      tile_rows(pc.tile, e, row0, nrows);
-      const int nt = pc.tile % args.n_tiles;
-      const uint8_t* wblk = args.w + e * args.w_expert_bytes + ((int64_t)nt * args.kst) * args.w_blk;
-      for (int g = pc.g0; g < pc.g1; ++g) {
-        if (!mbar_wait(&sh.empty[stage], phase ^ 1, abort_flag, WAIT_LIMIT_NS)) {
-          fail(ERR_TIMEOUT);
-          ok = false;
-          return;
-        }
-        uint8_t* sbase = smem + stage * C::STAGE_BYTES;
-        if (pt == 0) {
-          mbar_arrive_expect_tx(&sh.full[stage], (uint32_t)args.w_blk);
-          bulk_g2s(sbase, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk, &sh.full[stage]);
-          ++armed[stage];
-        }
-        uint8_t* act = sbase + C::W_REGION;
-        for (int idx = pt; idx < BT * C::CH; idx += 64) {
-          const int i = idx / C::CH, ch = idx % C::CH;
-          int src = -1;
-          if (i < nrows) src = args.moe ? args.region[e * args.region_cap + row0 + i] / args.topk : row0 + i;
-          const int atom = ch >> 3, cc = ch & 7;
-          uint8_t* dst = act + atom * (BT * 128) + (i >> 3) * 1024 + (i & 7) * 128 + ((cc ^ (i & 7)) << 4);
-          const uint8_t* s;
-          if (PATH == PATH_INT4)
-            s = args.a + ((int64_t)(src < 0 ? 0 : src) * args.K + (int64_t)g * 128) * 2 + ch * 16;
-          else if (PATH == PATH_NVFP4)
-            s = args.a + (int64_t)(src < 0 ? 0 : src) * (args.K / 2) + (int64_t)g * 128 + ch * 16;
-          else
-            s = args.a + (int64_t)(src < 0 ? 0 : src) * args.K + (int64_t)g * 128 + ch * 16;
-          cp_async_16(dst, s, src < 0 ? 0u : 16u);
-        }
-        if (PATH == PATH_NVFP4) {
-          uint8_t* asf = act + C::ACT_REGION;
-          for (int i = pt; i < C::SF_ROWS; i += 64) {
-            int src = -1;
-            if (i < nrows) src = args.moe ? args.region[e * args.region_cap + row0 + i] / args.topk : row0 + i;
-            const uint8_t* s = args.a_sf + (int64_t)(src < 0 ? 0 : src) * (args.K / 16) + (int64_t)g * 16;
-            cp_async_16(asf + i * 16, s, src < 0 ? 0u : 16u);
-          }
-        }
-        cp_async_mbar_arrive_noinc(&sh.full[stage]);
-        if (++stage == C::STAGES) {
-          stage = 0;
-          phase ^= 1;
-        }
-      }
-    });
-    cp_async_wait_all();
-    if (!ok && pt == 0) {
-      // aborted: let this CTA's bulk copies land before shared memory is released
-      int never = 0;
-      for (int s = 0; s < C::STAGES; ++s)
-        if (armed[s] > 0) mbar_wait(&sh.full[s], (uint32_t)((armed[s] - 1) & 1), &never, 200000000ull);
-    }
-  } else if (active && warp == MMA_WARP) {
-    // ============================================================ MMA issuer
+  if (active && warp == WPROD_WARP) {
+    // ============================================================ weight producer
     if (lane == 0) {
-      int stage = 0, aslot = 0;
-      uint32_t phase = 0, aphase = 0;
-      int pidx = 0;
+      int ws = 0;
+      uint32_t wph = 0;
       bool ok = true;
+      int armed[C::SW];
+#pragma unroll
+      for (int s = 0; s < C::SW; ++s) armed[s] = 0;
       for_each_piece(sched, [&](const Piece& pc) {
         if (!ok) return;
-        if (!mbar_wait(&sh.dempty, (pidx & 1) ^ 1, abort_flag, WAIT_LIMIT_NS)) {
-          fail(ERR_TIMEOUT);
-          ok = false;
-          return;
-        }
-        tc_fence_after();
+        int e, row0, nrows;
+        tile_rows(pc.tile, e, row0, nrows);
+        const int nt = pc.tile % args.n_tiles;
+        const uint8_t* wblk = args.w + e * args.w_expert_bytes + ((int64_t)nt * args.kst) * args.w_blk;
         for (int g = pc.g0; g < pc.g1; ++g) {
-          if (!mbar_wait(&sh.full[stage], phase, abort_flag, WAIT_LIMIT_NS)) {
+          if (!mbar_wait(&sh.w_empty[ws], wph ^ 1, abort_flag, WAIT_LIMIT_NS)) {
             fail(ERR_TIMEOUT);
             ok = false;
             return;
           }
-          if (PATH == PATH_INT4) {
-            if (!mbar_wait(&sh.afull[aslot], aphase, abort_flag, WAIT_LIMIT_NS)) {
+          mbar_arrive_expect_tx(&sh.w_full[ws], (uint32_t)args.w_blk);
+          bulk_g2s(wring + ws * C::W_STAGE, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk, &sh.w_full[ws]);
+          ++armed[ws];
+          if (++ws == C::SW) {
+            ws = 0;
+            wph ^= 1;
+          }
+        }
+      });
+      if (!ok) {
+        // aborted: let this CTA's bulk copies land before shared memory is released
+        int never = 0;
+        for (int s = 0; s < C::SW; ++s)
+          if (armed[s] > 0) mbar_wait(&sh.w_full[s], (uint32_t)((armed[s] - 1) & 1), &never, 200000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (active && warp == APROD_WARP) {
+    // ============================================================ activation producer
+    int as = 0;
+    uint32_t aph = 0;
+    bool ok = true;
+    int armed[C::SA];
+#pragma unroll
+    for (int s = 0; s < C::SA; ++s) armed[s] = 0;
+    constexpr int A_BOX_BYTES = BT * 128;
+    constexpr int SF_BOX_BYTES = BT * 16;
+    for_each_piece(sched, [&](const Piece& pc) {
+      if (!ok) return;
+      int e, row0, nrows;
+      tile_rows(pc.tile, e, row0, nrows);
+      if (args.moe) {
+        // token index of every row of the tile; rows past the expert's count read zeros (row M)
+        for (int i = lane; i < BT; i += 32)
+          sh.rows_tok[i] = i < nrows ? args.region[e * args.region_cap + row0 + i] / args.topk : args.M;
+        __syncwarp();
+      }
+      for (int g = pc.g0; g < pc.g1; ++g) {
+        for (int j = 0; j < C::SUB; ++j) {
+          if (lane == 0) {
+            if (!mbar_wait(&sh.a_empty[as], aph ^ 1, abort_flag, WAIT_LIMIT_NS)) {
               fail(ERR_TIMEOUT);
               ok = false;
-              return;
-            }
-          } else {
-            if (!mbar_wait(&sh.ready[stage], phase, abort_flag, WAIT_LIMIT_NS)) {
-              fail(ERR_TIMEOUT);
-              ok = false;
-              return;
             }
           }
-          tc_fence_after();
-          fence_proxy_async_smem();
-          uint8_t* sbase = smem + stage * C::STAGE_BYTES;
-          const uint32_t act = smem_u32(sbase + C::W_REGION);
-          if (PATH == PATH_INT4) {
-            constexpr uint32_t idesc = idesc_bf16(128, BT);
-            const uint32_t a_t = tmem + 256 + aslot * 64;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint64_t bd = smem_desc(act + (i >> 2) * (BT * 128) + (i & 3) * 32, 16, 1024, 2);
-              umma_bf16_ts(tmem, a_t + i * 8, bd, idesc, (g > pc.g0 || i > 0) ? 1u : 0u);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) return;
+          if (lane == 0) {
+            uint8_t* dst = aring + as * C::A_STAGE;
+            // x offset of this stage in the tensor map's element units (bf16: 64 per stage; bytes: 128)
+            const int x = PATH == PATH_INT4 ? g * 128 + j * 64 : g * 128;
+            mbar_arrive_expect_tx(&sh.a_full[as], A_BOX_BYTES + (PATH == PATH_NVFP4 ? SF_BOX_BYTES : 0));
+            if (!args.moe) {
+              tma_load_2d(dst, &args.tmap_a, x, row0, &sh.a_full[as]);
+              if (PATH == PATH_NVFP4) tma_load_2d(dst + C::ACT_REGION, &args.tmap_sf, g * 16, row0, &sh.a_full[as]);
+            } else {
+#pragma unroll 1
+              for (int i = 0; i < BT; i += 4) {
+                uint8_t* d = dst + (i >> 3) * 1024 + (i & 7) * 128;
+                tma_gather4(d, &args.tmap_a, x, sh.rows_tok[i], sh.rows_tok[i + 1], sh.rows_tok[i + 2],
+                            sh.rows_tok[i + 3], &sh.a_full[as]);
+                if (PATH == PATH_NVFP4)
+                  tma_gather4(dst + C::ACT_REGION + (i >> 2) * 128, &args.tmap_sf, g * 16, sh.rows_tok[i],
+                              sh.rows_tok[i + 1], sh.rows_tok[i + 2], sh.rows_tok[i + 3], &sh.a_full[as]);
+              }
             }
+            ++armed[as];
+          }
+          if (++as == C::SA) {
+            as = 0;
+            aph ^= 1;
+          }
+        }
+      }
+      __syncwarp();  // rows_tok is rewritten for the next piece
+    });
+    if (!ok && lane == 0) {
+      int never = 0;
+      for (int s = 0; s < C::SA; ++s)
+        if (armed[s] > 0) mbar_wait(&sh.a_full[s], (uint32_t)((armed[s] - 1) & 1), &never, 200000000ull);
+    }
+    __syncwarp();
+  } else if (active && warp == MMA_WARP) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      int ws = 0, as = 0, aslot = 0;
+      uint32_t wph = 0, aph = 0, aslph = 0;
+      int pidx = 0;
+      bool ok = true;
+      auto waitf = [&](uint64_t* bar, uint32_t par) {
+        if (!ok) return false;
+        if (!mbar_wait(bar, par, abort_flag, WAIT_LIMIT_NS)) {
+          fail(ERR_TIMEOUT);
+          ok = false;
+        }
+        return ok;
+      };
+      for_each_piece(sched, [&](const Piece& pc) {
+        if (!waitf(&sh.dempty, (pidx & 1) ^ 1)) return;
+        tc_fence_after();
+        for (int g = pc.g0; g < pc.g1; ++g) {
+          if (PATH == PATH_INT4) {
+            if (!waitf(&sh.afull[aslot], aslph)) return;
+          } else {
+            if (!waitf(&sh.w_full[ws], wph) || !waitf(&sh.ready[ws], wph)) return;
+          }
+          for (int j = 0; j < C::SUB; ++j) {
+            if (!waitf(&sh.a_full[as], aph)) return;
+            tc_fence_after();
+            fence_proxy_async_smem();
+            const uint32_t act = smem_u32(aring + as * C::A_STAGE);
+            const bool first = (g == pc.g0 && j == 0);
+            if (PATH == PATH_INT4) {
+              constexpr uint32_t idesc = idesc_bf16(128, BT);
+              const uint32_t a_t = tmem + 256 + aslot * 64 + j * 32;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint64_t bd = smem_desc(act + i * 32, 16, 1024, 2);
+                umma_bf16_ts(tmem, a_t + i * 8, bd, idesc, (first && i == 0) ? 0u : 1u);
+              }
+            } else if (PATH == PATH_NVFP4) {
+              constexpr uint32_t idesc = idesc_block_scaled(128, BT, 1, 1, 0, 0, 0);
+              const uint32_t wa = smem_u32(wring + ws * C::W_STAGE);
+              const uint32_t sf = tmem + 256 + ws * C::SF_STAGE_COLS;
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const uint64_t ad = smem_desc(wa + t * 32, 16, 1024, 2);
+                const uint64_t bd = smem_desc(act + t * 32, 16, 1024, 2);
+                umma_nvf4_ss(tmem, ad, bd, idesc, sf + 4 * t, sf + 16 + t * C::SFB_STEP,
+                             (first && t == 0) ? 0u : 1u);
+              }
+            } else {
+              const uint32_t xa = smem_u32(wring + ws * C::W_STAGE + C::W_REGION);
+              const uint32_t sfa = tmem + 256 + ws * 4;
+              const uint32_t sfb = tmem + 256 + 4 * C::SW;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint32_t idesc = idesc_block_scaled(128, BT, 5, 0, 1, i, 0);
+                const uint64_t ad = smem_desc(xa + i * 32, 16, 1024, 2);
+                const uint64_t bd = smem_desc(act + i * 32, 16, 1024, 2);
+                umma_mxf8_ss(tmem, ad, bd, idesc, sfa, sfb, (first && i == 0) ? 0u : 1u);
+              }
+            }
+            umma_commit(&sh.a_empty[as]);
+            if (++as == C::SA) {
+              as = 0;
+              aph ^= 1;
+            }
+          }
+          if (PATH == PATH_INT4) {
             umma_commit(&sh.aempty[aslot]);
             if (++aslot == C::NA) {
               aslot = 0;
-              aphase ^= 1;
-            }
-          } else if (PATH == PATH_NVFP4) {
-            constexpr uint32_t idesc = idesc_block_scaled(128, BT < 32 ? BT : BT, 1, 1, 0, 0, 0);
-            const uint32_t wa = smem_u32(sbase);
-            const uint32_t sf = tmem + 256 + stage * C::SF_STAGE_COLS;
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const uint64_t ad = smem_desc(wa + t * 32, 16, 1024, 2);
-              const uint64_t bd = smem_desc(act + t * 32, 16, 1024, 2);
-              umma_nvf4_ss(tmem, ad, bd, idesc, sf + 4 * t, sf + 16 + t * C::SFB_STEP,
-                           (g > pc.g0 || t > 0) ? 1u : 0u);
+              aslph ^= 1;
             }
           } else {
-            const uint32_t xa = smem_u32(sbase + C::W_REGION + C::ACT_REGION);
-            const uint32_t sfa = tmem + 256 + stage * 4;
-            const uint32_t sfb = tmem + 256 + 4 * 8;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint32_t idesc = idesc_block_scaled(128, BT, 5, 0, 1, i, 0);
-              const uint64_t ad = smem_desc(xa + i * 32, 16, 1024, 2);
-              const uint64_t bd = smem_desc(act + i * 32, 16, 1024, 2);
-              umma_mxf8_ss(tmem, ad, bd, idesc, sfa, sfb, (g > pc.g0 || i > 0) ? 1u : 0u);
+            umma_commit(&sh.w_empty[ws]);
+            if (++ws == C::SW) {
+              ws = 0;
+              wph ^= 1;
             }
-          }
-          umma_commit(&sh.empty[stage]);
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1;
           }
         }
         umma_commit(&sh.dfull);
@@ -478,52 +534,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const GemmArgs 
     __syncwarp();
   } else if (active && warp < 8) {
     // ============================================================ decode / scales / epilogue
-    const int q = warp & 3;   // tensor-memory lane quarter
-    const int h = warp >> 2;  // K half (INT4) / column half (epilogue)
+    const int q = warp & 3;       // tensor-memory lane quarter
+    const int h = warp >> 2;      // K half (INT4) / column half (epilogue)
     const int r = q * 32 + lane;  // weight row within the tile
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    int stage = 0, aslot = 0;
-    uint32_t phase = 0, aphase = 0;
+    int ws = 0, as = 0, aslot = 0;
+    uint32_t wph = 0, aph = 0, aslph = 0;
     int pidx = 0;
     bool ok = true;
+    auto waitf = [&](uint64_t* bar, uint32_t par) {
+      if (!ok) return false;
+      if (!mbar_wait(bar, par, abort_flag, WAIT_LIMIT_NS)) {
+        fail(ERR_TIMEOUT);
+        ok = false;
+      }
+      return ok;
+    };
     if (PATH == PATH_MXFP4 && warp < 4) {
       // unit activation block scales (2^0) for every MMA, written once
       uint32_t ones[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) ones[j] = 0x7F7F7F7Fu;
-      tmem_st_x<8>(tmem + lane_base + 256 + 4 * 8, ones);
+      tmem_st_x<8>(tmem + lane_base + 256 + 4 * C::SW, ones);
       tmem_wait_st();
     }
+    const bool in_mainloop = !(PATH == PATH_NVFP4 && warp >= 4);
     for_each_piece(sched, [&](const Piece& pc) {
       if (!ok) return;
       int e, row0, nrows;
       tile_rows(pc.tile, e, row0, nrows);
       const int nt = pc.tile % args.n_tiles;
       // ---------------------------------------------------- mainloop role
-      const bool in_mainloop = !(PATH == PATH_NVFP4 && warp >= 4);
       for (int g = pc.g0; in_mainloop && g < pc.g1; ++g) {
-        if (!mbar_wait(&sh.full[stage], phase, abort_flag, WAIT_LIMIT_NS)) {
-          fail(ERR_TIMEOUT);
-          ok = false;
-          return;
-        }
-        uint8_t* sbase = smem + stage * C::STAGE_BYTES;
+        if (!waitf(&sh.w_full[ws], wph)) return;
+        uint8_t* wb = wring + ws * C::W_STAGE;
         if (PATH == PATH_INT4) {
-          const uint32_t s16 = reinterpret_cast<const uint16_t*>(sbase + 8192)[r];
+          const uint32_t s16 = reinterpret_cast<const uint16_t*>(wb + 8192)[r];
           const uint32_t ss = s16 | (s16 << 16);
-          const uint32_t z = args.zp ? (uint32_t)sbase[8448 + r] : 8u;
+          const uint32_t z = args.zp ? (uint32_t)wb[8448 + r] : 8u;
           const uint32_t zz = (0x4300u + z) * 0x00010001u;
           uint4 raw[2];
 #pragma unroll
           for (int jj = 0; jj < 2; ++jj)
-            raw[jj] = *reinterpret_cast<const uint4*>(sbase + ((2 * h + jj) * 128 + r) * 16);
+            raw[jj] = *reinterpret_cast<const uint4*>(wb + ((2 * h + jj) * 128 + r) * 16);
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sh.empty[stage]);
-          if (!mbar_wait(&sh.aempty[aslot], aphase ^ 1, abort_flag, WAIT_LIMIT_NS)) {
-            fail(ERR_TIMEOUT);
-            ok = false;
-            return;
-          }
+          if (lane == 0) mbar_arrive(&sh.w_empty[ws]);
+          if (!waitf(&sh.aempty[aslot], aslph ^ 1)) return;
           tc_fence_after();
 #pragma unroll
           for (int jj = 0; jj < 2; ++jj) {
@@ -545,44 +601,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const GemmArgs 
           if (lane == 0) mbar_arrive(&sh.afull[aslot]);
           if (++aslot == C::NA) {
             aslot = 0;
-            aphase ^= 1;
+            aslph ^= 1;
           }
         } else {
           if (warp < 4) {
             // scale factors -> tensor memory (replicated in every lane quarter)
             if (PATH == PATH_NVFP4) {
-              const uint32_t* wsf = reinterpret_cast<const uint32_t*>(sbase + 16384);
+              const uint32_t* wsf = reinterpret_cast<const uint32_t*>(wb + 16384);
               uint32_t v[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) v[j] = wsf[j * 32 + lane];
-              const uint32_t sf = tmem + lane_base + 256 + stage * C::SF_STAGE_COLS;
+              const uint32_t sf = tmem + lane_base + 256 + ws * C::SF_STAGE_COLS;
               tmem_st_x<16>(sf, v);
-              const uint8_t* asf = sbase + C::W_REGION + C::ACT_REGION;
+              if (!waitf(&sh.a_full[as], aph)) return;
+              const uint8_t* asf = aring + as * C::A_STAGE + C::ACT_REGION;
 #pragma unroll
               for (int t = 0; t < 4; ++t) {
                 uint32_t b[C::CB];
 #pragma unroll
-                for (int cc = 0; cc < C::CB; ++cc)
-                  b[cc] = *reinterpret_cast<const uint32_t*>(asf + (cc * 32 + lane) * 16 + t * 4);
+                for (int cc = 0; cc < C::CB; ++cc) {
+                  const int j = cc * 32 + lane;
+                  const int off = args.moe ? (j >> 2) * 128 + (j & 3) * 16 : j * 16;
+                  b[cc] = *reinterpret_cast<const uint32_t*>(asf + off + t * 4);
+                }
                 tmem_st_x<C::CB>(sf + 16 + t * C::SFB_STEP, b);
               }
             } else {
-              const uint32_t* wsf = reinterpret_cast<const uint32_t*>(sbase + 8192);
+              const uint32_t* wsf = reinterpret_cast<const uint32_t*>(wb + 8192);
               uint32_t v[4];
 #pragma unroll
               for (int j = 0; j < 4; ++j) v[j] = wsf[j * 32 + lane];
-              tmem_st_x<4>(tmem + lane_base + 256 + stage * 4, v);
+              tmem_st_x<4>(tmem + lane_base + 256 + ws * 4, v);
             }
             tmem_wait_st();
             tc_fence_before();
           } else if (PATH == PATH_MXFP4) {
             // expand packed e2m1 (8 bytes per 16 K) into the padded 16-byte chunks
-            const uint8_t* raw = sbase;
-            uint8_t* xt = sbase + C::W_REGION + C::ACT_REGION;
+            uint8_t* xt = wb + C::W_REGION;
             const int t128 = tid - 128;
 #pragma unroll 4
             for (int p = t128; p < 1024; p += 128) {
-              const uint2 v = *reinterpret_cast<const uint2*>(raw + p * 8);
+              const uint2 v = *reinterpret_cast<const uint2*>(wb + p * 8);
               const int rr = p >> 3, cc = p & 7;
               *reinterpret_cast<uint4*>(xt + (rr >> 3) * 1024 + (rr & 7) * 128 + ((cc ^ (rr & 7)) << 4)) =
                   make_uint4(v.x, v.y, 0u, 0u);
@@ -590,22 +649,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const GemmArgs 
             fence_proxy_async_smem();
           }
           __syncwarp();
-          if (lane == 0 && (PATH == PATH_MXFP4 || warp < 4)) {
-            mbar_arrive(&sh.ready[stage]);
-            mbar_arrive(&sh.empty[stage]);
+          if (lane == 0) {
+            mbar_arrive(&sh.ready[ws]);
+            mbar_arrive(&sh.w_empty[ws]);
+            if (PATH == PATH_NVFP4) mbar_arrive(&sh.a_empty[as]);
+          }
+          if (PATH == PATH_NVFP4) {
+            if (++as == C::SA) {
+              as = 0;
+              aph ^= 1;
+            }
           }
         }
-        if (++stage == C::STAGES) {
-          stage = 0;
-          phase ^= 1;
+        if (++ws == C::SW) {
+          ws = 0;
+          wph ^= 1;
         }
       }
       // ---------------------------------------------------- epilogue
-      if (!mbar_wait(&sh.dfull, pidx & 1, abort_flag, WAIT_LIMIT_NS)) {
-        fail(ERR_TIMEOUT);
-        ok = false;
-        return;
-      }
+      if (!waitf(&sh.dfull, pidx & 1)) return;
       tc_fence_after();
       constexpr int HC = BT / 2;  // columns per warp
       constexpr int CHUNK = HC < 16 ? HC : 16;
@@ -615,35 +677,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const GemmArgs 
       if (PATH == PATH_NVFP4) post = args.a_scale[0] * args.w_gscale[e];
       const float bias_v = (args.bias && n < args.N) ? bf16_to_f32(args.bias[n]) : 0.0f;
       float* part = args.partials + ((int64_t)pc.slot * BT) * TILE_N;
+      auto store = [&](int col, float acc) {
+        if (col < nrows && n < args.N) {
+          int orow, tok;
+          float f = post;
+          if (args.moe) {
+            orow = args.region[e * args.region_cap + row0 + col];
+            tok = orow / args.topk;
+            if (args.topk_w) f *= args.topk_w[orow];
+          } else {
+            orow = row0 + col;
+            tok = orow;
+          }
+          if (PATH == PATH_MXFP4) f *= args.a_scale[tok];
+          args.c[(int64_t)orow * args.N + n] = f32_to_bf16(acc * f + bias_v);
+        }
+      };
 #pragma unroll 1
       for (int cb = 0; cb < HC; cb += CHUNK) {
         uint32_t v[CHUNK];
-        if (CHUNK == 16) {
-          tmem_ld16(tmem + lane_base + col0 + cb, *reinterpret_cast<uint32_t(*)[16]>(v));
-        } else {
-          tmem_ld8(tmem + lane_base + col0 + cb, *reinterpret_cast<uint32_t(*)[8]>(v));
-        }
+        if (CHUNK == 16) tmem_ld16(tmem + lane_base + col0 + cb, *reinterpret_cast<uint32_t(*)[16]>(v));
+        else tmem_ld8(tmem + lane_base + col0 + cb, *reinterpret_cast<uint32_t(*)[8]>(v));
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < CHUNK; ++j) {
           const int col = col0 + cb + j;
-          const float acc = __uint_as_float(v[j]);
-          if (!pc.full) {
-            part[col * TILE_N + r] = acc;
-          } else if (col < nrows && n < args.N) {
-            int orow, tok;
-            float f = post;
-            if (args.moe) {
-              orow = args.region[e * args.region_cap + row0 + col];
-              tok = orow / args.topk;
-              if (args.topk_w) f *= args.topk_w[orow];
-            } else {
-              orow = row0 + col;
-              tok = orow;
-            }
-            if (PATH == PATH_MXFP4) f *= args.a_scale[tok];
-            args.c[(int64_t)orow * args.N + n] = f32_to_bf16(acc * f + bias_v);
-          }
+          if (!pc.full) part[col * TILE_N + r] = __uint_as_float(v[j]);
+          else store(col, __uint_as_float(v[j]));
         }
       }
       tc_fence_before();
@@ -653,10 +713,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const GemmArgs 
         // ---------------------------------------------- Stream-K fix-up (last arriver sums)
         __threadfence();
         named_bar_sync(1, NUM_EPI_THREADS);
+        const int64_t first_it = (int64_t)pc.tile * sched.kst;
+        const int c_first = sched.cta_of(first_it);
+        const int c_last = sched.cta_of(first_it + sched.kst - 1);
         if (tid == 0) {
-          const int64_t first_it = (int64_t)pc.tile * sched.kst;
-          const int c_first = sched.cta_of(first_it);
-          const int c_last = sched.cta_of(first_it + sched.kst - 1);
           const int nctr = c_last - c_first + 1;
           const int old = atomicAdd(&args.counters[pc.tile], 1);
           sh.fix_last = (old == nctr - 1) ? 1 : 0;
@@ -665,9 +725,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const GemmArgs 
         named_bar_sync(1, NUM_EPI_THREADS);
         if (sh.fix_last) {
           __threadfence();
-          const int64_t first_it = (int64_t)pc.tile * sched.kst;
-          const int c_first = sched.cta_of(first_it);
-          const int c_last = sched.cta_of(first_it + sched.kst - 1);
           for (int j = 0; j < HC; ++j) {
             const int col = col0 + j;
             float acc = 0.0f;
@@ -675,20 +732,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const GemmArgs 
               const int slot = (c == c_first && sched.start(c) < first_it) ? 2 * c + 1 : 2 * c;
               acc += __ldcg(args.partials + ((int64_t)slot * BT + col) * TILE_N + r);
             }
-            if (col < nrows && n < args.N) {
-              int orow, tok;
-              float f = post;
-              if (args.moe) {
-                orow = args.region[e * args.region_cap + row0 + col];
-                tok = orow / args.topk;
-                if (args.topk_w) f *= args.topk_w[orow];
-              } else {
-                orow = row0 + col;
-                tok = orow;
-              }
-              if (PATH == PATH_MXFP4) f *= args.a_scale[tok];
-              args.c[(int64_t)orow * args.N + n] = f32_to_bf16(acc * f + bias_v);
-            }
+            store(col, acc);
           }
         }
       }
