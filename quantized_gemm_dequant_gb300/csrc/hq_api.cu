@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "../../include/hq.h"
@@ -17,6 +18,7 @@ cudaError_t launch_route(const int32_t* ids, int64_t rows, int E, int cap, int* 
 cudaError_t launch_gemm_int4(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_nvfp4(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_mxfp4(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_small(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 
 namespace {
 
@@ -73,6 +75,7 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // Launch plan of one call; also fixes the workspace layout.
 struct Plan {
   int path = 0;
+  int small = 0;  // INT4 with at most 32 tokens per tile: register-decode mma.sync kernel
   int bt = 16;
   int sk = 0;
   int grid = 1;
@@ -95,6 +98,15 @@ int pick_bt_moe(int64_t rows, int64_t E) {
   if (avg <= 32) return 32;
   if (avg <= 64) return 64;
   return 128;
+}
+
+// HQ_FORCE_PATH=small|umma overrides the choice between the two INT4 kernels (tests compare both).
+int forced_path() {
+  const char* v = getenv("HQ_FORCE_PATH");
+  if (!v) return 0;
+  if (!strcmp(v, "small")) return 1;
+  if (!strcmp(v, "umma")) return 2;
+  return 0;
 }
 
 Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int sms) {
@@ -126,6 +138,24 @@ Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int
     p.off_counts = off;
     off = align256(off + sizeof(int) * (size_t)E);
   }
+  if (p.path == PATH_INT4) {
+    const int force = forced_path();
+    p.small = force == 1 ? 1 : (force == 2 ? 0 : (p.bt <= 32 ? 1 : 0));
+    if (p.small && p.bt > 32) {  // forced: re-tile with 32-token tiles
+      p.bt = 32;
+      if (!moe) {
+        p.m_tiles = (M_or_T + p.bt - 1) / p.bt;
+        p.max_tiles = p.m_tiles * p.n_tiles;
+      } else {
+        const int64_t rows = M_or_T * topk;
+        const int64_t active = rows < f->num_experts ? rows : f->num_experts;
+        p.max_tiles = p.n_tiles * (active + (rows + p.bt - 1) / p.bt);
+      }
+      p.sk = (p.max_tiles < 2 * (int64_t)sms && p.kst > 1) ? 1 : 0;
+      const int64_t W = p.max_tiles * (p.sk ? p.kst : 1);
+      p.grid = (int)(W < sms ? (W < 1 ? 1 : W) : sms);
+    }
+  }
   p.off_counters = off;
   off = align256(off + sizeof(int) * (size_t)(p.max_tiles > 0 ? p.max_tiles : 1));
   if (moe) {
@@ -141,7 +171,7 @@ Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int
 }
 
 cudaError_t launch_path(const Plan& p, const GemmArgs& a, cudaStream_t s) {
-  if (p.path == PATH_INT4) return launch_gemm_int4(a, p.bt, p.grid, s);
+  if (p.path == PATH_INT4) return p.small ? launch_gemm_small(a, p.bt, p.grid, s) : launch_gemm_int4(a, p.bt, p.grid, s);
   if (p.path == PATH_NVFP4) return launch_gemm_nvfp4(a, p.bt, p.grid, s);
   return launch_gemm_mxfp4(a, p.bt, p.grid, s);
 }

@@ -725,14 +725,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
         named_bar_sync(1, NUM_EPI_THREADS);
         if (sh.fix_last) {
           __threadfence();
-          for (int j = 0; j < HC; ++j) {
-            const int col = col0 + j;
-            float acc = 0.0f;
-            for (int c = c_first; c <= c_last; ++c) {
-              const int slot = (c == c_first && sched.start(c) < first_it) ? 2 * c + 1 : 2 * c;
-              acc += __ldcg(args.partials + ((int64_t)slot * BT + col) * TILE_N + r);
+          // every partial of a column chunk is requested before any is summed: one L2 round trip per chunk
+#pragma unroll 1
+          for (int cb = 0; cb < HC; cb += CHUNK) {
+            float acc[CHUNK];
+#pragma unroll
+            for (int j = 0; j < CHUNK; ++j) acc[j] = 0.0f;
+            int c = c_first;
+            for (; c + 1 <= c_last; c += 2) {
+              const int s0 = (c == c_first && sched.start(c) < first_it) ? 2 * c + 1 : 2 * c;
+              const int s1 = 2 * (c + 1);
+              const float* p0 = args.partials + ((int64_t)s0 * BT + col0 + cb) * TILE_N + r;
+              const float* p1 = args.partials + ((int64_t)s1 * BT + col0 + cb) * TILE_N + r;
+              float v0[CHUNK], v1[CHUNK];
+#pragma unroll
+              for (int j = 0; j < CHUNK; ++j) {
+                v0[j] = __ldcg(p0 + j * TILE_N);
+                v1[j] = __ldcg(p1 + j * TILE_N);
+              }
+#pragma unroll
+              for (int j = 0; j < CHUNK; ++j) acc[j] += v0[j] + v1[j];
             }
-            store(col, acc);
+            if (c <= c_last) {
+              const int s0 = (c == c_first && sched.start(c) < first_it) ? 2 * c + 1 : 2 * c;
+              const float* p0 = args.partials + ((int64_t)s0 * BT + col0 + cb) * TILE_N + r;
+              float v0[CHUNK];
+#pragma unroll
+              for (int j = 0; j < CHUNK; ++j) v0[j] = __ldcg(p0 + j * TILE_N);
+#pragma unroll
+              for (int j = 0; j < CHUNK; ++j) acc[j] += v0[j];
+            }
+#pragma unroll
+            for (int j = 0; j < CHUNK; ++j) store(col0 + cb + j, acc[j]);
           }
         }
       }

@@ -1,0 +1,380 @@
+// Small-token weight-streaming path for the 4-bit integer formats (dense and MoE).
+//
+// With at most 32 tokens per tile the UMMA path is limited by its fixed cost
+// per 128 x 16 instruction, not by the bytes it moves, so this kernel decodes
+// in registers and feeds the legacy warp-level tensor-core instruction
+// (mma.sync m16n8k16, bf16 x bf16 -> fp32), in the spirit of the multistage
+// copy + MMA pipeline that the Humming announcement reports to beat TMA + UMMA
+// at small batch ("Tuning and JIT compilation per workload").
+//
+// It reads the same packed weight blocks as the UMMA path (see hq_layout.h).
+// Each weight row of a block is one row of a 16-row MMA tile; lane (g, t) of
+// a warp extracts the (2t, 2t+1) code pair of rows g and g+8 from the shared
+// words, so every nibble is decoded by exactly one thread.  Codes become
+// exact integers (q - z) in bf16; the group scale multiplies the fp32 group
+// partial after the MMA, so the decode adds no rounding.
+//
+// Warps 0-7 compute (warp w owns rows 16w..16w+15 of the 128-row tile); warp 8
+// produces: one bulk copy of the weight block plus the TMA load (dense) or
+// gather4 (MoE) of the token tile for the same 128 K, all on one barrier.
+// Pieces and the Stream-K fix-up are those of the UMMA path.
+#include "hq_gemm_kernel.cuh"
+
+namespace hq {
+
+constexpr int SM_THREADS = 288;
+constexpr int SM_PROD_WARP = 8;
+
+template <int BT>
+struct SmallCfg {
+  static constexpr int W_REGION = 9216;          // one INT4 block (<= 8576 bytes), 1 KB aligned
+  static constexpr int ACT_BYTES = 2 * BT * 128;  // two 64-K swizzled atoms
+  static constexpr int STAGE = W_REGION + ACT_BYTES;
+  static constexpr int STAGES = (200 * 1024) / STAGE > 16 ? 16 : (200 * 1024) / STAGE;
+  static constexpr int NT = BT / 8;  // 8-token MMA tiles
+  static constexpr int SMEM_RAW = STAGES * STAGE + 1024 + 5120;
+  static constexpr int SMEM_BYTES = SMEM_RAW < 120 * 1024 ? 120 * 1024 : SMEM_RAW;
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
+
+struct SmallSmem {
+  uint64_t full[16];
+  uint64_t empty[16];
+  int abort_flag;
+  int fix_last;
+  int tile_prefix_total;
+  int rows_tok[32];
+};
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int BT>
+__global__ void __launch_bounds__(SM_THREADS, 1) hq_gemm_small_kernel(const __grid_constant__ GemmArgs args) {
+  using C = SmallCfg<BT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  SmallSmem& sh = *reinterpret_cast<SmallSmem*>(smem + C::STAGES * C::STAGE);
+  int* prefix = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE + 1024);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], 8);
+    }
+    sh.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (tid == SM_PROD_WARP * 32) prefetch_tmap(&args.tmap_a);
+  if (args.moe) {
+    for (int e = tid; e < args.E; e += SM_THREADS) {
+      int cnt = args.counts[e];
+      cnt = cnt < 0 ? 0 : (cnt > args.region_cap ? args.region_cap : cnt);
+      prefix[e + 1] = (cnt + BT - 1) / BT;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const int per = (args.E + 31) / 32;
+      const int b0 = 1 + lane * per;
+      int run = 0;
+      for (int i = 0; i < per; ++i)
+        if (b0 + i <= args.E) run += prefix[b0 + i];
+      int incl = run;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      int acc = incl - run;
+      for (int i = 0; i < per; ++i)
+        if (b0 + i <= args.E) {
+          acc += prefix[b0 + i];
+          prefix[b0 + i] = acc;
+        }
+      if (lane == 0) prefix[0] = 0;
+      if (lane == 31) sh.tile_prefix_total = incl;
+    }
+  }
+  __syncthreads();
+  const int total_tiles = args.moe ? sh.tile_prefix_total * args.n_tiles : args.m_tiles * args.n_tiles;
+  Sched sched;
+  sched.tiles = total_tiles;
+  sched.kst = args.kst;
+  sched.W = (int64_t)total_tiles * args.kst;
+  sched.P = args.sk ? (int)((int64_t)gridDim.x < sched.W ? gridDim.x : sched.W) : (int)gridDim.x;
+  sched.cta = blockIdx.x;
+  sched.sk = args.sk;
+  const bool active = (int)blockIdx.x < sched.P && total_tiles > 0;
+  volatile int* abort_flag = &sh.abort_flag;
+  auto fail = [&](int code) {
+    *abort_flag = 1;
+    atomicCAS(args.status, 0, code);
+  };
+  auto tile_rows = [&](int tile, int& e, int& row0, int& nrows) {
+    const int mt = tile / args.n_tiles;
+    if (args.moe) {
+      int lm;
+      moe_locate(prefix, args.E, mt, e, lm);
+      int cnt = args.counts[e];
+      cnt = cnt > args.region_cap ? args.region_cap : cnt;
+      row0 = lm * BT;
+      nrows = cnt - row0 < BT ? cnt - row0 : BT;
+    } else {
+      e = 0;
+      row0 = mt * BT;
+      nrows = args.M - row0 < BT ? args.M - row0 : BT;
+    }
+  };
+
+  if (active && warp == SM_PROD_WARP) {
+    // ============================================================ producer
+    int st = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    int armed[C::STAGES];
+#pragma unroll
+    for (int s = 0; s < C::STAGES; ++s) armed[s] = 0;
+    for_each_piece(sched, [&](const Piece& pc) {
+      if (!ok) return;
+      int e, row0, nrows;
+      tile_rows(pc.tile, e, row0, nrows);
+      const int nt = pc.tile % args.n_tiles;
+      if (args.moe) {
+        for (int i = lane; i < BT; i += 32)
+          sh.rows_tok[i] = i < nrows ? args.region[e * args.region_cap + row0 + i] / args.topk : args.M;
+        __syncwarp();
+      }
+      const uint8_t* wblk = args.w + e * args.w_expert_bytes + ((int64_t)nt * args.kst) * args.w_blk;
+      for (int g = pc.g0; g < pc.g1; ++g) {
+        if (lane == 0 && !mbar_wait(&sh.empty[st], ph ^ 1, abort_flag, WAIT_LIMIT_NS)) {
+          fail(ERR_TIMEOUT);
+          ok = false;
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) return;
+        if (lane == 0) {
+          uint8_t* base = smem + st * C::STAGE;
+          uint8_t* act = base + C::W_REGION;
+          mbar_arrive_expect_tx(&sh.full[st], (uint32_t)args.w_blk + C::ACT_BYTES);
+          bulk_g2s(base, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk, &sh.full[st]);
+          for (int j = 0; j < 2; ++j) {
+            uint8_t* dst = act + j * (BT * 128);
+            if (!args.moe) {
+              tma_load_2d(dst, &args.tmap_a, g * 128 + j * 64, row0, &sh.full[st]);
+            } else {
+#pragma unroll 1
+              for (int i = 0; i < BT; i += 4)
+                tma_gather4(dst + (i >> 3) * 1024 + (i & 7) * 128, &args.tmap_a, g * 128 + j * 64, sh.rows_tok[i],
+                            sh.rows_tok[i + 1], sh.rows_tok[i + 2], sh.rows_tok[i + 3], &sh.full[st]);
+            }
+          }
+          ++armed[st];
+        }
+        if (++st == C::STAGES) {
+          st = 0;
+          ph ^= 1;
+        }
+      }
+      __syncwarp();
+    });
+    if (!ok && lane == 0) {
+      int never = 0;
+      for (int s = 0; s < C::STAGES; ++s)
+        if (armed[s] > 0) mbar_wait(&sh.full[s], (uint32_t)((armed[s] - 1) & 1), &never, 200000000ull);
+    }
+    __syncwarp();
+  } else if (active && warp < 8) {
+    // ============================================================ compute warps
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const int rA = warp * 16 + g8, rB = rA + 8;  // rows of this lane within the 128-row tile
+    const uint32_t sh4 = 4u * (uint32_t)t4;
+    int st = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for_each_piece(sched, [&](const Piece& pc) {
+      if (!ok) return;
+      int e, row0, nrows;
+      tile_rows(pc.tile, e, row0, nrows);
+      const int nt = pc.tile % args.n_tiles;
+      float acc[C::NT][4];
+#pragma unroll
+      for (int i = 0; i < C::NT; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+      for (int g = pc.g0; g < pc.g1; ++g) {
+        if (!mbar_wait(&sh.full[st], ph, abort_flag, WAIT_LIMIT_NS)) {
+          fail(ERR_TIMEOUT);
+          ok = false;
+          return;
+        }
+        const uint8_t* wb = smem + st * C::STAGE;
+        const uint8_t* act = wb + C::W_REGION;
+        const float sA = bf16_to_f32(reinterpret_cast<const uint16_t*>(wb + 8192)[rA]);
+        const float sB = bf16_to_f32(reinterpret_cast<const uint16_t*>(wb + 8192)[rB]);
+        const uint32_t zA = args.zp ? (uint32_t)wb[8448 + rA] : 8u;
+        const uint32_t zB = args.zp ? (uint32_t)wb[8448 + rB] : 8u;
+        const uint32_t zzA = (0x4300u + zA) * 0x00010001u, zzB = (0x4300u + zB) * 0x00010001u;
+        float blk[C::NT][4];
+#pragma unroll
+        for (int i = 0; i < C::NT; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) blk[i][j] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {  // 32-K chunk
+          const uint4 wa = *reinterpret_cast<const uint4*>(wb + (j * 128 + rA) * 16);
+          const uint4 wbv = *reinterpret_cast<const uint4*>(wb + (j * 128 + rB) * 16);
+          const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
+          const uint32_t wB[4] = {wbv.x, wbv.y, wbv.z, wbv.w};
+#pragma unroll
+          for (int s2 = 0; s2 < 2; ++s2) {  // 16-K step within the chunk
+            uint32_t a[4];
+            a[0] = bf16x2_sub(lop3_and_or(wA[2 * s2] >> sh4, 0x000F000Fu, 0x43004300u), zzA);
+            a[1] = bf16x2_sub(lop3_and_or(wB[2 * s2] >> sh4, 0x000F000Fu, 0x43004300u), zzB);
+            a[2] = bf16x2_sub(lop3_and_or(wA[2 * s2 + 1] >> sh4, 0x000F000Fu, 0x43004300u), zzA);
+            a[3] = bf16x2_sub(lop3_and_or(wB[2 * s2 + 1] >> sh4, 0x000F000Fu, 0x43004300u), zzB);
+            const int kk = j * 32 + s2 * 16;  // K within the 128-K block
+            const int atom = kk >> 6;
+            const int byte = (kk & 63) * 2 + t4 * 4;  // b0b1 at k = kk + 2t; b2b3 eight K later
+#pragma unroll
+            for (int n8 = 0; n8 < C::NT; ++n8) {
+              const int row = n8 * 8 + g8;
+              const uint8_t* ab = act + atom * (BT * 128) + (row >> 3) * 1024 + (row & 7) * 128;
+              const int c0 = byte >> 4, c1 = (byte + 16) >> 4;
+              const uint32_t b0 = *reinterpret_cast<const uint32_t*>(ab + ((c0 ^ (row & 7)) << 4) + (byte & 15));
+              const uint32_t b1 = *reinterpret_cast<const uint32_t*>(ab + ((c1 ^ (row & 7)) << 4) + (byte & 15));
+              mma_bf16_16816(blk[n8], a, b0, b1);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.empty[st]);
+#pragma unroll
+        for (int i = 0; i < C::NT; ++i) {
+          acc[i][0] = fmaf(sA, blk[i][0], acc[i][0]);
+          acc[i][1] = fmaf(sA, blk[i][1], acc[i][1]);
+          acc[i][2] = fmaf(sB, blk[i][2], acc[i][2]);
+          acc[i][3] = fmaf(sB, blk[i][3], acc[i][3]);
+        }
+        if (++st == C::STAGES) {
+          st = 0;
+          ph ^= 1;
+        }
+      }
+      // ---------------------------------------------------- epilogue
+      const float biasA = (args.bias && nt * TILE_N + rA < args.N) ? bf16_to_f32(args.bias[nt * TILE_N + rA]) : 0.f;
+      const float biasB = (args.bias && nt * TILE_N + rB < args.N) ? bf16_to_f32(args.bias[nt * TILE_N + rB]) : 0.f;
+      auto store = [&](int col, int r, float v, float bias) {
+        const int n = nt * TILE_N + r;
+        if (col < nrows && n < args.N) {
+          int orow;
+          float f = 1.0f;
+          if (args.moe) {
+            orow = args.region[e * args.region_cap + row0 + col];
+            if (args.topk_w) f = args.topk_w[orow];
+          } else {
+            orow = row0 + col;
+          }
+          args.c[(int64_t)orow * args.N + n] = f32_to_bf16(v * f + bias);
+        }
+      };
+      if (pc.full) {
+#pragma unroll
+        for (int i = 0; i < C::NT; ++i) {
+          const int col = i * 8 + 2 * t4;
+          store(col, rA, acc[i][0], biasA);
+          store(col + 1, rA, acc[i][1], biasA);
+          store(col, rB, acc[i][2], biasB);
+          store(col + 1, rB, acc[i][3], biasB);
+        }
+      } else {
+        float* part = args.partials + ((int64_t)pc.slot * BT) * TILE_N;
+#pragma unroll
+        for (int i = 0; i < C::NT; ++i) {
+          const int col = i * 8 + 2 * t4;
+          part[col * TILE_N + rA] = acc[i][0];
+          part[(col + 1) * TILE_N + rA] = acc[i][1];
+          part[col * TILE_N + rB] = acc[i][2];
+          part[(col + 1) * TILE_N + rB] = acc[i][3];
+        }
+        __threadfence();
+        named_bar_sync(1, 256);
+        const int64_t first_it = (int64_t)pc.tile * sched.kst;
+        const int c_first = sched.cta_of(first_it);
+        const int c_last = sched.cta_of(first_it + sched.kst - 1);
+        if (tid == 0) {
+          const int nctr = c_last - c_first + 1;
+          const int old = atomicAdd(&args.counters[pc.tile], 1);
+          sh.fix_last = (old == nctr - 1) ? 1 : 0;
+          if (old == nctr - 1) args.counters[pc.tile] = 0;
+        }
+        named_bar_sync(1, 256);
+        if (sh.fix_last) {
+          __threadfence();
+          float sum[C::NT][4];
+#pragma unroll
+          for (int i = 0; i < C::NT; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sum[i][j] = 0.0f;
+          for (int c = c_first; c <= c_last; ++c) {
+            const int slot = (c == c_first && sched.start(c) < first_it) ? 2 * c + 1 : 2 * c;
+            const float* p = args.partials + ((int64_t)slot * BT) * TILE_N;
+            float v[C::NT][4];
+#pragma unroll
+            for (int i = 0; i < C::NT; ++i) {
+              const int col = i * 8 + 2 * t4;
+              v[i][0] = __ldcg(p + col * TILE_N + rA);
+              v[i][1] = __ldcg(p + (col + 1) * TILE_N + rA);
+              v[i][2] = __ldcg(p + col * TILE_N + rB);
+              v[i][3] = __ldcg(p + (col + 1) * TILE_N + rB);
+            }
+#pragma unroll
+            for (int i = 0; i < C::NT; ++i)
+#pragma unroll
+              for (int j = 0; j < 4; ++j) sum[i][j] += v[i][j];
+          }
+#pragma unroll
+          for (int i = 0; i < C::NT; ++i) {
+            const int col = i * 8 + 2 * t4;
+            store(col, rA, sum[i][0], biasA);
+            store(col + 1, rA, sum[i][1], biasA);
+            store(col, rB, sum[i][2], biasB);
+            store(col + 1, rB, sum[i][3], biasB);
+          }
+        }
+      }
+    });
+  }
+  __syncthreads();
+}
+
+template <int BT>
+static cudaError_t launch_small_bt(const GemmArgs& a, int grid, cudaStream_t stream) {
+  using C = SmallCfg<BT>;
+  static int attr_set[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(hq_gemm_small_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = 1;
+  }
+  hq_gemm_small_kernel<BT><<<grid, SM_THREADS, C::SMEM_BYTES, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_small(const GemmArgs& a, int bt, int grid, cudaStream_t stream) {
+  switch (bt) {
+    case 16: return launch_small_bt<16>(a, grid, stream);
+    case 32: return launch_small_bt<32>(a, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace hq

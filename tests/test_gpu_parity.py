@@ -219,3 +219,40 @@ def test_workspace_is_reusable_across_calls(lib):
     torch.cuda.synchronize()
     assert torch.equal(y1, y2)
     assert lib.last_device_status(ws) == lib.HQ_OK
+
+
+# ------------------------------------------------------------------ both INT4 kernels on the same inputs
+@pytest.mark.parametrize("path", ["small", "umma"])
+@pytest.mark.parametrize("wfmt", ["int4_sym", "uint4_zp"])
+@pytest.mark.parametrize("M", [1, 8, 16, 24, 32, 40, 64])
+def test_int4_kernels_forced(lib, monkeypatch, path, wfmt, M):
+    """HQ_FORCE_PATH selects the register-decode mma.sync kernel or the UMMA kernel; both must match the oracle."""
+    monkeypatch.setenv("HQ_FORCE_PATH", path)
+    inp = make_dense(DENSE_FORMS[wfmt], M, seed=100 + M, N=384, K=1024, with_bias=True)
+    R.assert_parity(_run_dense(lib, inp), R.dense_ref(inp), f"{wfmt} M={M} path={path}")
+
+
+@pytest.mark.parametrize("path", ["small", "umma"])
+@pytest.mark.parametrize("T", [1, 9, 70])
+def test_int4_moe_kernels_forced(lib, monkeypatch, path, T):
+    monkeypatch.setenv("HQ_FORCE_PATH", path)
+    inp = make_moe(MOE_FORMS["int4_sym"], T, seed=T, E=16, N=256, K=512, topk=4)
+    R.assert_parity(_run_moe(lib, inp), R.moe_ref(inp), f"moe T={T} path={path}")
+
+
+def test_int4_kernels_agree_exactly_on_integer_inputs(lib, monkeypatch):
+    """Integer codes and activations with power-of-two scales: both kernels give identical bits."""
+    gen = torch.Generator().manual_seed(21)
+    M, N, K = 16, 256, 512
+    q = torch.randint(-7, 8, (N, K), generator=gen)
+    j = torch.randint(-3, 1, (N, K // 128), generator=gen)
+    inp = dict(M=M, N=N, K=K, wfmt="int4_sym", afmt="bf16", G=128,
+               w=dict(codes=quant.pack_nibbles((q & 0xF).to(torch.uint8)),
+                      scales=((j + 127) << 7).to(torch.int16).view(torch.bfloat16)),
+               a=dict(data=torch.randint(-3, 4, (M, K), generator=gen).to(torch.bfloat16)))
+    outs = []
+    for path in ("small", "umma"):
+        monkeypatch.setenv("HQ_FORCE_PATH", path)
+        outs.append(_run_dense(lib, inp).cpu())
+    assert torch.equal(outs[0], outs[1])
+    assert torch.equal(outs[0], _bf16_rne(R.dense_ref(inp)))
