@@ -153,6 +153,33 @@ HQ_API hq_status_t hq_moe_gemm(const hq_format_t* fmt, const hq_act_t* A, const 
  * clear it.  *status_out receives HQ_OK or the first device-detected error. */
 HQ_API hq_status_t hq_last_device_status(void* workspace, int32_t* status_out, hq_stream_t stream);
 
+/* Size of the fixed device scratch used by hq_gemm_static_scratch (16 MiB per GPU). */
+#define HQ_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/* Dense GEMM, same operands and result as hq_gemm, for callers that cannot
+ * allocate device memory: code running inside a host framework that owns all
+ * device memory through its own pool and forbids outside allocations, or
+ * latency-critical loops where a cudaMalloc (which may synchronise the device)
+ * is not acceptable.  The Humming announcement has no counterpart to this call.
+ *  - No workspace argument: scratch comes from one file-scope device array of
+ *    HQ_STATIC_SCRATCH_BYTES that every GPU loading this library holds until
+ *    the process exits.  The call allocates nothing (no cudaMalloc or cudaFree).
+ *  - Calls whose hq_workspace_bytes(fmt, M, 1) exceeds HQ_STATIC_SCRATCH_BYTES
+ *    return HQ_ERR_WORKSPACE before enqueueing anything; use hq_gemm then.
+ *  - The first call on a device looks up the scratch's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture on the device.
+ *  - Every call on a device shares the scratch and leaves its contents behind;
+ *    each call first clears the part that must start at zero (one
+ *    cudaMemsetAsync on `stream`).  Calls whose executions overlap on the GPU
+ *    (different streams, no ordering between them) race on the scratch and
+ *    give undefined results: order them.
+ *  - Device-detected errors of this variant are not readable through
+ *    hq_last_device_status; use hq_gemm with a workspace to observe them. */
+HQ_API hq_status_t hq_gemm_static_scratch(const hq_format_t* fmt, const hq_act_t* A, const void* packedW,
+                                          const void* bias, void* C, int64_t M, int64_t N, int64_t K,
+                                          hq_stream_t stream);
+
 /* Static description of a status code. */
 HQ_API const char* hq_status_string(hq_status_t status);
 

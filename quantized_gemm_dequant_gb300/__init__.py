@@ -28,7 +28,7 @@ HQ_S_BF16, HQ_S_UE4M3, HQ_S_UE8M0 = 1, 2, 3
 HQ_A_BF16, HQ_A_E4M3_TOKEN, HQ_A_NVFP4 = 1, 2, 3
 
 EXPORTS = ["hq_packed_bytes", "hq_pack_weights", "hq_unpack_weights", "hq_workspace_bytes", "hq_workspace_init",
-           "hq_gemm", "hq_moe_gemm", "hq_last_device_status", "hq_status_string"]
+           "hq_gemm", "hq_moe_gemm", "hq_last_device_status", "hq_status_string", "hq_gemm_static_scratch"]
 
 
 class Format(ctypes.Structure):
@@ -60,6 +60,8 @@ _lib.hq_moe_gemm.argtypes = [_F, _A, _vp, _vp, _vp, _i64, _i32, _vp, _vp, _sz, _
 _lib.hq_moe_gemm.restype = ctypes.c_int
 _lib.hq_last_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32), _vp]
 _lib.hq_last_device_status.restype = ctypes.c_int
+_lib.hq_gemm_static_scratch.argtypes = [_F, _A, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
+_lib.hq_gemm_static_scratch.restype = ctypes.c_int
 _lib.hq_status_string.argtypes = [ctypes.c_int]
 _lib.hq_status_string.restype = ctypes.c_char_p
 
@@ -152,6 +154,17 @@ def gemm(fmt, act, packed, M, bias=None, out=None, workspace=None, stream=None):
     A = _act(act)
     _check(_lib.hq_gemm(ctypes.byref(fmt), ctypes.byref(A), _ptr(packed), _ptr(bias), _ptr(out), int(M), fmt.N,
                         fmt.K, _ptr(workspace), workspace.numel(), _stream(stream)), "hq_gemm")
+    return out
+
+
+def gemm_static_scratch(fmt, act, packed, M, bias=None, out=None, stream=None):
+    """hq_gemm without a workspace: scratch comes from the library's fixed per-GPU device array."""
+    dev = act["data"].device
+    if out is None:
+        out = torch.empty((M, fmt.N), dtype=torch.bfloat16, device=dev)
+    A = _act(act)
+    _check(_lib.hq_gemm_static_scratch(ctypes.byref(fmt), ctypes.byref(A), _ptr(packed), _ptr(bias), _ptr(out),
+                                       int(M), fmt.N, fmt.K, _stream(stream)), "hq_gemm_static_scratch")
     return out
 
 

@@ -1,0 +1,60 @@
+// Dense GEMM entry point that needs no caller-provided workspace.
+//
+// Its scratch (device status word, Stream-K tile counters and partial sums)
+// lives in one file-scope device array of HQ_STATIC_SCRATCH_BYTES that every
+// GPU loading this library keeps until the process exits.  The call itself
+// allocates nothing.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/hq.h"
+
+namespace {
+
+constexpr size_t kScratchBytes = HQ_STATIC_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+
+// Shared by every call on a device; holds the last call's contents.
+static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
+
+// Device address of g_scratch, looked up once per device (the host-side name
+// of a __device__ array is only a stand-in and must never reach a kernel).
+void* g_scratch_ptr[kMaxDevices] = {nullptr};
+
+hq_status_t scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return HQ_ERR_CUDA;
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return HQ_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return HQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+hq_status_t hq_gemm_static_scratch(const hq_format_t* fmt, const hq_act_t* A, const void* packedW, const void* bias,
+                                   void* C, int64_t M, int64_t N, int64_t K, hq_stream_t stream) {
+  if (!fmt || M < 0 || N < 1) return HQ_ERR_INVALID_ARG;
+  if (M == 0) return HQ_OK;
+  const size_t need = hq_workspace_bytes(fmt, M, 1);
+  if (need == 0) return HQ_ERR_INVALID_ARG;
+  if (need > kScratchBytes) return HQ_ERR_WORKSPACE;  // beyond the fixed scratch: use hq_gemm with a workspace
+  void* ws = nullptr;
+  const hq_status_t st = scratch_address(&ws);
+  if (st != HQ_OK) return st;
+  // The status word and the tile counters (the leading part of the scratch, at
+  // most 4 bytes per 16-row x 128-column tile after a 256-byte header) must
+  // start at zero; clearing more than that is harmless.
+  size_t clear = 256 + 4 * (size_t)((M + 15) / 16) * (size_t)((N + 127) / 128);
+  clear = ((clear + 255) / 256) * 256;
+  if (clear > need) clear = need;
+  if (cudaMemsetAsync(ws, 0, clear, (cudaStream_t)stream) != cudaSuccess) return HQ_ERR_CUDA;
+  return hq_gemm(fmt, A, packedW, bias, C, M, N, K, ws, kScratchBytes, stream);
+}
+
+}  // extern "C"

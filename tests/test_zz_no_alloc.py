@@ -1,0 +1,48 @@
+"""hq_gemm_static_scratch: the dense GEMM for callers that cannot allocate device memory (GPU).
+
+Such callers (a host framework that owns all device memory through its own pool,
+or a latency-critical loop that must not risk a synchronising cudaMalloc) get
+their scratch from a fixed per-GPU array inside the library.  The test calls the
+entry point through the C ABI twice in a row, with different shapes that use
+the scratch differently (split-K partials in both), and checks each result
+against the workspace-taking hq_gemm within the parity tolerance.  It lives in
+its own file, collected last.
+"""
+import pytest
+import torch
+
+from tests import ref_helpers as R
+from workload import make_dense
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(lib, cfg, M, N, K, seed):
+    inp = make_dense(cfg, M, seed=seed, N=N, K=K, with_bias=True)
+    fmt, packed = lib.pack_inputs(inp, "cuda")
+    act = {k: v.cuda() for k, v in inp["a"].items()}
+    bias = inp["bias"].cuda()
+    return fmt, packed, act, bias
+
+
+def test_static_scratch_matches_workspace_call_twice(lib):
+    cases = [("w4a16_asym", 16, 1024, 2048, 1), ("w4a16_asym", 64, 2048, 4096, 2)]
+    for cfg, M, N, K, seed in cases:
+        fmt, packed, act, bias = _case(lib, cfg, M, N, K, seed)
+        assert lib.workspace_bytes(fmt, M) <= 16 << 20
+        y_ref = lib.gemm(fmt, act, packed, M, bias=bias)
+        y = lib.gemm_static_scratch(fmt, act, packed, M, bias=bias)
+        torch.cuda.synchronize()
+        r = R.error_ratio(y, y_ref.double().cpu().numpy())
+        assert r <= 1.0, f"{cfg} M={M}: error ratio {r:.4f} against hq_gemm"
+
+
+def test_static_scratch_rejects_oversized_calls(lib):
+    # 200 tokens over 14336 x 4096 needs ~40 MB of split-K partials: more than the fixed 16 MiB
+    fmt = lib.make_format("uint4_zp", 14336, 4096)
+    assert lib.workspace_bytes(fmt, 200) > 16 << 20
+    act = {"data": torch.zeros(200, 4096, dtype=torch.bfloat16, device="cuda")}
+    packed = torch.zeros(lib.packed_bytes(fmt), dtype=torch.uint8, device="cuda")
+    with pytest.raises(lib.HQError) as e:
+        lib.gemm_static_scratch(fmt, act, packed, 200)
+    assert e.value.code == lib.HQ_ERR_WORKSPACE
