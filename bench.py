@@ -4,10 +4,12 @@ Default workload: dense W4A16 with UINT4 codes + zero points (group 128),
 K=4096, N=14336, swept over M in {1, 16, 64, 256, 1024, 4096, 8192}.  One step
 is one call per M (the whole hot path: repacked weights are resident, every
 call decodes, multiplies and runs the epilogue).  Each call is timed alone with
-CUDA events on its stream after an L2 flush (a write of 2x the L2 size outside
-the event window), as in the microbenchmark protocol of the Humming
-announcement ("Results: kernel microbenchmarks": cold L2, warmed, independent
-samples).
+CUDA events on its stream, with a cold L2 as in the microbenchmark protocol of
+the Humming announcement ("Results: kernel microbenchmarks": cold L2, warmed,
+independent samples): every call reads its own replica of weights, activations
+and output, rotated over enough replicas that their total is far above the L2
+size, so no flush kernel runs (a write flush would leave the L2 full of dirty
+lines whose write-back slows the next kernel's reads).
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload instead.  `--config` selects another
@@ -32,6 +34,7 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # dense tensor-core peaks relative to bf16 (nominal 2.25 / 4.5 / 13.5 PFLOP/s)
 DTYPE_RATIO = {"bf16": 1.0, "fp8": 2.0, "fp4": 6.0}
 PATH_DTYPE = {"int4_sym": "bf16", "uint4_zp": "bf16", "nvfp4": "fp4", "mxfp4": "fp8"}
+SPIN_CYCLES = 400_000  # about 0.2 ms at 2 GHz: longer than the host side of one call
 
 
 def peaks():
@@ -49,7 +52,7 @@ def env_rank():
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -63,12 +66,13 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0=None, t1=None):
+        """Summary of the samples taken between wall times t0 and t1 (all samples if too few)."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -77,65 +81,96 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
+        import datetime
         rows = []
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) >= 9:
-                rows.append(parts)
+            if len(parts) >= 10:
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    ts = None
+                rows.append((ts, parts[1:]))
         if not rows:
             return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        inside = [p for ts, p in rows if ts is not None and t0 is not None and t0 <= ts <= t1]
+        window = "timed region"
+        if len(inside) < 3:
+            inside, window = [p for _, p in rows], "whole run"
+        sm = [float(r[1]) for r in inside if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in inside if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
-        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
-        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "window": window}
 
 
 # ------------------------------------------------------------------ workload
+def replicas_for(touched_min, packed_bytes, l2):
+    """Copies of every input so that a call never finds its data in L2: consecutive reuses of one
+    replica are separated by more than three L2 sizes of other replicas' data."""
+    r = max(2, -(-3 * l2 // max(1, touched_min)))
+    r = min(r, 12, max(2, (40 << 30) // max(1, packed_bytes)))
+    return int(r)
+
+
 def make_calls(cfg_name, seed, device):
-    """Inputs resident on the device for every size of the sweep: [(size, call, info)]."""
+    """Inputs resident on the device for every size of the sweep, R replicas each.
+
+    Returns (fmt, calls, R) with calls = [(size, call(r, stream), info, acts[r], outs[r], wss[r])]."""
     import quantized_gemm_dequant_gb300 as hq
     c = W.CONFIGS[cfg_name]
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
     calls = []
     if c["kind"] == "dense":
         base = W.make_dense(cfg_name, 1, seed=seed, device=device)
         fmt, packed = hq.pack_inputs(base, device)
+        del base
         wbytes = W.weight_bytes(c["wfmt"], c["N"], c["K"], c["G"])
+        R = replicas_for(wbytes, packed.numel(), l2)
+        packs = [packed] + [packed.clone() for _ in range(R - 1)]
         for M in c["sizes"]:
-            a = W.quantize_acts(c["afmt"], W.acts_fp32(seed, M, c["K"], outliers=c["afmt"] == "nvfp4", device=device))
-            ws = hq.make_workspace(fmt, M, 1, device)
-            out = torch.empty((M, c["N"]), dtype=torch.bfloat16, device=device)
+            a0 = W.quantize_acts(c["afmt"], W.acts_fp32(seed, M, c["K"], outliers=c["afmt"] == "nvfp4", device=device))
+            acts = [a0] + [{k: v.clone() for k, v in a0.items()} for _ in range(R - 1)]
+            wss = [hq.make_workspace(fmt, M, 1, device) for _ in range(R)]
+            outs = [torch.empty((M, c["N"]), dtype=torch.bfloat16, device=device) for _ in range(R)]
             info = dict(M=M, flops=W.dense_flops(M, c["N"], c["K"]), weight_bytes=wbytes,
                         total_bytes=wbytes + W.act_bytes(c["afmt"], M, c["K"]) + 2 * M * c["N"],
-                        h2d=sum(t.numel() * t.element_size() for t in a.values()), d2h=2 * M * c["N"])
+                        h2d=sum(t.numel() * t.element_size() for t in a0.values()), d2h=2 * M * c["N"])
 
-            def call(a=a, ws=ws, out=out, M=M, stream=None):
-                return hq.gemm(fmt, a, packed, M, out=out, workspace=ws, stream=stream)
+            def call(r, stream=None, acts=acts, wss=wss, outs=outs, M=M):
+                return hq.gemm(fmt, acts[r], packs[r], M, out=outs[r], workspace=wss[r], stream=stream)
 
-            calls.append((M, call, info, a, out, ws))
-        return fmt, packed, calls
+            calls.append((M, call, info, acts, outs, wss))
+        return fmt, calls, R
     E, k = c["E"], c["topk"]
     base = W.make_moe(cfg_name, 1, seed=seed, device=device)
     fmt, packed = hq.pack_inputs(base, device)
     del base
     per_expert = W.weight_bytes(c["wfmt"], c["N"], c["K"], c["G"])
+    routes = {T: W.zipf_route(seed, T, E, k, device=device) for T in c["sizes"]}
+    hit_min = min(int(torch.unique(ids).numel()) for ids, _ in routes.values())
+    R = replicas_for(per_expert * hit_min, packed.numel(), l2)
+    packs = [packed] + [packed.clone() for _ in range(R - 1)]
     for T in c["sizes"]:
-        a = W.quantize_acts(c["afmt"], W.acts_fp32(seed, T, c["K"], device=device))
-        ids, tw = W.zipf_route(seed, T, E, k, device=device)
+        a0 = W.quantize_acts(c["afmt"], W.acts_fp32(seed, T, c["K"], device=device))
+        ids, tw = routes[T]
         hit = int(torch.unique(ids).numel())
-        ws = hq.make_workspace(fmt, T, k, device)
-        out = torch.empty((T * k, c["N"]), dtype=torch.bfloat16, device=device)
+        acts = [dict(a0, ids=ids, tw=tw)] + [dict({kk: v.clone() for kk, v in a0.items()}, ids=ids.clone(), tw=tw.clone())
+                                             for _ in range(R - 1)]
+        wss = [hq.make_workspace(fmt, T, k, device) for _ in range(R)]
+        outs = [torch.empty((T * k, c["N"]), dtype=torch.bfloat16, device=device) for _ in range(R)]
         info = dict(M=T, flops=2.0 * T * k * c["N"] * c["K"], weight_bytes=per_expert * hit, experts_hit=hit,
                     total_bytes=per_expert * hit + W.act_bytes(c["afmt"], T, c["K"]) + 2 * T * k * c["N"] + 8 * T * k,
-                    h2d=sum(t.numel() * t.element_size() for t in a.values()) + 8 * T * k, d2h=2 * T * k * c["N"])
+                    h2d=sum(t.numel() * t.element_size() for t in a0.values()) + 8 * T * k, d2h=2 * T * k * c["N"])
 
-        def call(a=a, ids=ids, tw=tw, ws=ws, out=out, stream=None):
-            return hq.moe_gemm(fmt, a, packed, ids, tw, out=out, workspace=ws, stream=stream)
+        def call(r, stream=None, acts=acts, wss=wss, outs=outs):
+            a = acts[r]
+            return hq.moe_gemm(fmt, {kk: v for kk, v in a.items() if kk not in ("ids", "tw")}, packs[r], a["ids"],
+                               a["tw"], out=outs[r], workspace=wss[r], stream=stream)
 
-        calls.append((T, call, info, dict(a, ids=ids, tw=tw), out, ws))
-    return fmt, packed, calls
+        calls.append((T, call, info, acts, outs, wss))
+    return fmt, calls, R
 
 
 def roofline_of(info, t_s, pk, dt):
@@ -157,10 +192,9 @@ def run_ours(args):
     pk, pk_src = peaks()
     c = W.CONFIGS[args.config]
     dt = PATH_DTYPE[c["wfmt"]]
-    fmt, packed, calls = make_calls(args.config, args.seed, dev)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    fmt, calls, R = make_calls(args.config, args.seed, dev)
     stream = torch.cuda.current_stream(dev)
+    counter = [0]
 
     def barrier():
         if world > 1:
@@ -170,11 +204,15 @@ def run_ours(args):
 
     def one_step(times):
         for i, (M, call, info, _, _, _) in enumerate(calls):
-            flush.zero_()
+            r = counter[0] % R  # a different replica on every call: cold L2 without a flush kernel
+            counter[0] += 1
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
+            # keep the GPU busy (a spin with no memory traffic) while the host enqueues the call, so the
+            # event window holds the call's GPU work and not the host's launch latency
+            torch.cuda._sleep(SPIN_CYCLES)
             e0.record(stream)
-            call(stream=stream)
+            call(r, stream=stream)
             e1.record(stream)
             times[i].append((e0, e1))
 
@@ -185,21 +223,24 @@ def run_ours(args):
     times = [[] for _ in calls]
     clk = ClockSampler(local)
     clk.start()
+    time.sleep(0.5)  # nvidia-smi needs a moment before its first sample
     barrier()
     t_wall0 = time.perf_counter()
+    t_epoch0 = time.time()
     for _ in range(args.steps):
         one_step(times)
     barrier()
     t_wall = time.perf_counter() - t_wall0
-    clocks = clk.stop()
+    clocks = clk.stop(t_epoch0, time.time())
     per_call_ms = [[a.elapsed_time(b) for a, b in ts] for ts in times]
     step_ms = sum(sum(x) for x in per_call_ms) / args.steps
     # device status must be clean after the run
     import quantized_gemm_dequant_gb300 as hq
-    for (_, _, _, _, _, ws) in calls:
-        st = hq.last_device_status(ws)
-        if st != 0:
-            raise RuntimeError(f"device status {hq.status_string(st)} after the timed run")
+    for (_, _, _, _, _, wss) in calls:
+        for ws in wss:
+            st = hq.last_device_status(ws)
+            if st != 0:
+                raise RuntimeError(f"device status {hq.status_string(st)} after the timed run")
     if world > 1:
         import torch.distributed as dist
         tt = torch.tensor([step_ms], device=dev)
@@ -245,7 +286,8 @@ def run_ours(args):
         "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": dt, "data": "synthetic (seeded Philox draws, quantized by the workload recipe)",
         "config": {"workload": workload_name(args.config), "sizes": c["sizes"],
-                   "l2": "flushed before every call (write of max(2xL2, 256 MB), outside the event window)",
+                   "l2": f"inputs larger than L2: each call reads its own replica of the weights, activations "
+                         f"and output ({R} replicas, rotated; no flush kernel)",
                    "timing": "CUDA events around each call on its stream; step = sum over the sweep",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof, "sweep": sweep, "gpu_launches": gpu_launches(args.config, calls) * args.steps,
@@ -266,6 +308,8 @@ def kernel_name(cfg, M):
     else:
         avg = -(-M * c["topk"] // c["E"])
         bt = 16 if avg <= 16 else 32 if avg <= 32 else 64 if avg <= 64 else 128
+    if path == 0 and bt <= 32 and os.environ.get("HQ_FORCE_PATH") != "umma":
+        return f"hq::hq_gemm_small_kernel<{bt}>"
     return f"hq::hq_gemm_kernel<{path}, {bt}>"
 
 
@@ -300,20 +344,20 @@ def workload_name(cfg):
 def measure_e2e(args, calls, stream, dev):
     """Same sweep through the C ABI with pinned host buffers: H2D of the inputs, the call, D2H of C."""
     hosts = []
-    for (M, call, info, a, out, ws) in calls:
-        ha = {k: v.detach().cpu().pin_memory() for k, v in a.items()}
-        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    for (M, call, info, acts, outs, wss) in calls:
+        ha = {k: v.detach().cpu().pin_memory() for k, v in acts[0].items()}
+        hout = torch.empty(outs[0].shape, dtype=outs[0].dtype).pin_memory()
         hosts.append((ha, hout))
 
     def one(times):
-        for (M, call, info, a, out, ws), (ha, hout) in zip(calls, hosts):
+        for (M, call, info, acts, outs, wss), (ha, hout) in zip(calls, hosts):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             for k, v in ha.items():
-                a[k].copy_(v, non_blocking=True)
-            call(stream=stream)
-            hout.copy_(out, non_blocking=True)
+                acts[0][k].copy_(v, non_blocking=True)
+            call(0, stream=stream)
+            hout.copy_(outs[0], non_blocking=True)
             e1.record(stream)
             times.append((e0, e1))
 
@@ -321,15 +365,16 @@ def measure_e2e(args, calls, stream, dev):
         one([])
     torch.cuda.synchronize(dev)
     ts = []
-    for _ in range(args.steps):
+    steps = min(args.steps, 20)  # every step moves the whole sweep's activations and outputs over PCIe/C2C
+    for _ in range(steps):
         one(ts)
     torch.cuda.synchronize(dev)
-    ms = sum(a.elapsed_time(b) for a, b in ts) / args.steps
+    ms = sum(a.elapsed_time(b) for a, b in ts) / steps
     flops = sum(info["flops"] for (_, _, info, _, _, _) in calls)
     return {"value": round(flops / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(sum(info["h2d"] for (_, _, info, _, _, _) in calls)),
             "d2h_bytes_per_step": int(sum(info["d2h"] for (_, _, info, _, _, _) in calls)),
-            "ms_per_step": round(ms, 4), "note": "weights packed once and resident; per call: H2D of the "
+            "ms_per_step": round(ms, 4), "steps": steps, "note": "weights packed once and resident; per call: H2D of the "
             "activations (pinned), the C-ABI call, D2H of C; no L2 flush"}
 
 
@@ -409,7 +454,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="w4a16_asym", choices=list(W.CONFIGS))

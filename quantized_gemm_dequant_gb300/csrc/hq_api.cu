@@ -152,8 +152,11 @@ Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int
         p.max_tiles = p.n_tiles * (active + (rows + p.bt - 1) / p.bt);
       }
       p.sk = (p.max_tiles < 2 * (int64_t)sms && p.kst > 1) ? 1 : 0;
+    }
+    if (p.small) {  // the register-decode kernel runs two CTAs per SM with 16-token tiles
       const int64_t W = p.max_tiles * (p.sk ? p.kst : 1);
-      p.grid = (int)(W < sms ? (W < 1 ? 1 : W) : sms);
+      const int64_t slots = p.bt <= 16 ? 2 * (int64_t)sms : sms;
+      p.grid = (int)(W < slots ? (W < 1 ? 1 : W) : slots);
     }
   }
   p.off_counters = off;

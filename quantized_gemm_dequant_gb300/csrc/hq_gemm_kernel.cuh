@@ -711,20 +711,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
       if (lane == 0) mbar_arrive(&sh.dempty);
       if (!pc.full) {
         // ---------------------------------------------- Stream-K fix-up (last arriver sums)
-        __threadfence();
-        named_bar_sync(1, NUM_EPI_THREADS);
+        named_bar_sync(1, NUM_EPI_THREADS);  // every partial store of this CTA precedes thread 0's release below
         const int64_t first_it = (int64_t)pc.tile * sched.kst;
         const int c_first = sched.cta_of(first_it);
         const int c_last = sched.cta_of(first_it + sched.kst - 1);
         if (tid == 0) {
           const int nctr = c_last - c_first + 1;
+          __threadfence();  // release this CTA's partials before its arrival is counted
           const int old = atomicAdd(&args.counters[pc.tile], 1);
           sh.fix_last = (old == nctr - 1) ? 1 : 0;
-          if (old == nctr - 1) args.counters[pc.tile] = 0;
+          if (old == nctr - 1) {
+            args.counters[pc.tile] = 0;
+            __threadfence();  // acquire: the other CTAs' partials before the reads below
+          }
         }
         named_bar_sync(1, NUM_EPI_THREADS);
         if (sh.fix_last) {
-          __threadfence();
           // every partial of a column chunk is requested before any is summed: one L2 round trip per chunk
 #pragma unroll 1
           for (int cb = 0; cb < HC; cb += CHUNK) {

@@ -14,7 +14,7 @@
 // exact integers (q - z) in bf16; the group scale multiplies the fp32 group
 // partial after the MMA, so the decode adds no rounding.
 //
-// Warps 0-7 compute (warp w owns rows 16w..16w+15 of the 128-row tile); warp 8
+// Two CTAs per SM for 16-token tiles.  Warps 0-7 compute (warp w owns rows 16w..16w+15 of the 128-row tile); warp 8
 // produces: one bulk copy of the weight block plus the TMA load (dense) or
 // gather4 (MoE) of the token tile for the same 128 K, all on one barrier.
 // Pieces and the Stream-K fix-up are those of the UMMA path.
@@ -27,14 +27,15 @@ constexpr int SM_PROD_WARP = 8;
 
 template <int BT>
 struct SmallCfg {
+  static constexpr int CTAS_PER_SM = BT <= 16 ? 2 : 1;  // 32-token tiles need more registers than two CTAs allow
   static constexpr int W_REGION = 9216;          // one INT4 block (<= 8576 bytes), 1 KB aligned
   static constexpr int ACT_BYTES = 2 * BT * 128;  // two 64-K swizzled atoms
   static constexpr int STAGE = W_REGION + ACT_BYTES;
-  static constexpr int STAGES = (200 * 1024) / STAGE > 16 ? 16 : (200 * 1024) / STAGE;
+  // a ring of about 104 KB, so that two CTAs fit on an SM (no tensor memory here)
+  static constexpr int STAGES = (104 * 1024) / STAGE > 16 ? 16 : (104 * 1024) / STAGE;
   static constexpr int NT = BT / 8;  // 8-token MMA tiles
-  static constexpr int SMEM_RAW = STAGES * STAGE + 1024 + 5120;
-  static constexpr int SMEM_BYTES = SMEM_RAW < 120 * 1024 ? 120 * 1024 : SMEM_RAW;
-  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+  static constexpr int SMEM_BYTES = STAGES * STAGE + 1024 + 5120;
+  static_assert(CTAS_PER_SM * (SMEM_BYTES + 1024) <= 228 * 1024, "CTAs per SM");
 };
 
 struct SmallSmem {
@@ -55,7 +56,7 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
 }
 
 template <int BT>
-__global__ void __launch_bounds__(SM_THREADS, 1) hq_gemm_small_kernel(const __grid_constant__ GemmArgs args) {
+__global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm_small_kernel(const __grid_constant__ GemmArgs args) {
   using C = SmallCfg<BT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -220,11 +221,13 @@ __global__ void __launch_bounds__(SM_THREADS, 1) hq_gemm_small_kernel(const __gr
         const uint32_t zA = args.zp ? (uint32_t)wb[8448 + rA] : 8u;
         const uint32_t zB = args.zp ? (uint32_t)wb[8448 + rB] : 8u;
         const uint32_t zzA = (0x4300u + zA) * 0x00010001u, zzB = (0x4300u + zB) * 0x00010001u;
-        float blk[C::NT][4];
+        float blk[2][C::NT][4];  // even / odd 16-K steps: two independent MMA chains per token tile
 #pragma unroll
-        for (int i = 0; i < C::NT; ++i)
+        for (int u = 0; u < 2; ++u)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) blk[i][j] = 0.0f;
+          for (int i = 0; i < C::NT; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) blk[u][i][j] = 0.0f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {  // 32-K chunk
           const uint4 wa = *reinterpret_cast<const uint4*>(wb + (j * 128 + rA) * 16);
@@ -248,7 +251,7 @@ __global__ void __launch_bounds__(SM_THREADS, 1) hq_gemm_small_kernel(const __gr
               const int c0 = byte >> 4, c1 = (byte + 16) >> 4;
               const uint32_t b0 = *reinterpret_cast<const uint32_t*>(ab + ((c0 ^ (row & 7)) << 4) + (byte & 15));
               const uint32_t b1 = *reinterpret_cast<const uint32_t*>(ab + ((c1 ^ (row & 7)) << 4) + (byte & 15));
-              mma_bf16_16816(blk[n8], a, b0, b1);
+              mma_bf16_16816(blk[s2][n8], a, b0, b1);
             }
           }
         }
@@ -256,10 +259,10 @@ __global__ void __launch_bounds__(SM_THREADS, 1) hq_gemm_small_kernel(const __gr
         if (lane == 0) mbar_arrive(&sh.empty[st]);
 #pragma unroll
         for (int i = 0; i < C::NT; ++i) {
-          acc[i][0] = fmaf(sA, blk[i][0], acc[i][0]);
-          acc[i][1] = fmaf(sA, blk[i][1], acc[i][1]);
-          acc[i][2] = fmaf(sB, blk[i][2], acc[i][2]);
-          acc[i][3] = fmaf(sB, blk[i][3], acc[i][3]);
+          acc[i][0] = fmaf(sA, blk[0][i][0] + blk[1][i][0], acc[i][0]);
+          acc[i][1] = fmaf(sA, blk[0][i][1] + blk[1][i][1], acc[i][1]);
+          acc[i][2] = fmaf(sB, blk[0][i][2] + blk[1][i][2], acc[i][2]);
+          acc[i][3] = fmaf(sB, blk[0][i][3] + blk[1][i][3], acc[i][3]);
         }
         if (++st == C::STAGES) {
           st = 0;
@@ -302,20 +305,22 @@ __global__ void __launch_bounds__(SM_THREADS, 1) hq_gemm_small_kernel(const __gr
           part[col * TILE_N + rB] = acc[i][2];
           part[(col + 1) * TILE_N + rB] = acc[i][3];
         }
-        __threadfence();
-        named_bar_sync(1, 256);
+        named_bar_sync(1, 256);  // every partial store of this CTA precedes thread 0's release below
         const int64_t first_it = (int64_t)pc.tile * sched.kst;
         const int c_first = sched.cta_of(first_it);
         const int c_last = sched.cta_of(first_it + sched.kst - 1);
         if (tid == 0) {
           const int nctr = c_last - c_first + 1;
+          __threadfence();  // release this CTA's partials before its arrival is counted
           const int old = atomicAdd(&args.counters[pc.tile], 1);
           sh.fix_last = (old == nctr - 1) ? 1 : 0;
-          if (old == nctr - 1) args.counters[pc.tile] = 0;
+          if (old == nctr - 1) {
+            args.counters[pc.tile] = 0;
+            __threadfence();  // acquire: the other CTAs' partials before the reads below
+          }
         }
         named_bar_sync(1, 256);
         if (sh.fix_last) {
-          __threadfence();
           float sum[C::NT][4];
 #pragma unroll
           for (int i = 0; i < C::NT; ++i)
