@@ -19,6 +19,9 @@ cudaError_t launch_gemm_int4(const GemmArgs& a, int bt, int grid, cudaStream_t s
 cudaError_t launch_gemm_nvfp4(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_mxfp4(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_small(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
+cudaError_t launch_moe_permute(const int* counts, const int* region, int cap, int E, int topk, int64_t rows,
+                               const void* src, int row_bytes, void* dst, const void* sf_src, int sf_bytes, void* sf_dst,
+                               int* row_off, cudaStream_t stream);
 
 namespace {
 
@@ -76,6 +79,7 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 struct Plan {
   int path = 0;
   int small = 0;  // INT4 with at most 32 tokens per tile: register-decode mma.sync kernel
+  int grouped = 0;  // MoE: routed rows copied into expert-contiguous order first (2-D TMA boxes)
   int bt = 16;
   int sk = 0;
   int grid = 1;
@@ -83,6 +87,7 @@ struct Plan {
   int64_t max_tiles = 0;   // upper bound of tiles (split-K counters)
   int64_t region_cap = 0;  // MoE rows per expert
   size_t off_counts = 0, off_counters = 0, off_region = 0, off_partials = 0, ws_bytes = 0;
+  size_t off_rowoff = 0, off_gact = 0, off_gsf = 0;  // MoE grouped: expert row offsets, rows, NVFP4 scales
 };
 
 int pick_bt_dense(int64_t M) {
@@ -98,6 +103,20 @@ int pick_bt_moe(int64_t rows, int64_t E) {
   if (avg <= 32) return 32;
   if (avg <= 64) return 64;
   return 128;
+}
+
+// HQ_MOE_PATH=indexed|grouped overrides the choice of MoE activation path (tests compare both).
+int forced_moe_path() {
+  const char* v = getenv("HQ_MOE_PATH");
+  if (!v) return 0;
+  if (!strcmp(v, "indexed")) return 1;
+  if (!strcmp(v, "grouped")) return 2;
+  return 0;
+}
+
+// Activation bytes per row and NVFP4 scale bytes per row.
+int64_t act_row_bytes(const hq_format_t* f) {
+  return f->act_type == HQ_A_BF16 ? 2 * f->K : (f->act_type == HQ_A_E4M3_TOKEN ? f->K : f->K / 2);
 }
 
 // HQ_FORCE_PATH=small|umma overrides the choice between the two INT4 kernels (tests compare both).
@@ -164,6 +183,20 @@ Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int
   if (moe) {
     p.off_region = off;
     off = align256(off + sizeof(int) * (size_t)(f->num_experts * (p.region_cap > 0 ? p.region_cap : 1)));
+    // Grouped when tiles are wide: tile::gather4 cannot feed 64+ routed rows per stage fast enough
+    const int fm = forced_moe_path();
+    p.grouped = fm == 2 ? 1 : (fm == 1 ? 0 : (p.bt >= 64 ? 1 : 0));
+    if (p.grouped) {
+      const int64_t rows = M_or_T * topk;
+      p.off_rowoff = off;
+      off = align256(off + sizeof(int) * (size_t)(f->num_experts + 1));
+      p.off_gact = off;
+      off = align256(off + (size_t)(rows * act_row_bytes(f)));
+      if (f->act_type == HQ_A_NVFP4) {
+        p.off_gsf = off;
+        off = align256(off + (size_t)(rows * (f->K / 16)));
+      }
+    }
   }
   if (p.sk) {
     p.off_partials = off;
@@ -339,10 +372,28 @@ hq_status_t hq_moe_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* p
   int* counts = reinterpret_cast<int*>(ws + p.off_counts);
   int* region = reinterpret_cast<int*>(ws + p.off_region);
   GemmArgs a{};
-  if (!act_maps(a, fmt, A, T, p.bt, true)) return HQ_ERR_INVALID_ARG;
+  if (p.grouped) {
+    // the GEMM reads the expert-contiguous copy with BT-row boxes
+    hq_act_t G = *A;
+    G.data = ws + p.off_gact;
+    if (fmt->act_type == HQ_A_NVFP4) G.scale = ws + p.off_gsf;
+    if (!act_maps(a, fmt, &G, T * topk, p.bt, false)) return HQ_ERR_INVALID_ARG;
+  } else if (!act_maps(a, fmt, A, T, p.bt, true)) {
+    return HQ_ERR_INVALID_ARG;
+  }
   cudaError_t err =
       launch_route(topk_ids, T * topk, (int)E, (int)p.region_cap, counts, region, status, (cudaStream_t)stream);
   if (err != cudaSuccess) return HQ_ERR_CUDA;
+  if (p.grouped) {
+    err = launch_moe_permute(counts, region, (int)p.region_cap, (int)E, topk, T * topk, A->data,
+                             (int)act_row_bytes(fmt), ws + p.off_gact,
+                             fmt->act_type == HQ_A_NVFP4 ? A->scale : nullptr, (int)(fmt->K / 16),
+                             fmt->act_type == HQ_A_NVFP4 ? ws + p.off_gsf : nullptr,
+                             reinterpret_cast<int*>(ws + p.off_rowoff), (cudaStream_t)stream);
+    if (err != cudaSuccess) return HQ_ERR_CUDA;
+  }
+  a.grouped = p.grouped;
+  a.row_off = p.grouped ? reinterpret_cast<const int*>(ws + p.off_rowoff) : nullptr;
   a.w = static_cast<const uint8_t*>(packedW);
   a.w_expert_bytes = g.expert_bytes;
   a.w_blk = g.blk_bytes;

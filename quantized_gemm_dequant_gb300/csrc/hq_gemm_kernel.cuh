@@ -67,6 +67,8 @@ struct GemmArgs {
   const int* counts;    // MoE [E] routed rows per expert
   const int* region;    // MoE [E][region_cap] flat (t*topk + j) rows per expert
   int region_cap;
+  int grouped;          // MoE: activations already copied into expert-contiguous rows (2-D boxes, no gather)
+  const int* row_off;   // MoE grouped: first row of each expert in those rows [E + 1]
   int m_tiles;  // dense: token tiles
   int sk;       // 1: Stream-K split over K blocks
   int* status;
@@ -99,7 +101,7 @@ struct Cfg {
   static constexpr int SF_STAGE_COLS = PATH == PATH_NVFP4 ? 16 + 4 * SFB_STEP : 4;
   static constexpr int NA = 4;  // INT4: tensor-memory A slots of 64 columns
   static constexpr int RING_BYTES = SW * W_STAGE + SA * A_STAGE;
-  static constexpr int SMEM_RAW = RING_BYTES + 1024 /*align*/ + 5120 /*barriers, MoE tables*/;
+  static constexpr int SMEM_RAW = RING_BYTES + 1024 /*align*/ + 8192 /*barriers, tile tables, MoE prefix*/;
   // at least 120 KB so that one CTA (and one 512-column tensor-memory allocation) owns each SM
   static constexpr int SMEM_BYTES = SMEM_RAW < 120 * 1024 ? 120 * 1024 : SMEM_RAW;
   static_assert(SA >= 2, "activation ring too small");
@@ -211,6 +213,7 @@ struct Smem {
   int fix_last;
   int tile_prefix_total;
   int rows_tok[256];  // MoE: token index of each row of the activation producer's current tile
+  uint64_t epi_bar;  // bounded barrier of the 8 epilogue warps (Stream-K fix-up)
 };
 
 // Map a global token-tile index to (expert, local token tile) for MoE via the
@@ -229,13 +232,13 @@ __device__ __forceinline__ void moe_locate(const int* prefix, int E, int mt, int
 template <int PATH, int BT>
 __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_constant__ GemmArgs args) {
   using C = Cfg<PATH, BT>;
-  static_assert(sizeof(Smem<PATH, BT>) <= 2048, "shared state");
+  static_assert(sizeof(Smem<PATH, BT>) <= 4096, "shared state");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* wring = smem;                       // SW x W_STAGE
   uint8_t* aring = smem + C::SW * C::W_STAGE;  // SA x A_STAGE
   Smem<PATH, BT>& sh = *reinterpret_cast<Smem<PATH, BT>*>(smem + C::RING_BYTES);
-  int* prefix = reinterpret_cast<int*>(smem + C::RING_BYTES + 2048);  // MoE: E + 1 ints (E <= 512)
+  int* prefix = reinterpret_cast<int*>(smem + C::RING_BYTES + 4096);  // MoE: E + 1 ints (E <= 512)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -262,6 +265,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
     mbar_init(&sh.dfull, 1);
     mbar_init(&sh.dempty, 8);
     mbar_init(&sh.drain, 1);
+    mbar_init(&sh.epi_bar, 8);
     sh.abort_flag = 0;
     fence_mbar_init();
   }
@@ -389,7 +393,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
       if (!ok) return;
       int e, row0, nrows;
       tile_rows(pc.tile, e, row0, nrows);
-      if (args.moe) {
+      int rbase = row0;  // first row of the 2-D box (dense, or grouped MoE)
+      if (args.moe && args.grouped) rbase += args.row_off[e];
+      if (args.moe && !args.grouped) {
         // token index of every row of the tile; rows past the expert's count read zeros (row M)
         for (int i = lane; i < BT; i += 32)
           sh.rows_tok[i] = i < nrows ? args.region[e * args.region_cap + row0 + i] / args.topk : args.M;
@@ -405,27 +411,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
           }
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!ok) return;
-          if (lane == 0) {
-            uint8_t* dst = aring + as * C::A_STAGE;
-            // x offset of this stage in the tensor map's element units (bf16: 64 per stage; bytes: 128)
-            const int x = PATH == PATH_INT4 ? g * 128 + j * 64 : g * 128;
-            mbar_arrive_expect_tx(&sh.a_full[as], A_BOX_BYTES + (PATH == PATH_NVFP4 ? SF_BOX_BYTES : 0));
-            if (!args.moe) {
-              tma_load_2d(dst, &args.tmap_a, x, row0, &sh.a_full[as]);
-              if (PATH == PATH_NVFP4) tma_load_2d(dst + C::ACT_REGION, &args.tmap_sf, g * 16, row0, &sh.a_full[as]);
-            } else {
-#pragma unroll 1
-              for (int i = 0; i < BT; i += 4) {
-                uint8_t* d = dst + (i >> 3) * 1024 + (i & 7) * 128;
-                tma_gather4(d, &args.tmap_a, x, sh.rows_tok[i], sh.rows_tok[i + 1], sh.rows_tok[i + 2],
-                            sh.rows_tok[i + 3], &sh.a_full[as]);
-                if (PATH == PATH_NVFP4)
-                  tma_gather4(dst + C::ACT_REGION + (i >> 2) * 128, &args.tmap_sf, g * 16, sh.rows_tok[i],
-                              sh.rows_tok[i + 1], sh.rows_tok[i + 2], sh.rows_tok[i + 3], &sh.a_full[as]);
-              }
+          uint8_t* dst = aring + as * C::A_STAGE;
+          // x offset of this stage in the tensor map's element units (bf16: 64 per stage; bytes: 128)
+          const int x = PATH == PATH_INT4 ? g * 128 + j * 64 : g * 128;
+          if (lane == 0) mbar_arrive_expect_tx(&sh.a_full[as], A_BOX_BYTES + (PATH == PATH_NVFP4 ? SF_BOX_BYTES : 0));
+          __syncwarp();
+          if (!args.moe || args.grouped) {
+            if (lane == 0) {
+              tma_load_2d(dst, &args.tmap_a, x, rbase, &sh.a_full[as]);
+              if (PATH == PATH_NVFP4) tma_load_2d(dst + C::ACT_REGION, &args.tmap_sf, g * 16, rbase, &sh.a_full[as]);
             }
-            ++armed[as];
+          } else {
+            // routed rows: the warp's lanes issue the four-row gathers in parallel
+            for (int i = lane * 4; i < BT; i += 128) {
+              uint8_t* d = dst + (i >> 3) * 1024 + (i & 7) * 128;
+              tma_gather4(d, &args.tmap_a, x, sh.rows_tok[i], sh.rows_tok[i + 1], sh.rows_tok[i + 2],
+                          sh.rows_tok[i + 3], &sh.a_full[as]);
+              if (PATH == PATH_NVFP4)
+                tma_gather4(dst + C::ACT_REGION + (i >> 2) * 128, &args.tmap_sf, g * 16, sh.rows_tok[i],
+                            sh.rows_tok[i + 1], sh.rows_tok[i + 2], sh.rows_tok[i + 3], &sh.a_full[as]);
+            }
           }
+          if (lane == 0) ++armed[as];
           if (++as == C::SA) {
             as = 0;
             aph ^= 1;
@@ -558,12 +565,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
       tmem_st_x<8>(tmem + lane_base + 256 + 4 * C::SW, ones);
       tmem_wait_st();
     }
+    // CTA-level sync of the 8 epilogue warps on an mbarrier (bounded, abort-aware: never a hang)
+    uint32_t epi_phase = 0;
+    auto epi_sync = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.epi_bar);
+      const bool good = waitf(&sh.epi_bar, epi_phase);
+      epi_phase ^= 1;
+      return good;
+    };
     const bool in_mainloop = !(PATH == PATH_NVFP4 && warp >= 4);
     for_each_piece(sched, [&](const Piece& pc) {
       if (!ok) return;
       int e, row0, nrows;
       tile_rows(pc.tile, e, row0, nrows);
       const int nt = pc.tile % args.n_tiles;
+      // this warp's epilogue columns [col0, col0 + HC): output row and multiplier of each, one per lane
+      // slot, loaded now so that their latency hides behind the mainloop (read back with shuffles)
+      constexpr int HC = BT / 2;
+      constexpr int TPL = (HC + 31) / 32;
+      const int col0 = h * HC;
+      int t_row[TPL];
+      float t_mul[TPL];
+#pragma unroll
+      for (int u = 0; u < TPL; ++u) {
+        const int i = col0 + u * 32 + lane;
+        int orow = -1;
+        float f = 1.0f;
+        if ((args.moe || PATH == PATH_MXFP4) && i < col0 + HC && i < nrows) {
+          int tok;
+          if (args.moe) {
+            orow = args.region[e * args.region_cap + row0 + i];
+            tok = orow / args.topk;
+            if (args.topk_w) f = args.topk_w[orow];
+          } else {
+            orow = row0 + i;
+            tok = orow;
+          }
+          if (PATH == PATH_MXFP4) f *= args.a_scale[tok];
+          if (PATH == PATH_NVFP4) f *= args.a_scale[0] * args.w_gscale[e];
+        }
+        t_row[u] = orow;
+        t_mul[u] = f;
+      }
       // ---------------------------------------------------- mainloop role
       for (int g = pc.g0; in_mainloop && g < pc.g1; ++g) {
         if (!waitf(&sh.w_full[ws], wph)) return;
@@ -621,7 +665,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
 #pragma unroll
                 for (int cc = 0; cc < C::CB; ++cc) {
                   const int j = cc * 32 + lane;
-                  const int off = args.moe ? (j >> 2) * 128 + (j & 3) * 16 : j * 16;
+                  const int off = (args.moe && !args.grouped) ? (j >> 2) * 128 + (j & 3) * 16 : j * 16;
                   b[cc] = *reinterpret_cast<const uint32_t*>(asf + off + t * 4);
                 }
                 tmem_st_x<C::CB>(sf + 16 + t * C::SFB_STEP, b);
@@ -669,29 +713,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
       // ---------------------------------------------------- epilogue
       if (!waitf(&sh.dfull, pidx & 1)) return;
       tc_fence_after();
-      constexpr int HC = BT / 2;  // columns per warp
       constexpr int CHUNK = HC < 16 ? HC : 16;
-      const int col0 = h * HC;
       const int n = nt * TILE_N + r;
-      float post = 1.0f;
-      if (PATH == PATH_NVFP4) post = args.a_scale[0] * args.w_gscale[e];
       const float bias_v = (args.bias && n < args.N) ? bf16_to_f32(args.bias[n]) : 0.0f;
       float* part = args.partials + ((int64_t)pc.slot * BT) * TILE_N;
+      // Dense INT4 / NVFP4 rows need no table.  Otherwise col is warp-uniform and the entry comes from
+      // lane (col - col0) % 32, slot (col - col0) / 32 (slot chosen by selects, so the table stays in registers).
+      constexpr bool kTable = true;
+      const bool use_table = args.moe || PATH == PATH_MXFP4;
+      const float dense_mul = PATH == PATH_NVFP4 ? args.a_scale[0] * args.w_gscale[e] : 1.0f;
       auto store = [&](int col, float acc) {
-        if (col < nrows && n < args.N) {
-          int orow, tok;
-          float f = post;
-          if (args.moe) {
-            orow = args.region[e * args.region_cap + row0 + col];
-            tok = orow / args.topk;
-            if (args.topk_w) f *= args.topk_w[orow];
-          } else {
-            orow = row0 + col;
-            tok = orow;
-          }
-          if (PATH == PATH_MXFP4) f *= args.a_scale[tok];
-          args.c[(int64_t)orow * args.N + n] = f32_to_bf16(acc * f + bias_v);
+        int orow;
+        float mul;
+        if (kTable && use_table) {
+          const int rel = col - col0;
+          const int slot = rel >> 5;
+          int tr = t_row[0];
+          float tm = t_mul[0];
+#pragma unroll
+          for (int u = 1; u < TPL; ++u)
+            if (slot == u) {
+              tr = t_row[u];
+              tm = t_mul[u];
+            }
+          orow = __shfl_sync(0xffffffffu, tr, rel & 31);
+          mul = __shfl_sync(0xffffffffu, tm, rel & 31);
+        } else {
+          orow = col < nrows ? row0 + col : -1;
+          mul = dense_mul;
         }
+        if (orow >= 0 && n < args.N) args.c[(int64_t)orow * args.N + n] = f32_to_bf16(acc * mul + bias_v);
       };
 #pragma unroll 1
       for (int cb = 0; cb < HC; cb += CHUNK) {
@@ -711,7 +762,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
       if (lane == 0) mbar_arrive(&sh.dempty);
       if (!pc.full) {
         // ---------------------------------------------- Stream-K fix-up (last arriver sums)
-        named_bar_sync(1, NUM_EPI_THREADS);  // every partial store of this CTA precedes thread 0's release below
+        if (!epi_sync()) return;  // every partial store of this CTA precedes thread 0's release below
         const int64_t first_it = (int64_t)pc.tile * sched.kst;
         const int c_first = sched.cta_of(first_it);
         const int c_last = sched.cta_of(first_it + sched.kst - 1);
@@ -725,7 +776,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
             __threadfence();  // acquire: the other CTAs' partials before the reads below
           }
         }
-        named_bar_sync(1, NUM_EPI_THREADS);
+        if (!epi_sync()) return;
         if (sh.fix_last) {
           // every partial of a column chunk is requested before any is summed: one L2 round trip per chunk
 #pragma unroll 1

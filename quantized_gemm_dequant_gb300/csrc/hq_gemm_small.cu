@@ -45,6 +45,7 @@ struct SmallSmem {
   int fix_last;
   int tile_prefix_total;
   int rows_tok[32];
+  uint64_t epi_bar;  // bounded barrier of the 8 compute warps (Stream-K fix-up)
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -69,6 +70,7 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
       mbar_init(&sh.full[s], 1);
       mbar_init(&sh.empty[s], 8);
     }
+    mbar_init(&sh.epi_bar, 8);
     sh.abort_flag = 0;
     fence_mbar_init();
   }
@@ -146,7 +148,9 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
       int e, row0, nrows;
       tile_rows(pc.tile, e, row0, nrows);
       const int nt = pc.tile % args.n_tiles;
-      if (args.moe) {
+      int rbase = row0;  // first row of the 2-D box (dense, or grouped MoE)
+      if (args.moe && args.grouped) rbase += args.row_off[e];
+      if (args.moe && !args.grouped) {
         for (int i = lane; i < BT; i += 32)
           sh.rows_tok[i] = i < nrows ? args.region[e * args.region_cap + row0 + i] / args.topk : args.M;
         __syncwarp();
@@ -159,23 +163,23 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) return;
+        uint8_t* base = smem + st * C::STAGE;
+        uint8_t* act = base + C::W_REGION;
         if (lane == 0) {
-          uint8_t* base = smem + st * C::STAGE;
-          uint8_t* act = base + C::W_REGION;
           mbar_arrive_expect_tx(&sh.full[st], (uint32_t)args.w_blk + C::ACT_BYTES);
           bulk_g2s(base, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk, &sh.full[st]);
-          for (int j = 0; j < 2; ++j) {
-            uint8_t* dst = act + j * (BT * 128);
-            if (!args.moe) {
-              tma_load_2d(dst, &args.tmap_a, g * 128 + j * 64, row0, &sh.full[st]);
-            } else {
-#pragma unroll 1
-              for (int i = 0; i < BT; i += 4)
-                tma_gather4(dst + (i >> 3) * 1024 + (i & 7) * 128, &args.tmap_a, g * 128 + j * 64, sh.rows_tok[i],
-                            sh.rows_tok[i + 1], sh.rows_tok[i + 2], sh.rows_tok[i + 3], &sh.full[st]);
-            }
-          }
+          if (!args.moe || args.grouped)
+            for (int j = 0; j < 2; ++j)
+              tma_load_2d(act + j * (BT * 128), &args.tmap_a, g * 128 + j * 64, rbase, &sh.full[st]);
           ++armed[st];
+        }
+        if (args.moe && !args.grouped) {
+          __syncwarp();  // the expected bytes are posted before any gather can complete
+          // lane l gathers rows 4l..4l+3 of one 64-K atom: BT / 4 lanes per atom
+          const int i = (lane * 4) % BT, j = (lane * 4) / BT;
+          if (j < 2)
+            tma_gather4(act + j * (BT * 128) + (i >> 3) * 1024 + (i & 7) * 128, &args.tmap_a, g * 128 + j * 64,
+                        sh.rows_tok[i], sh.rows_tok[i + 1], sh.rows_tok[i + 2], sh.rows_tok[i + 3], &sh.full[st]);
         }
         if (++st == C::STAGES) {
           st = 0;
@@ -198,6 +202,18 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
     int st = 0;
     uint32_t ph = 0;
     bool ok = true;
+    // CTA-level sync of the 8 compute warps on an mbarrier (bounded, abort-aware: never a hang)
+    uint32_t epi_phase = 0;
+    auto epi_sync = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.epi_bar);
+      if (!mbar_wait(&sh.epi_bar, epi_phase, abort_flag, WAIT_LIMIT_NS)) {
+        fail(ERR_TIMEOUT);
+        ok = false;
+      }
+      epi_phase ^= 1;
+      return ok;
+    };
     for_each_piece(sched, [&](const Piece& pc) {
       if (!ok) return;
       int e, row0, nrows;
@@ -208,6 +224,28 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
       for (int i = 0; i < C::NT; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+      // output row and multiplier of this lane's token columns (i*8 + 2t, +1), loaded now so that their
+      // latency hides behind the mainloop
+      int t_row[C::NT][2];
+      float t_mul[C::NT][2];
+#pragma unroll
+      for (int i = 0; i < C::NT; ++i)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int col = i * 8 + 2 * t4 + u;
+          int orow = -1;
+          float f = 1.0f;
+          if (col < nrows) {
+            if (args.moe) {
+              orow = args.region[e * args.region_cap + row0 + col];
+              if (args.topk_w) f = args.topk_w[orow];
+            } else {
+              orow = row0 + col;
+            }
+          }
+          t_row[i][u] = orow;
+          t_mul[i][u] = f;
+        }
       for (int g = pc.g0; g < pc.g1; ++g) {
         if (!mbar_wait(&sh.full[st], ph, abort_flag, WAIT_LIMIT_NS)) {
           fail(ERR_TIMEOUT);
@@ -272,28 +310,20 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
       // ---------------------------------------------------- epilogue
       const float biasA = (args.bias && nt * TILE_N + rA < args.N) ? bf16_to_f32(args.bias[nt * TILE_N + rA]) : 0.f;
       const float biasB = (args.bias && nt * TILE_N + rB < args.N) ? bf16_to_f32(args.bias[nt * TILE_N + rB]) : 0.f;
-      auto store = [&](int col, int r, float v, float bias) {
+      // (i, u): token tile i, column 2t + u of it (compile-time after unrolling)
+      auto store = [&](int i, int u, int r, float v, float bias) {
         const int n = nt * TILE_N + r;
-        if (col < nrows && n < args.N) {
-          int orow;
-          float f = 1.0f;
-          if (args.moe) {
-            orow = args.region[e * args.region_cap + row0 + col];
-            if (args.topk_w) f = args.topk_w[orow];
-          } else {
-            orow = row0 + col;
-          }
-          args.c[(int64_t)orow * args.N + n] = f32_to_bf16(v * f + bias);
-        }
+        const int orow = t_row[i][u];
+        if (orow >= 0 && n < args.N) args.c[(int64_t)orow * args.N + n] = f32_to_bf16(v * t_mul[i][u] + bias);
       };
+
       if (pc.full) {
 #pragma unroll
         for (int i = 0; i < C::NT; ++i) {
-          const int col = i * 8 + 2 * t4;
-          store(col, rA, acc[i][0], biasA);
-          store(col + 1, rA, acc[i][1], biasA);
-          store(col, rB, acc[i][2], biasB);
-          store(col + 1, rB, acc[i][3], biasB);
+          store(i, 0, rA, acc[i][0], biasA);
+          store(i, 1, rA, acc[i][1], biasA);
+          store(i, 0, rB, acc[i][2], biasB);
+          store(i, 1, rB, acc[i][3], biasB);
         }
       } else {
         float* part = args.partials + ((int64_t)pc.slot * BT) * TILE_N;
@@ -305,7 +335,7 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
           part[col * TILE_N + rB] = acc[i][2];
           part[(col + 1) * TILE_N + rB] = acc[i][3];
         }
-        named_bar_sync(1, 256);  // every partial store of this CTA precedes thread 0's release below
+        if (!epi_sync()) return;  // every partial store of this CTA precedes thread 0's release below
         const int64_t first_it = (int64_t)pc.tile * sched.kst;
         const int c_first = sched.cta_of(first_it);
         const int c_last = sched.cta_of(first_it + sched.kst - 1);
@@ -319,7 +349,7 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
             __threadfence();  // acquire: the other CTAs' partials before the reads below
           }
         }
-        named_bar_sync(1, 256);
+        if (!epi_sync()) return;
         if (sh.fix_last) {
           float sum[C::NT][4];
 #pragma unroll
@@ -345,11 +375,10 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
           }
 #pragma unroll
           for (int i = 0; i < C::NT; ++i) {
-            const int col = i * 8 + 2 * t4;
-            store(col, rA, sum[i][0], biasA);
-            store(col + 1, rA, sum[i][1], biasA);
-            store(col, rB, sum[i][2], biasB);
-            store(col + 1, rB, sum[i][3], biasB);
+            store(i, 0, rA, sum[i][0], biasA);
+            store(i, 1, rA, sum[i][1], biasA);
+            store(i, 0, rB, sum[i][2], biasB);
+            store(i, 1, rB, sum[i][3], biasB);
           }
         }
       }

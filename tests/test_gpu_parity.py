@@ -256,3 +256,25 @@ def test_int4_kernels_agree_exactly_on_integer_inputs(lib, monkeypatch):
         outs.append(_run_dense(lib, inp).cpu())
     assert torch.equal(outs[0], outs[1])
     assert torch.equal(outs[0], _bf16_rne(R.dense_ref(inp)))
+
+
+# ------------------------------------------------------------------ MoE: indexed (gather4) and grouped (permuted) paths
+@pytest.mark.parametrize("moe_path", ["indexed", "grouped"])
+@pytest.mark.parametrize("wfmt", list(MOE_FORMS))
+@pytest.mark.parametrize("T", [3, 150])
+def test_moe_activation_paths(lib, monkeypatch, moe_path, wfmt, T):
+    """HQ_MOE_PATH forces the row gather (Indexed) or the expert-contiguous copy (Grouped); both match the oracle."""
+    monkeypatch.setenv("HQ_MOE_PATH", moe_path)
+    inp = make_moe(MOE_FORMS[wfmt], T, seed=7 + T, E=6, N=256, K=512, topk=3)
+    R.assert_parity(_run_moe(lib, inp), R.moe_ref(inp), f"moe {wfmt} T={T} {moe_path}")
+
+
+def test_moe_grouped_wide_tiles_match_indexed(lib, monkeypatch):
+    """Wide token tiles (200 rows per expert) through both activation paths give the same bits."""
+    inp = make_moe(MOE_FORMS["int4_sym"], 400, seed=9, E=4, N=256, K=512, topk=2)
+    outs = []
+    for moe_path in ("indexed", "grouped"):
+        monkeypatch.setenv("HQ_MOE_PATH", moe_path)
+        outs.append(_run_moe(lib, inp).cpu())
+    assert torch.equal(outs[0], outs[1])
+    R.assert_parity(outs[1], R.moe_ref(inp), "grouped wide tiles")
