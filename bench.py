@@ -106,9 +106,14 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ workload
+REPLICAS_OVERRIDE = None  # --replicas (profiling runs keep the device footprint small)
+
+
 def replicas_for(touched_min, packed_bytes, l2):
     """Copies of every input so that a call never finds its data in L2: consecutive reuses of one
     replica are separated by more than three L2 sizes of other replicas' data."""
+    if REPLICAS_OVERRIDE:
+        return REPLICAS_OVERRIDE
     r = max(2, -(-3 * l2 // max(1, touched_min)))
     r = min(r, 12, max(2, (40 << 30) // max(1, packed_bytes)))
     return int(r)
@@ -318,8 +323,22 @@ def gpu_launches(cfg, calls):
     return len(calls) * (1 if W.CONFIGS[cfg]["kind"] == "dense" else 2)
 
 
+def kernel_source_hash():
+    """sha256 over the CUDA sources: DRAM counters recorded for another version of them are stale."""
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "quantized_gemm_dequant_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_of(kernel, cfg):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if one matches this build."""
+    """DRAM bytes per launch of `kernel` from the committed ncu summary (profiles/traffic.json), or None
+    when there is none or it was taken on other kernel sources."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -327,7 +346,9 @@ def traffic_of(kernel, cfg):
         with open(p) as f:
             d = json.load(f)
         e = d.get(cfg, {}).get(kernel)
-        return e.get("dram_bytes_per_launch") if e else None
+        if not e or e.get("source_hash") != kernel_source_hash():
+            return None
+        return e.get("dram_bytes_per_launch")
     except Exception:
         return None
 
@@ -462,7 +483,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--sizes", default=None, help="comma list overriding the sweep (profiling)")
+    ap.add_argument("--replicas", type=int, default=None, help="input replicas (default: enough to exceed L2)")
+    ap.add_argument("--source-hash", action="store_true", help="print the kernel-source hash and exit")
     args = ap.parse_args()
+    if args.source_hash:
+        print(kernel_source_hash())
+        return
+    global REPLICAS_OVERRIDE
+    REPLICAS_OVERRIDE = args.replicas
     if args.sizes:
         W.CONFIGS[args.config] = dict(W.CONFIGS[args.config], sizes=[int(x) for x in args.sizes.split(",")])
     args.warmup = max(3, args.warmup) if args.impl == "ours" else args.warmup
