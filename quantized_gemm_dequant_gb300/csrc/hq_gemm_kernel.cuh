@@ -123,6 +123,12 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
 __device__ __forceinline__ uint16_t f32_to_bf16(float x) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
+// two floats -> bf16x2 (round to nearest even); lo holds a
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(b), "f"(a));
+  return d;
+}
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
 
 template <int X>
@@ -575,42 +581,55 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
       return good;
     };
     const bool in_mainloop = !(PATH == PATH_NVFP4 && warp >= 4);
-    for_each_piece(sched, [&](const Piece& pc) {
-      if (!ok) return;
-      int e, row0, nrows;
-      tile_rows(pc.tile, e, row0, nrows);
-      const int nt = pc.tile % args.n_tiles;
+    constexpr int HC = BT / 2;
+    // Per-column output rows and multipliers: MoE rows and per-token activation scales.  INT4 and NVFP4
+    // tiles of 256 tokens are dense only (the host tiles MoE rows by at most 128), so they carry no table.
+    constexpr bool kTables = PATH == PATH_MXFP4 || BT <= 128;
+    constexpr int TPL = kTables ? (HC + 31) / 32 : 1;
+    const int col0 = h * HC;
+    if (!kTables && args.moe) {
+      fail(ERR_BAD_ROUTING);
+      ok = false;
+    }
+    // What a piece's epilogue needs, gathered when its mainloop starts.
+    struct Pend {
+      Piece pc;
+      int e, row0, nrows, nt;
       // this warp's epilogue columns [col0, col0 + HC): output row and multiplier of each, one per lane
-      // slot, loaded now so that their latency hides behind the mainloop (read back with shuffles)
-      constexpr int HC = BT / 2;
-      constexpr int TPL = (HC + 31) / 32;
-      const int col0 = h * HC;
+      // slot, loaded early so that their latency hides behind the mainloop (read back with shuffles)
       int t_row[TPL];
       float t_mul[TPL];
+    };
+    auto open_piece = [&](const Piece& pc, Pend& pd) {
+      pd.pc = pc;
+      tile_rows(pc.tile, pd.e, pd.row0, pd.nrows);
+      pd.nt = pc.tile % args.n_tiles;
 #pragma unroll
       for (int u = 0; u < TPL; ++u) {
         const int i = col0 + u * 32 + lane;
         int orow = -1;
         float f = 1.0f;
-        if ((args.moe || PATH == PATH_MXFP4) && i < col0 + HC && i < nrows) {
+        if (kTables && (args.moe || PATH == PATH_MXFP4) && i < col0 + HC && i < pd.nrows) {
           int tok;
           if (args.moe) {
-            orow = args.region[e * args.region_cap + row0 + i];
+            orow = args.region[pd.e * args.region_cap + pd.row0 + i];
             tok = orow / args.topk;
             if (args.topk_w) f = args.topk_w[orow];
           } else {
-            orow = row0 + i;
+            orow = pd.row0 + i;
             tok = orow;
           }
           if (PATH == PATH_MXFP4) f *= args.a_scale[tok];
-          if (PATH == PATH_NVFP4) f *= args.a_scale[0] * args.w_gscale[e];
+          if (PATH == PATH_NVFP4) f *= args.a_scale[0] * args.w_gscale[pd.e];
         }
-        t_row[u] = orow;
-        t_mul[u] = f;
+        pd.t_row[u] = orow;
+        pd.t_mul[u] = f;
       }
-      // ---------------------------------------------------- mainloop role
-      for (int g = pc.g0; in_mainloop && g < pc.g1; ++g) {
-        if (!waitf(&sh.w_full[ws], wph)) return;
+    };
+    // mainloop role for the next nblk weight blocks, in ring order
+    auto mainloop = [&](int nblk) -> bool {
+      for (int k = 0; in_mainloop && k < nblk; ++k) {
+        if (!waitf(&sh.w_full[ws], wph)) return false;
         uint8_t* wb = wring + ws * C::W_STAGE;
         if (PATH == PATH_INT4) {
           const uint32_t s16 = reinterpret_cast<const uint16_t*>(wb + 8192)[r];
@@ -623,7 +642,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
             raw[jj] = *reinterpret_cast<const uint4*>(wb + ((2 * h + jj) * 128 + r) * 16);
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh.w_empty[ws]);
-          if (!waitf(&sh.aempty[aslot], aslph ^ 1)) return;
+          if (!waitf(&sh.aempty[aslot], aslph ^ 1)) return false;
           tc_fence_after();
 #pragma unroll
           for (int jj = 0; jj < 2; ++jj) {
@@ -657,7 +676,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
               for (int j = 0; j < 16; ++j) v[j] = wsf[j * 32 + lane];
               const uint32_t sf = tmem + lane_base + 256 + ws * C::SF_STAGE_COLS;
               tmem_st_x<16>(sf, v);
-              if (!waitf(&sh.a_full[as], aph)) return;
+              if (!waitf(&sh.a_full[as], aph)) return false;
               const uint8_t* asf = aring + as * C::A_STAGE + C::ACT_REGION;
 #pragma unroll
               for (int t = 0; t < 4; ++t) {
@@ -710,22 +729,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
           wph ^= 1;
         }
       }
+      return ok;
+    };
+    auto epilogue = [&](const Pend& pd) -> bool {
+      const Piece& pc = pd.pc;
+      const int e = pd.e, row0 = pd.row0, nrows = pd.nrows, nt = pd.nt;
+      const int* t_row = pd.t_row;
+      const float* t_mul = pd.t_mul;
       // ---------------------------------------------------- epilogue
-      if (!waitf(&sh.dfull, pidx & 1)) return;
+      if (!waitf(&sh.dfull, pidx & 1)) return false;
       tc_fence_after();
+      // This warp's whole column range goes to registers first: tensor memory is handed back to the next
+      // tile's MMAs before any global store is issued.
       constexpr int CHUNK = HC < 16 ? HC : 16;
+      uint32_t v[HC];
+#pragma unroll
+      for (int cb = 0; cb < HC; cb += CHUNK) {
+        if (CHUNK == 16) tmem_ld16(tmem + lane_base + col0 + cb, *reinterpret_cast<uint32_t(*)[16]>(v + cb));
+        else tmem_ld8(tmem + lane_base + col0 + cb, *reinterpret_cast<uint32_t(*)[8]>(v + cb));
+      }
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.dempty);
       const int n = nt * TILE_N + r;
       const float bias_v = (args.bias && n < args.N) ? bf16_to_f32(args.bias[n]) : 0.0f;
       float* part = args.partials + ((int64_t)pc.slot * BT) * TILE_N;
       // Dense INT4 / NVFP4 rows need no table.  Otherwise col is warp-uniform and the entry comes from
       // lane (col - col0) % 32, slot (col - col0) / 32 (slot chosen by selects, so the table stays in registers).
-      constexpr bool kTable = true;
-      const bool use_table = args.moe || PATH == PATH_MXFP4;
+      const bool use_table = kTables && (args.moe || PATH == PATH_MXFP4);
       const float dense_mul = PATH == PATH_NVFP4 ? args.a_scale[0] * args.w_gscale[e] : 1.0f;
       auto store = [&](int col, float acc) {
         int orow;
         float mul;
-        if (kTable && use_table) {
+        if (use_table) {
           const int rel = col - col0;
           const int slot = rel >> 5;
           int tr = t_row[0];
@@ -744,25 +781,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
         }
         if (orow >= 0 && n < args.N) args.c[(int64_t)orow * args.N + n] = f32_to_bf16(acc * mul + bias_v);
       };
-#pragma unroll 1
-      for (int cb = 0; cb < HC; cb += CHUNK) {
-        uint32_t v[CHUNK];
-        if (CHUNK == 16) tmem_ld16(tmem + lane_base + col0 + cb, *reinterpret_cast<uint32_t(*)[16]>(v));
-        else tmem_ld8(tmem + lane_base + col0 + cb, *reinterpret_cast<uint32_t(*)[8]>(v));
-        tmem_wait_ld();
+      if (!pc.full) {
 #pragma unroll
-        for (int j = 0; j < CHUNK; ++j) {
-          const int col = col0 + cb + j;
-          if (!pc.full) part[col * TILE_N + r] = __uint_as_float(v[j]);
-          else store(col, __uint_as_float(v[j]));
+        for (int j = 0; j < HC; ++j) part[(col0 + j) * TILE_N + r] = __uint_as_float(v[j]);
+      } else if (!use_table && (args.N & 1) == 0 && (reinterpret_cast<uintptr_t>(args.c) & 3) == 0) {
+        // Dense rows, even N: lanes 2i and 2i+1 swap one value per pair of tokens, so that every lane writes
+        // two adjacent outputs (n, n+1) of one token with a single 4-byte store: the even lane token col, the
+        // odd lane token col + 1.
+        const bool odd = lane & 1;
+        const int n_even = n & ~1;
+#pragma unroll
+        for (int j = 0; j < HC; j += 2) {
+          const int col = col0 + j;
+          const uint32_t pk = pack_bf16x2(__uint_as_float(v[j]) * dense_mul + bias_v,
+                                          __uint_as_float(v[j + 1]) * dense_mul + bias_v);  // lo: col, hi: col+1
+          const uint32_t recv = __shfl_xor_sync(0xffffffffu, odd ? (pk & 0xFFFFu) : (pk >> 16), 1);
+          const uint32_t out = odd ? (recv | (pk & 0xFFFF0000u)) : ((pk & 0xFFFFu) | (recv << 16));
+          const int tok = col + (odd ? 1 : 0);
+          if (tok < nrows && n_even < args.N)
+            *reinterpret_cast<uint32_t*>(args.c + (int64_t)(row0 + tok) * args.N + n_even) = out;
         }
+      } else {
+#pragma unroll
+        for (int j = 0; j < HC; ++j) store(col0 + j, __uint_as_float(v[j]));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.dempty);
       if (!pc.full) {
         // ---------------------------------------------- Stream-K fix-up (last arriver sums)
-        if (!epi_sync()) return;  // every partial store of this CTA precedes thread 0's release below
+        if (!epi_sync()) return false;  // every partial store of this CTA precedes thread 0's release below
         const int64_t first_it = (int64_t)pc.tile * sched.kst;
         const int c_first = sched.cta_of(first_it);
         const int c_last = sched.cta_of(first_it + sched.kst - 1);
@@ -776,7 +821,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
             __threadfence();  // acquire: the other CTAs' partials before the reads below
           }
         }
-        if (!epi_sync()) return;
+        if (!epi_sync()) return false;
         if (sh.fix_last) {
           // every partial of a column chunk is requested before any is summed: one L2 round trip per chunk
 #pragma unroll 1
@@ -814,7 +859,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
         }
       }
       ++pidx;
+      return ok;
+    };
+    // A piece's epilogue runs after the first blocks of the next piece are prepared, so that the MMA finds
+    // them ready as soon as the accumulator is released (the last ring slot frees only with the accumulator).
+    constexpr int PREFILL = (PATH == PATH_INT4 ? C::NA : C::SW) - 1;
+    Pend prev;
+    bool has_prev = false;
+    for_each_piece(sched, [&](const Piece& pc) {
+      if (!ok) return;
+      Pend cur;
+      open_piece(pc, cur);
+      const int nblk = pc.g1 - pc.g0;
+      const int pre = nblk < PREFILL ? nblk : PREFILL;
+      if (!mainloop(pre)) return;
+      if (has_prev && !epilogue(prev)) return;
+      if (!mainloop(nblk - pre)) return;
+      prev = cur;
+      has_prev = true;
     });
+    if (ok && has_prev) epilogue(prev);
   }
 
   // ---------------------------------------------------------------- teardown
