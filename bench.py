@@ -3,13 +3,15 @@
 Default workload: dense W4A16 with UINT4 codes + zero points (group 128),
 K=4096, N=14336, swept over M in {1, 16, 64, 256, 1024, 4096, 8192}.  One step
 is one call per M (the whole hot path: repacked weights are resident, every
-call decodes, multiplies and runs the epilogue).  Each call is timed alone with
-CUDA events on its stream, with a cold L2 as in the microbenchmark protocol of
-the Humming announcement ("Results: kernel microbenchmarks": cold L2, warmed,
-independent samples): every call reads its own replica of weights, activations
-and output, rotated over enough replicas that their total is far above the L2
-size, so no flush kernel runs (a write flush would leave the L2 full of dirty
-lines whose write-back slows the next kernel's reads).
+call decodes, multiplies and runs the epilogue).  Calls of one size are timed
+as bursts of back-to-back launches with CUDA events on their stream (the way
+the GEMMs of a decode step follow one another), with a cold L2 as in the
+microbenchmark protocol of the Humming announcement ("Results: kernel
+microbenchmarks": cold L2, warmed, independent samples): every call reads its
+own replica of weights, activations and output, rotated over enough replicas
+that their total is far above the L2 size, so no flush kernel runs (a write
+flush would leave the L2 full of dirty lines whose write-back slows the next
+kernel's reads).
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload instead.  `--config` selects another
@@ -34,7 +36,7 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # dense tensor-core peaks relative to bf16 (nominal 2.25 / 4.5 / 13.5 PFLOP/s)
 DTYPE_RATIO = {"bf16": 1.0, "fp8": 2.0, "fp4": 6.0}
 PATH_DTYPE = {"int4_sym": "bf16", "uint4_zp": "bf16", "nvfp4": "fp4", "mxfp4": "fp8"}
-SPIN_CYCLES = 400_000  # about 0.2 ms at 2 GHz: longer than the host side of one call
+SPIN_CYCLES = 1_000_000  # about 0.5 ms at 2 GHz: longer than the host side of one burst of calls
 
 
 def peaks():
@@ -207,23 +209,32 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    def one_step(times):
-        for i, (M, call, info, _, _, _) in enumerate(calls):
-            r = counter[0] % R  # a different replica on every call: cold L2 without a flush kernel
-            counter[0] += 1
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            # keep the GPU busy (a spin with no memory traffic) while the host enqueues the call, so the
-            # event window holds the call's GPU work and not the host's launch latency
-            torch.cuda._sleep(SPIN_CYCLES)
-            e0.record(stream)
-            call(r, stream=stream)
-            e1.record(stream)
-            times[i].append((e0, e1))
+    burst = R if args.burst is None else max(1, args.burst)
+
+    def run_steps(n_steps, times):
+        # n_steps steps, one call per size each.  Calls of a size run in bursts of back-to-back launches (as
+        # the layers of a decode step do), each on the next input replica; a burst's event window holds
+        # `count` calls of one size.
+        done = 0
+        while done < n_steps:
+            count = min(burst, n_steps - done)
+            for i, (M, call, info, _, _, _) in enumerate(calls):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                # keep the GPU busy (a spin with no memory traffic) while the host enqueues the burst, so the
+                # event window holds the calls' GPU work and not the host's launch latency
+                torch.cuda._sleep(SPIN_CYCLES)
+                e0.record(stream)
+                for _ in range(count):
+                    r = counter[0] % R  # a different replica on every call: cold L2 without a flush kernel
+                    counter[0] += 1
+                    call(r, stream=stream)
+                e1.record(stream)
+                times[i].append((e0, e1, count))
+            done += count
 
     warm = [[] for _ in calls]
-    for _ in range(args.warmup):
-        one_step(warm)
+    run_steps(args.warmup, warm)
     barrier()
     times = [[] for _ in calls]
     clk = ClockSampler(local)
@@ -232,13 +243,14 @@ def run_ours(args):
     barrier()
     t_wall0 = time.perf_counter()
     t_epoch0 = time.time()
-    for _ in range(args.steps):
-        one_step(times)
+    run_steps(args.steps, times)
     barrier()
     t_wall = time.perf_counter() - t_wall0
     clocks = clk.stop(t_epoch0, time.time())
-    per_call_ms = [[a.elapsed_time(b) for a, b in ts] for ts in times]
-    step_ms = sum(sum(x) for x in per_call_ms) / args.steps
+    # per size: the mean time of one call in each burst, and the weight (calls) of that burst
+    per_call_ms = [[a.elapsed_time(b) / n for a, b, n in ts] for ts in times]
+    per_call_n = [[n for _, _, n in ts] for ts in times]
+    step_ms = sum(sum(a.elapsed_time(b) for a, b, _ in ts) for ts in times) / args.steps
     # device status must be clean after the run
     import quantized_gemm_dequant_gb300 as hq
     for (_, _, _, _, _, wss) in calls:
@@ -255,7 +267,7 @@ def run_ours(args):
     value = world * flops_step / (step_ms * 1e-3) / 1e12
 
     sweep, by_kernel = [], {}
-    for (M, _, info, _, _, _), ms in zip(calls, per_call_ms):
+    for (M, _, info, _, _, _), ms, ns in zip(calls, per_call_ms, per_call_n):
         t = statistics.median(ms) * 1e-3
         bound, frac = roofline_of(info, t, pk, dt)
         e = dict(M=M, us=round(t * 1e6, 2), tflops=round(info["flops"] / t / 1e12, 3),
@@ -266,10 +278,10 @@ def run_ours(args):
         sweep.append(e)
         key = kernel_name(args.config, M)
         k = by_kernel.setdefault(key, dict(flops=0.0, bytes=0.0, t=0.0, n=0))
-        k["flops"] += info["flops"] * len(ms)
-        k["bytes"] += info["total_bytes"] * len(ms)
-        k["t"] += sum(ms) * 1e-3
-        k["n"] += len(ms)
+        k["flops"] += info["flops"] * sum(ns)
+        k["bytes"] += info["total_bytes"] * sum(ns)
+        k["t"] += sum(m * n for m, n in zip(ms, ns)) * 1e-3
+        k["n"] += sum(ns)
     dom = max(by_kernel, key=lambda k: by_kernel[k]["t"])
     d = by_kernel[dom]
     tc_peak = pk["bf16_tflops"] * DTYPE_RATIO[dt]
@@ -293,7 +305,9 @@ def run_ours(args):
         "config": {"workload": workload_name(args.config), "sizes": c["sizes"],
                    "l2": f"inputs larger than L2: each call reads its own replica of the weights, activations "
                          f"and output ({R} replicas, rotated; no flush kernel)",
-                   "timing": "CUDA events around each call on its stream; step = sum over the sweep",
+                   "timing": f"CUDA events around bursts of {burst} back-to-back calls of one size on their "
+                             f"stream (each call on its own replica), divided by the burst length; step = one call "
+                             f"per size",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof, "sweep": sweep, "gpu_launches": gpu_launches(args.config, calls) * args.steps,
         "clocks": clocks, "wall_s_timed": round(t_wall, 3), "e2e": e2e, "cpu_baseline": cpu,
@@ -475,7 +489,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="w4a16_asym", choices=list(W.CONFIGS))
@@ -484,6 +498,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--sizes", default=None, help="comma list overriding the sweep (profiling)")
     ap.add_argument("--replicas", type=int, default=None, help="input replicas (default: enough to exceed L2)")
+    ap.add_argument("--burst", type=int, default=None, help="back-to-back calls per timed window (default: replicas)")
     ap.add_argument("--source-hash", action="store_true", help="print the kernel-source hash and exit")
     args = ap.parse_args()
     if args.source_hash:

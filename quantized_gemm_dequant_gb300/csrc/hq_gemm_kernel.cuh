@@ -200,6 +200,25 @@ __device__ __forceinline__ void for_each_piece(const Sched& s, F&& f) {
   }
 }
 
+// Dense: L2 prefetch of the first `limit` weight blocks of this CTA's pieces, in the order its producer loads
+// them.  Issued before pdl_wait, so the stream of weights starts while the previous kernel finishes.
+__device__ __forceinline__ void prefetch_dense_weights(const GemmArgs& args, int limit) {
+  Sched s;
+  s.tiles = args.m_tiles * args.n_tiles;
+  s.kst = args.kst;
+  s.W = (int64_t)s.tiles * s.kst;
+  s.P = args.sk ? (int)((int64_t)gridDim.x < s.W ? gridDim.x : s.W) : (int)gridDim.x;
+  s.cta = blockIdx.x;
+  s.sk = args.sk;
+  if ((int)blockIdx.x >= s.P || s.tiles <= 0) return;
+  int left = limit;
+  for_each_piece(s, [&](const Piece& pc) {
+    const uint8_t* wblk = args.w + ((int64_t)(pc.tile % args.n_tiles) * args.kst) * args.w_blk;
+    for (int g = pc.g0; g < pc.g1 && left > 0; ++g, --left)
+      prefetch_l2(wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk);
+  });
+}
+
 // ----------------------------------------------------------------- shared state
 template <int PATH, int BT>
 struct Smem {
@@ -279,6 +298,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
     prefetch_tmap(&args.tmap_a);
     if (PATH == PATH_NVFP4) prefetch_tmap(&args.tmap_sf);
   }
+  pdl_trigger();
+  if (!args.moe && tid == WPROD_WARP * 32) prefetch_dense_weights(args, 2 * C::SW);
+  pdl_wait();  // no global memory a previous kernel may write is touched before this point
   // MoE: tile prefix over experts (E <= 512 enforced on the host)
   if (args.moe) {
     for (int e = tid; e < args.E; e += NUM_THREADS) {

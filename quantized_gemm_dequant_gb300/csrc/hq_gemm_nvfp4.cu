@@ -1,5 +1,6 @@
 // Kernel instances of the NVFP4 path for every token-tile width.
 #include "hq_gemm_kernel.cuh"
+#include "hq_launch.h"
 
 namespace hq {
 
@@ -15,8 +16,7 @@ static cudaError_t launch_bt(const GemmArgs& a, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = 1;
   }
-  hq_gemm_kernel<PATH_NVFP4, BT><<<grid, NUM_THREADS, C::SMEM_BYTES, stream>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(hq_gemm_kernel<PATH_NVFP4, BT>, dim3(grid), dim3(NUM_THREADS), C::SMEM_BYTES, stream, a);
 }
 
 cudaError_t launch_gemm_nvfp4(const GemmArgs& a, int bt, int grid, cudaStream_t stream) {

@@ -19,6 +19,7 @@
 // gather4 (MoE) of the token tile for the same 128 K, all on one barrier.
 // Pieces and the Stream-K fix-up are those of the UMMA path.
 #include "hq_gemm_kernel.cuh"
+#include "hq_launch.h"
 
 namespace hq {
 
@@ -75,6 +76,9 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
     fence_mbar_init();
   }
   if (tid == SM_PROD_WARP * 32) prefetch_tmap(&args.tmap_a);
+  pdl_trigger();
+  if (!args.moe && tid == SM_PROD_WARP * 32) prefetch_dense_weights(args, 32);
+  pdl_wait();  // no global memory a previous kernel may write is touched before this point
   if (args.moe) {
     for (int e = tid; e < args.E; e += SM_THREADS) {
       int cnt = args.counts[e];
@@ -399,8 +403,7 @@ static cudaError_t launch_small_bt(const GemmArgs& a, int grid, cudaStream_t str
     if (e != cudaSuccess) return e;
     attr_set[dev] = 1;
   }
-  hq_gemm_small_kernel<BT><<<grid, SM_THREADS, C::SMEM_BYTES, stream>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(hq_gemm_small_kernel<BT>, dim3(grid), dim3(SM_THREADS), C::SMEM_BYTES, stream, a);
 }
 
 cudaError_t launch_gemm_small(const GemmArgs& a, int bt, int grid, cudaStream_t stream) {

@@ -96,6 +96,19 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (16-byte aligned address and size).  A hint only: L2 is the
+// device's point of coherence, so data prefetched before a writer's stores land is still read current.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Programmatic dependent launch.  pdl_trigger lets the next kernel of the stream be scheduled once every CTA
+// of this grid has triggered (it still waits for this grid in its own pdl_wait); pdl_wait blocks until the
+// previous kernel of the stream has completed and its memory operations are visible.  Both are no-ops for
+// a launch without the programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // 16-byte cp.async global -> shared; src_bytes < 16 zero-fills the tail (0 = all zeros).
 __device__ __forceinline__ void cp_async_16(void* dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)

@@ -8,6 +8,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "hq_launch.h"
+#include "hq_ptx.cuh"
+
 namespace hq {
 
 constexpr int ROUTE_ROWS = 1024;
@@ -17,6 +20,8 @@ __global__ void __launch_bounds__(256) route_kernel(const int32_t* __restrict__ 
                                                     int* __restrict__ counts, int* __restrict__ region,
                                                     int* __restrict__ status) {
   extern __shared__ int sh[];  // hist[E], base[E]
+  pdl_trigger();
+  pdl_wait();  // ids may come from the previous kernel
   int* hist = sh;
   int* base = sh + E;
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
@@ -57,6 +62,7 @@ cudaError_t launch_route(const int32_t* ids, int64_t rows, int E, int cap, int* 
   if (err != cudaSuccess) return err;
   if (rows == 0) return cudaSuccess;
   const int64_t blocks = (rows + ROUTE_ROWS - 1) / ROUTE_ROWS;
+  // plain stream order after the memset above
   route_kernel<<<(unsigned)blocks, 256, 2 * E * sizeof(int), stream>>>(ids, rows, E, cap, counts, region, status);
   return cudaGetLastError();
 }
@@ -79,6 +85,8 @@ __global__ void __launch_bounds__(256) moe_permute_kernel(const int* __restrict_
   __shared__ int off[513];
   __shared__ int src_row[PERMUTE_ROWS];
   const int tid = threadIdx.x;
+  pdl_trigger();
+  pdl_wait();  // counts and region come from the routing kernel
   // exclusive scan of the clamped counts (two entries per thread)
   __shared__ int part[256];
   int c0 = 0, c1 = 0;
@@ -141,10 +149,9 @@ cudaError_t launch_moe_permute(const int* counts, const int* region, int cap, in
                                int* row_off, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
   const int64_t blocks = (rows + PERMUTE_ROWS - 1) / PERMUTE_ROWS;
-  moe_permute_kernel<<<(unsigned)blocks, 256, 0, stream>>>(counts, region, cap, E, topk, (const uint8_t*)src, row_bytes,
-                                                           (uint8_t*)dst, (const uint8_t*)sf_src, sf_bytes,
-                                                           (uint8_t*)sf_dst, row_off);
-  return cudaGetLastError();
+  return launch_kernel(moe_permute_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, counts, region, cap, E, topk,
+                       (const uint8_t*)src, row_bytes, (uint8_t*)dst, (const uint8_t*)sf_src, sf_bytes, (uint8_t*)sf_dst,
+                       row_off);
 }
 
 }  // namespace hq
