@@ -309,7 +309,7 @@ def run_ours(args):
                              f"stream (each call on its own replica), divided by the burst length; step = one call "
                              f"per size",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": roof, "sweep": sweep, "gpu_launches": gpu_launches(args.config, calls) * args.steps,
+        "roofline": roof, "sweep": sweep, "gpu_launches": gpu_launches(args.config, fmt, calls) * args.steps,
         "clocks": clocks, "wall_s_timed": round(t_wall, 3), "e2e": e2e, "cpu_baseline": cpu,
     }
     if rank == 0:
@@ -332,9 +332,13 @@ def kernel_name(cfg, M):
     return f"hq::hq_gemm_kernel<{path}, {bt}>"
 
 
-def gpu_launches(cfg, calls):
-    # dense: one GEMM kernel per call; MoE: routing kernel + GEMM kernel (+ a memset of the expert counts)
-    return len(calls) * (1 if W.CONFIGS[cfg]["kind"] == "dense" else 2)
+def gpu_launches(cfg, fmt, calls):
+    """This library's kernels per step (one call per size): GEMM, split-K reduction, MoE routing and row
+    permutation, as the launch plan of each call has them."""
+    import quantized_gemm_dequant_gb300 as hq
+    c = W.CONFIGS[cfg]
+    moe = c["kind"] != "dense"
+    return sum(hq.kernels_per_call(fmt, M, c.get("topk", 1), moe) for (M, *_rest) in calls)
 
 
 def kernel_source_hash():

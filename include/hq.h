@@ -120,10 +120,15 @@ HQ_API hq_status_t hq_unpack_weights(const hq_format_t* fmt, const void* packed,
 
 /* Workspace bytes for a call with M rows (dense) or T tokens with `topk`
  * experts each (MoE; pass topk = 1 for dense).  The workspace holds the
- * device status word, split-K partial sums and tile counters, and the MoE
- * routing tables.  It must be zeroed once with hq_workspace_init before its
- * first use; calls leave it reusable.  One workspace serves one stream at a time. */
+ * device status word, split-K partial sums and the MoE routing tables.  It
+ * must be zeroed once with hq_workspace_init before its first use; calls
+ * leave it reusable.  One workspace serves one stream at a time. */
 HQ_API size_t hq_workspace_bytes(const hq_format_t* fmt, int64_t M_or_T, int32_t topk);
+
+/* Number of kernels one call launches on the current device: hq_gemm (moe = 0) or hq_moe_gemm (moe = 1)
+ * with M rows / T tokens and `topk` experts each (1 for dense).  Counts this library's kernels only
+ * (the routing memset of hq_moe_gemm is not a kernel); 0 for an invalid format or size.  Host-only. */
+HQ_API int32_t hq_kernels_per_call(const hq_format_t* fmt, int64_t M_or_T, int32_t topk, int32_t moe);
 
 /* Zero `bytes` of workspace on `stream` (cudaMemsetAsync). */
 HQ_API hq_status_t hq_workspace_init(void* workspace, size_t bytes, hq_stream_t stream);

@@ -28,7 +28,8 @@ HQ_S_BF16, HQ_S_UE4M3, HQ_S_UE8M0 = 1, 2, 3
 HQ_A_BF16, HQ_A_E4M3_TOKEN, HQ_A_NVFP4 = 1, 2, 3
 
 EXPORTS = ["hq_packed_bytes", "hq_pack_weights", "hq_unpack_weights", "hq_workspace_bytes", "hq_workspace_init",
-           "hq_gemm", "hq_moe_gemm", "hq_last_device_status", "hq_status_string", "hq_gemm_static_scratch"]
+           "hq_gemm", "hq_moe_gemm", "hq_last_device_status", "hq_status_string", "hq_gemm_static_scratch",
+           "hq_kernels_per_call"]
 
 
 class Format(ctypes.Structure):
@@ -62,6 +63,8 @@ _lib.hq_last_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32), _vp]
 _lib.hq_last_device_status.restype = ctypes.c_int
 _lib.hq_gemm_static_scratch.argtypes = [_F, _A, _vp, _vp, _vp, _i64, _i64, _i64, _vp]
 _lib.hq_gemm_static_scratch.restype = ctypes.c_int
+_lib.hq_kernels_per_call.argtypes = [_F, _i64, _i32, _i32]
+_lib.hq_kernels_per_call.restype = _i32
 _lib.hq_status_string.argtypes = [ctypes.c_int]
 _lib.hq_status_string.restype = ctypes.c_char_p
 
@@ -127,6 +130,11 @@ def unpack_weights(fmt, packed, codes, scales, zeros=None, global_scale=None, st
 
 def workspace_bytes(fmt, rows, topk=1):
     return int(_lib.hq_workspace_bytes(ctypes.byref(fmt), int(rows), int(topk)))
+
+
+def kernels_per_call(fmt, rows, topk=1, moe=False):
+    """Kernels one gemm (moe=False) or moe_gemm call launches on the current device."""
+    return int(_lib.hq_kernels_per_call(ctypes.byref(fmt), int(rows), int(topk), 1 if moe else 0))
 
 
 def make_workspace(fmt, rows, topk=1, device="cuda", stream=None):

@@ -19,6 +19,7 @@ cudaError_t launch_gemm_int4(const GemmArgs& a, int bt, int grid, cudaStream_t s
 cudaError_t launch_gemm_nvfp4(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_mxfp4(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_small(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
+cudaError_t launch_splitk_reduce(int path, const GemmArgs& a, int bt, int gemm_grid, int grid, cudaStream_t stream);
 cudaError_t launch_moe_permute(const int* counts, const int* region, int cap, int E, int topk, int64_t rows,
                                const void* src, int row_bytes, void* dst, const void* sf_src, int sf_bytes, void* sf_dst,
                                int* row_off, cudaStream_t stream);
@@ -84,9 +85,9 @@ struct Plan {
   int sk = 0;
   int grid = 1;
   int64_t n_tiles = 0, kst = 0, m_tiles = 0;
-  int64_t max_tiles = 0;   // upper bound of tiles (split-K counters)
+  int64_t max_tiles = 0;   // upper bound of tiles
   int64_t region_cap = 0;  // MoE rows per expert
-  size_t off_counts = 0, off_counters = 0, off_region = 0, off_partials = 0, ws_bytes = 0;
+  size_t off_counts = 0, off_region = 0, off_partials = 0, ws_bytes = 0;
   size_t off_rowoff = 0, off_gact = 0, off_gsf = 0;  // MoE grouped: expert row offsets, rows, NVFP4 scales
 };
 
@@ -178,8 +179,6 @@ Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int
       p.grid = (int)(W < slots ? (W < 1 ? 1 : W) : slots);
     }
   }
-  p.off_counters = off;
-  off = align256(off + sizeof(int) * (size_t)(p.max_tiles > 0 ? p.max_tiles : 1));
   if (moe) {
     p.off_region = off;
     off = align256(off + sizeof(int) * (size_t)(f->num_experts * (p.region_cap > 0 ? p.region_cap : 1)));
@@ -207,9 +206,16 @@ Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int
 }
 
 cudaError_t launch_path(const Plan& p, const GemmArgs& a, cudaStream_t s) {
-  if (p.path == PATH_INT4) return p.small ? launch_gemm_small(a, p.bt, p.grid, s) : launch_gemm_int4(a, p.bt, p.grid, s);
-  if (p.path == PATH_NVFP4) return launch_gemm_nvfp4(a, p.bt, p.grid, s);
-  return launch_gemm_mxfp4(a, p.bt, p.grid, s);
+  cudaError_t e;
+  if (p.path == PATH_INT4) e = p.small ? launch_gemm_small(a, p.bt, p.grid, s) : launch_gemm_int4(a, p.bt, p.grid, s);
+  else if (p.path == PATH_NVFP4) e = launch_gemm_nvfp4(a, p.bt, p.grid, s);
+  else e = launch_gemm_mxfp4(a, p.bt, p.grid, s);
+  if (e != cudaSuccess || !p.sk) return e;
+  // tiles cut between CTAs: sum their partial slots, one CTA per 32 token columns of a tile
+  const int64_t items = p.max_tiles * ((p.bt + 31) / 32);
+  const int64_t cap = 4 * (int64_t)p.grid;
+  const int64_t rg = items < cap ? items : cap;
+  return launch_splitk_reduce(p.path, a, p.bt, p.grid, (int)(rg < 1 ? 1 : rg), s);
 }
 
 hq_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? HQ_OK : HQ_ERR_CUDA; }
@@ -299,6 +305,14 @@ size_t hq_workspace_bytes(const hq_format_t* fmt, int64_t M_or_T, int32_t topk) 
   return d > m ? d : m;
 }
 
+int32_t hq_kernels_per_call(const hq_format_t* fmt, int64_t M_or_T, int32_t topk, int32_t moe) {
+  if (check_format(fmt) != HQ_OK || M_or_T < 1 || topk < 1) return 0;
+  const Plan p = make_plan(fmt, M_or_T, topk, moe != 0, num_sms());
+  int32_t n = 1 + (p.sk ? 1 : 0);  // GEMM (+ split-K reduction)
+  if (moe) n += 1 + (p.grouped ? 1 : 0);  // routing (+ row permutation)
+  return n;
+}
+
 hq_status_t hq_workspace_init(void* workspace, size_t bytes, hq_stream_t stream) {
   if (!workspace || bytes == 0) return HQ_ERR_INVALID_ARG;
   return cuda_status(cudaMemsetAsync(workspace, 0, bytes, (cudaStream_t)stream));
@@ -344,7 +358,6 @@ hq_status_t hq_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* packe
   a.m_tiles = (int)p.m_tiles;
   a.sk = p.sk;
   a.status = reinterpret_cast<int*>(ws);
-  a.counters = reinterpret_cast<int*>(ws + p.off_counters);
   a.partials = p.sk ? reinterpret_cast<float*>(ws + p.off_partials) : nullptr;
   return cuda_status(launch_path(p, a, (cudaStream_t)stream));
 }
@@ -419,7 +432,6 @@ hq_status_t hq_moe_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* p
   a.m_tiles = 0;
   a.sk = p.sk;
   a.status = status;
-  a.counters = reinterpret_cast<int*>(ws + p.off_counters);
   a.partials = p.sk ? reinterpret_cast<float*>(ws + p.off_partials) : nullptr;
   return cuda_status(launch_path(p, a, (cudaStream_t)stream));
 }

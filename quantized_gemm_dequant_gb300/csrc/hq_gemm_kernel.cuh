@@ -27,8 +27,9 @@
 //
 // Work is split into pieces (tile, range of weight blocks along K).  With few
 // tiles the K blocks of all tiles are dealt out evenly to the CTAs
-// (Stream-K); tiles cut between CTAs are finished by the last CTA to arrive,
-// which sums the partial sums in a fixed order.  No CTA waits for another.
+// (Stream-K); a piece that is not a whole tile leaves fp32 partial sums in
+// its own slot, summed afterwards by the split-K reduction kernel.  No CTA
+// waits for another.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -72,8 +73,7 @@ struct GemmArgs {
   int m_tiles;  // dense: token tiles
   int sk;       // 1: Stream-K split over K blocks
   int* status;
-  int* counters;
-  float* partials;
+  float* partials;  // Stream-K: [2 * grid][BT][128] fp32, slot 2*cta + {0 first piece, 1 later piece}
 };
 
 template <int PATH, int BT>
@@ -200,25 +200,6 @@ __device__ __forceinline__ void for_each_piece(const Sched& s, F&& f) {
   }
 }
 
-// Dense: L2 prefetch of the first `limit` weight blocks of this CTA's pieces, in the order its producer loads
-// them.  Issued before pdl_wait, so the stream of weights starts while the previous kernel finishes.
-__device__ __forceinline__ void prefetch_dense_weights(const GemmArgs& args, int limit) {
-  Sched s;
-  s.tiles = args.m_tiles * args.n_tiles;
-  s.kst = args.kst;
-  s.W = (int64_t)s.tiles * s.kst;
-  s.P = args.sk ? (int)((int64_t)gridDim.x < s.W ? gridDim.x : s.W) : (int)gridDim.x;
-  s.cta = blockIdx.x;
-  s.sk = args.sk;
-  if ((int)blockIdx.x >= s.P || s.tiles <= 0) return;
-  int left = limit;
-  for_each_piece(s, [&](const Piece& pc) {
-    const uint8_t* wblk = args.w + ((int64_t)(pc.tile % args.n_tiles) * args.kst) * args.w_blk;
-    for (int g = pc.g0; g < pc.g1 && left > 0; ++g, --left)
-      prefetch_l2(wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk);
-  });
-}
-
 // ----------------------------------------------------------------- shared state
 template <int PATH, int BT>
 struct Smem {
@@ -235,10 +216,8 @@ struct Smem {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
-  int fix_last;
   int tile_prefix_total;
   int rows_tok[256];  // MoE: token index of each row of the activation producer's current tile
-  uint64_t epi_bar;  // bounded barrier of the 8 epilogue warps (Stream-K fix-up)
 };
 
 // Map a global token-tile index to (expert, local token tile) for MoE via the
@@ -290,7 +269,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
     mbar_init(&sh.dfull, 1);
     mbar_init(&sh.dempty, 8);
     mbar_init(&sh.drain, 1);
-    mbar_init(&sh.epi_bar, 8);
     sh.abort_flag = 0;
     fence_mbar_init();
   }
@@ -299,7 +277,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
     if (PATH == PATH_NVFP4) prefetch_tmap(&args.tmap_sf);
   }
   pdl_trigger();
-  if (!args.moe && tid == WPROD_WARP * 32) prefetch_dense_weights(args, 2 * C::SW);
   pdl_wait();  // no global memory a previous kernel may write is touched before this point
   // MoE: tile prefix over experts (E <= 512 enforced on the host)
   if (args.moe) {
@@ -593,15 +570,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
       tmem_st_x<8>(tmem + lane_base + 256 + 4 * C::SW, ones);
       tmem_wait_st();
     }
-    // CTA-level sync of the 8 epilogue warps on an mbarrier (bounded, abort-aware: never a hang)
-    uint32_t epi_phase = 0;
-    auto epi_sync = [&]() {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.epi_bar);
-      const bool good = waitf(&sh.epi_bar, epi_phase);
-      epi_phase ^= 1;
-      return good;
-    };
     const bool in_mainloop = !(PATH == PATH_NVFP4 && warp >= 4);
     constexpr int HC = BT / 2;
     // Per-column output rows and multipliers: MoE rows and per-token activation scales.  INT4 and NVFP4
@@ -826,59 +794,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
       } else {
 #pragma unroll
         for (int j = 0; j < HC; ++j) store(col0 + j, __uint_as_float(v[j]));
-      }
-      if (!pc.full) {
-        // ---------------------------------------------- Stream-K fix-up (last arriver sums)
-        if (!epi_sync()) return false;  // every partial store of this CTA precedes thread 0's release below
-        const int64_t first_it = (int64_t)pc.tile * sched.kst;
-        const int c_first = sched.cta_of(first_it);
-        const int c_last = sched.cta_of(first_it + sched.kst - 1);
-        if (tid == 0) {
-          const int nctr = c_last - c_first + 1;
-          __threadfence();  // release this CTA's partials before its arrival is counted
-          const int old = atomicAdd(&args.counters[pc.tile], 1);
-          sh.fix_last = (old == nctr - 1) ? 1 : 0;
-          if (old == nctr - 1) {
-            args.counters[pc.tile] = 0;
-            __threadfence();  // acquire: the other CTAs' partials before the reads below
-          }
-        }
-        if (!epi_sync()) return false;
-        if (sh.fix_last) {
-          // every partial of a column chunk is requested before any is summed: one L2 round trip per chunk
-#pragma unroll 1
-          for (int cb = 0; cb < HC; cb += CHUNK) {
-            float acc[CHUNK];
-#pragma unroll
-            for (int j = 0; j < CHUNK; ++j) acc[j] = 0.0f;
-            int c = c_first;
-            for (; c + 1 <= c_last; c += 2) {
-              const int s0 = (c == c_first && sched.start(c) < first_it) ? 2 * c + 1 : 2 * c;
-              const int s1 = 2 * (c + 1);
-              const float* p0 = args.partials + ((int64_t)s0 * BT + col0 + cb) * TILE_N + r;
-              const float* p1 = args.partials + ((int64_t)s1 * BT + col0 + cb) * TILE_N + r;
-              float v0[CHUNK], v1[CHUNK];
-#pragma unroll
-              for (int j = 0; j < CHUNK; ++j) {
-                v0[j] = __ldcg(p0 + j * TILE_N);
-                v1[j] = __ldcg(p1 + j * TILE_N);
-              }
-#pragma unroll
-              for (int j = 0; j < CHUNK; ++j) acc[j] += v0[j] + v1[j];
-            }
-            if (c <= c_last) {
-              const int s0 = (c == c_first && sched.start(c) < first_it) ? 2 * c + 1 : 2 * c;
-              const float* p0 = args.partials + ((int64_t)s0 * BT + col0 + cb) * TILE_N + r;
-              float v0[CHUNK];
-#pragma unroll
-              for (int j = 0; j < CHUNK; ++j) v0[j] = __ldcg(p0 + j * TILE_N);
-#pragma unroll
-              for (int j = 0; j < CHUNK; ++j) acc[j] += v0[j];
-            }
-#pragma unroll
-            for (int j = 0; j < CHUNK; ++j) store(col0 + cb + j, acc[j]);
-          }
-        }
       }
       ++pidx;
       return ok;

@@ -17,7 +17,7 @@
 // Two CTAs per SM for 16-token tiles.  Warps 0-7 compute (warp w owns rows 16w..16w+15 of the 128-row tile); warp 8
 // produces: one bulk copy of the weight block plus the TMA load (dense) or
 // gather4 (MoE) of the token tile for the same 128 K, all on one barrier.
-// Pieces and the Stream-K fix-up are those of the UMMA path.
+// Pieces and the Stream-K partial slots are those of the UMMA path.
 #include "hq_gemm_kernel.cuh"
 #include "hq_launch.h"
 
@@ -32,10 +32,11 @@ struct SmallCfg {
   static constexpr int W_REGION = 9216;          // one INT4 block (<= 8576 bytes), 1 KB aligned
   static constexpr int ACT_BYTES = 2 * BT * 128;  // two 64-K swizzled atoms
   static constexpr int STAGE = W_REGION + ACT_BYTES;
-  // a ring of about 104 KB, so that two CTAs fit on an SM (no tensor memory here)
-  static constexpr int STAGES = (104 * 1024) / STAGE > 16 ? 16 : (104 * 1024) / STAGE;
+  // a ring of about 96 KB, so that two CTAs fit on an SM (no tensor memory here)
+  static constexpr int STAGES = (96 * 1024) / STAGE > 16 ? 16 : (96 * 1024) / STAGE;
   static constexpr int NT = BT / 8;  // 8-token MMA tiles
-  static constexpr int SMEM_BYTES = STAGES * STAGE + 1024 + 5120;
+  static constexpr int RED_BYTES = 4 * 32 * 2 * NT * 4 * 4;  // K-half exchange of the compute warps
+  static constexpr int SMEM_BYTES = STAGES * STAGE + 1024 + 5120 + RED_BYTES;
   static_assert(CTAS_PER_SM * (SMEM_BYTES + 1024) <= 228 * 1024, "CTAs per SM");
 };
 
@@ -43,10 +44,9 @@ struct SmallSmem {
   uint64_t full[16];
   uint64_t empty[16];
   int abort_flag;
-  int fix_last;
   int tile_prefix_total;
   int rows_tok[32];
-  uint64_t epi_bar;  // bounded barrier of the 8 compute warps (Stream-K fix-up)
+  uint64_t epi_bar;  // bounded barrier of the 8 compute warps (K-half exchange)
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -77,7 +77,6 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
   }
   if (tid == SM_PROD_WARP * 32) prefetch_tmap(&args.tmap_a);
   pdl_trigger();
-  if (!args.moe && tid == SM_PROD_WARP * 32) prefetch_dense_weights(args, 32);
   pdl_wait();  // no global memory a previous kernel may write is touched before this point
   if (args.moe) {
     for (int e = tid; e < args.E; e += SM_THREADS) {
@@ -200,12 +199,23 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
     __syncwarp();
   } else if (active && warp < 8) {
     // ============================================================ compute warps
+    // Warp (rg, kh): rows 32*rg .. 32*rg+31 of the tile as two 16-row MMA tiles, and K half kh (two 32-K
+    // chunks) of every weight block.  The two K halves meet in shared memory at the end of each piece.
+    const int rg = warp & 3, kh = warp >> 2;
     const int g8 = lane >> 2, t4 = lane & 3;
-    const int rA = warp * 16 + g8, rB = rA + 8;  // rows of this lane within the 128-row tile
     const uint32_t sh4 = 4u * (uint32_t)t4;
+    int rows[4];  // MMA tile m: rows[2m] (fragment rows 0-7), rows[2m+1] (rows 8-15)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) rows[i] = 32 * rg + 8 * i + g8;
+    // ldmatrix.x4 addresses: lanes 8q..8q+7 give the 8 token rows of matrix q = (token group q/2, K half q%2)
+    // of the 128-byte-swizzled activation atom; one x4 covers 16 tokens of a 16-K step
+    const int lm_tok = ((lane >> 4) << 3) + (lane & 7);  // token within a 16-token group
+    const int lm_khi = (lane >> 3) & 1;
+    const uint32_t lm_row = (uint32_t)((lm_tok >> 3) * 1024 + (lm_tok & 7) * 128);
     int st = 0;
     uint32_t ph = 0;
     bool ok = true;
+    float* red = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE + 1024 + 5120);  // [4][32 lanes][2][NT][4]
     // CTA-level sync of the 8 compute warps on an mbarrier (bounded, abort-aware: never a hang)
     uint32_t epi_phase = 0;
     auto epi_sync = [&]() {
@@ -223,11 +233,13 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
       int e, row0, nrows;
       tile_rows(pc.tile, e, row0, nrows);
       const int nt = pc.tile % args.n_tiles;
-      float acc[C::NT][4];
+      float acc[2][C::NT][4];
 #pragma unroll
-      for (int i = 0; i < C::NT; ++i)
+      for (int m = 0; m < 2; ++m)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+        for (int i = 0; i < C::NT; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[m][i][j] = 0.0f;
       // output row and multiplier of this lane's token columns (i*8 + 2t, +1), loaded now so that their
       // latency hides behind the mainloop
       int t_row[C::NT][2];
@@ -239,7 +251,7 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
           const int col = i * 8 + 2 * t4 + u;
           int orow = -1;
           float f = 1.0f;
-          if (col < nrows) {
+          if (kh == 0 && col < nrows) {
             if (args.moe) {
               orow = args.region[e * args.region_cap + row0 + col];
               if (args.topk_w) f = args.topk_w[orow];
@@ -257,135 +269,113 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
           return;
         }
         const uint8_t* wb = smem + st * C::STAGE;
-        const uint8_t* act = wb + C::W_REGION;
-        const float sA = bf16_to_f32(reinterpret_cast<const uint16_t*>(wb + 8192)[rA]);
-        const float sB = bf16_to_f32(reinterpret_cast<const uint16_t*>(wb + 8192)[rB]);
-        const uint32_t zA = args.zp ? (uint32_t)wb[8448 + rA] : 8u;
-        const uint32_t zB = args.zp ? (uint32_t)wb[8448 + rB] : 8u;
-        const uint32_t zzA = (0x4300u + zA) * 0x00010001u, zzB = (0x4300u + zB) * 0x00010001u;
-        float blk[2][C::NT][4];  // even / odd 16-K steps: two independent MMA chains per token tile
+        const uint32_t act_s = smem_u32(wb + C::W_REGION);
+        // each decoded weight is (q - z) * s rounded to bf16 (as in the tensor-core path), so the MMAs
+        // accumulate straight into acc and never wait for a block's sums before the next block
+        uint32_t ss[4], zz[4];
 #pragma unroll
-        for (int u = 0; u < 2; ++u)
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t s16 = reinterpret_cast<const uint16_t*>(wb + 8192)[rows[i]];
+          ss[i] = s16 | (s16 << 16);
+          const uint32_t z = args.zp ? (uint32_t)wb[8448 + rows[i]] : 8u;
+          zz[i] = (0x4300u + z) * 0x00010001u;
+        }
 #pragma unroll
-          for (int i = 0; i < C::NT; ++i)
+        for (int jj = 0; jj < 2; ++jj) {  // 32-K chunk of this warp's K half
+          const int j = 2 * kh + jj;
+          uint4 w[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) blk[u][i][j] = 0.0f;
+          for (int i = 0; i < 4; ++i) w[i] = *reinterpret_cast<const uint4*>(wb + (j * 128 + rows[i]) * 16);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {  // 32-K chunk
-          const uint4 wa = *reinterpret_cast<const uint4*>(wb + (j * 128 + rA) * 16);
-          const uint4 wbv = *reinterpret_cast<const uint4*>(wb + (j * 128 + rB) * 16);
-          const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
-          const uint32_t wB[4] = {wbv.x, wbv.y, wbv.z, wbv.w};
-#pragma unroll
-          for (int s2 = 0; s2 < 2; ++s2) {  // 16-K step within the chunk
-            uint32_t a[4];
-            a[0] = bf16x2_sub(lop3_and_or(wA[2 * s2] >> sh4, 0x000F000Fu, 0x43004300u), zzA);
-            a[1] = bf16x2_sub(lop3_and_or(wB[2 * s2] >> sh4, 0x000F000Fu, 0x43004300u), zzB);
-            a[2] = bf16x2_sub(lop3_and_or(wA[2 * s2 + 1] >> sh4, 0x000F000Fu, 0x43004300u), zzA);
-            a[3] = bf16x2_sub(lop3_and_or(wB[2 * s2 + 1] >> sh4, 0x000F000Fu, 0x43004300u), zzB);
+          for (int s2 = 0; s2 < 2; ++s2) {  // 16-K step
             const int kk = j * 32 + s2 * 16;  // K within the 128-K block
-            const int atom = kk >> 6;
-            const int byte = (kk & 63) * 2 + t4 * 4;  // b0b1 at k = kk + 2t; b2b3 eight K later
+            const uint32_t atom_s = act_s + (uint32_t)((kk >> 6) * (BT * 128));
+            const uint32_t chunk = (uint32_t)(((kk & 63) >> 3) + lm_khi);
+            uint32_t b[C::NT][2];
 #pragma unroll
-            for (int n8 = 0; n8 < C::NT; ++n8) {
-              const int row = n8 * 8 + g8;
-              const uint8_t* ab = act + atom * (BT * 128) + (row >> 3) * 1024 + (row & 7) * 128;
-              const int c0 = byte >> 4, c1 = (byte + 16) >> 4;
-              const uint32_t b0 = *reinterpret_cast<const uint32_t*>(ab + ((c0 ^ (row & 7)) << 4) + (byte & 15));
-              const uint32_t b1 = *reinterpret_cast<const uint32_t*>(ab + ((c1 ^ (row & 7)) << 4) + (byte & 15));
-              mma_bf16_16816(blk[s2][n8], a, b0, b1);
+            for (int q = 0; q < C::NT / 2; ++q) {
+              const uint32_t addr = atom_s + (uint32_t)(q * 2048) + lm_row + ((chunk ^ (uint32_t)(lm_tok & 7)) << 4);
+              ldsm_x4(addr, b[2 * q][0], b[2 * q][1], b[2 * q + 1][0], b[2 * q + 1][1]);
+            }
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+              const uint32_t lo = s2 == 0 ? 0 : 2;  // words 2*s2 (K 0-7 of the step) and 2*s2+1 (K 8-15)
+              const uint32_t wlo0 = lo == 0 ? w[2 * m].x : w[2 * m].z, whi0 = lo == 0 ? w[2 * m].y : w[2 * m].w;
+              const uint32_t wlo1 = lo == 0 ? w[2 * m + 1].x : w[2 * m + 1].z;
+              const uint32_t whi1 = lo == 0 ? w[2 * m + 1].y : w[2 * m + 1].w;
+              uint32_t a[4];
+              a[0] = bf16x2_mul(bf16x2_sub(lop3_and_or(wlo0 >> sh4, 0x000F000Fu, 0x43004300u), zz[2 * m]), ss[2 * m]);
+              a[1] = bf16x2_mul(bf16x2_sub(lop3_and_or(wlo1 >> sh4, 0x000F000Fu, 0x43004300u), zz[2 * m + 1]),
+                                ss[2 * m + 1]);
+              a[2] = bf16x2_mul(bf16x2_sub(lop3_and_or(whi0 >> sh4, 0x000F000Fu, 0x43004300u), zz[2 * m]), ss[2 * m]);
+              a[3] = bf16x2_mul(bf16x2_sub(lop3_and_or(whi1 >> sh4, 0x000F000Fu, 0x43004300u), zz[2 * m + 1]),
+                                ss[2 * m + 1]);
+#pragma unroll
+              for (int n8 = 0; n8 < C::NT; ++n8) mma_bf16_16816(acc[m][n8], a, b[n8][0], b[n8][1]);
             }
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.empty[st]);
-#pragma unroll
-        for (int i = 0; i < C::NT; ++i) {
-          acc[i][0] = fmaf(sA, blk[0][i][0] + blk[1][i][0], acc[i][0]);
-          acc[i][1] = fmaf(sA, blk[0][i][1] + blk[1][i][1], acc[i][1]);
-          acc[i][2] = fmaf(sB, blk[0][i][2] + blk[1][i][2], acc[i][2]);
-          acc[i][3] = fmaf(sB, blk[0][i][3] + blk[1][i][3], acc[i][3]);
-        }
         if (++st == C::STAGES) {
           st = 0;
           ph ^= 1;
         }
       }
-      // ---------------------------------------------------- epilogue
-      const float biasA = (args.bias && nt * TILE_N + rA < args.N) ? bf16_to_f32(args.bias[nt * TILE_N + rA]) : 0.f;
-      const float biasB = (args.bias && nt * TILE_N + rB < args.N) ? bf16_to_f32(args.bias[nt * TILE_N + rB]) : 0.f;
-      // (i, u): token tile i, column 2t + u of it (compile-time after unrolling)
-      auto store = [&](int i, int u, int r, float v, float bias) {
-        const int n = nt * TILE_N + r;
-        const int orow = t_row[i][u];
-        if (orow >= 0 && n < args.N) args.c[(int64_t)orow * args.N + n] = f32_to_bf16(v * t_mul[i][u] + bias);
-      };
-
-      if (pc.full) {
+      // ---------------------------------------------------- K halves meet, epilogue
+      float* mine = red + ((rg * 32 + lane) * 2) * (C::NT * 4);
+      if (kh == 1) {
 #pragma unroll
-        for (int i = 0; i < C::NT; ++i) {
-          store(i, 0, rA, acc[i][0], biasA);
-          store(i, 1, rA, acc[i][1], biasA);
-          store(i, 0, rB, acc[i][2], biasB);
-          store(i, 1, rB, acc[i][3], biasB);
-        }
-      } else {
-        float* part = args.partials + ((int64_t)pc.slot * BT) * TILE_N;
-#pragma unroll
-        for (int i = 0; i < C::NT; ++i) {
-          const int col = i * 8 + 2 * t4;
-          part[col * TILE_N + rA] = acc[i][0];
-          part[(col + 1) * TILE_N + rA] = acc[i][1];
-          part[col * TILE_N + rB] = acc[i][2];
-          part[(col + 1) * TILE_N + rB] = acc[i][3];
-        }
-        if (!epi_sync()) return;  // every partial store of this CTA precedes thread 0's release below
-        const int64_t first_it = (int64_t)pc.tile * sched.kst;
-        const int c_first = sched.cta_of(first_it);
-        const int c_last = sched.cta_of(first_it + sched.kst - 1);
-        if (tid == 0) {
-          const int nctr = c_last - c_first + 1;
-          __threadfence();  // release this CTA's partials before its arrival is counted
-          const int old = atomicAdd(&args.counters[pc.tile], 1);
-          sh.fix_last = (old == nctr - 1) ? 1 : 0;
-          if (old == nctr - 1) {
-            args.counters[pc.tile] = 0;
-            __threadfence();  // acquire: the other CTAs' partials before the reads below
-          }
-        }
-        if (!epi_sync()) return;
-        if (sh.fix_last) {
-          float sum[C::NT][4];
+        for (int m = 0; m < 2; ++m)
 #pragma unroll
           for (int i = 0; i < C::NT; ++i)
+            *reinterpret_cast<float4*>(mine + (m * C::NT + i) * 4) =
+                make_float4(acc[m][i][0], acc[m][i][1], acc[m][i][2], acc[m][i][3]);
+      }
+      if (!epi_sync()) return;
+      if (kh == 0) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) sum[i][j] = 0.0f;
-          for (int c = c_first; c <= c_last; ++c) {
-            const int slot = (c == c_first && sched.start(c) < first_it) ? 2 * c + 1 : 2 * c;
-            const float* p = args.partials + ((int64_t)slot * BT) * TILE_N;
-            float v[C::NT][4];
-#pragma unroll
-            for (int i = 0; i < C::NT; ++i) {
-              const int col = i * 8 + 2 * t4;
-              v[i][0] = __ldcg(p + col * TILE_N + rA);
-              v[i][1] = __ldcg(p + (col + 1) * TILE_N + rA);
-              v[i][2] = __ldcg(p + col * TILE_N + rB);
-              v[i][3] = __ldcg(p + (col + 1) * TILE_N + rB);
-            }
-#pragma unroll
-            for (int i = 0; i < C::NT; ++i)
-#pragma unroll
-              for (int j = 0; j < 4; ++j) sum[i][j] += v[i][j];
-          }
+        for (int m = 0; m < 2; ++m)
 #pragma unroll
           for (int i = 0; i < C::NT; ++i) {
-            store(i, 0, rA, sum[i][0], biasA);
-            store(i, 1, rA, sum[i][1], biasA);
-            store(i, 0, rB, sum[i][2], biasB);
-            store(i, 1, rB, sum[i][3], biasB);
+            const float4 o = *reinterpret_cast<const float4*>(mine + (m * C::NT + i) * 4);
+            acc[m][i][0] += o.x;
+            acc[m][i][1] += o.y;
+            acc[m][i][2] += o.z;
+            acc[m][i][3] += o.w;
           }
+        if (pc.full) {
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+              const int n = nt * TILE_N + rows[2 * m + rr];
+              if (n >= args.N) continue;
+              const float bias = args.bias ? bf16_to_f32(args.bias[n]) : 0.0f;
+#pragma unroll
+              for (int i = 0; i < C::NT; ++i)
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                  const int orow = t_row[i][u];
+                  if (orow >= 0)
+                    args.c[(int64_t)orow * args.N + n] = f32_to_bf16(acc[m][i][2 * rr + u] * t_mul[i][u] + bias);
+                }
+            }
+          }
+        } else {
+          float* part = args.partials + ((int64_t)pc.slot * BT) * TILE_N;
+#pragma unroll
+          for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+              for (int i = 0; i < C::NT; ++i)
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+                  part[(i * 8 + 2 * t4 + u) * TILE_N + rows[2 * m + rr]] = acc[m][i][2 * rr + u];
         }
       }
+      if (!epi_sync()) return;  // the exchange buffer is reused by the next piece
     });
   }
   __syncthreads();

@@ -1,6 +1,6 @@
 // Dense GEMM entry point that needs no caller-provided workspace.
 //
-// Its scratch (device status word, Stream-K tile counters and partial sums)
+// Its scratch (device status word, Stream-K partial sums)
 // lives in one file-scope device array of HQ_STATIC_SCRATCH_BYTES that every
 // GPU loading this library keeps until the process exits.  The call itself
 // allocates nothing.
@@ -47,13 +47,8 @@ hq_status_t hq_gemm_static_scratch(const hq_format_t* fmt, const hq_act_t* A, co
   void* ws = nullptr;
   const hq_status_t st = scratch_address(&ws);
   if (st != HQ_OK) return st;
-  // The status word and the tile counters (the leading part of the scratch, at
-  // most 4 bytes per 16-row x 128-column tile after a 256-byte header) must
-  // start at zero; clearing more than that is harmless.
-  size_t clear = 256 + 4 * (size_t)((M + 15) / 16) * (size_t)((N + 127) / 128);
-  clear = ((clear + 255) / 256) * 256;
-  if (clear > need) clear = need;
-  if (cudaMemsetAsync(ws, 0, clear, (cudaStream_t)stream) != cudaSuccess) return HQ_ERR_CUDA;
+  // The status word (the scratch's 256-byte header) must start at zero.
+  if (cudaMemsetAsync(ws, 0, 256, (cudaStream_t)stream) != cudaSuccess) return HQ_ERR_CUDA;
   return hq_gemm(fmt, A, packedW, bias, C, M, N, K, ws, kScratchBytes, stream);
 }
 

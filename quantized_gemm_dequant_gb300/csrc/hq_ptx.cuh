@@ -96,12 +96,6 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
-// Bulk prefetch of global memory into L2 (16-byte aligned address and size).  A hint only: L2 is the
-// device's point of coherence, so data prefetched before a writer's stores land is still read current.
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // Programmatic dependent launch.  pdl_trigger lets the next kernel of the stream be scheduled once every CTA
 // of this grid has triggered (it still waits for this grid in its own pdl_wait); pdl_wait blocks until the
 // previous kernel of the stream has completed and its memory operations are visible.  Both are no-ops for
@@ -120,6 +114,15 @@ __device__ __forceinline__ void cp_async_wait_group() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Four 8x8 b16 matrices from shared memory; lanes 8q..8q+7 give the row addresses of matrix q, and
+// register q of lane (4i + j) receives row i, columns 2j and 2j+1 of matrix q.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
 
 // Generic-proxy writes to shared memory made visible to the async proxy (UMMA, bulk copies).
 __device__ __forceinline__ void fence_proxy_async_smem() {
