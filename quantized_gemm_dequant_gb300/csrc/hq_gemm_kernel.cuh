@@ -174,10 +174,33 @@ struct Piece {
 
 struct Sched {
   int tiles, kst, P, cta, sk;
-  int64_t W;  // total block iterations
-  __device__ int64_t start(int c) const { return (int64_t)c * W / P; }
+  int64_t W;    // total block iterations
+  bool narrow;  // W * P < 2^32: every product below fits 32 bits (64-bit division is a long software routine)
+  __device__ void init(int tiles_, int kst_, int grid, int cta_, int sk_) {
+    tiles = tiles_;
+    kst = kst_;
+    W = (int64_t)tiles * kst;
+    P = sk_ ? (int)((int64_t)grid < W ? grid : W) : grid;
+    cta = cta_;
+    sk = sk_;
+    narrow = (uint64_t)W * (uint64_t)(P > 0 ? P : 1) < (1ull << 32);
+  }
+  __device__ int64_t start(int c) const {
+    return narrow ? (int64_t)(((uint32_t)c * (uint32_t)W) / (uint32_t)P) : (int64_t)c * W / P;
+  }
   // largest CTA whose range starts at or before iteration it
-  __device__ int cta_of(int64_t it) const { return (int)(((it + 1) * P - 1) / W); }
+  __device__ int cta_of(int64_t it) const {
+    return narrow ? (int)(((uint32_t)(it + 1) * (uint32_t)P - 1u) / (uint32_t)W) : (int)(((it + 1) * P - 1) / W);
+  }
+  __device__ void split(int64_t it, int& t, int& g) const {  // iteration -> (tile, K block)
+    if (narrow) {
+      t = (int)((uint32_t)it / (uint32_t)kst);
+      g = (int)((uint32_t)it - (uint32_t)t * (uint32_t)kst);
+    } else {
+      t = (int)(it / kst);
+      g = (int)(it - (int64_t)t * kst);
+    }
+  }
 };
 
 template <typename F>
@@ -190,8 +213,8 @@ __device__ __forceinline__ void for_each_piece(const Sched& s, F&& f) {
   int64_t it = it0;
   bool first = true;
   while (it < it1) {
-    const int t = (int)(it / s.kst);
-    const int g0 = (int)(it % s.kst);
+    int t, g0;
+    s.split(it, t, g0);
     const int64_t left = it1 - it;
     const int g1 = (int)((int64_t)g0 + left < s.kst ? g0 + left : s.kst);
     f(Piece{t, g0, g1, g0 == 0 && g1 == s.kst, 2 * s.cta + (first ? 0 : 1)});
@@ -315,12 +338,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
   const int total_tiles = args.moe ? sh.tile_prefix_total * args.n_tiles : args.m_tiles * args.n_tiles;
 
   Sched sched;
-  sched.tiles = total_tiles;
-  sched.kst = args.kst;
-  sched.W = (int64_t)total_tiles * args.kst;
-  sched.P = args.sk ? (int)((int64_t)gridDim.x < sched.W ? gridDim.x : sched.W) : (int)gridDim.x;
-  sched.cta = blockIdx.x;
-  sched.sk = args.sk;
+  sched.init(total_tiles, args.kst, (int)gridDim.x, (int)blockIdx.x, args.sk);
   const bool active = (int)blockIdx.x < sched.P && total_tiles > 0;
   volatile int* abort_flag = &sh.abort_flag;
 
@@ -386,48 +404,77 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
     __syncwarp();
   } else if (active && warp == APROD_WARP) {
     // ============================================================ activation producer
-    int as = 0;
-    uint32_t aph = 0;
-    bool ok = true;
-    int armed[C::SA];
-#pragma unroll
-    for (int s = 0; s < C::SA; ++s) armed[s] = 0;
     constexpr int A_BOX_BYTES = BT * 128;
     constexpr int SF_BOX_BYTES = BT * 16;
-    for_each_piece(sched, [&](const Piece& pc) {
-      if (!ok) return;
-      int e, row0, nrows;
-      tile_rows(pc.tile, e, row0, nrows);
-      int rbase = row0;  // first row of the 2-D box (dense, or grouped MoE)
-      if (args.moe && args.grouped) rbase += args.row_off[e];
-      if (args.moe && !args.grouped) {
+    if (!args.moe || args.grouped) {
+      // 2-D boxes: one thread runs the loop (a warp-wide loop would reconverge around every wait)
+      if (lane == 0) {
+        int as = 0;
+        uint32_t aph = 0;
+        bool ok = true;
+        uint32_t armed = 0;  // stages with a load issued (bit s)
+        for_each_piece(sched, [&](const Piece& pc) {
+          if (!ok) return;
+          int e, row0, nrows;
+          tile_rows(pc.tile, e, row0, nrows);
+          const int rbase = row0 + (args.moe ? args.row_off[e] : 0);  // first row of the box
+          for (int g = pc.g0; g < pc.g1; ++g) {
+            for (int j = 0; j < C::SUB; ++j) {
+              if (!mbar_wait(&sh.a_empty[as], aph ^ 1, abort_flag, WAIT_LIMIT_NS)) {
+                fail(ERR_TIMEOUT);
+                ok = false;
+                return;
+              }
+              uint8_t* dst = aring + as * C::A_STAGE;
+              // x offset of this stage in the tensor map's element units (bf16: 64 per stage; bytes: 128)
+              const int x = PATH == PATH_INT4 ? g * 128 + j * 64 : g * 128;
+              mbar_arrive_expect_tx(&sh.a_full[as], A_BOX_BYTES + (PATH == PATH_NVFP4 ? SF_BOX_BYTES : 0));
+              tma_load_2d(dst, &args.tmap_a, x, rbase, &sh.a_full[as]);
+              if (PATH == PATH_NVFP4) tma_load_2d(dst + C::ACT_REGION, &args.tmap_sf, g * 16, rbase, &sh.a_full[as]);
+              armed |= 1u << as;
+              if (++as == C::SA) {
+                as = 0;
+                aph ^= 1;
+              }
+            }
+          }
+        });
+        if (!ok) {
+          // aborted: let this CTA's loads land before shared memory is released
+          int never = 0;
+          for (int s = 0; s < C::SA; ++s)
+            if (armed & (1u << s)) mbar_wait(&sh.a_full[s], (s < as) ? aph : (aph ^ 1), &never, 200000000ull);
+        }
+      }
+      __syncwarp();
+    } else {
+      // routed rows: the warp's lanes issue the four-row gathers in parallel
+      int as = 0;
+      uint32_t aph = 0;
+      bool ok = true;
+      uint32_t armed = 0;
+      for_each_piece(sched, [&](const Piece& pc) {
+        if (!ok) return;
+        int e, row0, nrows;
+        tile_rows(pc.tile, e, row0, nrows);
         // token index of every row of the tile; rows past the expert's count read zeros (row M)
         for (int i = lane; i < BT; i += 32)
           sh.rows_tok[i] = i < nrows ? args.region[e * args.region_cap + row0 + i] / args.topk : args.M;
         __syncwarp();
-      }
-      for (int g = pc.g0; g < pc.g1; ++g) {
-        for (int j = 0; j < C::SUB; ++j) {
-          if (lane == 0) {
-            if (!mbar_wait(&sh.a_empty[as], aph ^ 1, abort_flag, WAIT_LIMIT_NS)) {
-              fail(ERR_TIMEOUT);
-              ok = false;
-            }
-          }
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-          if (!ok) return;
-          uint8_t* dst = aring + as * C::A_STAGE;
-          // x offset of this stage in the tensor map's element units (bf16: 64 per stage; bytes: 128)
-          const int x = PATH == PATH_INT4 ? g * 128 + j * 64 : g * 128;
-          if (lane == 0) mbar_arrive_expect_tx(&sh.a_full[as], A_BOX_BYTES + (PATH == PATH_NVFP4 ? SF_BOX_BYTES : 0));
-          __syncwarp();
-          if (!args.moe || args.grouped) {
+        for (int g = pc.g0; g < pc.g1; ++g) {
+          for (int j = 0; j < C::SUB; ++j) {
             if (lane == 0) {
-              tma_load_2d(dst, &args.tmap_a, x, rbase, &sh.a_full[as]);
-              if (PATH == PATH_NVFP4) tma_load_2d(dst + C::ACT_REGION, &args.tmap_sf, g * 16, rbase, &sh.a_full[as]);
+              if (!mbar_wait(&sh.a_empty[as], aph ^ 1, abort_flag, WAIT_LIMIT_NS)) {
+                fail(ERR_TIMEOUT);
+                ok = false;
+              }
             }
-          } else {
-            // routed rows: the warp's lanes issue the four-row gathers in parallel
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) return;
+            uint8_t* dst = aring + as * C::A_STAGE;
+            const int x = PATH == PATH_INT4 ? g * 128 + j * 64 : g * 128;
+            if (lane == 0) mbar_arrive_expect_tx(&sh.a_full[as], A_BOX_BYTES + (PATH == PATH_NVFP4 ? SF_BOX_BYTES : 0));
+            __syncwarp();
             for (int i = lane * 4; i < BT; i += 128) {
               uint8_t* d = dst + (i >> 3) * 1024 + (i & 7) * 128;
               tma_gather4(d, &args.tmap_a, x, sh.rows_tok[i], sh.rows_tok[i + 1], sh.rows_tok[i + 2],
@@ -436,22 +483,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
                 tma_gather4(dst + C::ACT_REGION + (i >> 2) * 128, &args.tmap_sf, g * 16, sh.rows_tok[i],
                             sh.rows_tok[i + 1], sh.rows_tok[i + 2], sh.rows_tok[i + 3], &sh.a_full[as]);
             }
-          }
-          if (lane == 0) ++armed[as];
-          if (++as == C::SA) {
-            as = 0;
-            aph ^= 1;
+            armed |= 1u << as;
+            if (++as == C::SA) {
+              as = 0;
+              aph ^= 1;
+            }
           }
         }
+        __syncwarp();  // rows_tok is rewritten for the next piece
+      });
+      if (!ok && lane == 0) {
+        int never = 0;
+        for (int s = 0; s < C::SA; ++s)
+          if (armed & (1u << s)) mbar_wait(&sh.a_full[s], (s < as) ? aph : (aph ^ 1), &never, 200000000ull);
       }
-      __syncwarp();  // rows_tok is rewritten for the next piece
-    });
-    if (!ok && lane == 0) {
-      int never = 0;
-      for (int s = 0; s < C::SA; ++s)
-        if (armed[s] > 0) mbar_wait(&sh.a_full[s], (uint32_t)((armed[s] - 1) & 1), &never, 200000000ull);
+      __syncwarp();
     }
-    __syncwarp();
   } else if (active && warp == MMA_WARP) {
     // ============================================================ MMA issuer
     if (lane == 0) {

@@ -45,7 +45,6 @@ struct SmallSmem {
   uint64_t empty[16];
   int abort_flag;
   int tile_prefix_total;
-  int rows_tok[32];
   uint64_t epi_bar;  // bounded barrier of the 8 compute warps (K-half exchange)
 };
 
@@ -110,12 +109,7 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
   __syncthreads();
   const int total_tiles = args.moe ? sh.tile_prefix_total * args.n_tiles : args.m_tiles * args.n_tiles;
   Sched sched;
-  sched.tiles = total_tiles;
-  sched.kst = args.kst;
-  sched.W = (int64_t)total_tiles * args.kst;
-  sched.P = args.sk ? (int)((int64_t)gridDim.x < sched.W ? gridDim.x : sched.W) : (int)gridDim.x;
-  sched.cta = blockIdx.x;
-  sched.sk = args.sk;
+  sched.init(total_tiles, args.kst, (int)gridDim.x, (int)blockIdx.x, args.sk);
   const bool active = (int)blockIdx.x < sched.P && total_tiles > 0;
   volatile int* abort_flag = &sh.abort_flag;
   auto fail = [&](int code) {
@@ -139,62 +133,63 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
   };
 
   if (active && warp == SM_PROD_WARP) {
-    // ============================================================ producer
-    int st = 0;
-    uint32_t ph = 0;
-    bool ok = true;
-    int armed[C::STAGES];
-#pragma unroll
-    for (int s = 0; s < C::STAGES; ++s) armed[s] = 0;
-    for_each_piece(sched, [&](const Piece& pc) {
-      if (!ok) return;
-      int e, row0, nrows;
-      tile_rows(pc.tile, e, row0, nrows);
-      const int nt = pc.tile % args.n_tiles;
-      int rbase = row0;  // first row of the 2-D box (dense, or grouped MoE)
-      if (args.moe && args.grouped) rbase += args.row_off[e];
-      if (args.moe && !args.grouped) {
-        for (int i = lane; i < BT; i += 32)
-          sh.rows_tok[i] = i < nrows ? args.region[e * args.region_cap + row0 + i] / args.topk : args.M;
-        __syncwarp();
-      }
-      const uint8_t* wblk = args.w + e * args.w_expert_bytes + ((int64_t)nt * args.kst) * args.w_blk;
-      for (int g = pc.g0; g < pc.g1; ++g) {
-        if (lane == 0 && !mbar_wait(&sh.empty[st], ph ^ 1, abort_flag, WAIT_LIMIT_NS)) {
-          fail(ERR_TIMEOUT);
-          ok = false;
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    // ============================================================ producer (one thread: a warp-wide loop
+    // would reconverge the warp around every wait)
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      uint32_t armed = 0;  // stages with a copy issued (bit s)
+      for_each_piece(sched, [&](const Piece& pc) {
         if (!ok) return;
-        uint8_t* base = smem + st * C::STAGE;
-        uint8_t* act = base + C::W_REGION;
-        if (lane == 0) {
+        int e, row0, nrows;
+        tile_rows(pc.tile, e, row0, nrows);
+        const int nt = pc.tile % args.n_tiles;
+        int rbase = row0;  // first row of the 2-D box (dense, or grouped MoE)
+        if (args.moe && args.grouped) rbase += args.row_off[e];
+        int rows_tok[BT];  // MoE indexed: token of each row of the tile; rows past the expert's count read zeros
+        if (args.moe && !args.grouped)
+          for (int i = 0; i < BT; ++i)
+            rows_tok[i] = i < nrows ? args.region[e * args.region_cap + row0 + i] / args.topk : args.M;
+        const uint8_t* wblk = args.w + e * args.w_expert_bytes + ((int64_t)nt * args.kst) * args.w_blk;
+        for (int g = pc.g0; g < pc.g1; ++g) {
+          if (!mbar_wait(&sh.empty[st], ph ^ 1, abort_flag, WAIT_LIMIT_NS)) {
+            fail(ERR_TIMEOUT);
+            ok = false;
+            return;
+          }
+          uint8_t* base = smem + st * C::STAGE;
+          uint8_t* act = base + C::W_REGION;
           mbar_arrive_expect_tx(&sh.full[st], (uint32_t)args.w_blk + C::ACT_BYTES);
           bulk_g2s(base, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk, &sh.full[st]);
-          if (!args.moe || args.grouped)
+          if (!args.moe || args.grouped) {
             for (int j = 0; j < 2; ++j)
               tma_load_2d(act + j * (BT * 128), &args.tmap_a, g * 128 + j * 64, rbase, &sh.full[st]);
-          ++armed[st];
+          } else {
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+              for (int i = 0; i < BT; i += 4)
+                tma_gather4(act + j * (BT * 128) + (i >> 3) * 1024 + (i & 7) * 128, &args.tmap_a, g * 128 + j * 64,
+                            rows_tok[i], rows_tok[i + 1], rows_tok[i + 2], rows_tok[i + 3], &sh.full[st]);
+          }
+          armed |= 1u << st;
+          if (++st == C::STAGES) {
+            st = 0;
+            ph ^= 1;
+          }
         }
-        if (args.moe && !args.grouped) {
-          __syncwarp();  // the expected bytes are posted before any gather can complete
-          // lane l gathers rows 4l..4l+3 of one 64-K atom: BT / 4 lanes per atom
-          const int i = (lane * 4) % BT, j = (lane * 4) / BT;
-          if (j < 2)
-            tma_gather4(act + j * (BT * 128) + (i >> 3) * 1024 + (i & 7) * 128, &args.tmap_a, g * 128 + j * 64,
-                        sh.rows_tok[i], sh.rows_tok[i + 1], sh.rows_tok[i + 2], sh.rows_tok[i + 3], &sh.full[st]);
-        }
-        if (++st == C::STAGES) {
-          st = 0;
-          ph ^= 1;
-        }
+      });
+      if (!ok) {
+        // aborted: let this CTA's copies land before shared memory is released (every armed stage's last
+        // phase completes once its bytes arrive)
+        int never = 0;
+        for (int s = 0; s < C::STAGES; ++s)
+          if (armed & (1u << s)) {
+            const uint32_t par = (s < st) ? ph : (ph ^ 1);  // phase of the stage's most recent fill
+            mbar_wait(&sh.full[s], par, &never, 200000000ull);
+          }
       }
-      __syncwarp();
-    });
-    if (!ok && lane == 0) {
-      int never = 0;
-      for (int s = 0; s < C::STAGES; ++s)
-        if (armed[s] > 0) mbar_wait(&sh.full[s], (uint32_t)((armed[s] - 1) & 1), &never, 200000000ull);
     }
     __syncwarp();
   } else if (active && warp < 8) {

@@ -41,20 +41,15 @@ __global__ void __launch_bounds__(RED_THREADS) splitk_reduce_kernel(const __grid
   const int total_tiles = args.moe ? total_sh * args.n_tiles : args.m_tiles * args.n_tiles;
   if (total_tiles <= 0) return;
   Sched s;
-  s.tiles = total_tiles;
-  s.kst = args.kst;
-  s.W = (int64_t)total_tiles * args.kst;
-  s.P = (int)((int64_t)gemm_grid < s.W ? gemm_grid : s.W);
-  s.cta = 0;
-  s.sk = 1;
+  s.init(total_tiles, args.kst, gemm_grid, 0, 1);
   const int chunks = (bt + RED_COLS - 1) / RED_COLS;
   const bool vec_store = (args.N & 3) == 0 && (reinterpret_cast<uintptr_t>(args.c) & 7) == 0;
   // work item = (tile, chunk of RED_COLS columns); thread = 4 consecutive rows of one column, 4 columns apart
   const int r4 = (tid & 31) * 4;
   const int cq = tid >> 5;  // 0..7
-  for (int64_t item = blockIdx.x; item < (int64_t)total_tiles * chunks; item += gridDim.x) {
-    const int tile = (int)(item / chunks);
-    const int col0 = (int)(item % chunks) * RED_COLS;
+  for (int item = blockIdx.x; item < total_tiles * chunks; item += gridDim.x) {
+    const int tile = (int)((uint32_t)item / (uint32_t)chunks);
+    const int col0 = (int)((uint32_t)item - (uint32_t)tile * (uint32_t)chunks) * RED_COLS;
     const int64_t first_it = (int64_t)tile * s.kst;
     const int c_first = s.cta_of(first_it);
     const int c_last = s.cta_of(first_it + s.kst - 1);
