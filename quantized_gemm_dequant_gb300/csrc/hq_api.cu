@@ -98,11 +98,15 @@ int pick_bt_dense(int64_t M) {
   if (M <= 128) return 128;
   return 256;
 }
-int pick_bt_moe(int64_t rows, int64_t E) {
+// MoE token tile by the mean routed rows per expert.  The UMMA step costs the same for any tile up to 128 tokens
+// (256 for the FP4 kinds' wide tiles), so once experts carry more than a handful of rows the widest tile wins even
+// with the padding of the rarely routed experts; 16-token tiles keep the INT4 register-decode kernel for sparse
+// routing.  Dense-only 256-token INT4 and NVFP4 tiles carry no per-row tables, hence at most 128 for them.
+int pick_bt_moe(int path, int64_t rows, int64_t E) {
+  if (E == 1) return pick_bt_dense(rows);  // one expert is a dense GEMM over the routed rows
   const int64_t avg = (rows + E - 1) / E;
   if (avg <= 16) return 16;
-  if (avg <= 32) return 32;
-  if (avg <= 64) return 64;
+  if (path == PATH_MXFP4 && avg > 128) return 256;
   return 128;
 }
 
@@ -147,7 +151,7 @@ Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int
   } else {
     const int64_t rows = M_or_T * topk;
     const int64_t E = f->num_experts;
-    p.bt = pick_bt_moe(rows, E);
+    p.bt = pick_bt_moe(g.path, rows, E);
     p.region_cap = M_or_T;
     const int64_t active = rows < E ? rows : E;
     p.max_tiles = p.n_tiles * (active + (rows + p.bt - 1) / p.bt);

@@ -278,3 +278,11 @@ def test_moe_grouped_wide_tiles_match_indexed(lib, monkeypatch):
         outs.append(_run_moe(lib, inp).cpu())
     assert torch.equal(outs[0], outs[1])
     R.assert_parity(outs[1], R.moe_ref(inp), "grouped wide tiles")
+
+
+@pytest.mark.parametrize("moe_path", ["indexed", "grouped"])
+def test_moe_mxfp4_256_token_tiles(lib, monkeypatch, moe_path):
+    """More than 128 routed rows per expert take MXFP4's 256-token tiles (wide tiles with per-row tables)."""
+    monkeypatch.setenv("HQ_MOE_PATH", moe_path)
+    inp = make_moe(MOE_FORMS["mxfp4"], 300, seed=11, E=4, N=256, K=512, topk=2)
+    R.assert_parity(_run_moe(lib, inp), R.moe_ref(inp), f"moe mxfp4 256-token tiles {moe_path}")
