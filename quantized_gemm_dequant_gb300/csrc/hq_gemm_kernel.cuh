@@ -16,8 +16,9 @@
 //              tiles in tensor memory (warp w: lane quarter w%4, K half w/4).
 //              FP4 paths: warps 0-3 copy block scales into tensor memory;
 //              MXFP4 warps 4-7 expand packed e2m1 into the MMA's 16-byte
-//              padded layout.  All 8: epilogue (tensor memory -> scales ->
-//              bf16 store, or a split-K partial + last-arriver reduction).
+//              padded layout.
+//              All 8: epilogue (tensor memory -> scales -> bf16 store, or a
+//              split-K partial).
 //   warp 8     weight producer (one thread): bulk copies.
 //   warp 9     activation producer: TMA loads (one thread issues; the warp
 //              reads the routed-row table for MoE).
@@ -617,7 +618,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
       tmem_st_x<8>(tmem + lane_base + 256 + 4 * C::SW, ones);
       tmem_wait_st();
     }
-    const bool in_mainloop = !(PATH == PATH_NVFP4 && warp >= 4);
     constexpr int HC = BT / 2;
     // Per-column output rows and multipliers: MoE rows and per-token activation scales.  INT4 and NVFP4
     // tiles of 256 tokens are dense only (the host tiles MoE rows by at most 128), so they carry no table.
@@ -665,7 +665,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
     };
     // mainloop role for the next nblk weight blocks, in ring order
     auto mainloop = [&](int nblk) -> bool {
-      for (int k = 0; in_mainloop && k < nblk; ++k) {
+      for (int k = 0; !(PATH == PATH_NVFP4 && warp >= 4) && k < nblk; ++k) {  // NVFP4 warps 4-7: epilogue only
         if (!waitf(&sh.w_full[ws], wph)) return false;
         uint8_t* wb = wring + ws * C::W_STAGE;
         if (PATH == PATH_INT4) {
@@ -704,35 +704,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
             aslph ^= 1;
           }
         } else {
-          if (warp < 4) {
+          if (PATH == PATH_NVFP4 && warp < 4) {
             // scale factors -> tensor memory (replicated in every lane quarter)
-            if (PATH == PATH_NVFP4) {
-              const uint32_t* wsf = reinterpret_cast<const uint32_t*>(wb + 16384);
-              uint32_t v[16];
+            const uint32_t sf = tmem + lane_base + 256 + ws * C::SF_STAGE_COLS;
+            // lane l's 16 words (4 MMA steps x 4 row groups) are contiguous: four 16-byte loads
+            const uint4* wsf = reinterpret_cast<const uint4*>(wb + 16384) + lane * 4;
+            uint32_t v[16];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] = wsf[j * 32 + lane];
-              const uint32_t sf = tmem + lane_base + 256 + ws * C::SF_STAGE_COLS;
-              tmem_st_x<16>(sf, v);
-              if (!waitf(&sh.a_full[as], aph)) return false;
-              const uint8_t* asf = aring + as * C::A_STAGE + C::ACT_REGION;
-#pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                uint32_t b[C::CB];
-#pragma unroll
-                for (int cc = 0; cc < C::CB; ++cc) {
-                  const int j = cc * 32 + lane;
-                  const int off = (args.moe && !args.grouped) ? (j >> 2) * 128 + (j & 3) * 16 : j * 16;
-                  b[cc] = *reinterpret_cast<const uint32_t*>(asf + off + t * 4);
-                }
-                tmem_st_x<C::CB>(sf + 16 + t * C::SFB_STEP, b);
-              }
-            } else {
-              const uint32_t* wsf = reinterpret_cast<const uint32_t*>(wb + 8192);
-              uint32_t v[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) v[j] = wsf[j * 32 + lane];
-              tmem_st_x<4>(tmem + lane_base + 256 + ws * 4, v);
+            for (int j = 0; j < 4; ++j) {
+              const uint4 q = wsf[j];
+              v[4 * j] = q.x;
+              v[4 * j + 1] = q.y;
+              v[4 * j + 2] = q.z;
+              v[4 * j + 3] = q.w;
             }
+            tmem_st_x<16>(sf, v);
+            if (!waitf(&sh.a_full[as], aph)) return false;
+            const uint8_t* asf = aring + as * C::A_STAGE + C::ACT_REGION;
+            // one 16-byte load per activation row holds its scales of all four MMA steps
+            uint4 rq[C::CB];
+#pragma unroll
+            for (int cc = 0; cc < C::CB; ++cc) {
+              const int j = cc * 32 + lane;
+              const int off = (args.moe && !args.grouped) ? (j >> 2) * 128 + (j & 3) * 16 : j * 16;
+              rq[cc] = *reinterpret_cast<const uint4*>(asf + off);
+            }
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              uint32_t b[C::CB];
+#pragma unroll
+              for (int cc = 0; cc < C::CB; ++cc)
+                b[cc] = t == 0 ? rq[cc].x : (t == 1 ? rq[cc].y : (t == 2 ? rq[cc].z : rq[cc].w));
+              tmem_st_x<C::CB>(sf + 16 + t * C::SFB_STEP, b);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+          } else if (warp < 4) {
+            // MXFP4 weight scale factors -> tensor memory (replicated in every lane quarter)
+            const uint32_t* wsf = reinterpret_cast<const uint32_t*>(wb + 8192);
+            uint32_t v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = wsf[j * 32 + lane];
+            tmem_st_x<4>(tmem + lane_base + 256 + ws * 4, v);
             tmem_wait_st();
             tc_fence_before();
           } else if (PATH == PATH_MXFP4) {

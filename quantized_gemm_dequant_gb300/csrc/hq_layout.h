@@ -18,8 +18,8 @@
 //                   K-major tile with the 128-byte swizzle (16-byte chunk c of row r
 //                   at (r/8)*1024 + (r%8)*128 + ((c ^ r%8) * 16)), low nibble = even k
 //    [16384, 18432) ue4m3 block-16 scales as tensor-memory words: word
-//                   ((t*4 + c)*32 + l) holds the 4 scales of MMA step t (64 K) of
-//                   row 32c + l
+//                   (l*16 + t*4 + c) holds the 4 scales of MMA step t (64 K) of
+//                   row 32c + l (the 16 words of lane l are contiguous)
 //    global scales: fp32 [E] after the last expert's blocks
 //  MXFP4, K stage = 128:
 //    [0, 8192)      e2m1 codes, 8 bytes (16 K) per piece, piece p = r*8 + c lands in

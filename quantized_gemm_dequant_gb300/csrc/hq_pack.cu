@@ -84,7 +84,7 @@ __global__ void pack_kernel(PackArgs p, uint8_t* codes, uint8_t* scales, uint8_t
       const int l = r & 31, cq = r >> 5;
       const int64_t nb = p.K / 16;
       for (int tt = 0; tt < 4; ++tt) {
-        uint8_t* d = blk + 16384 + ((tt * 4 + cq) * 32 + l) * 4;
+        uint8_t* d = blk + 16384 + (l * 16 + tt * 4 + cq) * 4;
         uint8_t* s = scales + (e * p.N + n) * nb + ks * 16 + tt * 4;
         for (int b = 0; b < 4; ++b) {
           if (DIR == 0) d[b] = valid ? s[b] : (uint8_t)0;
