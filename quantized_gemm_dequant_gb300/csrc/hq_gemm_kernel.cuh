@@ -14,9 +14,9 @@
 // Warp roles (352 threads):
 //   warps 0-7  INT4 path: decode the weight block's 4-bit codes into bf16 A
 //              tiles in tensor memory (warp w: lane quarter w%4, K half w/4).
-//              FP4 paths: warps 0-3 copy block scales into tensor memory;
-//              MXFP4 warps 4-7 expand packed e2m1 into the MMA's 16-byte
-//              padded layout.
+//              NVFP4: warps 0-3 copy block scales into tensor memory.
+//              MXFP4: warps 0-3 copy the weight block scales, and all 8
+//              expand packed e2m1 into the MMA's 16-byte padded layout.
 //              All 8: epilogue (tensor memory -> scales -> bf16 store, or a
 //              split-K partial).
 //   warp 8     weight producer (one thread): bulk copies.
@@ -739,27 +739,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
             }
             tmem_wait_st();
             tc_fence_before();
-          } else if (warp < 4) {
-            // MXFP4 weight scale factors -> tensor memory (replicated in every lane quarter)
-            const uint32_t* wsf = reinterpret_cast<const uint32_t*>(wb + 8192);
-            uint32_t v[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = wsf[j * 32 + lane];
-            tmem_st_x<4>(tmem + lane_base + 256 + ws * 4, v);
-            tmem_wait_st();
-            tc_fence_before();
           } else if (PATH == PATH_MXFP4) {
-            // expand packed e2m1 (8 bytes per 16 K) into the padded 16-byte chunks
+            if (warp < 4) {
+              // weight scale factors -> tensor memory (replicated in every lane quarter)
+              const uint32_t* wsf = reinterpret_cast<const uint32_t*>(wb + 8192);
+              uint32_t v[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) v[j] = wsf[j * 32 + lane];
+              tmem_st_x<4>(tmem + lane_base + 256 + ws * 4, v);
+            }
+            // all 8 warps: expand packed e2m1 (8 bytes per 16 K) into the padded 16-byte chunks, two chunks of a
+            // row per 16-byte load
             uint8_t* xt = wb + C::W_REGION;
-            const int t128 = tid - 128;
-#pragma unroll 4
-            for (int p = t128; p < 1024; p += 128) {
-              const uint2 v = *reinterpret_cast<const uint2*>(wb + p * 8);
-              const int rr = p >> 3, cc = p & 7;
-              *reinterpret_cast<uint4*>(xt + (rr >> 3) * 1024 + (rr & 7) * 128 + ((cc ^ (rr & 7)) << 4)) =
-                  make_uint4(v.x, v.y, 0u, 0u);
+#pragma unroll
+            for (int q = tid; q < 512; q += 256) {
+              const uint4 v = *reinterpret_cast<const uint4*>(wb + q * 16);
+              const int rr = q >> 2, cc = (q & 3) * 2;
+              uint8_t* row = xt + (rr >> 3) * 1024 + (rr & 7) * 128;
+              *reinterpret_cast<uint4*>(row + ((cc ^ (rr & 7)) << 4)) = make_uint4(v.x, v.y, 0u, 0u);
+              *reinterpret_cast<uint4*>(row + (((cc + 1) ^ (rr & 7)) << 4)) = make_uint4(v.z, v.w, 0u, 0u);
             }
             fence_proxy_async_smem();
+            if (warp < 4) {
+              tmem_wait_st();
+              tc_fence_before();
+            }
           }
           __syncwarp();
           if (lane == 0) {
