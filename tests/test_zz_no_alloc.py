@@ -38,11 +38,12 @@ def test_static_scratch_matches_workspace_call_twice(lib):
 
 
 def test_static_scratch_rejects_oversized_calls(lib):
-    # 200 tokens over 14336 x 4096 needs ~40 MB of split-K partials: more than the fixed 16 MiB
-    fmt = lib.make_format("uint4_zp", 14336, 4096)
-    assert lib.workspace_bytes(fmt, 200) > 16 << 20
-    act = {"data": torch.zeros(200, 4096, dtype=torch.bfloat16, device="cuda")}
+    # 512 tokens over 4096 x 4096: 64 tiles of 256 tokens are split along K (Stream-K), whose ~40 MB of partial
+    # sums exceed the fixed 16 MiB
+    fmt = lib.make_format("uint4_zp", 4096, 4096)
+    assert lib.workspace_bytes(fmt, 512) > 16 << 20
+    act = {"data": torch.zeros(512, 4096, dtype=torch.bfloat16, device="cuda")}
     packed = torch.zeros(lib.packed_bytes(fmt), dtype=torch.uint8, device="cuda")
     with pytest.raises(lib.HQError) as e:
-        lib.gemm_static_scratch(fmt, act, packed, 200)
+        lib.gemm_static_scratch(fmt, act, packed, 512)
     assert e.value.code == lib.HQ_ERR_WORKSPACE
