@@ -270,7 +270,9 @@ def run_ours(args):
     for (M, _, info, _, _, _), ms, ns in zip(calls, per_call_ms, per_call_n):
         t = statistics.median(ms) * 1e-3
         bound, frac = roofline_of(info, t, pk, dt)
-        e = dict(M=M, us=round(t * 1e6, 2), tflops=round(info["flops"] / t / 1e12, 3),
+        q = sorted(ms)
+        e = dict(M=M, us=round(t * 1e6, 2), p10_us=round(q[len(q) // 10] * 1e3, 2),
+                 p90_us=round(q[min(len(q) - 1, (9 * len(q)) // 10)] * 1e3, 2), tflops=round(info["flops"] / t / 1e12, 3),
                  weight_gbs=round(info["weight_bytes"] / t / 1e9, 1), total_gbs=round(info["total_bytes"] / t / 1e9, 1),
                  bound=bound, roofline_frac=round(frac, 4))
         if "experts_hit" in info:
@@ -296,6 +298,7 @@ def run_ours(args):
                 f"{'burst bf16 x nominal ratio' if dt != 'bf16' else 'burst'})", traffic=traffic_of(dom, args.config))
 
     e2e = measure_e2e(args, calls, stream, dev) if not args.no_e2e else None
+    ctx = cublas_context(args, calls, sweep, stream, dev) if (rank == 0 and not args.no_context) else None
     cpu = cpu_baseline_line(args) if (rank == 0 and not args.no_cpu) else None
     line = {
         "metric": "quantized GEMM TFLOP/s and weight GB/s vs M; % of HBM / tensor-core roofline",
@@ -311,6 +314,7 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof, "sweep": sweep, "gpu_launches": gpu_launches(args.config, fmt, calls) * args.steps,
         "clocks": clocks, "wall_s_timed": round(t_wall, 3), "e2e": e2e, "cpu_baseline": cpu,
+        "context_cublas_bf16": ctx,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -378,6 +382,37 @@ def workload_name(cfg):
                 f"M in {c['sizes']}")
     return (f"MoE {c['wfmt']} x {c['afmt']}, E={c['E']}, top-{c['topk']}, K={c['K']}, N={c['N']}, "
             f"T in {c['sizes']}, Zipf(1.1) routing")
+
+
+def cublas_context(args, calls, sweep, stream, dev):
+    """Context only (the pages compare W4A16 with cuBLAS at small batch): torch.matmul in bf16 on bf16 weights of the
+    same shape, timed with the same protocol (bursts of back-to-back calls over replicas larger than L2)."""
+    c = W.CONFIGS[args.config]
+    if c["kind"] != "dense" or c["afmt"] != "bf16":
+        return None
+    R = 4
+    wts = [W.weights_fp32(args.seed, 1, c["N"], c["K"], device=dev).to(torch.bfloat16) for _ in range(R)]
+    rows = []
+    for (M, call, info, acts, outs, wss), ours in zip(calls, sweep):
+        a = acts[0]["data"]
+        outs_c = [torch.empty((M, c["N"]), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+        samples = []
+        for it in range(6):
+            torch.cuda._sleep(SPIN_CYCLES)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for r in range(R):
+                torch.matmul(a, wts[r].t(), out=outs_c[r])
+            e1.record(stream)
+            samples.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        t = statistics.median(e0.elapsed_time(e1) / R for e0, e1 in samples[1:]) * 1e-3
+        rows.append(dict(M=M, us=round(t * 1e6, 2), tflops=round(info["flops"] / t / 1e12, 3),
+                         ours_speedup=round(t / (ours["us"] * 1e-6), 3)))
+    del wts
+    return {"what": "torch.matmul bf16 x bf16 weights of the same shape (cuBLAS), same burst protocol; context, "
+                    "not the metric", "sweep": rows}
 
 
 def measure_e2e(args, calls, stream, dev):
@@ -500,6 +535,7 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-context", action="store_true", help="skip the cuBLAS bf16 context timing")
     ap.add_argument("--sizes", default=None, help="comma list overriding the sweep (profiling)")
     ap.add_argument("--replicas", type=int, default=None, help="input replicas (default: enough to exceed L2)")
     ap.add_argument("--burst", type=int, default=None, help="back-to-back calls per timed window (default: replicas)")

@@ -10,6 +10,7 @@ import torch
 
 from tests import ref_helpers as R
 from workload import make_dense, make_moe, quant
+from workload import configs as W
 
 pytestmark = pytest.mark.gpu
 
@@ -286,3 +287,77 @@ def test_moe_mxfp4_256_token_tiles(lib, monkeypatch, moe_path):
     monkeypatch.setenv("HQ_MOE_PATH", moe_path)
     inp = make_moe(MOE_FORMS["mxfp4"], 300, seed=11, E=4, N=256, K=512, topk=2)
     R.assert_parity(_run_moe(lib, inp), R.moe_ref(inp), f"moe mxfp4 256-token tiles {moe_path}")
+
+
+# ------------------------------------------------------------------ code and scale bit patterns, odd N, degenerate groups
+def _random_bits(inp, seed):
+    """Replace the weight codes, scales (and zeros) and the quantized activations of a dense input by random valid
+    bit patterns covering each format's whole code range and a wide scale range (NaN encodings excluded)."""
+    g = torch.Generator().manual_seed(seed)
+    w = inp["w"]
+    w["codes"] = torch.randint(0, 256, w["codes"].shape, generator=g, dtype=torch.int32).to(torch.uint8)
+    if inp["wfmt"] in ("int4_sym", "uint4_zp"):
+        mag = torch.randn(w["scales"].shape, generator=g) * torch.exp2(torch.randint(-12, 4, w["scales"].shape, generator=g).float())
+        w["scales"] = mag.to(torch.bfloat16)
+        if "zeros" in w:
+            w["zeros"] = torch.randint(0, 16, w["zeros"].shape, generator=g, dtype=torch.int32).to(torch.uint8)
+    elif inp["wfmt"] == "nvfp4":
+        w["scales"] = torch.randint(1, 0x7F, w["scales"].shape, generator=g, dtype=torch.int32).to(torch.uint8)
+    else:  # mxfp4: e8m0 2^-30 .. 2^30
+        w["scales"] = torch.randint(97, 158, w["scales"].shape, generator=g, dtype=torch.int32).to(torch.uint8)
+    a = inp["a"]
+    if inp["afmt"] == "e4m3_tok":
+        b = torch.randint(0, 256, a["data"].shape, generator=g, dtype=torch.int32).to(torch.uint8)
+        b[(b & 0x7F) == 0x7F] = 0x3C  # no NaN
+        a["data"] = b
+        a["scale"] = torch.rand(a["scale"].shape, generator=g) * 4 + 0.01
+    elif inp["afmt"] == "nvfp4":
+        a["data"] = torch.randint(0, 256, a["data"].shape, generator=g, dtype=torch.int32).to(torch.uint8)
+        a["scale"] = torch.randint(1, 0x7F, a["scale"].shape, generator=g, dtype=torch.int32).to(torch.uint8)
+    return inp
+
+
+@pytest.mark.parametrize("wfmt", list(DENSE_FORMS))
+@pytest.mark.parametrize("M", [7, 40, 300])
+def test_dense_random_bit_patterns(lib, wfmt, M):
+    """Every code value and a wide range of scale exponents (ue4m3 subnormals included) decode as the oracle does.
+
+    FP4 operands enter the MMA exactly, so the general parity bound applies.  INT4 weights enter as bf16((q - z) * s),
+    one rounding of the exact weight (relative error at most 2^-9), accumulated in fp32 and rounded once to bf16: the
+    bound is then 2^-9 * sum_k |a_k w_k| + 2^-8 * |y| (+ fp32 accumulation), taken from the oracle's exact operands.
+    Random scales spanning 2^-12 .. 2^4 make the general bound too tight for that rounding; a decode error (a wrong
+    code, zero point or scale) is of the size of the weight itself and fails either bound."""
+    inp = make_dense(DENSE_FORMS[wfmt], M, seed=M, N=264, K=512)
+    inp = _random_bits(inp, seed=1000 + M)
+    y = _run_dense(lib, inp)
+    ref = np.asarray(R.dense_ref(inp))
+    if wfmt in ("int4_sym", "uint4_zp"):
+        s_abs = np.abs(np.asarray(R.acts_of(inp))) @ np.abs(np.asarray(R.weights_of(inp))).T
+        bound = 2.0**-9 * s_abs * 1.01 + 2.0**-8 * np.abs(ref) + 1e-6 * s_abs
+        err = np.abs(y.float().cpu().numpy().astype(np.float64) - ref)
+        worst = float(np.max(err / np.maximum(bound, 1e-300)))
+        assert worst <= 1.0, f"{wfmt} M={M} random bits: error {worst:.3f} of the bf16-decode bound"
+    else:
+        R.assert_parity(y, ref, f"{wfmt} M={M} random bits")
+
+
+@pytest.mark.parametrize("wfmt", list(DENSE_FORMS))
+@pytest.mark.parametrize("N", [129, 131])
+@pytest.mark.parametrize("M", [5, 300])
+def test_dense_odd_n(lib, wfmt, N, M):
+    """An odd N leaves a ragged last weight tile and forbids paired 4-byte stores (the per-element path runs)."""
+    inp = make_dense(DENSE_FORMS[wfmt], M, seed=N + M, N=N, K=512, with_bias=wfmt in ("int4_sym", "uint4_zp"))
+    R.assert_parity(_run_dense(lib, inp), R.dense_ref(inp), f"{wfmt} M={M} N={N}")
+
+
+@pytest.mark.parametrize("wfmt", ["int4_sym", "uint4_zp"])
+def test_degenerate_groups(lib, wfmt):
+    """All-zero and constant weight groups quantize to zero scale (and zero point); the rest of the row is unaffected."""
+    c = DENSE_FORMS[wfmt]
+    w = W.weights_fp32(3, 1, 256, 512)
+    w[:, 0:128] = 0.0
+    w[:64, 128:256] = 0.75
+    inp = make_dense(c, 24, seed=3, N=256, K=512)
+    inp["w"] = W.quantize_weights(c["wfmt"], w, c["G"])
+    assert float(inp["w"]["scales"].float()[:, 0].abs().max()) == 0.0
+    R.assert_parity(_run_dense(lib, inp), R.dense_ref(inp), f"{wfmt} degenerate groups")
