@@ -330,7 +330,7 @@ def kernel_name(cfg, M):
         bt = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128 if M <= 128 else 256
     else:
         avg = -(-M * c["topk"] // c["E"])
-        bt = 16 if avg <= 16 else (256 if path == 2 and avg > 128 else 128)
+        bt = 16 if avg <= 16 else (256 if path != 1 and avg > 128 else 128)
     if path == 0 and bt <= 32 and os.environ.get("HQ_FORCE_PATH") != "umma":
         return f"hq::hq_gemm_small_kernel<{bt}>"
     return f"hq::hq_gemm_kernel<{path}, {bt}>"

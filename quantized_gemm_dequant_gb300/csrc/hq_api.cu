@@ -98,15 +98,15 @@ int pick_bt_dense(int64_t M) {
   if (M <= 128) return 128;
   return 256;
 }
-// MoE token tile by the mean routed rows per expert.  The UMMA step costs the same for any tile up to 128 tokens
-// (256 for the FP4 kinds' wide tiles), so once experts carry more than a handful of rows the widest tile wins even
-// with the padding of the rarely routed experts; 16-token tiles keep the INT4 register-decode kernel for sparse
-// routing.  Dense-only 256-token INT4 and NVFP4 tiles carry no per-row tables, hence at most 128 for them.
+// MoE token tile by the mean routed rows per expert.  The UMMA step costs nearly the same for any tile up to 256
+// tokens, so once experts carry more than a handful of rows the wide tiles win even with the padding of the rarely
+// routed experts; 16-token tiles keep the INT4 register-decode kernel for sparse routing.  Dense-only 256-token
+// NVFP4 tiles carry no per-row tables, hence at most 128 for NVFP4.
 int pick_bt_moe(int path, int64_t rows, int64_t E) {
   if (E == 1) return pick_bt_dense(rows);  // one expert is a dense GEMM over the routed rows
   const int64_t avg = (rows + E - 1) / E;
   if (avg <= 16) return 16;
-  if (path == PATH_MXFP4 && avg > 128) return 256;
+  if (path != PATH_NVFP4 && avg > 128) return 256;
   return 128;
 }
 

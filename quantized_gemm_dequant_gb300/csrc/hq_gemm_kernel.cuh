@@ -102,7 +102,10 @@ struct Cfg {
   static constexpr int SF_STAGE_COLS = PATH == PATH_NVFP4 ? 16 + 4 * SFB_STEP : 4;
   static constexpr int NA = 4;  // INT4: tensor-memory A slots of 64 columns
   static constexpr int RING_BYTES = SW * W_STAGE + SA * A_STAGE;
-  static constexpr int SMEM_RAW = RING_BYTES + 1024 /*align*/ + 8192 /*barriers, tile tables, MoE prefix*/;
+  // INT4 256-token tiles keep the epilogue's per-column rows and multipliers (MoE) in shared memory: two pieces x
+  // 8 warps x 128 columns x (row, multiplier); in registers they would spill next to the 128-column accumulator slice
+  static constexpr int TAB_BYTES = (PATH == PATH_INT4 && BT == 256) ? 2 * 8 * (BT / 2) * 8 : 0;
+  static constexpr int SMEM_RAW = RING_BYTES + 1024 /*align*/ + 8192 /*barriers, tile tables, MoE prefix*/ + TAB_BYTES;
   // at least 120 KB so that one CTA (and one 512-column tensor-memory allocation) owns each SM
   static constexpr int SMEM_BYTES = SMEM_RAW < 120 * 1024 ? 120 * 1024 : SMEM_RAW;
   static_assert(SA >= 2, "activation ring too small");
@@ -619,10 +622,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
       tmem_wait_st();
     }
     constexpr int HC = BT / 2;
-    // Per-column output rows and multipliers: MoE rows and per-token activation scales.  INT4 and NVFP4
-    // tiles of 256 tokens are dense only (the host tiles MoE rows by at most 128), so they carry no table.
-    constexpr bool kTables = PATH == PATH_MXFP4 || BT <= 128;
-    constexpr int TPL = kTables ? (HC + 31) / 32 : 1;
+    // Per-column output rows and multipliers: MoE rows and per-token activation scales.  NVFP4 tiles of 256 tokens
+    // are dense only (the host tiles NVFP4 MoE rows by at most 128), so they carry no table; INT4 tiles of 256
+    // tokens keep theirs in shared memory.
+    constexpr bool kSmemTables = C::TAB_BYTES > 0;
+    constexpr bool kTables = PATH == PATH_MXFP4 || BT <= 128 || kSmemTables;
+    constexpr int TPL = (kTables && !kSmemTables) ? (HC + 31) / 32 : 1;
+    int2* tabs = reinterpret_cast<int2*>(smem + C::RING_BYTES + 8192);  // [2][8 warps][HC] when kSmemTables
     const int col0 = h * HC;
     if (!kTables && args.moe) {
       fail(ERR_BAD_ROUTING);
@@ -632,15 +638,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
     struct Pend {
       Piece pc;
       int e, row0, nrows, nt;
+      int ts;  // shared-memory table slot (alternates between consecutive pieces)
       // this warp's epilogue columns [col0, col0 + HC): output row and multiplier of each, one per lane
       // slot, loaded early so that their latency hides behind the mainloop (read back with shuffles)
       int t_row[TPL];
       float t_mul[TPL];
     };
+    int piece_no = 0;
     auto open_piece = [&](const Piece& pc, Pend& pd) {
       pd.pc = pc;
       tile_rows(pc.tile, pd.e, pd.row0, pd.nrows);
       pd.nt = pc.tile % args.n_tiles;
+      pd.ts = piece_no++ & 1;
+      if (kSmemTables) {
+        if (args.moe) {
+          for (int u = 0; u < HC / 32; ++u) {
+            const int i = col0 + u * 32 + lane;
+            int orow = -1;
+            float f = 1.0f;
+            if (i < pd.nrows) {
+              orow = args.region[pd.e * args.region_cap + pd.row0 + i];
+              if (args.topk_w) f = args.topk_w[orow];
+            }
+            tabs[(pd.ts * 8 + warp) * HC + u * 32 + lane] = make_int2(orow, __float_as_int(f));
+          }
+        }
+        return;
+      }
 #pragma unroll
       for (int u = 0; u < TPL; ++u) {
         const int i = col0 + u * 32 + lane;
@@ -791,6 +815,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
       const int* t_row = pd.t_row;
       const float* t_mul = pd.t_mul;
       // ---------------------------------------------------- epilogue
+      if (kSmemTables) __syncwarp();  // the piece's table entries were written by the warp's other lanes
       if (!waitf(&sh.dfull, pidx & 1)) return false;
       tc_fence_after();
       // This warp's whole column range goes to registers first: tensor memory is handed back to the next
@@ -816,7 +841,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
       auto store = [&](int col, float acc) {
         int orow;
         float mul;
-        if (use_table) {
+        if (kSmemTables && use_table) {
+          const int2 t = tabs[(pd.ts * 8 + warp) * HC + (col - col0)];
+          orow = t.x;
+          mul = __int_as_float(t.y);
+        } else if (use_table) {
           const int rel = col - col0;
           const int slot = rel >> 5;
           int tr = t_row[0];
