@@ -21,6 +21,14 @@
  *  - No C++ exception crosses this interface.  No global mutable state is
  *    kept, so calls on different streams with different workspaces may run
  *    concurrently.
+ *  - Kernels are launched with programmatic stream serialization: a call's
+ *    kernels may start while the previous kernel on the stream finishes, and
+ *    wait for it before touching activations, routing tables, workspace or
+ *    outputs.  Packed weights are read-only inputs that a dense GEMM starts
+ *    copying before that wait, so they must be complete when the preceding
+ *    kernel lets its dependents launch: true for hq_pack_weights and for any
+ *    kernel that never executes griddepcontrol.launch_dependents.  Setting
+ *    HQ_PDL=0 in the environment restores plain stream order.
  *  - Weights W are [N, K] per expert ("out, in", as for a linear layer);
  *    the product is C[m, n] = sum_k A[m, k] * Wdeq[n, k].
  *  - 4-bit codes are stored two per byte, the low nibble holding the even k.

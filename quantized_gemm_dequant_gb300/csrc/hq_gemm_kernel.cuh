@@ -19,7 +19,8 @@
 //              expand packed e2m1 into the MMA's 16-byte padded layout.
 //              All 8: epilogue (tensor memory -> scales -> bf16 store, or a
 //              split-K partial).
-//   warp 8     weight producer (one thread): bulk copies.
+//   warp 8     weight producer (one thread): bulk copies (dense calls: the
+//              first ring stages before the grid dependency wait).
 //   warp 9     activation producer: TMA loads (one thread issues; the warp
 //              reads the routed-row table for MoE).
 //   warp 10    MMA issuer (one thread): tcgen05.mma kind::f16 with A from
@@ -279,7 +280,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
     tmem_alloc(&sh.tmem_base, 512);
     tmem_relinquish();
   }
-  if (tid == 32) {
+  // Dense calls: the weight producer issues the copies of its first ring stages before the grid dependency wait
+  // (packed weights are read-only inputs, see hq_launch.h), so that they stream while the previous kernel drains.
+  int npre = 0;  // weight producer thread: stages whose copy is in flight
+  if (tid == WPROD_WARP * 32) {
     for (int s = 0; s < C::SW; ++s) {
       mbar_init(&sh.w_full[s], 1);
       mbar_init(&sh.w_empty[s], PATH == PATH_INT4 ? 8 : (PATH == PATH_NVFP4 ? 4 + 1 : 8 + 1));
@@ -298,13 +302,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
     mbar_init(&sh.drain, 1);
     sh.abort_flag = 0;
     fence_mbar_init();
+    if (!args.moe) {
+      Sched s0;
+      s0.init(args.m_tiles * args.n_tiles, args.kst, (int)gridDim.x, (int)blockIdx.x, args.sk);
+      if ((int)blockIdx.x < s0.P && s0.tiles > 0)
+        for_each_piece(s0, [&](const Piece& pc) {
+          const uint8_t* wblk = args.w + ((int64_t)(pc.tile % args.n_tiles) * args.kst) * args.w_blk;
+          for (int g = pc.g0; g < pc.g1 && npre < C::SW; ++g, ++npre) {
+            mbar_arrive_expect_tx(&sh.w_full[npre], (uint32_t)args.w_blk);
+            bulk_g2s(wring + npre * C::W_STAGE, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk, &sh.w_full[npre]);
+          }
+        });
+    }
   }
   if (tid == APROD_WARP * 32) {
     prefetch_tmap(&args.tmap_a);
     if (PATH == PATH_NVFP4) prefetch_tmap(&args.tmap_sf);
   }
   pdl_trigger();
-  pdl_wait();  // no global memory a previous kernel may write is touched before this point
+  pdl_wait();  // no global memory a previous kernel may write is touched before this point (weights aside)
   // MoE: tile prefix over experts (E <= 512 enforced on the host)
   if (args.moe) {
     for (int e = tid; e < args.E; e += NUM_THREADS) {
@@ -377,20 +393,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
       int armed[C::SW];
 #pragma unroll
       for (int s = 0; s < C::SW; ++s) armed[s] = 0;
+      int blk = 0;  // weight blocks of this CTA so far (the first npre were issued before the wait)
       for_each_piece(sched, [&](const Piece& pc) {
         if (!ok) return;
         int e, row0, nrows;
         tile_rows(pc.tile, e, row0, nrows);
         const int nt = pc.tile % args.n_tiles;
         const uint8_t* wblk = args.w + e * args.w_expert_bytes + ((int64_t)nt * args.kst) * args.w_blk;
-        for (int g = pc.g0; g < pc.g1; ++g) {
-          if (!mbar_wait(&sh.w_empty[ws], wph ^ 1, abort_flag, WAIT_LIMIT_NS)) {
-            fail(ERR_TIMEOUT);
-            ok = false;
-            return;
+        for (int g = pc.g0; g < pc.g1; ++g, ++blk) {
+          if (blk >= npre) {
+            if (!mbar_wait(&sh.w_empty[ws], wph ^ 1, abort_flag, WAIT_LIMIT_NS)) {
+              fail(ERR_TIMEOUT);
+              ok = false;
+              return;
+            }
+            mbar_arrive_expect_tx(&sh.w_full[ws], (uint32_t)args.w_blk);
+            bulk_g2s(wring + ws * C::W_STAGE, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk, &sh.w_full[ws]);
           }
-          mbar_arrive_expect_tx(&sh.w_full[ws], (uint32_t)args.w_blk);
-          bulk_g2s(wring + ws * C::W_STAGE, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk, &sh.w_full[ws]);
           ++armed[ws];
           if (++ws == C::SW) {
             ws = 0;

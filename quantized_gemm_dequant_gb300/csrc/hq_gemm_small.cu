@@ -14,8 +14,8 @@
 // exact integers (q - z) in bf16; the group scale multiplies the fp32 group
 // partial after the MMA, so the decode adds no rounding.
 //
-// Two CTAs per SM for 16-token tiles.  Warps 0-7 compute (warp w owns rows 16w..16w+15 of the 128-row tile); warp 8
-// produces: one bulk copy of the weight block plus the TMA load (dense) or
+// Two CTAs per SM for 16-token tiles.  Warps 0-7 compute (warp (rg, kh): rows 32rg..32rg+31 of the 128-row tile,
+// K half kh of every block); warp 8 produces: one bulk copy of the weight block plus the TMA load (dense) or
 // gather4 (MoE) of the token tile for the same 128 K, all on one barrier.
 // Pieces and the Stream-K partial slots are those of the UMMA path.
 #include "hq_gemm_kernel.cuh"
@@ -65,7 +65,11 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
   int* prefix = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE + 1024);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  if (tid == 0) {
+  // Dense calls: the producer thread issues the weight copies of its first ring stages before the grid
+  // dependency wait (packed weights are read-only inputs, see hq_launch.h), so that they stream while the
+  // previous kernel drains; the activation loads of those stages follow the wait on the same barriers.
+  int npre = 0;  // producer thread: stages whose weight copy is in flight
+  if (tid == SM_PROD_WARP * 32) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&sh.full[s], 1);
       mbar_init(&sh.empty[s], 8);
@@ -73,10 +77,22 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
     mbar_init(&sh.epi_bar, 8);
     sh.abort_flag = 0;
     fence_mbar_init();
+    prefetch_tmap(&args.tmap_a);
+    if (!args.moe) {
+      Sched s0;
+      s0.init(args.m_tiles * args.n_tiles, args.kst, (int)gridDim.x, (int)blockIdx.x, args.sk);
+      if ((int)blockIdx.x < s0.P && s0.tiles > 0)
+        for_each_piece(s0, [&](const Piece& pc) {
+          const uint8_t* wblk = args.w + ((int64_t)(pc.tile % args.n_tiles) * args.kst) * args.w_blk;
+          for (int g = pc.g0; g < pc.g1 && npre < C::STAGES; ++g, ++npre) {
+            mbar_arrive_expect_tx(&sh.full[npre], (uint32_t)args.w_blk + C::ACT_BYTES);
+            bulk_g2s(smem + npre * C::STAGE, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk, &sh.full[npre]);
+          }
+        });
+    }
   }
-  if (tid == SM_PROD_WARP * 32) prefetch_tmap(&args.tmap_a);
   pdl_trigger();
-  pdl_wait();  // no global memory a previous kernel may write is touched before this point
+  pdl_wait();  // no global memory a previous kernel may write is touched before this point (weights aside)
   if (args.moe) {
     for (int e = tid; e < args.E; e += SM_THREADS) {
       int cnt = args.counts[e];
@@ -140,6 +156,7 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
       uint32_t ph = 0;
       bool ok = true;
       uint32_t armed = 0;  // stages with a copy issued (bit s)
+      int blk = 0;         // weight blocks of this CTA so far (the first npre were issued before the wait)
       for_each_piece(sched, [&](const Piece& pc) {
         if (!ok) return;
         int e, row0, nrows;
@@ -152,16 +169,18 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
           for (int i = 0; i < BT; ++i)
             rows_tok[i] = i < nrows ? args.region[e * args.region_cap + row0 + i] / args.topk : args.M;
         const uint8_t* wblk = args.w + e * args.w_expert_bytes + ((int64_t)nt * args.kst) * args.w_blk;
-        for (int g = pc.g0; g < pc.g1; ++g) {
-          if (!mbar_wait(&sh.empty[st], ph ^ 1, abort_flag, WAIT_LIMIT_NS)) {
-            fail(ERR_TIMEOUT);
-            ok = false;
-            return;
-          }
+        for (int g = pc.g0; g < pc.g1; ++g, ++blk) {
           uint8_t* base = smem + st * C::STAGE;
           uint8_t* act = base + C::W_REGION;
-          mbar_arrive_expect_tx(&sh.full[st], (uint32_t)args.w_blk + C::ACT_BYTES);
-          bulk_g2s(base, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk, &sh.full[st]);
+          if (blk >= npre) {
+            if (!mbar_wait(&sh.empty[st], ph ^ 1, abort_flag, WAIT_LIMIT_NS)) {
+              fail(ERR_TIMEOUT);
+              ok = false;
+              return;
+            }
+            mbar_arrive_expect_tx(&sh.full[st], (uint32_t)args.w_blk + C::ACT_BYTES);
+            bulk_g2s(base, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk, &sh.full[st]);
+          }
           if (!args.moe || args.grouped) {
             for (int j = 0; j < 2; ++j)
               tma_load_2d(act + j * (BT * 128), &args.tmap_a, g * 128 + j * 64, rbase, &sh.full[st]);

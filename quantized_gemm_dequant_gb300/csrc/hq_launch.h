@@ -2,8 +2,11 @@
 //
 // A kernel launched this way may be scheduled while the previous kernel of the stream is still running;
 // every kernel of this library therefore executes pdl_wait() before its first access to global memory that
-// a previous kernel could write (inputs, workspace, outputs), and may only prefetch read-only weights into
-// L2 before it.  HQ_PDL=0 in the environment turns the attribute off (plain stream order).
+// a previous kernel could write (activations, routing tables, workspace, outputs).  Packed weights are
+// read-only inputs: the dense GEMM kernels start copying them before the wait.  They must therefore be
+// complete when the kernel before the call allows its dependents to launch; kernels that never execute
+// griddepcontrol.launch_dependents (the repack kernel, ordinary kernels) allow it only when they finish.
+// HQ_PDL=0 in the environment turns the attribute off (plain stream order).
 #pragma once
 #include <cuda_runtime.h>
 #include <stdlib.h>
