@@ -261,6 +261,41 @@ __device__ __forceinline__ void moe_locate(const int* prefix, int E, int mt, int
   lm = mt - prefix[lo];
 }
 
+// MoE token-tile prefix over experts into shared memory: prefix[e] = token tiles of experts before e (prefix[0] = 0,
+// prefix[E] = total, also written to *total).  Expert counts are clamped to [0, region_cap].  Every thread of the
+// block calls it (it holds a __syncthreads); the counts are read in parallel and one warp scans them.
+__device__ __forceinline__ void moe_tile_prefix(const int* counts, int E, int region_cap, int bt, int* prefix,
+                                                int* total) {
+  const int tid = threadIdx.x, nthreads = blockDim.x, warp = tid >> 5, lane = tid & 31;
+  for (int e = tid; e < E; e += nthreads) {
+    int cnt = counts[e];
+    cnt = cnt < 0 ? 0 : (cnt > region_cap ? region_cap : cnt);
+    prefix[e + 1] = (cnt + bt - 1) / bt;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int b0 = 1 + lane * per;
+    int run = 0;
+    for (int i = 0; i < per; ++i)
+      if (b0 + i <= E) run += prefix[b0 + i];
+    int incl = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    int acc = incl - run;
+    for (int i = 0; i < per; ++i)
+      if (b0 + i <= E) {
+        acc += prefix[b0 + i];
+        prefix[b0 + i] = acc;
+      }
+    if (lane == 0) prefix[0] = 0;
+    if (lane == 31) *total = incl;
+  }
+}
+
 template <int PATH, int BT>
 __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_constant__ GemmArgs args) {
   using C = Cfg<PATH, BT>;
@@ -322,35 +357,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
   pdl_trigger();
   pdl_wait();  // no global memory a previous kernel may write is touched before this point (weights aside)
   // MoE: tile prefix over experts (E <= 512 enforced on the host)
-  if (args.moe) {
-    for (int e = tid; e < args.E; e += NUM_THREADS) {
-      int cnt = args.counts[e];
-      cnt = cnt < 0 ? 0 : (cnt > args.region_cap ? args.region_cap : cnt);
-      prefix[e + 1] = (cnt + BT - 1) / BT;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const int per = (args.E + 31) / 32;
-      const int b0 = 1 + lane * per;
-      int run = 0;
-      for (int i = 0; i < per; ++i)
-        if (b0 + i <= args.E) run += prefix[b0 + i];
-      int incl = run;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += v;
-      }
-      int acc = incl - run;
-      for (int i = 0; i < per; ++i)
-        if (b0 + i <= args.E) {
-          acc += prefix[b0 + i];
-          prefix[b0 + i] = acc;
-        }
-      if (lane == 0) prefix[0] = 0;
-      if (lane == 31) sh.tile_prefix_total = incl;
-    }
-  }
+  if (args.moe) moe_tile_prefix(args.counts, args.E, args.region_cap, BT, prefix, &sh.tile_prefix_total);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -857,9 +864,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
       // lane (col - col0) % 32, slot (col - col0) / 32 (slot chosen by selects, so the table stays in registers).
       const bool use_table = kTables && (args.moe || PATH == PATH_MXFP4);
       const float dense_mul = PATH == PATH_NVFP4 ? args.a_scale[0] * args.w_gscale[e] : 1.0f;
-      auto store = [&](int col, float acc) {
-        int orow;
-        float mul;
+      // output row (-1: padding column) and multiplier of token column col
+      auto lookup = [&](int col, int& orow, float& mul) {
         if (kSmemTables && use_table) {
           const int2 t = tabs[(pd.ts * 8 + warp) * HC + (col - col0)];
           orow = t.x;
@@ -881,12 +887,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
           orow = col < nrows ? row0 + col : -1;
           mul = dense_mul;
         }
+      };
+      auto store = [&](int col, float acc) {
+        int orow;
+        float mul;
+        lookup(col, orow, mul);
         if (orow >= 0 && n < args.N) args.c[(int64_t)orow * args.N + n] = f32_to_bf16(acc * mul + bias_v);
       };
+      const bool pair_ok = (args.N & 1) == 0 && (reinterpret_cast<uintptr_t>(args.c) & 3) == 0;
       if (!pc.full) {
 #pragma unroll
         for (int j = 0; j < HC; ++j) part[(col0 + j) * TILE_N + r] = __uint_as_float(v[j]);
-      } else if (!use_table && (args.N & 1) == 0 && (reinterpret_cast<uintptr_t>(args.c) & 3) == 0) {
+      } else if (use_table && pair_ok) {
+        // Table rows (MoE, MXFP4), even N: the pair exchange of the dense case below, each token column with its
+        // own output row and multiplier.
+        const bool odd = lane & 1;
+        const int n_even = n & ~1;
+#pragma unroll
+        for (int j = 0; j < HC; j += 2) {
+          const int col = col0 + j;
+          int orow0, orow1;
+          float mul0, mul1;
+          lookup(col, orow0, mul0);
+          lookup(col + 1, orow1, mul1);
+          const uint32_t pk = pack_bf16x2(__uint_as_float(v[j]) * mul0 + bias_v,
+                                          __uint_as_float(v[j + 1]) * mul1 + bias_v);  // lo: col, hi: col+1
+          const uint32_t recv = __shfl_xor_sync(0xffffffffu, odd ? (pk & 0xFFFFu) : (pk >> 16), 1);
+          const uint32_t out = odd ? (recv | (pk & 0xFFFF0000u)) : ((pk & 0xFFFFu) | (recv << 16));
+          const int orow = odd ? orow1 : orow0;
+          if (orow >= 0 && n_even < args.N)
+            *reinterpret_cast<uint32_t*>(args.c + (int64_t)orow * args.N + n_even) = out;
+        }
+      } else if (!use_table && pair_ok) {
         // Dense rows, even N: lanes 2i and 2i+1 swap one value per pair of tokens, so that every lane writes
         // two adjacent outputs (n, n+1) of one token with a single 4-byte store: the even lane token col, the
         // odd lane token col + 1.

@@ -93,35 +93,7 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
   }
   pdl_trigger();
   pdl_wait();  // no global memory a previous kernel may write is touched before this point (weights aside)
-  if (args.moe) {
-    for (int e = tid; e < args.E; e += SM_THREADS) {
-      int cnt = args.counts[e];
-      cnt = cnt < 0 ? 0 : (cnt > args.region_cap ? args.region_cap : cnt);
-      prefix[e + 1] = (cnt + BT - 1) / BT;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const int per = (args.E + 31) / 32;
-      const int b0 = 1 + lane * per;
-      int run = 0;
-      for (int i = 0; i < per; ++i)
-        if (b0 + i <= args.E) run += prefix[b0 + i];
-      int incl = run;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += v;
-      }
-      int acc = incl - run;
-      for (int i = 0; i < per; ++i)
-        if (b0 + i <= args.E) {
-          acc += prefix[b0 + i];
-          prefix[b0 + i] = acc;
-        }
-      if (lane == 0) prefix[0] = 0;
-      if (lane == 31) sh.tile_prefix_total = incl;
-    }
-  }
+  if (args.moe) moe_tile_prefix(args.counts, args.E, args.region_cap, BT, prefix, &sh.tile_prefix_total);
   __syncthreads();
   const int total_tiles = args.moe ? sh.tile_prefix_total * args.n_tiles : args.m_tiles * args.n_tiles;
   Sched sched;

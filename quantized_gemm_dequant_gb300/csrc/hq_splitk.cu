@@ -24,18 +24,7 @@ __global__ void __launch_bounds__(RED_THREADS) splitk_reduce_kernel(const __grid
   pdl_trigger();
   pdl_wait();  // partials (and MoE counts) come from the GEMM
   if (args.moe) {
-    // token-tile prefix over experts, as the GEMM computed it
-    if (tid == 0) {
-      int acc = 0;
-      prefix[0] = 0;
-      for (int e = 0; e < args.E; ++e) {
-        int cnt = args.counts[e];
-        cnt = cnt < 0 ? 0 : (cnt > args.region_cap ? args.region_cap : cnt);
-        acc += (cnt + bt - 1) / bt;
-        prefix[e + 1] = acc;
-      }
-      total_sh = acc;
-    }
+    moe_tile_prefix(args.counts, args.E, args.region_cap, bt, prefix, &total_sh);  // as the GEMM computed it
     __syncthreads();
   }
   const int total_tiles = args.moe ? total_sh * args.n_tiles : args.m_tiles * args.n_tiles;
