@@ -15,7 +15,8 @@ kernel's reads).
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload instead.  `--config` selects another
-workload (nvfp4, moe_w4a16, moe_mxfp4, w4a16_sym) for ad-hoc measurement.
+workload (nvfp4, moe_w4a16, moe_mxfp4, w4a16_sym) for ad-hoc measurement, or the
+activation quantizers that feed the W4A8 / W4A4 paths (aq_e4m3_tok, aq_nvfp4).
 """
 import argparse
 import json
@@ -525,13 +526,221 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ activation quantization
+# bf16 activations -> the FP8 per-token / NVFP4 operands (the W4A8 and W4A4 paths), on the K = 7168 activations of
+# the MXFP4 MoE and NVFP4 workloads.  Memory-bound: the metric is GB/s of algorithmic bytes.
+AQ_CONFIGS = {
+    "aq_e4m3_tok": dict(afmt="e4m3_tok", K=7168, sizes=[1, 64, 1024, 8192]),
+    "aq_nvfp4": dict(afmt="nvfp4", K=7168, sizes=[1, 128, 1024, 8192]),
+}
+AQ_METRIC = "activation quantization GB/s of algorithmic bytes; % of the HBM roofline"
+
+
+def aq_bytes(afmt, M, K, calibrated=False):
+    """Algorithmic bytes of one call: bf16 reads of x (twice for NVFP4 with the tensor's own amax: the amax must be
+    known before the first block is quantized) plus the quantized data and scales written."""
+    x = 2 * M * K
+    if afmt == "e4m3_tok":
+        return x + M * K + 4 * M
+    return (x if calibrated else 2 * x) + M * K // 2 + M * K // 16 + 4
+
+
+def aq_workload_name(cfg):
+    c = AQ_CONFIGS[cfg]
+    what = "per-token FP8 e4m3" if c["afmt"] == "e4m3_tok" else "NVFP4 (block-16 e4m3 + fp32 tensor amax)"
+    return f"activation quantization bf16 -> {what}, K={c['K']}, M in {c['sizes']}"
+
+
+def aq_oracle_step(cfg, seed, rows=32):
+    """The CPU oracle on a bounded sample: `rows` rows of every size of the sweep.  Returns (bytes, seconds)."""
+    import numpy as np
+    import oracle
+    c = AQ_CONFIGS[cfg]
+    nbytes, t = 0.0, 0.0
+    for M in c["sizes"]:
+        r = min(M, rows)
+        x = W.acts_fp32(seed, r, c["K"], outliers=c["afmt"] == "nvfp4").to(torch.bfloat16)
+        bits = x.view(torch.int16).numpy().view(np.uint16)
+        t0 = time.perf_counter()
+        if c["afmt"] == "e4m3_tok":
+            oracle.quantize_act_e4m3_per_token(bits)
+        else:
+            oracle.quantize_act_nvfp4(bits)
+        t += time.perf_counter() - t0
+        nbytes += aq_bytes(c["afmt"], r, c["K"])
+    return nbytes, t
+
+
+def run_act_quant(args):
+    import quantized_gemm_dequant_gb300 as hq
+    rank, world, local = env_rank()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pk, pk_src = peaks()
+    c = AQ_CONFIGS[args.config]
+    afmt, K = c["afmt"], c["K"]
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    calls = []
+    for M in c["sizes"]:
+        R = REPLICAS_OVERRIDE or int(min(12, max(2, -(-3 * l2 // (2 * M * K)))))
+        x0 = W.acts_fp32(args.seed, M, K, outliers=afmt == "nvfp4", device=dev).to(torch.bfloat16)
+        xs = [x0] + [x0.clone() for _ in range(R - 1)]
+        outs = [hq.quantize_act(afmt, xs[r]) for r in range(R)]
+        nws = max(16, hq.quantize_act_workspace_bytes(afmt, M, K))
+        wss = [torch.empty(nws, dtype=torch.uint8, device=dev) for _ in range(R)]
+        amax = x0.float().abs().max().reshape(1).contiguous()  # calibrated-amax variant: the quantize kernel alone
+
+        def call(r, stream=None, xs=xs, outs=outs, wss=wss):
+            return hq.quantize_act(afmt, xs[r], out=outs[r], workspace=wss[r], stream=stream)
+
+        def call_cal(r, stream=None, xs=xs, outs=outs, amax=amax):
+            return hq.quantize_act(afmt, xs[r], global_amax=amax, out=outs[r], stream=stream)
+
+        calls.append(dict(M=M, R=R, call=call, call_cal=call_cal, xs=xs, outs=outs, bytes=aq_bytes(afmt, M, K),
+                          bytes_cal=aq_bytes(afmt, M, K, calibrated=True)))
+
+    def timed(fn, R, n):
+        out = []
+        done, i = 0, 0
+        while done < n:
+            cnt = min(R, n - done)
+            torch.cuda._sleep(SPIN_CYCLES)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(cnt):
+                fn(i % R, stream=stream)
+                i += 1
+            e1.record(stream)
+            out.append((e0, e1, cnt))
+            done += cnt
+        return out
+
+    for cl in calls:
+        timed(cl["call"], cl["R"], args.warmup * cl["R"])
+    torch.cuda.synchronize(dev)
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.5)
+    torch.cuda.synchronize(dev)
+    t_epoch0 = time.time()
+    t_wall0 = time.perf_counter()
+    rec = [timed(cl["call"], cl["R"], args.steps) for cl in calls]
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall0
+    clocks = clk.stop(t_epoch0, time.time())
+    rec_cal = None
+    if afmt == "nvfp4":  # the quantize kernel alone (calibrated amax), for its roofline
+        rec_cal = [timed(cl["call_cal"], cl["R"], args.steps) for cl in calls]
+        torch.cuda.synchronize(dev)
+    sweep, step_ms = [], 0.0
+    kern_t = kern_b = 0.0
+    for i, (cl, ts) in enumerate(zip(calls, rec)):
+        per = sorted(a.elapsed_time(b) / n for a, b, n in ts)
+        t = statistics.median(per) * 1e-3
+        step_ms += sum(a.elapsed_time(b) for a, b, _ in ts) / args.steps
+        e = dict(M=cl["M"], us=round(t * 1e6, 2), p10_us=round(per[len(per) // 10] * 1e3, 2),
+                 p90_us=round(per[min(len(per) - 1, 9 * len(per) // 10)] * 1e3, 2),
+                 gbs=round(cl["bytes"] / t / 1e9, 1), roofline_frac=round(cl["bytes"] / t / 1e9 / pk["hbm_gbs"], 4))
+        kts = rec_cal[i] if rec_cal else ts
+        kper = sorted(a.elapsed_time(b) / n for a, b, n in kts)
+        kt = statistics.median(kper) * 1e-3
+        if rec_cal:
+            e["quantize_kernel_us"] = round(kt * 1e6, 2)
+        sweep.append(e)
+        kern_t += kt
+        kern_b += cl["bytes_cal"] if rec_cal else cl["bytes"]
+    total_bytes = sum(cl["bytes"] for cl in calls)
+    value = world * total_bytes / (step_ms * 1e-3) / 1e9
+    kname = "hq::act_quant_e4m3_kernel" if afmt == "e4m3_tok" else "hq::act_quant_nvfp4_kernel"
+    ach = kern_b / kern_t / 1e9
+    roof = dict(bound="hbm", achieved=round(ach, 1), peak=pk["hbm_gbs"], unit="GB/s", frac=round(ach / pk["hbm_gbs"], 4),
+                kernel=kname, launches_per_step=len(calls), peak_source=f"{pk_src} (copy bandwidth)",
+                traffic=traffic_of(kname, args.config),
+                note="achieved = algorithmic bytes of the sweep's launches / their event time, one launch per size"
+                     + ("; NVFP4: the quantize kernel alone, with a calibrated amax (one read of x)" if rec_cal else ""))
+    e2e = None
+    if not args.no_e2e:
+        hosts = [(cl["xs"][0].cpu().pin_memory(), {k: torch.empty(v.shape, dtype=v.dtype).pin_memory()
+                                                   for k, v in cl["outs"][0].items()}) for cl in calls]
+
+        def one(tl):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for cl, (hx, ho) in zip(calls, hosts):
+                cl["xs"][0].copy_(hx, non_blocking=True)
+                cl["call"](0, stream=stream)
+                for k, v in ho.items():
+                    v.copy_(cl["outs"][0][k], non_blocking=True)
+            e1.record(stream)
+            tl.append((e0, e1))
+
+        for _ in range(3):
+            one([])
+        torch.cuda.synchronize(dev)
+        tl = []
+        nsteps = min(args.steps, 20)
+        for _ in range(nsteps):
+            one(tl)
+        torch.cuda.synchronize(dev)
+        ms = sum(a.elapsed_time(b) for a, b in tl) / nsteps
+        e2e = {"value": round(total_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+               "h2d_bytes_per_step": int(sum(2 * cl["M"] * K for cl in calls)),
+               "d2h_bytes_per_step": int(sum(sum(v.numel() * v.element_size() for v in cl["outs"][0].values())
+                                             for cl in calls)),
+               "ms_per_step": round(ms, 4), "steps": nsteps}
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        b, sec = aq_oracle_step(args.config, args.seed)
+        cpu = {"value": round(b / sec / 1e9, 4), "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": "32 rows (or M if smaller) of every size of the sweep, quantized by the numpy oracle",
+               "seconds": round(sec, 2)}
+    line = {"metric": AQ_METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded Philox draws, bf16)",
+            "config": {"workload": aq_workload_name(args.config), "sizes": c["sizes"],
+                       "l2": "each call reads its own replica of x; replicas exceed three L2 sizes except at small M",
+                       "timing": "CUDA events around bursts of back-to-back calls of one size"},
+            "roofline": roof, "sweep": sweep,
+            "gpu_launches": args.steps * len(calls) * (1 if afmt == "e4m3_tok" else 2),
+            "clocks": clocks, "wall_s_timed": round(t_wall, 3), "e2e": e2e, "cpu_baseline": cpu}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_act_quant_reference(args):
+    rank, world, _ = env_rank()
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        aq_oracle_step(args.config, args.seed)
+    b = sec = 0.0
+    for _ in range(args.steps):
+        bb, ss = aq_oracle_step(args.config, args.seed)
+        b += bb
+        sec += ss
+    value = b / sec / 1e9
+    c = AQ_CONFIGS[args.config]
+    print(json.dumps({
+        "metric": AQ_METRIC, "impl": "reference", "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": aq_workload_name(args.config), "sizes": c["sizes"]},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle", "cores": cpu_cores(),
+                         "sample": "per step: 32 rows (or M) of every size, numpy oracle"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+        flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="w4a16_asym", choices=list(W.CONFIGS))
+    ap.add_argument("--config", default="w4a16_asym", choices=list(W.CONFIGS) + list(AQ_CONFIGS))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -547,9 +756,12 @@ def main():
     global REPLICAS_OVERRIDE
     REPLICAS_OVERRIDE = args.replicas
     if args.sizes:
-        W.CONFIGS[args.config] = dict(W.CONFIGS[args.config], sizes=[int(x) for x in args.sizes.split(",")])
+        table = AQ_CONFIGS if args.config in AQ_CONFIGS else W.CONFIGS
+        table[args.config] = dict(table[args.config], sizes=[int(x) for x in args.sizes.split(",")])
     args.warmup = max(3, args.warmup) if args.impl == "ours" else args.warmup
-    if args.impl == "reference":
+    if args.config in AQ_CONFIGS:
+        (run_act_quant_reference if args.impl == "reference" else run_act_quant)(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

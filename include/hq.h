@@ -193,6 +193,36 @@ HQ_API hq_status_t hq_gemm_static_scratch(const hq_format_t* fmt, const hq_act_t
                                           const void* bias, void* C, int64_t M, int64_t N, int64_t K,
                                           hq_stream_t stream);
 
+/* Activation quantization: bf16 activations -> the E4M3_TOKEN or NVFP4 operand
+ * of hq_gemm / hq_moe_gemm.  The deployment picks a layer's activation type
+ * ("Selecting activation types"): token-wise FP8 for W4A8 ("End-to-end
+ * inference performance"), NVFP4 for W4A4 ("W8A8 / W4A8 / W4A4").  Scales map
+ * the largest magnitude of each scaled unit to the format's largest value;
+ * every step is one IEEE binary32 operation and conversions round to nearest
+ * even, saturating:
+ *   E4M3_TOKEN  s[m] = absmax(x[m, :]) / 448, data = e4m3(x / s[m]); a zero
+ *               row gets s = 0 and zero codes.  An e4m3 zero keeps its sign.
+ *   NVFP4       g = amax / (6 * 448), amax = the tensor's largest magnitude or
+ *               the calibrated *global_amax; per 16 elements of a row
+ *               sb = e4m3(amax_b / (6 * g)), d = value(sb) * g,
+ *               code = e2m1(x / d) (+0 for a zero result; d = 0: zero codes).
+ * Arguments (device pointers, 16-byte aligned, caller-owned):
+ *   act_type     HQ_A_E4M3_TOKEN or HQ_A_NVFP4 (else HQ_ERR_UNSUPPORTED)
+ *   x            bf16 [M, K] row-major; K a multiple of 16 (else HQ_ERR_ALIGNMENT), M >= 0
+ *   global_amax  NVFP4: fp32 [1] calibrated largest magnitude, or NULL to take
+ *                the tensor's own (one more kernel reads x first); ignored for E4M3_TOKEN
+ *   out_data     E4M3_TOKEN: e4m3 [M, K]; NVFP4: e2m1 [M, K/2], low nibble = even k
+ *   out_scale    E4M3_TOKEN: fp32 [M]; NVFP4: ue4m3 [M, K/16]
+ *   out_global   NVFP4: fp32 [1] receives g; may be NULL for E4M3_TOKEN
+ *   workspace    NVFP4 without global_amax: hq_quantize_act_workspace_bytes()
+ *                bytes (HQ_ERR_WORKSPACE if smaller), no initialisation
+ *                needed; otherwise may be NULL
+ * Asynchronous on `stream`: one kernel, two for NVFP4 without global_amax. */
+HQ_API size_t hq_quantize_act_workspace_bytes(int32_t act_type, int64_t M, int64_t K);
+HQ_API hq_status_t hq_quantize_act(int32_t act_type, const void* x, int64_t M, int64_t K, const float* global_amax,
+                                   void* out_data, void* out_scale, float* out_global, void* workspace,
+                                   size_t ws_bytes, hq_stream_t stream);
+
 /* Static description of a status code. */
 HQ_API const char* hq_status_string(hq_status_t status);
 

@@ -18,6 +18,10 @@ its format, named at the function:
     Y[m, n]    = sum_k Adeq[m, k] * Wdeq[n, k]          (float64 matmul)
     MoE row t*k+j = topk_w[t, j] * (Adeq[t] . Wdeq[ids[t, j]]),  + bias for dense
 
+It also quantizes bf16 activations to the FP8 (per-token scale) and NVFP4
+operands of the W4A8 and W4A4 paths ("Selecting activation types"; section
+"activation quantization" at the end), taking every decision in IEEE binary32.
+
 Conventions (the pages are silent on them): codes are two per byte with the low
 nibble holding the even k; W is [N, K] ("out, in"); scale groups run along K.
 """
@@ -180,3 +184,100 @@ def moe_gemm(adeq, wdeq_of_expert, n_out, topk_ids, topk_weights=None, rows=None
             v = v * float(np.asarray(topk_weights)[t, j])
         y[i] = v
     return y
+
+
+# ---------------------------------------------------------------- activation quantization
+#
+# The deployment picks the activation type of a quantized layer ("Selecting activation types"): token-wise FP8 for
+# the W4A8 path ("End-to-end inference performance") and NVFP4 for W4A4 ("W8A8 / W4A8 / W4A4").  The pages give no
+# recipe for the scales, so these follow the format definitions with the plainest scale choice: the largest magnitude
+# of the scaled unit maps to the format's largest value.  Every step is one IEEE binary32 operation (float32 numpy),
+# because the codes are integers decided by those float results: the device quantizer takes the same decisions in
+# the same precision.
+
+E4M3_MAX = np.float32(448.0)
+E2M1_MAX = np.float32(6.0)
+
+
+def _nearest_code(mag, values):
+    """Index of the nearest entry of the ascending table `values` to each magnitude (float64 compare of exact float32
+    inputs), ties to the even index: round to nearest even on the format's grid.  Magnitudes beyond the last entry
+    saturate to it."""
+    mag = np.asarray(mag, dtype=np.float64)
+    hi = np.clip(np.searchsorted(values, mag, side="left"), 1, len(values) - 1)
+    lo = hi - 1
+    d_lo = mag - values[lo]
+    d_hi = values[hi] - mag
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    idx = np.where(pick_hi, hi, lo)
+    return np.where(mag >= values[-1], len(values) - 1, idx)
+
+
+_E4M3_POS = decode_e4m3(np.arange(0x7F))  # codes 0x00 .. 0x7E: 0 .. 448 ascending (0x7F is NaN)
+_E2M1_POS = decode_e2m1(np.arange(8))  # 0, 0.5, 1, 1.5, 2, 3, 4, 6
+
+
+def encode_e4m3(v):
+    """float32 -> OCP OFP8 E4M3 byte: nearest value, ties to even, saturating at +-448.  The sign is kept, also on
+    a zero result (IEEE conversion: -0 is 0x80)."""
+    v = np.asarray(v, dtype=np.float32)
+    m = _nearest_code(np.abs(v), _E4M3_POS).astype(np.uint8)
+    return np.where(np.signbit(v), m | np.uint8(0x80), m).astype(np.uint8)
+
+
+def encode_e2m1(v):
+    """float32 -> OCP MX FP4 E2M1 code: nearest value, ties to even, saturating at +-6.  A zero result is +0 (code 0)
+    whatever the sign, as the weight and activation recipes of the workloads encode it."""
+    v = np.asarray(v, dtype=np.float32)
+    m = _nearest_code(np.abs(v), _E2M1_POS).astype(np.uint8)
+    return np.where(np.signbit(v) & (m > 0), m | np.uint8(0x8), m).astype(np.uint8)
+
+
+def _bf16_to_f32(bits):
+    return (np.asarray(bits).astype(np.uint32) << 16).view(np.float32)
+
+
+def quantize_act_e4m3_per_token(x_bits):
+    """bf16 [M, K] (bit patterns) -> (e4m3 bytes [M, K], fp32 scale [M]).
+
+    s_t = absmax_t / 448 (float32 division); code = e4m3(x / s_t); a row of zeros gets s_t = 0 and zero codes.
+    Decoding gives x ~ code * s_t, the per-token activation the W4A8 GEMM consumes.
+    """
+    x = _bf16_to_f32(x_bits)
+    amax = np.abs(x).max(axis=1) if x.shape[1] else np.zeros(x.shape[0], np.float32)
+    s = (amax / E4M3_MAX).astype(np.float32)
+    safe = np.where(s > 0, s, np.float32(1.0)).astype(np.float32)
+    q = encode_e4m3((x / safe[:, None]).astype(np.float32))
+    q = np.where((s > 0)[:, None], q, np.uint8(0)).astype(np.uint8)
+    return q, s
+
+
+def quantize_act_nvfp4(x_bits, global_amax=None):
+    """bf16 [M, K] (bit patterns), K a multiple of 16 -> (packed e2m1 [M, K/2], ue4m3 scales [M, K/16], g fp32).
+
+    NVIDIA's NVFP4: e2m1 values, an e4m3 scale per 16 consecutive elements of a row and one fp32 tensor scale.
+    g = amax / (6 * 448) with amax the tensor's largest magnitude (or a calibrated `global_amax`); per block
+    sb = e4m3(amax_b / (6 * g)) (saturating), d = value(sb) * g, code = e2m1(x / d); d = 0 gives zero codes.
+    Decoding gives x ~ e2m1 * value(sb) * g.
+    """
+    x = _bf16_to_f32(x_bits)
+    M, K = x.shape
+    if global_amax is None:
+        amax = np.float32(np.abs(x).max()) if x.size else np.float32(0.0)
+    else:
+        amax = np.float32(global_amax)
+    g = np.float32(amax / np.float32(E2M1_MAX * E4M3_MAX))
+    xb = x.reshape(M, K // 16, 16)
+    amax_b = np.abs(xb).max(axis=2).astype(np.float32)
+    if g > 0:
+        six_g = np.float32(E2M1_MAX * g)
+        sb = encode_e4m3((amax_b / six_g).astype(np.float32))
+        d = (decode_e4m3(sb).astype(np.float32) * g).astype(np.float32)
+    else:
+        sb = np.zeros_like(amax_b, dtype=np.uint8)
+        d = np.zeros_like(amax_b, dtype=np.float32)
+    safe = np.where(d > 0, d, np.float32(1.0)).astype(np.float32)
+    q = encode_e2m1((xb / safe[:, :, None]).astype(np.float32))
+    q = np.where((d > 0)[:, :, None], q, np.uint8(0)).reshape(M, K).astype(np.uint8)
+    packed = (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8)
+    return packed, sb.astype(np.uint8), g

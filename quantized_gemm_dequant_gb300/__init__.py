@@ -29,7 +29,7 @@ HQ_A_BF16, HQ_A_E4M3_TOKEN, HQ_A_NVFP4 = 1, 2, 3
 
 EXPORTS = ["hq_packed_bytes", "hq_pack_weights", "hq_unpack_weights", "hq_workspace_bytes", "hq_workspace_init",
            "hq_gemm", "hq_moe_gemm", "hq_last_device_status", "hq_status_string", "hq_gemm_static_scratch",
-           "hq_kernels_per_call"]
+           "hq_kernels_per_call", "hq_quantize_act_workspace_bytes", "hq_quantize_act"]
 
 
 class Format(ctypes.Structure):
@@ -65,6 +65,10 @@ _lib.hq_gemm_static_scratch.argtypes = [_F, _A, _vp, _vp, _vp, _i64, _i64, _i64,
 _lib.hq_gemm_static_scratch.restype = ctypes.c_int
 _lib.hq_kernels_per_call.argtypes = [_F, _i64, _i32, _i32]
 _lib.hq_kernels_per_call.restype = _i32
+_lib.hq_quantize_act_workspace_bytes.argtypes = [_i32, _i64, _i64]
+_lib.hq_quantize_act_workspace_bytes.restype = _sz
+_lib.hq_quantize_act.argtypes = [_i32, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+_lib.hq_quantize_act.restype = ctypes.c_int
 _lib.hq_status_string.argtypes = [ctypes.c_int]
 _lib.hq_status_string.restype = ctypes.c_char_p
 
@@ -206,3 +210,39 @@ def pack_inputs(inputs, device="cuda", stream=None):
     scales = t["scales"].view(torch.uint8) if t["scales"].dtype == torch.bfloat16 else t["scales"]
     packed = pack_weights(fmt, t["codes"], scales, t.get("zeros"), t.get("gscale"), stream=stream)
     return fmt, packed
+
+
+_ACT_TYPE = {"e4m3_tok": HQ_A_E4M3_TOKEN, "nvfp4": HQ_A_NVFP4}
+
+
+def quantize_act_workspace_bytes(afmt, M, K):
+    return int(_lib.hq_quantize_act_workspace_bytes(_ACT_TYPE[afmt], int(M), int(K)))
+
+
+def quantize_act(afmt, x, global_amax=None, out=None, workspace=None, stream=None):
+    """bf16 activations x [M, K] (cuda) -> the activation operand dict of `gemm` / `moe_gemm`:
+    'e4m3_tok': {data e4m3 bytes [M, K], scale fp32 [M]}; 'nvfp4': {data packed e2m1 [M, K/2], scale ue4m3 [M, K/16],
+    gscale fp32 [1]}.  `global_amax` (NVFP4): fp32 tensor [1] with a calibrated largest magnitude, else the tensor's
+    own.  `out` (same dict layout) receives the result when given."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()
+    M, K = x.shape
+    at = _ACT_TYPE[afmt]
+    dev = x.device
+    if out is None:
+        if afmt == "e4m3_tok":
+            out = dict(data=torch.empty((M, K), dtype=torch.uint8, device=dev),
+                       scale=torch.empty((M,), dtype=torch.float32, device=dev))
+        else:
+            out = dict(data=torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
+                       scale=torch.empty((M, K // 16), dtype=torch.uint8, device=dev),
+                       gscale=torch.empty((1,), dtype=torch.float32, device=dev))
+    need = quantize_act_workspace_bytes(afmt, M, K)
+    if workspace is None and need > 0 and global_amax is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(_lib.hq_quantize_act(at, _ptr(x), M, K, _ptr(global_amax) if global_amax is not None else None,
+                                _ptr(out["data"]), _ptr(out["scale"]),
+                                _ptr(out["gscale"]) if "gscale" in out else None,
+                                _ptr(workspace) if workspace is not None else None, ws_bytes, _stream(stream)),
+           "hq_quantize_act")
+    return out

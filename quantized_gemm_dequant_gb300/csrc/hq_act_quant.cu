@@ -1,0 +1,220 @@
+// Activation quantization: bf16 activations -> the FP8 (e4m3, per-token scale) or NVFP4 operand of the GEMMs.
+//
+// The deployment chooses the activation type of a quantized layer ("Selecting activation types"): token-wise FP8
+// feeds the W4A8 path ("End-to-end inference performance"), NVFP4 the W4A4 path ("W8A8 / W4A8 / W4A4").  The
+// scales follow the format definitions with the largest magnitude of each scaled unit mapped to the format's
+// largest value:
+//   FP8 per token   s_t = absmax_t / 448,            code = e4m3(x / s_t)              (s_t = 0: zero codes)
+//   NVFP4           g = amax / (6 * 448),            per 16 elements of a row:
+//                   sb = e4m3(amax_b / (6 g)),       d = value(sb) * g,  code = e2m1(x / d)  (d = 0: zero codes)
+// Conversions round to nearest even and saturate (e4m3 at 448, e2m1 at 6).  Every step is one IEEE binary32
+// operation, because the codes are integer decisions taken on those results; an e2m1 zero is stored as +0, an e4m3
+// zero keeps its sign.
+//
+// Memory-bound kernels: 16-byte loads of 8 bf16, grids in multiples of the SM count, programmatic dependent launch.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "hq_act_quant.h"
+#include "hq_launch.h"
+#include "hq_ptx.cuh"
+
+namespace hq {
+
+namespace {
+
+constexpr int AQ_THREADS = 256;
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// two floats -> two e4m3 bytes (lo = a), round to nearest even, saturating
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float a, float b) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(b), "f"(a));
+  return d;
+}
+
+// two floats -> one byte of two e2m1 codes (low nibble = a), round to nearest even, saturating; zeros become +0
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float a, float b) {
+  uint16_t d;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}" : "=h"(d) : "f"(b), "f"(a));
+  uint32_t r = d & 0xFFu;
+  if ((r & 0x07u) == 0) r &= 0xF0u;
+  if ((r & 0x70u) == 0) r &= 0x0Fu;
+  return r;
+}
+
+// e4m3 byte (non-negative, finite) -> float, exact
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+  uint32_t h;
+  asm("{\n\t.reg .b16 t;\n\tmov.b16 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h) : "h"((uint16_t)b));
+  return __half2float(__ushort_as_half((uint16_t)(h & 0xFFFFu)));
+}
+
+__device__ __forceinline__ float block_max(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();  // red is reused by consecutive calls
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  v = lane < (int)(blockDim.x >> 5) ? red[lane] : 0.0f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// FP8 per token: one CTA per row (grid-stride over rows).  K % 8 == 0.
+__global__ void __launch_bounds__(AQ_THREADS) act_quant_e4m3_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
+                                                                    uint8_t* __restrict__ q, float* __restrict__ s_out) {
+  __shared__ float red[AQ_THREADS / 32];
+  pdl_trigger();
+  pdl_wait();
+  const int64_t chunks = K >> 3;
+  for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + row * K);
+    float m = 0.0f;
+    for (int64_t c = threadIdx.x; c < chunks; c += AQ_THREADS) {
+      float f[8];
+      bf16x8_to_f32(__ldg(xr + c), f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+    }
+    const float amax = block_max(m, red);
+    const float s = __fdiv_rn(amax, 448.0f);
+    if (threadIdx.x == 0) s_out[row] = s;
+    uint2* qr = reinterpret_cast<uint2*>(q + row * K);
+    for (int64_t c = threadIdx.x; c < chunks; c += AQ_THREADS) {
+      uint2 o = make_uint2(0u, 0u);
+      if (s > 0.0f) {
+        float f[8];
+        bf16x8_to_f32(__ldg(xr + c), f);  // the row was read just above: an L1/L2 hit
+        uint32_t b[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) b[i] = cvt_e4m3x2(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
+        o = make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
+      }
+      qr[c] = o;
+    }
+  }
+}
+
+// NVFP4, first pass (only without a calibrated amax): largest magnitude, one partial per CTA.
+__global__ void __launch_bounds__(AQ_THREADS) act_amax_kernel(const uint16_t* __restrict__ x, int64_t n8,
+                                                              float* __restrict__ partial) {
+  __shared__ float red[AQ_THREADS / 32];
+  pdl_trigger();
+  pdl_wait();
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+  float m = 0.0f;
+  for (int64_t c = (int64_t)blockIdx.x * AQ_THREADS + threadIdx.x; c < n8; c += (int64_t)gridDim.x * AQ_THREADS) {
+    float f[8];
+    bf16x8_to_f32(__ldg(xv + c), f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+  }
+  m = block_max(m, red);
+  if (threadIdx.x == 0) partial[blockIdx.x] = m;
+}
+
+// NVFP4 quantization: one 16-element block per thread and step.  K % 16 == 0.
+__global__ void __launch_bounds__(AQ_THREADS) act_quant_nvfp4_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
+                                                                     const float* __restrict__ amax_in,
+                                                                     const float* __restrict__ partial, int nparts,
+                                                                     uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
+                                                                     float* __restrict__ g_out) {
+  __shared__ float red[AQ_THREADS / 32];
+  pdl_trigger();
+  pdl_wait();
+  float amax;
+  if (amax_in) {
+    amax = *amax_in;
+  } else {
+    float m = 0.0f;
+    for (int i = threadIdx.x; i < nparts; i += AQ_THREADS) m = fmaxf(m, partial[i]);
+    amax = block_max(m, red);
+  }
+  const float g = __fdiv_rn(amax, 2688.0f);  // 6 * 448
+  if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
+  const float six_g = __fmul_rn(6.0f, g);
+  const int64_t nblk = M * (K >> 4);
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+  uint2* qv = reinterpret_cast<uint2*>(q);
+  for (int64_t b = (int64_t)blockIdx.x * AQ_THREADS + threadIdx.x; b < nblk; b += (int64_t)gridDim.x * AQ_THREADS) {
+    float f[16];
+    bf16x8_to_f32(__ldg(xv + 2 * b), *reinterpret_cast<float(*)[8]>(f));
+    bf16x8_to_f32(__ldg(xv + 2 * b + 1), *reinterpret_cast<float(*)[8]>(f + 8));
+    float mb = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) mb = fmaxf(mb, fabsf(f[i]));
+    uint32_t sb = 0;
+    float d = 0.0f;
+    if (g > 0.0f) {
+      sb = cvt_e4m3x2(__fdiv_rn(mb, six_g), 0.0f) & 0xFFu;
+      d = __fmul_rn(e4m3_to_f32(sb), g);
+    }
+    uint32_t by[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) by[i] = d > 0.0f ? cvt_e2m1x2(__fdiv_rn(f[2 * i], d), __fdiv_rn(f[2 * i + 1], d)) : 0u;
+    qv[b] = make_uint2(by[0] | (by[1] << 8) | (by[2] << 16) | (by[3] << 24),
+                       by[4] | (by[5] << 8) | (by[6] << 16) | (by[7] << 24));
+    sf[b] = (uint8_t)sb;
+  }
+}
+
+int sm_count() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n < 1) n = 1;
+  }
+  return n;
+}
+
+}  // namespace
+
+// CTAs of the NVFP4 amax pass: one float of workspace each, at most ACT_AMAX_MAX_PARTS.
+int act_amax_grid(int64_t M, int64_t K) {
+  const int64_t n8 = M * (K >> 3);
+  const int64_t want = (n8 + AQ_THREADS * 8 - 1) / (AQ_THREADS * 8);  // about 8 chunks per thread
+  int64_t cap = 4 * (int64_t)sm_count();
+  if (cap > ACT_AMAX_MAX_PARTS) cap = ACT_AMAX_MAX_PARTS;
+  return (int)(want < 1 ? 1 : (want < cap ? want : cap));
+}
+
+cudaError_t launch_act_quant(int fp8, const void* x, int64_t M, int64_t K, const float* global_amax,
+                             void* data, void* scale, float* gscale, void* workspace, cudaStream_t stream) {
+  const int sms = sm_count();
+  if (fp8) {
+    const int64_t grid = M < 8 * (int64_t)sms ? M : 8 * (int64_t)sms;
+    return launch_kernel(act_quant_e4m3_kernel, dim3((unsigned)grid), dim3(AQ_THREADS), 0, stream,
+                         (const uint16_t*)x, M, K, (uint8_t*)data, (float*)scale);
+  }
+  int nparts = 0;
+  float* partial = reinterpret_cast<float*>(workspace);
+  if (!global_amax) {
+    nparts = act_amax_grid(M, K);
+    cudaError_t e = launch_kernel(act_amax_kernel, dim3((unsigned)nparts), dim3(AQ_THREADS), 0, stream,
+                                  (const uint16_t*)x, M * (K >> 3), partial);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t nblk = M * (K >> 4);
+  int64_t grid = (nblk + AQ_THREADS - 1) / AQ_THREADS;
+  if (grid > 8 * (int64_t)sms) grid = 8 * (int64_t)sms;
+  if (grid < 1) grid = 1;
+  return launch_kernel(act_quant_nvfp4_kernel, dim3((unsigned)grid), dim3(AQ_THREADS), 0, stream, (const uint16_t*)x, M,
+                       K, global_amax, (const float*)partial, nparts, (uint8_t*)data, (uint8_t*)scale, gscale);
+}
+
+}  // namespace hq

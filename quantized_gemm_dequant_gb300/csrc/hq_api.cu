@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include "../../include/hq.h"
+#include "hq_act_quant.h"
 #include "hq_gemm_kernel.cuh"
 #include "hq_layout.h"
 
@@ -450,6 +451,31 @@ hq_status_t hq_moe_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* p
   a.status = status;
   a.partials = p.sk ? reinterpret_cast<float*>(ws + p.off_partials) : nullptr;
   return cuda_status(launch_path(p, a, (cudaStream_t)stream));
+}
+
+size_t hq_quantize_act_workspace_bytes(int32_t act_type, int64_t M, int64_t K) {
+  if (act_type != HQ_A_E4M3_TOKEN && act_type != HQ_A_NVFP4) return 0;
+  if (M < 0 || M > kMaxRows || K < 16 || K > kMaxRows || K % 16) return 0;
+  return act_type == HQ_A_NVFP4 ? sizeof(float) * (size_t)hq::ACT_AMAX_MAX_PARTS : 0;
+}
+
+hq_status_t hq_quantize_act(int32_t act_type, const void* x, int64_t M, int64_t K, const float* global_amax,
+                            void* out_data, void* out_scale, float* out_global, void* workspace, size_t ws_bytes,
+                            hq_stream_t stream) {
+  if (act_type != HQ_A_E4M3_TOKEN && act_type != HQ_A_NVFP4) return HQ_ERR_UNSUPPORTED;
+  if (M < 0 || M > kMaxRows || K < 16 || K > kMaxRows) return HQ_ERR_INVALID_ARG;
+  if (K % 16) return HQ_ERR_ALIGNMENT;
+  const bool fp8 = act_type == HQ_A_E4M3_TOKEN;
+  if (!fp8 && !out_global) return HQ_ERR_INVALID_ARG;
+  if (M > 0 && (!x || !out_data || !out_scale)) return HQ_ERR_INVALID_ARG;
+  if (M > 0 && (!aligned16(x) || !aligned16(out_data) || !aligned16(out_scale))) return HQ_ERR_ALIGNMENT;
+  if (!fp8 && !global_amax) {
+    if (!workspace || ws_bytes < hq_quantize_act_workspace_bytes(act_type, M, K)) return HQ_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return HQ_ERR_ALIGNMENT;
+  }
+  if (fp8 && M == 0) return HQ_OK;
+  return cuda_status(hq::launch_act_quant(fp8 ? 1 : 0, x, M, K, global_amax, out_data, out_scale, out_global,
+                                          workspace, (cudaStream_t)stream));
 }
 
 hq_status_t hq_last_device_status(void* workspace, int32_t* status_out, hq_stream_t stream) {

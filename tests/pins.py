@@ -281,5 +281,101 @@ def pin_moe_reduces_to_dense(o, rng=None):
     assert np.array_equal(moe_p, dense[perm])
 
 
+# ------------------------------------------------------------ pins on the activation quantizers
+
+def _bf16_bits(x):
+    """fp32 torch tensor -> bf16 bit patterns (numpy uint16), round to nearest even by torch."""
+    return x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _act_inputs(rng_seed, M, K):
+    """bf16 activations with the awkward cases: a zero row, a single-spike row, tiny and huge values, ties."""
+    g = torch.Generator().manual_seed(rng_seed)
+    x = torch.randn(M, K, generator=g) * torch.exp2(torch.randint(-6, 7, (M, 1), generator=g).float())
+    x[0] = 0.0
+    if M > 1:
+        x[1] = 0.0
+        x[1, K // 3] = -3.0e4
+    if M > 2:
+        x[2] = torch.randn(K, generator=g) * 1e-30  # bf16 keeps these; their scales underflow
+    return _bf16_bits(x)
+
+
+def pin_encode_e4m3(o):
+    """The saturating RNE e4m3 encoder is torch's float8_e4m3fn conversion of the input clamped to +-448, on random
+    values, on every midpoint between neighbouring e4m3 values (exact ties) and one ulp either side of them."""
+    vals = torch.arange(127, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    mids = ((vals[:-1].astype(np.float64) + vals[1:]) / 2).astype(np.float32)
+    rng = np.random.default_rng(7)
+    rand = (rng.standard_normal(20000) * rng.choice([1e-3, 1.0, 30.0, 500.0], 20000)).astype(np.float32)
+    v = np.concatenate([rand, mids, np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(1e9)),
+                        np.array([0.0, 448.0, 460.0, 464.0, 480.0, 1e30, 2.0 ** -10, 3 * 2.0 ** -10], np.float32)])
+    v = np.concatenate([v, -v]).astype(np.float32)
+    ref = torch.from_numpy(np.clip(v, -448.0, 448.0)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(o.encode_e4m3(v), ref)
+
+
+def pin_encode_e2m1(o):
+    """Brute force over the 16 codes of the generic minifloat decoder: the nearest value, ties to the even code,
+    +-6 saturation, and +0 for a zero result, on a grid that holds every tie and the points around it."""
+    table = e2m1_table()
+    grid = [Fraction(i, 16) for i in range(-128, 129)] + [Fraction(100), Fraction(-7)]
+    v = np.array([float(x) for x in grid], np.float32)
+    got = o.encode_e2m1(v)
+    for x, c in zip(grid, got):
+        best = None
+        for code in range(8):  # magnitudes
+            d = abs(abs(x) - table[code])
+            key = (d, code % 2)  # nearest, then the even code
+            if best is None or key < best[0]:
+                best = (key, code)
+        m = 7 if abs(x) >= 6 else best[1]
+        want = m | (8 if (x < 0 and m > 0) else 0)
+        assert int(c) == want, (x, int(c), want)
+
+
+def pin_act_quant_e4m3(o):
+    """Per-token FP8: the workloads' torch recipe gives the same bytes and scales; every non-zero row has an
+    element at +-448; each element is within half an e4m3 step of x / s; zero rows have s = 0 and zero codes."""
+    from workload import quant as WQ
+    bits = _act_inputs(1, 9, 160)
+    x = (bits.astype(np.uint32) << 16).view(np.float32)
+    q, s = o.quantize_act_e4m3_per_token(bits)
+    rq, rs = WQ.quant_e4m3_per_token(torch.from_numpy(x.copy()))
+    assert np.array_equal(q, rq.numpy()) and np.array_equal(s.view(np.uint32), rs.numpy().view(np.uint32))
+    dec = torch.from_numpy(q.copy()).view(torch.float8_e4m3fn).double().numpy()
+    for m in range(x.shape[0]):
+        if s[m] == 0:
+            assert not x[m].any() and not q[m].any()
+            continue
+        assert np.abs(dec[m]).max() == 448.0
+        y = x[m].astype(np.float64) / np.float64(s[m])
+        assert np.all(np.abs(dec[m] - y) <= np.maximum(np.abs(y) * 2.0 ** -4, 2.0 ** -10) * (1 + 1e-6))
+
+
+def pin_act_quant_nvfp4(o):
+    """NVFP4: the workloads' torch recipe gives the same codes, block scales and tensor scale (also with a calibrated
+    amax); g * 2688 is the amax; in each block whose scale is a normal unsaturated e4m3 the largest code is +-6."""
+    from workload import quant as WQ
+    bits = _act_inputs(2, 6, 96)
+    x = (bits.astype(np.uint32) << 16).view(np.float32)
+    for amax in (None, np.float32(np.abs(x).max() / 4)):
+        q, sb, g = o.quantize_act_nvfp4(bits, global_amax=amax)
+        ga = None if amax is None else torch.tensor(amax)
+        rq, rsb, rg = WQ.quant_nvfp4(torch.from_numpy(x.copy()), global_amax=ga)
+        assert np.array_equal(q, rq.numpy()) and np.array_equal(sb, rsb.numpy())
+        assert np.float32(g).view(np.uint32) == rg.numpy().astype(np.float32).view(np.uint32)
+    q, sb, g = o.quantize_act_nvfp4(bits)
+    assert abs(float(g) * 2688.0 - float(np.abs(x).max())) <= 1e-6 * float(np.abs(x).max())
+    codes = np.empty((q.shape[0], q.shape[1] * 2), np.uint8)
+    codes[:, 0::2], codes[:, 1::2] = q & 0xF, q >> 4
+    mag = np.array([float(v) for v in e2m1_table()])[codes & 7].reshape(q.shape[0], -1, 16)
+    normal = (sb >= 8) & (sb < 0x7E)
+    assert normal.any() and np.all(mag.max(axis=2)[normal] == 6.0)
+    zero_rows = ~x.reshape(x.shape[0], -1).any(axis=1)
+    assert not q[zero_rows].any() and not sb[zero_rows].any()
+
+
 ALL_PINS = [pin_e4m3, pin_e8m0, pin_e2m1, pin_bf16, pin_int4, pin_e0m_equivalence, pin_exact_int4,
-            pin_exact_fp4, pin_library_special_case, pin_brute_force, pin_moe_reduces_to_dense]
+            pin_exact_fp4, pin_library_special_case, pin_brute_force, pin_moe_reduces_to_dense, pin_encode_e4m3,
+            pin_encode_e2m1, pin_act_quant_e4m3, pin_act_quant_nvfp4]

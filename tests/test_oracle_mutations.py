@@ -37,6 +37,19 @@ MUTATIONS = {
     "bias_dropped": ("y = y + decode_bf16(bias).reshape(1, -1)", "y = y"),
     "topk_weight_dropped": ("v = v * float(np.asarray(topk_weights)[t, j])", "v = v"),
     "moe_slot_order": ("t, j = divmod(int(r), k)", "j, t = divmod(int(r), T)"),
+    "encode_ties_to_odd": ("(d_hi == d_lo) & (hi % 2 == 0)", "(d_hi == d_lo) & (hi % 2 == 1)"),
+    "encode_ties_away": ("(d_hi == d_lo) & (hi % 2 == 0)", "(d_hi == d_lo)"),
+    "e2m1_signed_zero": ("np.signbit(v) & (m > 0)", "np.signbit(v)"),
+    "e4m3_sign_dropped": ("np.where(np.signbit(v), m | np.uint8(0x80), m)", "np.where(v < -1e30, m | np.uint8(0x80), m)"),
+    "act_fp8_max": ("s = (amax / E4M3_MAX).astype(np.float32)", "s = (amax / np.float32(447.0)).astype(np.float32)"),
+    "act_fp8_reciprocal": ("q = encode_e4m3((x / safe[:, None]).astype(np.float32))",
+                           "q = encode_e4m3((x * (np.float32(1.0) / safe)[:, None]).astype(np.float32))"),
+    "act_nvfp4_six": ("six_g = np.float32(E2M1_MAX * g)", "six_g = np.float32(np.float32(4.0) * g)"),
+    "act_nvfp4_global": ("g = np.float32(amax / np.float32(E2M1_MAX * E4M3_MAX))",
+                         "g = np.float32(amax / np.float32(E4M3_MAX))"),
+    "act_nvfp4_block_scale_unrounded": ("d = (decode_e4m3(sb).astype(np.float32) * g).astype(np.float32)",
+                                        "d = (amax_b / np.float32(6.0)).astype(np.float32)"),
+    "act_nvfp4_nibbles": ("packed = (q[:, 0::2] | (q[:, 1::2] << 4))", "packed = (q[:, 1::2] | (q[:, 0::2] << 4))"),
 }
 
 
