@@ -109,6 +109,13 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ workload
+# Down GEMMs of the two MoE workloads' layers (hidden N, intermediate K = half the Gate-up N), with the top-k
+# combine fused into the epilogue: the routed rows T*k of K in, T token rows of N out.
+DOWN_CONFIGS = {
+    "moe_w4a16_down": dict(W.CONFIGS["moe_w4a16"], N=2048, K=768, down=True),
+    "moe_mxfp4_down": dict(W.CONFIGS["moe_mxfp4"], N=7168, K=2048, down=True),
+}
+W.CONFIGS.update(DOWN_CONFIGS)
 REPLICAS_OVERRIDE = None  # --replicas (profiling runs keep the device footprint small)
 
 
@@ -160,22 +167,28 @@ def make_calls(cfg_name, seed, device):
     hit_min = min(int(torch.unique(ids).numel()) for ids, _ in routes.values())
     R = replicas_for(per_expert * hit_min, packed.numel(), l2)
     packs = [packed] + [packed.clone() for _ in range(R - 1)]
+    down = bool(c.get("down"))
     for T in c["sizes"]:
-        a0 = W.quantize_acts(c["afmt"], W.acts_fp32(seed, T, c["K"], device=device))
+        a_rows = T * k if down else T  # the Down GEMM reads one activation row per routed row
+        a0 = W.quantize_acts(c["afmt"], W.acts_fp32(seed, a_rows, c["K"], device=device))
         ids, tw = routes[T]
         hit = int(torch.unique(ids).numel())
         acts = [dict(a0, ids=ids, tw=tw)] + [dict({kk: v.clone() for kk, v in a0.items()}, ids=ids.clone(), tw=tw.clone())
                                              for _ in range(R - 1)]
-        wss = [hq.make_workspace(fmt, T, k, device) for _ in range(R)]
-        outs = [torch.empty((T * k, c["N"]), dtype=torch.bfloat16, device=device) for _ in range(R)]
+        out_rows = T if down else T * k
+        wss = [(hq.make_combine_workspace(fmt, T, k, device) if down else hq.make_workspace(fmt, T, k, device))
+               for _ in range(R)]
+        outs = [torch.empty((out_rows, c["N"]), dtype=torch.bfloat16, device=device) for _ in range(R)]
         info = dict(M=T, flops=2.0 * T * k * c["N"] * c["K"], weight_bytes=per_expert * hit, experts_hit=hit,
-                    total_bytes=per_expert * hit + W.act_bytes(c["afmt"], T, c["K"]) + 2 * T * k * c["N"] + 8 * T * k,
-                    h2d=sum(t.numel() * t.element_size() for t in a0.values()) + 8 * T * k, d2h=2 * T * k * c["N"])
+                    total_bytes=per_expert * hit + W.act_bytes(c["afmt"], a_rows, c["K"]) + 2 * out_rows * c["N"]
+                    + 8 * T * k,
+                    h2d=sum(t.numel() * t.element_size() for t in a0.values()) + 8 * T * k, d2h=2 * out_rows * c["N"])
+        gemm_fn = hq.moe_gemm_combine if down else hq.moe_gemm
 
-        def call(r, stream=None, acts=acts, wss=wss, outs=outs):
+        def call(r, stream=None, acts=acts, wss=wss, outs=outs, gemm_fn=gemm_fn):
             a = acts[r]
-            return hq.moe_gemm(fmt, {kk: v for kk, v in a.items() if kk not in ("ids", "tw")}, packs[r], a["ids"],
-                               a["tw"], out=outs[r], workspace=wss[r], stream=stream)
+            return gemm_fn(fmt, {kk: v for kk, v in a.items() if kk not in ("ids", "tw")}, packs[r], a["ids"],
+                           a["tw"], out=outs[r], workspace=wss[r], stream=stream)
 
         calls.append((T, call, info, acts, outs, wss))
     return fmt, calls, R
@@ -334,7 +347,7 @@ def kernel_name(cfg, M):
         bt = 16 if avg <= 16 else (256 if path != 1 and avg > 128 else 128)
     if path == 0 and bt <= 32 and os.environ.get("HQ_FORCE_PATH") != "umma":
         return f"hq::hq_gemm_small_kernel<{bt}>"
-    return f"hq::hq_gemm_kernel<{path}, {bt}>"
+    return f"hq::hq_gemm_kernel<{path}, {bt}, {'true' if c.get('down') else 'false'}>"
 
 
 def gpu_launches(cfg, fmt, calls):
@@ -343,6 +356,8 @@ def gpu_launches(cfg, fmt, calls):
     import quantized_gemm_dequant_gb300 as hq
     c = W.CONFIGS[cfg]
     moe = c["kind"] != "dense"
+    if moe and c.get("down"):
+        moe = "combine"
     return sum(hq.kernels_per_call(fmt, M, c.get("topk", 1), moe) for (M, *_rest) in calls)
 
 
@@ -381,7 +396,8 @@ def workload_name(cfg):
     if c["kind"] == "dense":
         return (f"dense {c['wfmt']} x {c['afmt']} (group {c['G']}), K={c['K']}, N={c['N']}, "
                 f"M in {c['sizes']}")
-    return (f"MoE {c['wfmt']} x {c['afmt']}, E={c['E']}, top-{c['topk']}, K={c['K']}, N={c['N']}, "
+    what = "MoE Down GEMM + top-k combine" if c.get("down") else "MoE"
+    return (f"{what} {c['wfmt']} x {c['afmt']}, E={c['E']}, top-{c['topk']}, K={c['K']}, N={c['N']}, "
             f"T in {c['sizes']}, Zipf(1.1) routing")
 
 

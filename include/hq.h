@@ -133,8 +133,8 @@ HQ_API hq_status_t hq_unpack_weights(const hq_format_t* fmt, const void* packed,
  * leave it reusable.  One workspace serves one stream at a time. */
 HQ_API size_t hq_workspace_bytes(const hq_format_t* fmt, int64_t M_or_T, int32_t topk);
 
-/* Number of kernels one call launches on the current device: hq_gemm (moe = 0) or hq_moe_gemm (moe = 1)
- * with M rows / T tokens and `topk` experts each (1 for dense).  Counts this library's kernels only
+/* Number of kernels one call launches on the current device: hq_gemm (moe = 0), hq_moe_gemm (moe = 1) or
+ * hq_moe_gemm_combine (moe = 2) with M rows / T tokens and `topk` experts each (1 for dense).  Counts this library's kernels only
  * (the routing memset of hq_moe_gemm is not a kernel); 0 for an invalid format or size.  Host-only. */
 HQ_API int32_t hq_kernels_per_call(const hq_format_t* fmt, int64_t M_or_T, int32_t topk, int32_t moe);
 
@@ -161,6 +161,36 @@ HQ_API hq_status_t hq_gemm(const hq_format_t* fmt, const hq_act_t* A, const void
 HQ_API hq_status_t hq_moe_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* packedW, const int32_t* topk_ids,
                         const float* topk_weights, int64_t T, int32_t topk, void* C, void* workspace, size_t ws_bytes,
                         hq_stream_t stream);
+
+/* MoE Down GEMM with the top-k combine fused into its epilogue: the k routed
+ * rows of a token are multiplied by their experts and summed with their top-k
+ * weights into one output row.  A MoE layer's speed-up counts its Gate-up and
+ * Down GEMMs ("Results: kernel microbenchmarks"); this is the second.
+ *   A            T * topk routed rows of K (row t*topk + j feeds expert
+ *                topk_ids[t, j]), in fmt->act_type: bf16, e4m3 + fp32 scale
+ *                per routed row, or NVFP4
+ *   topk_ids     int32 [T, topk], distinct expert ids per token in [0, E)
+ *   topk_weights fp32 [T, topk] or NULL (NULL = weight 1)
+ *   C            bf16 [T, N]: C[t] = sum_j topk_weights[t, j] * (A[t*topk + j] . Wdeq[topk_ids[t, j]]^T)
+ *   workspace    hq_moe_combine_workspace_bytes(fmt, T, topk) bytes, zeroed
+ *                once by hq_workspace_init before its first use (it holds
+ *                the routing tables and an fp32 row per token)
+ * N must be a multiple of 4 (HQ_ERR_ALIGNMENT).  The routed rows' products are
+ * added into the fp32 rows with atomic reductions (the order of the k additions
+ * is not fixed, so the last bits may vary between runs), then rounded to
+ * nearest-even bf16.  A routed row whose id is out of range adds nothing and
+ * records HQ_ERR_BAD_ROUTING in the workspace status. */
+HQ_API size_t hq_moe_combine_workspace_bytes(const hq_format_t* fmt, int64_t T, int32_t topk);
+HQ_API hq_status_t hq_moe_gemm_combine(const hq_format_t* fmt, const hq_act_t* A, const void* packedW,
+                                       const int32_t* topk_ids, const float* topk_weights, int64_t T, int32_t topk,
+                                       void* C, void* workspace, size_t ws_bytes, hq_stream_t stream);
+
+/* Gated activation between a MoE layer's Gate-up and Down GEMMs:
+ * out[r, c] = silu(x[r, c]) * x[r, I + c], silu(g) = g / (1 + exp(-g)), for
+ * R rows of x = [gate | up] (bf16 [R, 2I], the Gate-up GEMM's output), out
+ * bf16 [R, I]; fp32 arithmetic, one rounding to nearest-even bf16.  I must be
+ * a multiple of 8 (HQ_ERR_ALIGNMENT); pointers 16-byte aligned. One kernel. */
+HQ_API hq_status_t hq_swiglu(const void* x, int64_t R, int64_t I, void* out, hq_stream_t stream);
 
 /* Copy the device status word out of `workspace` (synchronizes `stream`) and
  * clear it.  *status_out receives HQ_OK or the first device-detected error. */

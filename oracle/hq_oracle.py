@@ -281,3 +281,44 @@ def quantize_act_nvfp4(x_bits, global_amax=None):
     q = np.where((d > 0)[:, :, None], q, np.uint8(0)).reshape(M, K).astype(np.uint8)
     packed = (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8)
     return packed, sb.astype(np.uint8), g
+
+
+# ---------------------------------------------------------------- MoE layer: Down GEMM with combine, gated activation
+#
+# A MoE layer's speed-up counts its Gate-up and its Down GEMM ("Results: kernel microbenchmarks").  Between them the
+# gated activation joins the gate and up halves of each routed row; the Down GEMM takes the routed rows (row t*k + j
+# goes to expert ids[t, j]) and the k results of a token are summed with their top-k weights into one row.
+
+
+def moe_combine(adeq_rows, wdeq_of_expert, n_out, topk_ids, topk_weights=None, tokens=None):
+    """out[t] = sum_j topk_w[t, j] * (Adeq_rows[t*k + j] . Wdeq[ids[t, j]]^T), float64.
+
+    `wdeq_of_expert(e)` returns expert e's decoded [N, K] weights, or None for an id that names no expert (that
+    routed row adds nothing).  `tokens` restricts the tokens computed; None computes all T.
+    """
+    ids = np.asarray(topk_ids)
+    T, k = ids.shape
+    toks = np.arange(T) if tokens is None else np.asarray(tokens)
+    y = np.zeros((len(toks), n_out))
+    cache = {}
+    for i, t in enumerate(toks):
+        for j in range(k):
+            e = int(ids[t, j])
+            if e not in cache:
+                cache[e] = wdeq_of_expert(e)
+            w = cache[e]
+            if w is None:
+                continue
+            v = np.asarray(adeq_rows[int(t) * k + j], dtype=np.float64) @ np.asarray(w, dtype=np.float64).T
+            if topk_weights is not None:
+                v = v * float(np.asarray(topk_weights)[t, j])
+            y[i] += v
+    return y
+
+
+def swiglu(x):
+    """Gated activation of x = [gate | up] ([R, 2I]): silu(gate) * up with silu(g) = g / (1 + exp(-g)), float64."""
+    x = np.asarray(x, dtype=np.float64)
+    half = x.shape[1] // 2
+    g, u = x[:, :half], x[:, half:]
+    return g / (1.0 + np.exp(-g)) * u

@@ -29,7 +29,8 @@ HQ_A_BF16, HQ_A_E4M3_TOKEN, HQ_A_NVFP4 = 1, 2, 3
 
 EXPORTS = ["hq_packed_bytes", "hq_pack_weights", "hq_unpack_weights", "hq_workspace_bytes", "hq_workspace_init",
            "hq_gemm", "hq_moe_gemm", "hq_last_device_status", "hq_status_string", "hq_gemm_static_scratch",
-           "hq_kernels_per_call", "hq_quantize_act_workspace_bytes", "hq_quantize_act"]
+           "hq_kernels_per_call", "hq_quantize_act_workspace_bytes", "hq_quantize_act",
+           "hq_moe_combine_workspace_bytes", "hq_moe_gemm_combine", "hq_swiglu"]
 
 
 class Format(ctypes.Structure):
@@ -69,6 +70,12 @@ _lib.hq_quantize_act_workspace_bytes.argtypes = [_i32, _i64, _i64]
 _lib.hq_quantize_act_workspace_bytes.restype = _sz
 _lib.hq_quantize_act.argtypes = [_i32, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
 _lib.hq_quantize_act.restype = ctypes.c_int
+_lib.hq_moe_combine_workspace_bytes.argtypes = [_F, _i64, _i32]
+_lib.hq_moe_combine_workspace_bytes.restype = _sz
+_lib.hq_moe_gemm_combine.argtypes = [_F, _A, _vp, _vp, _vp, _i64, _i32, _vp, _vp, _sz, _vp]
+_lib.hq_moe_gemm_combine.restype = ctypes.c_int
+_lib.hq_swiglu.argtypes = [_vp, _i64, _i64, _vp, _vp]
+_lib.hq_swiglu.restype = ctypes.c_int
 _lib.hq_status_string.argtypes = [ctypes.c_int]
 _lib.hq_status_string.restype = ctypes.c_char_p
 
@@ -137,8 +144,10 @@ def workspace_bytes(fmt, rows, topk=1):
 
 
 def kernels_per_call(fmt, rows, topk=1, moe=False):
-    """Kernels one gemm (moe=False) or moe_gemm call launches on the current device."""
-    return int(_lib.hq_kernels_per_call(ctypes.byref(fmt), int(rows), int(topk), 1 if moe else 0))
+    """Kernels one gemm (moe=False), moe_gemm (moe=True) or moe_gemm_combine (moe="combine") call launches on the
+    current device."""
+    m = 2 if moe == "combine" else (1 if moe else 0)
+    return int(_lib.hq_kernels_per_call(ctypes.byref(fmt), int(rows), int(topk), m))
 
 
 def make_workspace(fmt, rows, topk=1, device="cuda", stream=None):
@@ -192,6 +201,42 @@ def moe_gemm(fmt, act, packed, topk_ids, topk_weights=None, out=None, workspace=
     _check(_lib.hq_moe_gemm(ctypes.byref(fmt), ctypes.byref(A), _ptr(packed), _ptr(topk_ids), _ptr(topk_weights),
                             int(T), int(k), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)),
            "hq_moe_gemm")
+    return out
+
+
+def make_combine_workspace(fmt, T, topk, device="cuda", stream=None):
+    """Allocate and zero a workspace for `moe_gemm_combine` with T tokens of `topk` routed rows."""
+    nb = int(_lib.hq_moe_combine_workspace_bytes(ctypes.byref(fmt), int(T), int(topk)))
+    if nb == 0:
+        raise HQError(HQ_ERR_INVALID_ARG, "hq_moe_combine_workspace_bytes")
+    ws = torch.empty(nb, dtype=torch.uint8, device=device)
+    _check(_lib.hq_workspace_init(_ptr(ws), nb, _stream(stream)), "hq_workspace_init")
+    return ws
+
+
+def moe_gemm_combine(fmt, act, packed, topk_ids, topk_weights=None, out=None, workspace=None, stream=None):
+    """MoE Down GEMM + top-k combine: act holds the T*topk routed rows (row t*topk+j -> expert ids[t, j]);
+    C[T, N] bf16 with C[t] = sum_j topk_w[t, j] * (A[t*topk+j] . Wdeq[ids[t, j]]^T)."""
+    T, k = topk_ids.shape
+    dev = act["data"].device
+    if out is None:
+        out = torch.empty((T, fmt.N), dtype=torch.bfloat16, device=dev)
+    if workspace is None:
+        workspace = make_combine_workspace(fmt, T, k, dev, stream)
+    A = _act(act)
+    _check(_lib.hq_moe_gemm_combine(ctypes.byref(fmt), ctypes.byref(A), _ptr(packed), _ptr(topk_ids),
+                                    _ptr(topk_weights), int(T), int(k), _ptr(out), _ptr(workspace), workspace.numel(),
+                                    _stream(stream)), "hq_moe_gemm_combine")
+    return out
+
+
+def swiglu(x, out=None, stream=None):
+    """x bf16 [R, 2I] = [gate | up] -> bf16 [R, I] = silu(gate) * up."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous() and x.shape[1] % 2 == 0
+    R, I2 = x.shape
+    if out is None:
+        out = torch.empty((R, I2 // 2), dtype=torch.bfloat16, device=x.device)
+    _check(_lib.hq_swiglu(_ptr(x), int(R), int(I2 // 2), _ptr(out), _stream(stream)), "hq_swiglu")
     return out
 
 

@@ -21,6 +21,8 @@ cudaError_t launch_gemm_nvfp4(const GemmArgs& a, int bt, int grid, cudaStream_t 
 cudaError_t launch_gemm_mxfp4(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_small(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(int path, const GemmArgs& a, int bt, int gemm_grid, int grid, cudaStream_t stream);
+cudaError_t launch_combine_round(const float* acc, int64_t n, uint16_t* c, cudaStream_t stream);
+cudaError_t launch_swiglu(const void* x, int64_t R, int64_t I, void* out, cudaStream_t stream);
 cudaError_t launch_moe_permute(const int* counts, const int* region, int cap, int E, int topk, int64_t rows,
                                const void* src, int row_bytes, void* dst, const void* sf_src, int sf_bytes, void* sf_dst,
                                int* row_off, cudaStream_t stream);
@@ -327,6 +329,7 @@ int32_t hq_kernels_per_call(const hq_format_t* fmt, int64_t M_or_T, int32_t topk
   const Plan p = make_plan(fmt, M_or_T, topk, moe != 0, num_sms());
   int32_t n = 1 + (p.sk ? 1 : 0);  // GEMM (+ split-K reduction)
   if (moe) n += 1 + (p.grouped ? 1 : 0);  // routing (+ row permutation)
+  if (moe == 2) n += 1;                    // combine: rounding of the summed token rows
   return n;
 }
 
@@ -379,9 +382,18 @@ hq_status_t hq_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* packe
   return cuda_status(launch_path(p, a, (cudaStream_t)stream));
 }
 
-hq_status_t hq_moe_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* packedW, const int32_t* topk_ids,
-                        const float* topk_weights, int64_t T, int32_t topk, void* C, void* workspace, size_t ws_bytes,
-                        hq_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Workspace offset of the combine's fp32 token rows (after everything the plan places).
+size_t comb_offset(const Plan& p) { return align256(p.ws_bytes); }
+
+// hq_moe_gemm (combine = false: A holds T token rows, C the T*topk routed rows) and hq_moe_gemm_combine (A holds the
+// T*topk routed rows, C the T token rows summed over their top-k slots).
+hq_status_t moe_call(const hq_format_t* fmt, const hq_act_t* A, const void* packedW, const int32_t* topk_ids,
+                     const float* topk_weights, int64_t T, int32_t topk, void* C, void* workspace, size_t ws_bytes,
+                     hq_stream_t stream, bool combine) {
   hq_status_t st = check_format(fmt);
   if (st != HQ_OK) return st;
   if (T < 0 || topk < 1 || T * topk > kMaxRows) return HQ_ERR_INVALID_ARG;
@@ -394,7 +406,11 @@ hq_status_t hq_moe_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* p
   const int sms = num_sms();
   if (sms < 1) return HQ_ERR_CUDA;
   const Plan p = make_plan(fmt, T, topk, true, sms);
-  if (!workspace || ws_bytes < p.ws_bytes) return HQ_ERR_WORKSPACE;
+  if (combine && fmt->N % 4) return HQ_ERR_ALIGNMENT;
+  const size_t need = combine ? comb_offset(p) + sizeof(float) * (size_t)(T * fmt->N) : p.ws_bytes;
+  if (!workspace || ws_bytes < need) return HQ_ERR_WORKSPACE;
+  const int64_t a_rows = combine ? T * topk : T;  // activation rows: tokens, or routed rows for the combine
+  const int a_div = combine ? 1 : topk;          // routed row -> activation row
   const int64_t E = fmt->num_experts;
   const PackGeom g = pack_geom(fmt->weight_type, fmt->N, fmt->K, E);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -408,14 +424,17 @@ hq_status_t hq_moe_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* p
     G.data = ws + p.off_gact;
     if (fmt->act_type == HQ_A_NVFP4) G.scale = ws + p.off_gsf;
     if (!act_maps(a, fmt, &G, T * topk, p.bt, false)) return HQ_ERR_INVALID_ARG;
-  } else if (!act_maps(a, fmt, A, T, p.bt, true)) {
+  } else if (!act_maps(a, fmt, A, a_rows, p.bt, true)) {
     return HQ_ERR_INVALID_ARG;
   }
+  float* comb = combine ? reinterpret_cast<float*>(ws + comb_offset(p)) : nullptr;
+  if (combine && cudaMemsetAsync(comb, 0, sizeof(float) * (size_t)(T * fmt->N), (cudaStream_t)stream) != cudaSuccess)
+    return HQ_ERR_CUDA;
   cudaError_t err =
       launch_route(topk_ids, T * topk, (int)E, (int)p.region_cap, counts, region, status, (cudaStream_t)stream);
   if (err != cudaSuccess) return HQ_ERR_CUDA;
   if (p.grouped) {
-    err = launch_moe_permute(counts, region, (int)p.region_cap, (int)E, topk, T * topk, A->data,
+    err = launch_moe_permute(counts, region, (int)p.region_cap, (int)E, a_div, T * topk, A->data,
                              (int)act_row_bytes(fmt), ws + p.off_gact,
                              fmt->act_type == HQ_A_NVFP4 ? A->scale : nullptr, (int)(fmt->K / 16),
                              fmt->act_type == HQ_A_NVFP4 ? ws + p.off_gsf : nullptr,
@@ -441,8 +460,10 @@ hq_status_t hq_moe_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* p
   a.zp = fmt->has_zero;
   a.moe = 1;
   a.E = (int)E;
-  a.topk = topk;
+  a.topk = a_div;
   a.topk_w = topk_weights;
+  a.comb = comb;
+  a.comb_k = topk;
   a.counts = counts;
   a.region = region;
   a.region_cap = (int)p.region_cap;
@@ -450,8 +471,42 @@ hq_status_t hq_moe_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* p
   a.sk = p.sk;
   a.status = status;
   a.partials = p.sk ? reinterpret_cast<float*>(ws + p.off_partials) : nullptr;
-  return cuda_status(launch_path(p, a, (cudaStream_t)stream));
+  err = launch_path(p, a, (cudaStream_t)stream);
+  if (err != cudaSuccess || !combine) return cuda_status(err);
+  return cuda_status(launch_combine_round(comb, T * fmt->N, static_cast<uint16_t*>(C), (cudaStream_t)stream));
 }
+
+}  // namespace
+
+extern "C" {
+
+hq_status_t hq_moe_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* packedW, const int32_t* topk_ids,
+                        const float* topk_weights, int64_t T, int32_t topk, void* C, void* workspace, size_t ws_bytes,
+                        hq_stream_t stream) {
+  return moe_call(fmt, A, packedW, topk_ids, topk_weights, T, topk, C, workspace, ws_bytes, stream, false);
+}
+
+hq_status_t hq_moe_gemm_combine(const hq_format_t* fmt, const hq_act_t* A, const void* packedW,
+                                const int32_t* topk_ids, const float* topk_weights, int64_t T, int32_t topk, void* C,
+                                void* workspace, size_t ws_bytes, hq_stream_t stream) {
+  return moe_call(fmt, A, packedW, topk_ids, topk_weights, T, topk, C, workspace, ws_bytes, stream, true);
+}
+
+size_t hq_moe_combine_workspace_bytes(const hq_format_t* fmt, int64_t T, int32_t topk) {
+  if (check_format(fmt) != HQ_OK || T < 0 || topk < 1) return 0;
+  const Plan p = make_plan(fmt, T, topk, true, num_sms());
+  return comb_offset(p) + sizeof(float) * (size_t)(T * fmt->N);
+}
+
+hq_status_t hq_swiglu(const void* x, int64_t R, int64_t I, void* out, hq_stream_t stream) {
+  if (R < 0 || R > kMaxRows || I < 8 || I > kMaxRows) return HQ_ERR_INVALID_ARG;
+  if (I % 8) return HQ_ERR_ALIGNMENT;
+  if (R == 0) return HQ_OK;
+  if (!x || !out) return HQ_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out)) return HQ_ERR_ALIGNMENT;
+  return cuda_status(launch_swiglu(x, R, I, out, (cudaStream_t)stream));
+}
+
 
 size_t hq_quantize_act_workspace_bytes(int32_t act_type, int64_t M, int64_t K) {
   if (act_type != HQ_A_E4M3_TOKEN && act_type != HQ_A_NVFP4) return 0;

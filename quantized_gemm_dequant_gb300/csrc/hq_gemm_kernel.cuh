@@ -38,6 +38,7 @@
 #include <stdint.h>
 
 #include "hq_layout.h"
+#include "hq_launch.h"
 #include "hq_ptx.cuh"
 
 namespace hq {
@@ -76,6 +77,8 @@ struct GemmArgs {
   int sk;       // 1: Stream-K split over K blocks
   int* status;
   float* partials;  // Stream-K: [2 * grid][BT][128] fp32, slot 2*cta + {0 first piece, 1 later piece}
+  float* comb;      // MoE combine: fp32 [T][N]; the output of routed row r is added into token r / comb_k (else null)
+  int comb_k;
 };
 
 template <int PATH, int BT>
@@ -296,7 +299,9 @@ __device__ __forceinline__ void moe_tile_prefix(const int* counts, int E, int re
   }
 }
 
-template <int PATH, int BT>
+// COMB instances carry the MoE combine epilogue (args.comb set: routed rows are added into their tokens' fp32 rows);
+// the others are compiled without it, so that their register allocation is not shaped by it.
+template <int PATH, int BT, bool COMB>
 __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_constant__ GemmArgs args) {
   using C = Cfg<PATH, BT>;
   static_assert(sizeof(Smem<PATH, BT>) <= 4096, "shared state");
@@ -898,6 +903,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
       if (!pc.full) {
 #pragma unroll
         for (int j = 0; j < HC; ++j) part[(col0 + j) * TILE_N + r] = __uint_as_float(v[j]);
+      } else if (COMB) {
+        // MoE combine: the routed row's values (x top-k weight) are added into its token's fp32 row.  N % 4 == 0: a
+        // quad of lanes (4 adjacent output features) transposes its 4 x 4 values of 4 token columns in two shuffle
+        // rounds, so that each lane adds 4 adjacent outputs of one token with one 16-byte reduction.
+        const bool quad = (args.N & 3) == 0;
+        const int b0 = lane & 1, b1 = (lane >> 1) & 1;
+        const int n4 = n & ~3;
+#pragma unroll
+        for (int j = 0; j < HC; j += 4) {
+          int orw[4];
+          float o[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float mul;
+            lookup(col0 + j + c, orw[c], mul);
+            o[c] = __uint_as_float(v[j + c]) * mul + bias_v;
+          }
+          if (quad) {
+            // round 1 (lane ^ 1): tokens b0 and b0 + 2, rows 2 b1 and 2 b1 + 1 of the quad
+            const float r1a = __shfl_xor_sync(0xffffffffu, b0 ? o[0] : o[1], 1);
+            const float r1b = __shfl_xor_sync(0xffffffffu, b0 ? o[2] : o[3], 1);
+            const float ta0 = b0 ? r1a : o[0], ta1 = b0 ? o[1] : r1a;  // token b0
+            const float tb0 = b0 ? r1b : o[2], tb1 = b0 ? o[3] : r1b;  // token b0 + 2
+            // round 2 (lane ^ 2): token b0 + 2 b1, rows 0..3 of the quad
+            const float s0 = __shfl_xor_sync(0xffffffffu, b1 ? ta0 : tb0, 2);
+            const float s1 = __shfl_xor_sync(0xffffffffu, b1 ? ta1 : tb1, 2);
+            const int tc = b0 + 2 * b1;
+            const int orow = tc == 0 ? orw[0] : (tc == 1 ? orw[1] : (tc == 2 ? orw[2] : orw[3]));
+            if (orow >= 0 && n4 < args.N)
+              red_add_v4_f32(args.comb + (int64_t)(orow / args.comb_k) * args.N + n4, b1 ? s0 : ta0, b1 ? s1 : ta1,
+                             b1 ? tb0 : s0, b1 ? tb1 : s1);
+          } else if (n < args.N) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              if (orw[c] >= 0) red_add_f32(args.comb + (int64_t)(orw[c] / args.comb_k) * args.N + n, o[c]);
+          }
+        }
       } else if (use_table && pair_ok) {
         // Table rows (MoE, MXFP4), even N: the pair exchange of the dense case below, each token column with its
         // own output row and multiplier.
@@ -968,6 +1010,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  }
+}
+
+// Launch one instance: token tile BT, combine epilogue or not.
+template <int PATH, int BT, bool COMB>
+cudaError_t launch_umma_bt(const GemmArgs& a, int grid, cudaStream_t stream) {
+  using C = Cfg<PATH, BT>;
+  void (*kernel)(GemmArgs) = hq_gemm_kernel<PATH, BT, COMB>;
+  static int attr_set[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = 1;
+  }
+  return launch_kernel(kernel, dim3(grid), dim3(NUM_THREADS), C::SMEM_BYTES, stream, a);
+}
+
+template <int PATH, bool COMB>
+cudaError_t launch_umma(const GemmArgs& a, int bt, int grid, cudaStream_t stream) {
+  switch (bt) {
+    case 16: return launch_umma_bt<PATH, 16, COMB>(a, grid, stream);
+    case 32: return launch_umma_bt<PATH, 32, COMB>(a, grid, stream);
+    case 64: return launch_umma_bt<PATH, 64, COMB>(a, grid, stream);
+    case 128: return launch_umma_bt<PATH, 128, COMB>(a, grid, stream);
+    case 256: return launch_umma_bt<PATH, 256, COMB>(a, grid, stream);
+    default: return cudaErrorInvalidValue;
   }
 }
 

@@ -343,8 +343,12 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                   const int orow = t_row[i][u];
-                  if (orow >= 0)
-                    args.c[(int64_t)orow * args.N + n] = f32_to_bf16(acc[m][i][2 * rr + u] * t_mul[i][u] + bias);
+                  if (orow < 0) continue;
+                  const float o = acc[m][i][2 * rr + u] * t_mul[i][u] + bias;
+                  if (args.comb)  // MoE combine: add into the token's fp32 row
+                    red_add_f32(args.comb + (int64_t)(orow / args.comb_k) * args.N + n, o);
+                  else
+                    args.c[(int64_t)orow * args.N + n] = f32_to_bf16(o);
                 }
             }
           }

@@ -108,6 +108,17 @@ __global__ void __launch_bounds__(RED_THREADS) splitk_reduce_kernel(const __grid
       }
       const float o[4] = {acc[u].x * mul + bias4[0], acc[u].y * mul + bias4[1], acc[u].z * mul + bias4[2],
                           acc[u].w * mul + bias4[3]};
+      if (args.comb) {  // MoE combine: add into the token's fp32 row
+        float* dst = args.comb + (int64_t)(orow / args.comb_k) * args.N + n0;
+        if ((args.N & 3) == 0 && n0 + 3 < args.N) {
+          red_add_v4_f32(dst, o[0], o[1], o[2], o[3]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (n0 + i < args.N) red_add_f32(dst + i, o[i]);
+        }
+        continue;
+      }
       uint16_t* dst = args.c + (int64_t)orow * args.N + n0;
       if (vec_store && n0 + 3 < args.N) {
         *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));

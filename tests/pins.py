@@ -376,6 +376,44 @@ def pin_act_quant_nvfp4(o):
     assert not q[zero_rows].any() and not sb[zero_rows].any()
 
 
+# ------------------------------------------------------------ pins on the MoE layer pieces
+
+def pin_moe_combine(o, rng=None):
+    """The combine equals an exact rational brute force on a tiny case (integer activations and weights, dyadic top-k
+    weights), reduces to the routed-row product for k = 1, and does not depend on the order of a token's k slots."""
+    rng = rng or np.random.default_rng(5)
+    T, k, K, N, E = 3, 2, 4, 3, 3
+    rows = rng.integers(-3, 4, size=(T * k, K)).astype(np.float64)
+    W = rng.integers(-2, 3, size=(E, N, K)).astype(np.float64)
+    ids = np.array([[0, 2], [1, 0], [2, 1]])
+    tw = rng.integers(1, 8, size=(T, k)) / 8.0
+    got = o.moe_combine(rows, lambda e: W[e], N, ids, tw)
+    for t in range(T):
+        for n in range(N):
+            want = sum(Fraction(tw[t, j]) * sum(Fraction(rows[t * k + j, kk]) * Fraction(W[ids[t, j], n, kk])
+                                                 for kk in range(K)) for j in range(k))
+            assert Fraction(got[t, n]) == want
+    one = o.moe_combine(rows, lambda e: W[e], N, ids.reshape(-1, 1))
+    assert np.array_equal(one, np.stack([rows[i] @ W[ids.reshape(-1)[i]].T for i in range(T * k)]))
+    perm = np.array([1, 0])
+    rows_p = rows.reshape(T, k, K)[:, perm].reshape(T * k, K)
+    assert np.array_equal(o.moe_combine(rows_p, lambda e: W[e], N, ids[:, perm], tw[:, perm]), got)
+
+
+def pin_swiglu(o):
+    """silu(gate) * up against torch's silu in float64, and the closed forms silu(0) = 0, silu(g) - silu(-g) = g."""
+    g = torch.linspace(-30, 30, 241, dtype=torch.float64)
+    u = torch.cos(g) * 3
+    x = torch.cat([g.reshape(1, -1), u.reshape(1, -1)], dim=1).numpy()
+    want = (torch.nn.functional.silu(g) * u).numpy()
+    assert np.allclose(o.swiglu(x)[0], want, rtol=1e-14, atol=1e-300)
+    ones = np.ones_like(g.numpy())
+    sp = o.swiglu(np.concatenate([g.numpy(), ones])[None])[0]
+    sm = o.swiglu(np.concatenate([-g.numpy(), ones])[None])[0]
+    assert np.allclose(sp - sm, g.numpy(), rtol=1e-12, atol=1e-12)
+    assert o.swiglu(np.array([[0.0, 5.0]]))[0, 0] == 0.0
+
+
 ALL_PINS = [pin_e4m3, pin_e8m0, pin_e2m1, pin_bf16, pin_int4, pin_e0m_equivalence, pin_exact_int4,
             pin_exact_fp4, pin_library_special_case, pin_brute_force, pin_moe_reduces_to_dense, pin_encode_e4m3,
-            pin_encode_e2m1, pin_act_quant_e4m3, pin_act_quant_nvfp4]
+            pin_encode_e2m1, pin_act_quant_e4m3, pin_act_quant_nvfp4, pin_moe_combine, pin_swiglu]

@@ -49,6 +49,12 @@ MUTATIONS = {
                          "g = np.float32(amax / np.float32(E4M3_MAX))"),
     "act_nvfp4_block_scale_unrounded": ("d = (decode_e4m3(sb).astype(np.float32) * g).astype(np.float32)",
                                         "d = (amax_b / np.float32(6.0)).astype(np.float32)"),
+    "combine_weight_dropped": ("                v = v * float(np.asarray(topk_weights)[t, j])\n            y[i] += v",
+                               "                v = v\n            y[i] += v"),
+    "combine_row_index": ("np.asarray(adeq_rows[int(t) * k + j]", "np.asarray(adeq_rows[j * T + int(t)]"),
+    "combine_overwrites": ("            y[i] += v", "            y[i] = v"),
+    "silu_sign": ("return g / (1.0 + np.exp(-g)) * u", "return g / (1.0 + np.exp(g)) * u"),
+    "gate_up_swapped": ("g, u = x[:, :half], x[:, half:]", "u, g = x[:, :half], x[:, half:]"),
     "act_nvfp4_nibbles": ("packed = (q[:, 0::2] | (q[:, 1::2] << 4))", "packed = (q[:, 1::2] | (q[:, 0::2] << 4))"),
 }
 
