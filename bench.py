@@ -347,7 +347,7 @@ def kernel_name(cfg, M):
         bt = 16 if avg <= 16 else (256 if path != 1 and avg > 128 else 128)
     if path == 0 and bt <= 32 and os.environ.get("HQ_FORCE_PATH") != "umma":
         return f"hq::hq_gemm_small_kernel<{bt}>"
-    return f"hq::hq_gemm_kernel<{path}, {bt}, {'true' if c.get('down') else 'false'}>"
+    return f"hq::hq_gemm_kernel<{path}, {bt}, {1 if c.get('down') else 0}>"
 
 
 def gpu_launches(cfg, fmt, calls):
