@@ -37,3 +37,62 @@ def test_host_only_queries_work_without_a_gpu():
     assert hq.packed_bytes(hq.make_format("int4_sym", 100, 100)) == 0
     assert hq.status_string(hq.HQ_ERR_BAD_ROUTING).startswith("top-k")
     assert set(hq.EXPORTS) == set(declared())
+
+
+def _lib():
+    import quantized_gemm_dequant_gb300 as hq
+    return hq
+
+
+def test_quantize_act_host_checks_without_a_gpu():
+    """Argument errors of hq_quantize_act come back before anything touches the device (fake pointers are never
+    dereferenced on these paths)."""
+    hq = _lib()
+    L = hq._lib
+    X, D, S, G, WS = 0x10000, 0x20000, 0x30000, 0x40000, 0x50000
+    nv, f8 = hq.HQ_A_NVFP4, hq.HQ_A_E4M3_TOKEN
+    assert L.hq_quantize_act(99, X, 4, 64, None, D, S, G, WS, 1 << 20, None) == hq.HQ_ERR_UNSUPPORTED
+    assert L.hq_quantize_act(nv, X, -1, 64, None, D, S, G, WS, 1 << 20, None) == hq.HQ_ERR_INVALID_ARG
+    assert L.hq_quantize_act(nv, X, 4, 8, None, D, S, G, WS, 1 << 20, None) == hq.HQ_ERR_INVALID_ARG
+    assert L.hq_quantize_act(nv, X, 4, 24, None, D, S, G, WS, 1 << 20, None) == hq.HQ_ERR_ALIGNMENT
+    assert L.hq_quantize_act(nv, X, 4, 64, None, D, S, None, WS, 1 << 20, None) == hq.HQ_ERR_INVALID_ARG
+    assert L.hq_quantize_act(f8, None, 4, 64, None, D, S, None, None, 0, None) == hq.HQ_ERR_INVALID_ARG
+    assert L.hq_quantize_act(f8, X + 8, 4, 64, None, D, S, None, None, 0, None) == hq.HQ_ERR_ALIGNMENT
+    assert L.hq_quantize_act(nv, X, 4, 64, None, D, S, G, None, 0, None) == hq.HQ_ERR_WORKSPACE
+    assert L.hq_quantize_act(nv, X, 4, 64, None, D, S, G, WS, 64, None) == hq.HQ_ERR_WORKSPACE
+    assert L.hq_quantize_act(f8, X, 0, 64, None, D, S, None, None, 0, None) == hq.HQ_OK  # nothing to do
+    assert hq.quantize_act_workspace_bytes("nvfp4", 8192, 7168) == 4 * 4096
+    assert hq.quantize_act_workspace_bytes("e4m3_tok", 8192, 7168) == 0
+    assert L.hq_quantize_act_workspace_bytes(nv, 8, 24) == 0
+
+
+def test_swiglu_host_checks_without_a_gpu():
+    hq = _lib()
+    L = hq._lib
+    assert L.hq_swiglu(0x10000, -1, 64, 0x20000, None) == hq.HQ_ERR_INVALID_ARG
+    assert L.hq_swiglu(0x10000, 4, 12, 0x20000, None) == hq.HQ_ERR_ALIGNMENT
+    assert L.hq_swiglu(None, 4, 64, 0x20000, None) == hq.HQ_ERR_INVALID_ARG
+    assert L.hq_swiglu(0x10008, 4, 64, 0x20000, None) == hq.HQ_ERR_ALIGNMENT
+    assert L.hq_swiglu(None, 0, 64, None, None) == hq.HQ_OK  # no rows
+
+
+def test_moe_combine_host_checks_without_a_gpu():
+    import ctypes
+    hq = _lib()
+    L = hq._lib
+    f = hq.make_format("int4_sym", 2048, 768, num_experts=128)
+    A = hq.Act(0x10000, None, None)
+    args = lambda T, k, ids=0x30000, C=0x40000: (ctypes.byref(f), ctypes.byref(A), 0x20000, ids, None, T, k, C,
+                                                 0x50000, 1 << 30, None)
+    assert L.hq_moe_gemm_combine(*args(-1, 8)) == hq.HQ_ERR_INVALID_ARG
+    assert L.hq_moe_gemm_combine(*args(4, 0)) == hq.HQ_ERR_INVALID_ARG
+    assert L.hq_moe_gemm_combine(*args(0, 8)) == hq.HQ_OK  # no tokens
+    assert L.hq_moe_gemm_combine(*args(4, 8, ids=None)) == hq.HQ_ERR_INVALID_ARG
+    assert L.hq_moe_gemm_combine(*args(4, 8, C=None)) == hq.HQ_ERR_INVALID_ARG
+    bad = hq.make_format("int4_sym", 2048, 768, num_experts=128, group_size=64)
+    assert L.hq_moe_gemm_combine(ctypes.byref(bad), ctypes.byref(A), 0x20000, 0x30000, None, 4, 8, 0x40000, 0x50000,
+                                 1 << 30, None) == hq.HQ_ERR_UNSUPPORTED
+    # the workspace holds the plan's regions and one fp32 row of N per token; the call adds one rounding kernel
+    assert L.hq_moe_combine_workspace_bytes(ctypes.byref(f), 4096, 8) >= 4096 * 2048 * 4 + 256
+    assert L.hq_moe_combine_workspace_bytes(ctypes.byref(f), -1, 8) == 0
+    assert hq.kernels_per_call(f, 4096, 8, moe="combine") == hq.kernels_per_call(f, 4096, 8, moe=True) + 1
