@@ -470,9 +470,18 @@ def measure_e2e(args, calls, stream, dev):
 
 
 # ------------------------------------------------------------------ CPU oracle
-def oracle_step(cfg_name, seed, state):
+def _slice_weights(inp, n_feat):
+    """The workload dict with only the first n_feat output features of every expert's weights (a bounded sample)."""
+    if not n_feat or n_feat >= inp["N"]:
+        return inp
+    w = {k: (v if k == "gscale" else v[..., :n_feat, :]) for k, v in inp["w"].items()}
+    return dict(inp, w=w, N=n_feat)
+
+
+def oracle_step(cfg_name, seed, state, n_feat=None):
     """One bounded sample of the workload through the CPU oracle: for each size of the sweep,
-    decode the weights and compute min(M, 2) output rows in fp64.  Returns (flops, seconds)."""
+    decode the weights (the first n_feat output features when given) and compute min(M, 2) output rows in fp64.
+    Returns (flops, seconds)."""
     import numpy as np
     import oracle
     from tests import ref_helpers as R
@@ -483,19 +492,18 @@ def oracle_step(cfg_name, seed, state):
         else:
             state["inp"] = W.make_moe(cfg_name, 2, seed=seed, experts_subset=None) if c["E"] <= 128 else None
     inp = state["inp"]
+    if inp is None and "one" not in state:  # too large for the host: one expert stands for the sample
+        state["one"] = W.make_moe(cfg_name, 2, seed=seed, experts_subset=[0])
+    src = _slice_weights(inp if inp is not None else state["one"], n_feat)
+    n_out = src["N"]
     flops, t0 = 0.0, time.perf_counter()
     for M in c["sizes"]:
         rows = min(M, 2)
         if c["kind"] == "dense":
-            y = oracle.gemm(R.acts_of(inp, list(range(rows))), R.weights_of(inp))
-            flops += 2.0 * rows * c["N"] * c["K"]
+            y = oracle.gemm(R.acts_of(src, list(range(rows))), R.weights_of(src))
         else:
-            if inp is None:  # too large for the host: one expert stands for the sample
-                one = W.make_moe(cfg_name, 2, seed=seed, experts_subset=[0])
-                y = oracle.gemm(R.acts_of(one, list(range(rows))), R.weights_of(one, 0))
-            else:
-                y = oracle.gemm(R.acts_of(inp, list(range(rows))), R.weights_of(inp, 0))
-            flops += 2.0 * rows * c["N"] * c["K"]
+            y = oracle.gemm(R.acts_of(src, list(range(rows))), R.weights_of(src, 0))
+        flops += 2.0 * rows * n_out * c["K"]
         assert np.all(np.isfinite(y))
     return flops, time.perf_counter() - t0
 
@@ -515,16 +523,19 @@ def cpu_baseline_line(args):
                       "plus the fp64 matmul of those rows (numpy)", "seconds": round(s, 2)}
 
 
+REF_FEATURES = 64  # output features per size in a reference-arm step: about 0.1 s of numpy per step
+
+
 def run_reference(args):
     rank, world, _ = env_rank()
     if rank != 0:
         return
     state = {}
     for _ in range(args.warmup):
-        oracle_step(args.config, args.seed, state)
+        oracle_step(args.config, args.seed, state, n_feat=REF_FEATURES)
     flops = secs = 0.0
     for _ in range(args.steps):
-        f, s = oracle_step(args.config, args.seed, state)
+        f, s = oracle_step(args.config, args.seed, state, n_feat=REF_FEATURES)
         flops += f
         secs += s
     value = flops / secs / 1e12
@@ -536,7 +547,8 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": workload_name(args.config), "sizes": c["sizes"]},
         "cpu_baseline": {"value": round(value, 9), "unit": "TFLOP/s", "kind": "oracle", "cores": cpu_cores(),
-                         "sample": "per step: each size of the sweep, weight decode + fp64 matmul of min(M, 2) rows"},
+                         "sample": f"per step: each size of the sweep, weight decode of the first {REF_FEATURES} output "
+                                   f"features + fp64 matmul of min(M, 2) rows (bounded so that the run takes minutes)"},
         "e2e": {"value": round(value, 9), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -567,7 +579,7 @@ def aq_workload_name(cfg):
     return f"activation quantization bf16 -> {what}, K={c['K']}, M in {c['sizes']}"
 
 
-def aq_oracle_step(cfg, seed, rows=32):
+def aq_oracle_step(cfg, seed, rows=32):  # 32 rows per size: about 0.06 s (a reference-arm step)
     """The CPU oracle on a bounded sample: `rows` rows of every size of the sweep.  Returns (bytes, seconds)."""
     import numpy as np
     import oracle
@@ -709,9 +721,9 @@ def run_act_quant(args):
                "ms_per_step": round(ms, 4), "steps": nsteps}
     cpu = None
     if rank == 0 and not args.no_cpu:
-        b, sec = aq_oracle_step(args.config, args.seed)
+        b, sec = aq_oracle_step(args.config, args.seed, rows=4096)
         cpu = {"value": round(b / sec / 1e9, 4), "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
-               "sample": "32 rows (or M if smaller) of every size of the sweep, quantized by the numpy oracle",
+               "sample": "4096 rows (or M if smaller) of every size of the sweep, quantized by the numpy oracle",
                "seconds": round(sec, 2)}
     line = {"metric": AQ_METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
