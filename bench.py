@@ -49,6 +49,16 @@ def peaks():
     return dict(FALLBACK), "fallback"
 
 
+def max_over_ranks(x, device=None):
+    """The largest value of x over the ranks of the initialised process group (x itself on one rank)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def env_rank():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
 
@@ -272,11 +282,7 @@ def run_ours(args):
             st = hq.last_device_status(ws)
             if st != 0:
                 raise RuntimeError(f"device status {hq.status_string(st)} after the timed run")
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([step_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        step_ms = float(tt.item())
+    step_ms = max_over_ranks(step_ms, dev)  # the slowest rank's step time
     flops_step = sum(info["flops"] for (_, _, info, _, _, _) in calls)
     value = world * flops_step / (step_ms * 1e-3) / 1e12
 
