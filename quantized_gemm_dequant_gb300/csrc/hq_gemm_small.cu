@@ -11,8 +11,9 @@
 // Each weight row of a block is one row of a 16-row MMA tile; lane (g, t) of
 // a warp extracts the (2t, 2t+1) code pair of rows g and g+8 from the shared
 // words, so every nibble is decoded by exactly one thread.  Codes become
-// exact integers (q - z) in bf16; the group scale multiplies the fp32 group
-// partial after the MMA, so the decode adds no rounding.
+// exact integers (q - z) in bf16 and are multiplied by the group scale in
+// bf16: the same single rounding of (q - z) * s as in the UMMA path, so the
+// MMAs accumulate every block straight into the fp32 accumulators.
 //
 // Two CTAs per SM for 16-token tiles.  Warps 0-7 compute (warp (rg, kh): rows 32rg..32rg+31 of the 128-row tile,
 // K half kh of every block); warp 8 produces: one bulk copy of the weight block plus the TMA load (dense) or
