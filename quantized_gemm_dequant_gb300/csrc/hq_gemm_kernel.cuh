@@ -184,7 +184,7 @@ struct Sched {
   int tiles, kst, P, cta, sk;
   int64_t W;    // total block iterations
   bool narrow;  // W * P < 2^32: every product below fits 32 bits (64-bit division is a long software routine)
-  __device__ void init(int tiles_, int kst_, int grid, int cta_, int sk_) {
+  __host__ __device__ void init(int tiles_, int kst_, int grid, int cta_, int sk_) {
     tiles = tiles_;
     kst = kst_;
     W = (int64_t)tiles * kst;
@@ -193,14 +193,14 @@ struct Sched {
     sk = sk_;
     narrow = (uint64_t)W * (uint64_t)(P > 0 ? P : 1) < (1ull << 32);
   }
-  __device__ int64_t start(int c) const {
+  __host__ __device__ int64_t start(int c) const {
     return narrow ? (int64_t)(((uint32_t)c * (uint32_t)W) / (uint32_t)P) : (int64_t)c * W / P;
   }
   // largest CTA whose range starts at or before iteration it
-  __device__ int cta_of(int64_t it) const {
+  __host__ __device__ int cta_of(int64_t it) const {
     return narrow ? (int)(((uint32_t)(it + 1) * (uint32_t)P - 1u) / (uint32_t)W) : (int)(((it + 1) * P - 1) / W);
   }
-  __device__ void split(int64_t it, int& t, int& g) const {  // iteration -> (tile, K block)
+  __host__ __device__ void split(int64_t it, int& t, int& g) const {  // iteration -> (tile, K block)
     if (narrow) {
       t = (int)((uint32_t)it / (uint32_t)kst);
       g = (int)((uint32_t)it - (uint32_t)t * (uint32_t)kst);
@@ -211,8 +211,9 @@ struct Sched {
   }
 };
 
+// (host-callable as well: tests/sched_check.cu checks the partition on the CPU)
 template <typename F>
-__device__ __forceinline__ void for_each_piece(const Sched& s, F&& f) {
+__host__ __device__ __forceinline__ void for_each_piece(const Sched& s, F&& f) {
   if (!s.sk) {
     for (int t = s.cta; t < s.tiles; t += s.P) f(Piece{t, 0, s.kst, true, 0});
     return;
