@@ -71,7 +71,8 @@ class ClockSampler:
 
     def __init__(self, gpu_index):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        import tempfile
+        self.path = os.path.join(tempfile.gettempdir(), f"hq_clocks_{os.getpid()}.csv")  # raw samples; summary in the line
         self.gpu = gpu_index
 
     def start(self):
