@@ -214,6 +214,124 @@ def roofline_of(info, t_s, pk, dt):
 
 
 # ------------------------------------------------------------------ GPU arm
+MIN_SAMPLES = 20       # samples per size (bursts, and isolated calls)
+MIN_SAMPLES_FAST = 100  # below 10 us per call
+OTHER_CONFIGS = ["w4a16_sym", "nvfp4", "moe_w4a16", "moe_mxfp4", "moe_w4a16_down", "moe_mxfp4_down"]
+
+
+def _burst(call, n, R, stream, counter):
+    """One event window holding n back-to-back calls of one size (each on the next input replica), preceded by a
+    GPU spin so that the window holds the calls' GPU work and not the host's launch latency."""
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(SPIN_CYCLES)
+    e0.record(stream)
+    for _ in range(n):
+        call(counter[0] % R, stream=stream)
+        counter[0] += 1
+    e1.record(stream)
+    return (e0, e1, n)
+
+
+def sample_sizes(calls, R, burst, stream, counter, dev):
+    """Per size: >= 20 bursts of back-to-back calls (>= 100 below 10 us per call) and as many isolated calls (one
+    call alone in its event window after a spin: no overlap with a previous GEMM, cold L2 through the replicas).
+    Returns [(burst samples in ms per call, burst call counts, isolated samples in ms)] per size."""
+    out = []
+    for (M, call, info, _, _, _) in calls:
+        bs = [_burst(call, burst, R, stream, counter) for _ in range(MIN_SAMPLES)]
+        iso = [_burst(call, 1, R, stream, counter) for _ in range(MIN_SAMPLES)]
+        torch.cuda.synchronize(dev)
+        per = [a.elapsed_time(b) / n for a, b, n in bs]
+        if statistics.median(per) < 0.010:
+            bs += [_burst(call, burst, R, stream, counter) for _ in range(MIN_SAMPLES_FAST - MIN_SAMPLES)]
+            iso += [_burst(call, 1, R, stream, counter) for _ in range(MIN_SAMPLES_FAST - MIN_SAMPLES)]
+            torch.cuda.synchronize(dev)
+        out.append(([a.elapsed_time(b) / n for a, b, n in bs], [n for _, _, n in bs],
+                    [a.elapsed_time(b) for a, b, _ in iso]))
+    return out
+
+
+def _q(xs, f):
+    q = sorted(xs)
+    return q[min(len(q) - 1, int(f * len(q)))]
+
+
+def summarize(cfg_name, calls, samples, pk, pk_src, dt):
+    """Per-size records (burst median / p10 / p90 and isolated median / p10 / p90, throughput, roofline fraction)
+    and the roofline of the dominant kernel over the burst samples."""
+    sweep, by_kernel = [], {}
+    for (M, _, info, _, _, _), (ms, ns, iso) in zip(calls, samples):
+        t = statistics.median(ms) * 1e-3
+        ti = statistics.median(iso) * 1e-3
+        bound, frac = roofline_of(info, t, pk, dt)
+        _, frac_i = roofline_of(info, ti, pk, dt)
+        e = dict(M=M, us=round(t * 1e6, 2), p10_us=round(_q(ms, 0.1) * 1e3, 2), p90_us=round(_q(ms, 0.9) * 1e3, 2),
+                 samples=len(ms), tflops=round(info["flops"] / t / 1e12, 3),
+                 weight_gbs=round(info["weight_bytes"] / t / 1e9, 1), total_gbs=round(info["total_bytes"] / t / 1e9, 1),
+                 bound=bound, roofline_frac=round(frac, 4),
+                 iso_us=round(ti * 1e6, 2), iso_p10_us=round(_q(iso, 0.1) * 1e3, 2),
+                 iso_p90_us=round(_q(iso, 0.9) * 1e3, 2), iso_roofline_frac=round(frac_i, 4))
+        if "experts_hit" in info:
+            e["experts_hit"] = info["experts_hit"]
+        sweep.append(e)
+        key = kernel_name(cfg_name, M)
+        k = by_kernel.setdefault(key, dict(flops=0.0, bytes=0.0, t=0.0, n=0))
+        k["flops"] += info["flops"] * sum(ns)
+        k["bytes"] += info["total_bytes"] * sum(ns)
+        k["t"] += sum(m * n for m, n in zip(ms, ns)) * 1e-3
+        k["n"] += sum(ns)
+    dom = max(by_kernel, key=lambda k: by_kernel[k]["t"])
+    d = by_kernel[dom]
+    tc_peak = pk["bf16_tflops"] * DTYPE_RATIO[dt]
+    t_launch = d["t"] / d["n"]
+    if d["flops"] / (tc_peak * 1e12) >= d["bytes"] / (pk["hbm_gbs"] * 1e9):
+        ach = d["flops"] / d["n"] / t_launch / 1e12
+        roof = dict(bound="tensor", achieved=round(ach, 2), peak=tc_peak, unit="TFLOP/s", frac=round(ach / tc_peak, 4))
+    else:
+        ach = d["bytes"] / d["n"] / t_launch / 1e9
+        roof = dict(bound="hbm", achieved=round(ach, 1), peak=pk["hbm_gbs"], unit="GB/s",
+                    frac=round(ach / pk["hbm_gbs"], 4))
+    roof.update(kernel=dom, peak_source=f"{pk_src} ({dt} {'burst bf16 x nominal ratio' if dt != 'bf16' else 'burst'})",
+                traffic=traffic_of(dom, cfg_name),
+                note="achieved = algorithmic bytes (or FLOPs) of the kernel's launches / their CUDA-event time in "
+                     "the burst samples")
+    return sweep, roof
+
+
+def measure_other_config(cfg_name, args, pk, pk_src, stream, dev):
+    """The burst + isolated samples of another workload (no timed steps): per-size records and its dominant
+    kernel's roofline, as for the headline workload."""
+    c = W.CONFIGS[cfg_name]
+    dt = PATH_DTYPE[c["wfmt"]]
+    fmt, calls, R = make_calls(cfg_name, args.seed, dev)
+    counter = [0]
+    burst = R if args.burst is None else max(1, args.burst)
+    for (M, call, *_r) in calls:  # warm-up
+        for _ in range(max(3, args.warmup)):
+            _burst(call, burst, R, stream, counter)
+    torch.cuda.synchronize(dev)
+    samples = sample_sizes(calls, R, burst, stream, counter, dev)
+    sweep, roof = summarize(cfg_name, calls, samples, pk, pk_src, dt)
+    import quantized_gemm_dequant_gb300 as hq
+    for (_, _, _, _, _, wss) in calls:
+        for ws in wss:
+            st = hq.last_device_status(ws)
+            if st != 0:
+                raise RuntimeError(f"{cfg_name}: device status {hq.status_string(st)} after sampling")
+    flops = sum(info["flops"] for (_, _, info, *_r) in calls)
+    t = sum(e["us"] for e in sweep) * 1e-6
+    out = {"workload": workload_name(cfg_name), "dtype": dt, "replicas": R, "burst": burst,
+           "value": round(flops / t / 1e12, 3), "unit": "TFLOP/s",
+           "value_note": "one call per size: total FLOPs / sum of the per-size burst medians",
+           "roofline": roof, "sweep": sweep}
+    del calls
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return out
+
+
+# ------------------------------------------------------------------ GPU arm
 def run_ours(args):
     rank, world, local = env_rank()
     torch.cuda.set_device(local)
@@ -244,18 +362,7 @@ def run_ours(args):
         while done < n_steps:
             count = min(burst, n_steps - done)
             for i, (M, call, info, _, _, _) in enumerate(calls):
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                # keep the GPU busy (a spin with no memory traffic) while the host enqueues the burst, so the
-                # event window holds the calls' GPU work and not the host's launch latency
-                torch.cuda._sleep(SPIN_CYCLES)
-                e0.record(stream)
-                for _ in range(count):
-                    r = counter[0] % R  # a different replica on every call: cold L2 without a flush kernel
-                    counter[0] += 1
-                    call(r, stream=stream)
-                e1.record(stream)
-                times[i].append((e0, e1, count))
+                times[i].append(_burst(call, count, R, stream, counter))
             done += count
 
     warm = [[] for _ in calls]
@@ -271,11 +378,10 @@ def run_ours(args):
     run_steps(args.steps, times)
     barrier()
     t_wall = time.perf_counter() - t_wall0
-    clocks = clk.stop(t_epoch0, time.time())
-    # per size: the mean time of one call in each burst, and the weight (calls) of that burst
-    per_call_ms = [[a.elapsed_time(b) / n for a, b, n in ts] for ts in times]
-    per_call_n = [[n for _, _, n in ts] for ts in times]
     step_ms = sum(sum(a.elapsed_time(b) for a, b, _ in ts) for ts in times) / args.steps
+    # per-size statistics: their own samples (>= 20 bursts per size, >= 100 below 10 us), whatever --steps is
+    samples = sample_sizes(calls, R, burst, stream, counter, dev)
+    clocks = clk.stop(t_epoch0, time.time())
     # device status must be clean after the run
     import quantized_gemm_dequant_gb300 as hq
     for (_, _, _, _, _, wss) in calls:
@@ -286,40 +392,23 @@ def run_ours(args):
     step_ms = max_over_ranks(step_ms, dev)  # the slowest rank's step time
     flops_step = sum(info["flops"] for (_, _, info, _, _, _) in calls)
     value = world * flops_step / (step_ms * 1e-3) / 1e12
-
-    sweep, by_kernel = [], {}
-    for (M, _, info, _, _, _), ms, ns in zip(calls, per_call_ms, per_call_n):
-        t = statistics.median(ms) * 1e-3
-        bound, frac = roofline_of(info, t, pk, dt)
-        q = sorted(ms)
-        e = dict(M=M, us=round(t * 1e6, 2), p10_us=round(q[len(q) // 10] * 1e3, 2),
-                 p90_us=round(q[min(len(q) - 1, (9 * len(q)) // 10)] * 1e3, 2), tflops=round(info["flops"] / t / 1e12, 3),
-                 weight_gbs=round(info["weight_bytes"] / t / 1e9, 1), total_gbs=round(info["total_bytes"] / t / 1e9, 1),
-                 bound=bound, roofline_frac=round(frac, 4))
-        if "experts_hit" in info:
-            e["experts_hit"] = info["experts_hit"]
-        sweep.append(e)
-        key = kernel_name(args.config, M)
-        k = by_kernel.setdefault(key, dict(flops=0.0, bytes=0.0, t=0.0, n=0))
-        k["flops"] += info["flops"] * sum(ns)
-        k["bytes"] += info["total_bytes"] * sum(ns)
-        k["t"] += sum(m * n for m, n in zip(ms, ns)) * 1e-3
-        k["n"] += sum(ns)
-    dom = max(by_kernel, key=lambda k: by_kernel[k]["t"])
-    d = by_kernel[dom]
-    tc_peak = pk["bf16_tflops"] * DTYPE_RATIO[dt]
-    t_launch = d["t"] / d["n"]
-    if d["flops"] / (tc_peak * 1e12) >= d["bytes"] / (pk["hbm_gbs"] * 1e9):
-        ach = d["flops"] / d["n"] / t_launch / 1e12
-        roof = dict(bound="tensor", achieved=round(ach, 2), peak=tc_peak, unit="TFLOP/s", frac=round(ach / tc_peak, 4))
-    else:
-        ach = d["bytes"] / d["n"] / t_launch / 1e9
-        roof = dict(bound="hbm", achieved=round(ach, 1), peak=pk["hbm_gbs"], unit="GB/s", frac=round(ach / pk["hbm_gbs"], 4))
-    roof.update(kernel=dom, launches_per_step=d["n"] // args.steps, peak_source=f"{pk_src} ({dt} "
-                f"{'burst bf16 x nominal ratio' if dt != 'bf16' else 'burst'})", traffic=traffic_of(dom, args.config))
+    sweep, roof = summarize(args.config, calls, samples, pk, pk_src, dt)
+    roof["launches_per_step"] = sum(1 for (M, *_r) in calls if kernel_name(args.config, M) == roof["kernel"])
 
     e2e = measure_e2e(args, calls, stream, dev) if not args.no_e2e else None
     ctx = cublas_context(args, calls, sweep, stream, dev) if (rank == 0 and not args.no_context) else None
+    n_launch = gpu_launches(args.config, fmt, calls) * args.steps
+    del calls
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    others = None
+    if rank == 0 and not args.no_others and not args.sizes:
+        others = {}
+        for name in OTHER_CONFIGS:
+            if name != args.config:
+                others[name] = measure_other_config(name, args, pk, pk_src, stream, dev)
+        for name in AQ_CONFIGS:
+            others[name] = measure_act_quant(name, args, pk, pk_src, stream, dev)
     cpu = cpu_baseline_line(args) if (rank == 0 and not args.no_cpu) else None
     line = {
         "metric": "quantized GEMM TFLOP/s and weight GB/s vs M; % of HBM / tensor-core roofline",
@@ -331,11 +420,12 @@ def run_ours(args):
                          f"and output ({R} replicas, rotated; no flush kernel)",
                    "timing": f"CUDA events around bursts of {burst} back-to-back calls of one size on their "
                              f"stream (each call on its own replica), divided by the burst length; step = one call "
-                             f"per size",
+                             f"per size; per-size records: >= {MIN_SAMPLES} bursts (>= {MIN_SAMPLES_FAST} below "
+                             f"10 us) plus as many isolated single calls (iso_*)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": roof, "sweep": sweep, "gpu_launches": gpu_launches(args.config, fmt, calls) * args.steps,
+        "roofline": roof, "sweep": sweep, "gpu_launches": n_launch,
         "clocks": clocks, "wall_s_timed": round(t_wall, 3), "e2e": e2e, "cpu_baseline": cpu,
-        "context_cublas_bf16": ctx,
+        "context_cublas_bf16": ctx, "configs": others,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -614,15 +704,10 @@ def aq_oracle_step(cfg, seed, rows=32):  # 32 rows per size: about 0.06 s (a ref
     return nbytes, t
 
 
-def run_act_quant(args):
+def _aq_calls(cfg, args, dev):
     import quantized_gemm_dequant_gb300 as hq
-    rank, world, local = env_rank()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    pk, pk_src = peaks()
-    c = AQ_CONFIGS[args.config]
+    c = AQ_CONFIGS[cfg]
     afmt, K = c["afmt"], c["K"]
-    stream = torch.cuda.current_stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     calls = []
     for M in c["sizes"]:
@@ -642,49 +727,37 @@ def run_act_quant(args):
 
         calls.append(dict(M=M, R=R, call=call, call_cal=call_cal, xs=xs, outs=outs, bytes=aq_bytes(afmt, M, K),
                           bytes_cal=aq_bytes(afmt, M, K, calibrated=True)))
+    return calls
 
-    def timed(fn, R, n):
-        out = []
-        done, i = 0, 0
-        while done < n:
-            cnt = min(R, n - done)
-            torch.cuda._sleep(SPIN_CYCLES)
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(cnt):
-                fn(i % R, stream=stream)
-                i += 1
-            e1.record(stream)
-            out.append((e0, e1, cnt))
-            done += cnt
-        return out
 
-    for cl in calls:
-        timed(cl["call"], cl["R"], args.warmup * cl["R"])
-    torch.cuda.synchronize(dev)
-    clk = ClockSampler(local)
-    clk.start()
-    time.sleep(0.5)
-    torch.cuda.synchronize(dev)
-    t_epoch0 = time.time()
-    t_wall0 = time.perf_counter()
-    rec = [timed(cl["call"], cl["R"], args.steps) for cl in calls]
-    torch.cuda.synchronize(dev)
-    t_wall = time.perf_counter() - t_wall0
-    clocks = clk.stop(t_epoch0, time.time())
-    rec_cal = None
-    if afmt == "nvfp4":  # the quantize kernel alone (calibrated amax), for its roofline
-        rec_cal = [timed(cl["call_cal"], cl["R"], args.steps) for cl in calls]
-        torch.cuda.synchronize(dev)
-    sweep, step_ms = [], 0.0
+def _aq_timed(fn, R, n, stream):
+    out = []
+    done, i = 0, 0
+    while done < n:
+        cnt = min(R, n - done)
+        torch.cuda._sleep(SPIN_CYCLES)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(cnt):
+            fn(i % R, stream=stream)
+            i += 1
+        e1.record(stream)
+        out.append((e0, e1, cnt))
+        done += cnt
+    return out
+
+
+def _aq_summary(cfg, calls, rec, rec_cal, pk, pk_src):
+    c = AQ_CONFIGS[cfg]
+    afmt = c["afmt"]
+    sweep = []
     kern_t = kern_b = 0.0
     for i, (cl, ts) in enumerate(zip(calls, rec)):
         per = sorted(a.elapsed_time(b) / n for a, b, n in ts)
         t = statistics.median(per) * 1e-3
-        step_ms += sum(a.elapsed_time(b) for a, b, _ in ts) / args.steps
-        e = dict(M=cl["M"], us=round(t * 1e6, 2), p10_us=round(per[len(per) // 10] * 1e3, 2),
-                 p90_us=round(per[min(len(per) - 1, 9 * len(per) // 10)] * 1e3, 2),
+        e = dict(M=cl["M"], us=round(t * 1e6, 2), p10_us=round(_q(per, 0.1) * 1e3, 2),
+                 p90_us=round(_q(per, 0.9) * 1e3, 2), samples=len(per),
                  gbs=round(cl["bytes"] / t / 1e9, 1), roofline_frac=round(cl["bytes"] / t / 1e9 / pk["hbm_gbs"], 4))
         kts = rec_cal[i] if rec_cal else ts
         kper = sorted(a.elapsed_time(b) / n for a, b, n in kts)
@@ -694,15 +767,71 @@ def run_act_quant(args):
         sweep.append(e)
         kern_t += kt
         kern_b += cl["bytes_cal"] if rec_cal else cl["bytes"]
-    total_bytes = sum(cl["bytes"] for cl in calls)
-    value = world * total_bytes / (step_ms * 1e-3) / 1e9
     kname = "hq::act_quant_e4m3_kernel" if afmt == "e4m3_tok" else "hq::act_quant_nvfp4_kernel"
     ach = kern_b / kern_t / 1e9
     roof = dict(bound="hbm", achieved=round(ach, 1), peak=pk["hbm_gbs"], unit="GB/s", frac=round(ach / pk["hbm_gbs"], 4),
                 kernel=kname, launches_per_step=len(calls), peak_source=f"{pk_src} (copy bandwidth)",
-                traffic=traffic_of(kname, args.config),
-                note="achieved = algorithmic bytes of the sweep's launches / their event time, one launch per size"
-                     + ("; NVFP4: the quantize kernel alone, with a calibrated amax (one read of x)" if rec_cal else ""))
+                traffic=traffic_of(kname, cfg),
+                note="achieved = algorithmic bytes of the sweep's launches / their median event time, one launch "
+                     "per size" + ("; NVFP4: the quantize kernel alone, with a calibrated amax (one read of x)"
+                                   if rec_cal else ""))
+    return sweep, roof
+
+
+def measure_act_quant(cfg, args, pk, pk_src, stream, dev):
+    """Per-size samples of an activation quantizer (>= 20 bursts per size, 100 below 10 us): its sweep and its
+    kernel's roofline, for the per-config block of the default benchmark line."""
+    calls = _aq_calls(cfg, args, dev)
+    for cl in calls:
+        _aq_timed(cl["call"], cl["R"], 3 * cl["R"], stream)
+    torch.cuda.synchronize(dev)
+    rec, rec_cal = [], []
+    for cl in calls:
+        n = MIN_SAMPLES_FAST if cl["M"] <= 1024 else MIN_SAMPLES
+        rec.append(_aq_timed(cl["call"], cl["R"], n * cl["R"], stream))
+        if AQ_CONFIGS[cfg]["afmt"] == "nvfp4":
+            rec_cal.append(_aq_timed(cl["call_cal"], cl["R"], n * cl["R"], stream))
+    torch.cuda.synchronize(dev)
+    sweep, roof = _aq_summary(cfg, calls, rec, rec_cal or None, pk, pk_src)
+    total = sum(cl["bytes"] for cl in calls)
+    t = sum(e["us"] for e in sweep) * 1e-6
+    del calls
+    torch.cuda.empty_cache()
+    return {"workload": aq_workload_name(cfg), "dtype": "f32", "value": round(total / t / 1e9, 1), "unit": "GB/s",
+            "value_note": "one call per size: algorithmic bytes / sum of the per-size burst medians",
+            "roofline": roof, "sweep": sweep}
+
+
+def run_act_quant(args):
+    rank, world, local = env_rank()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pk, pk_src = peaks()
+    c = AQ_CONFIGS[args.config]
+    afmt, K = c["afmt"], c["K"]
+    stream = torch.cuda.current_stream(dev)
+    calls = _aq_calls(args.config, args, dev)
+    for cl in calls:
+        _aq_timed(cl["call"], cl["R"], args.warmup * cl["R"], stream)
+    torch.cuda.synchronize(dev)
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.5)
+    torch.cuda.synchronize(dev)
+    t_epoch0 = time.time()
+    t_wall0 = time.perf_counter()
+    rec = [_aq_timed(cl["call"], cl["R"], args.steps, stream) for cl in calls]
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall0
+    clocks = clk.stop(t_epoch0, time.time())
+    rec_cal = None
+    if afmt == "nvfp4":  # the quantize kernel alone (calibrated amax), for its roofline
+        rec_cal = [_aq_timed(cl["call_cal"], cl["R"], args.steps, stream) for cl in calls]
+        torch.cuda.synchronize(dev)
+    step_ms = sum(sum(a.elapsed_time(b) for a, b, _ in ts) for ts in rec) / args.steps
+    sweep, roof = _aq_summary(args.config, calls, rec, rec_cal, pk, pk_src)
+    total_bytes = sum(cl["bytes"] for cl in calls)
+    value = world * total_bytes / (step_ms * 1e-3) / 1e9
     e2e = None
     if not args.no_e2e:
         hosts = [(cl["xs"][0].cpu().pin_memory(), {k: torch.empty(v.shape, dtype=v.dtype).pin_memory()
@@ -788,6 +917,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-context", action="store_true", help="skip the cuBLAS bf16 context timing")
+    ap.add_argument("--no-others", action="store_true", help="time only the selected workload (no per-config block)")
     ap.add_argument("--sizes", default=None, help="comma list overriding the sweep (profiling)")
     ap.add_argument("--replicas", type=int, default=None, help="input replicas (default: enough to exceed L2)")
     ap.add_argument("--burst", type=int, default=None, help="back-to-back calls per timed window (default: replicas)")

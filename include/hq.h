@@ -18,9 +18,12 @@
  *    before anything is enqueued.  Errors found by a kernel (a bounded wait
  *    that timed out, a routing id out of range) are recorded in the status
  *    word at the start of the workspace; read it with hq_last_device_status.
- *  - No C++ exception crosses this interface.  No global mutable state is
- *    kept, so calls on different streams with different workspaces may run
- *    concurrently.
+ *  - No C++ exception crosses this interface.  Calls on different streams
+ *    with different workspaces may run concurrently: the library keeps no
+ *    mutable state of its own between calls, with two exceptions, both
+ *    described at their declarations: hq_gemm_static_scratch, whose calls on a
+ *    device share one scratch array and must be ordered, and the process-wide
+ *    wait bound set by hq_set_wait_limit_ns.
  *  - Kernels are launched with programmatic stream serialization: a call's
  *    kernels may start while the previous kernel on the stream finishes, and
  *    wait for it before touching activations, routing tables, workspace or
@@ -106,11 +109,14 @@ typedef struct {
   const float* global_scale;
 } hq_act_t;
 
-/* Bytes of the packed (kernel-layout) weight buffer for `fmt` (all experts).
- * Returns 0 for an invalid or unsupported descriptor. */
+/* Bytes of the packed (kernel-layout) weight buffer for `fmt` (all experts):
+ * the size of the preprocessing output ("Tuning and JIT compilation per
+ * workload", preprocessing paragraph).  Returns 0 for an invalid or
+ * unsupported descriptor. */
 HQ_API size_t hq_packed_bytes(const hq_format_t* fmt);
 
-/* Repack standard-format weights into the kernel layout (preprocessing: validate,
+/* Repack standard-format weights into the kernel layout ("Tuning and JIT
+ * compilation per workload", preprocessing paragraph: validate the parameters,
  * pad N to the 128-row tile, reorder codes, scales and zeros into tile order).
  *   codes        uint8 [E][N][K/2]
  *   scales       [E][N][K/group] of scale_type (bf16 as 16-bit patterns, ue4m3/e8m0 bytes)
@@ -122,13 +128,17 @@ HQ_API hq_status_t hq_pack_weights(const hq_format_t* fmt, const uint8_t* codes,
                             const float* global_scale, void* packed, hq_stream_t stream);
 
 /* Inverse of hq_pack_weights: writes the standard-format tensors back (same
- * shapes; zeros / global_scale may be NULL when the format has none). */
+ * shapes; zeros / global_scale may be NULL when the format has none).  The
+ * repack preserves each scheme's semantics ("A unified quantization
+ * representation"); this call makes that checkable bit for bit. */
 HQ_API hq_status_t hq_unpack_weights(const hq_format_t* fmt, const void* packed, uint8_t* codes, void* scales,
                               uint8_t* zeros, float* global_scale, hq_stream_t stream);
 
 /* Workspace bytes for a call with M rows (dense) or T tokens with `topk`
  * experts each (MoE; pass topk = 1 for dense).  The workspace holds the
- * device status word, split-K partial sums and the MoE routing tables.  It
+ * device status word, split-K partial sums of the Stream-K schedule and the
+ * MoE routing tables (task mapping and scheduling, "Shared CUDA components
+ * across formats and architectures").  It
  * must be zeroed once with hq_workspace_init before its first use; calls
  * leave it reusable.  One workspace serves one stream at a time. */
 HQ_API size_t hq_workspace_bytes(const hq_format_t* fmt, int64_t M_or_T, int32_t topk);
@@ -138,10 +148,14 @@ HQ_API size_t hq_workspace_bytes(const hq_format_t* fmt, int64_t M_or_T, int32_t
  * (the routing memset of hq_moe_gemm is not a kernel); 0 for an invalid format or size.  Host-only. */
 HQ_API int32_t hq_kernels_per_call(const hq_format_t* fmt, int64_t M_or_T, int32_t topk, int32_t moe);
 
-/* Zero `bytes` of workspace on `stream` (cudaMemsetAsync). */
+/* Zero `bytes` of workspace on `stream` (cudaMemsetAsync).  Errors:
+ * HQ_ERR_INVALID_ARG for a null pointer or zero size, HQ_ERR_CUDA. */
 HQ_API hq_status_t hq_workspace_init(void* workspace, size_t bytes, hq_stream_t stream);
 
 /* Dense quantized GEMM: C[M, N] (bf16, row-major) = A . Wdeq^T (+ bias[n]).
+ * Dequantization and scaling run inside the kernel, scales and the bias in the
+ * output stage ("Shared CUDA components across formats and architectures");
+ * the dense WnA16 / W4A4 GEMMs of "Results: kernel microbenchmarks".
  *   A       activation operand, M rows of K
  *   packedW hq_pack_weights output with num_experts == 1
  *   bias    bf16 [N] or NULL
@@ -151,7 +165,10 @@ HQ_API hq_status_t hq_workspace_init(void* workspace, size_t bytes, hq_stream_t 
 HQ_API hq_status_t hq_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* packedW, const void* bias, void* C,
                     int64_t M, int64_t N, int64_t K, void* workspace, size_t ws_bytes, hq_stream_t stream);
 
-/* MoE grouped GEMM over E = fmt->num_experts experts.
+/* MoE grouped GEMM over E = fmt->num_experts experts: the tokens of a batch
+ * spread over experts with per-expert work that varies with the routing
+ * ("Results: kernel microbenchmarks", WnA16 paragraph on the Indexed and
+ * Grouped MoE paths); the top-k weight is applied in the output stage.
  *   A            T token rows of K
  *   topk_ids     int32 [T, topk], distinct expert ids per token in [0, E)
  *   topk_weights fp32 [T, topk] or NULL (NULL = weight 1)
@@ -193,8 +210,21 @@ HQ_API hq_status_t hq_moe_gemm_combine(const hq_format_t* fmt, const hq_act_t* A
 HQ_API hq_status_t hq_swiglu(const void* x, int64_t R, int64_t I, void* out, hq_stream_t stream);
 
 /* Copy the device status word out of `workspace` (synchronizes `stream`) and
- * clear it.  *status_out receives HQ_OK or the first device-detected error. */
+ * clear it.  *status_out receives HQ_OK or the first device-detected error
+ * (HQ_ERR_TIMEOUT, HQ_ERR_BAD_ROUTING); the return value reports only whether
+ * the copy itself worked (HQ_ERR_INVALID_ARG, HQ_ERR_CUDA), so a failed copy is
+ * never mistaken for a device error.  The announcement describes no status
+ * interface; this is the library's own error channel. */
 HQ_API hq_status_t hq_last_device_status(void* workspace, int32_t* status_out, hq_stream_t stream);
+
+/* Diagnostic: bound, in nanoseconds, of every in-kernel pipeline wait of the
+ * GEMM calls enqueued after this call, process-wide (default 2 s; 0 restores
+ * the default).  A wait that runs out ends its kernel early with
+ * HQ_ERR_TIMEOUT in the workspace status and the output undefined; the
+ * kernel still lets its own copies and MMAs finish, so the workspace stays
+ * reusable.  Meant for tests of that error path.  The announcement has no
+ * counterpart. */
+HQ_API void hq_set_wait_limit_ns(uint64_t ns);
 
 /* Size of the fixed device scratch used by hq_gemm_static_scratch (16 MiB per GPU). */
 #define HQ_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
@@ -253,7 +283,7 @@ HQ_API hq_status_t hq_quantize_act(int32_t act_type, const void* x, int64_t M, i
                                    void* out_data, void* out_scale, float* out_global, void* workspace,
                                    size_t ws_bytes, hq_stream_t stream);
 
-/* Static description of a status code. */
+/* Static description of a status code (never NULL). */
 HQ_API const char* hq_status_string(hq_status_t status);
 
 #ifdef __cplusplus

@@ -30,7 +30,7 @@ HQ_A_BF16, HQ_A_E4M3_TOKEN, HQ_A_NVFP4 = 1, 2, 3
 EXPORTS = ["hq_packed_bytes", "hq_pack_weights", "hq_unpack_weights", "hq_workspace_bytes", "hq_workspace_init",
            "hq_gemm", "hq_moe_gemm", "hq_last_device_status", "hq_status_string", "hq_gemm_static_scratch",
            "hq_kernels_per_call", "hq_quantize_act_workspace_bytes", "hq_quantize_act",
-           "hq_moe_combine_workspace_bytes", "hq_moe_gemm_combine", "hq_swiglu"]
+           "hq_moe_combine_workspace_bytes", "hq_moe_gemm_combine", "hq_swiglu", "hq_set_wait_limit_ns"]
 
 
 class Format(ctypes.Structure):
@@ -76,6 +76,8 @@ _lib.hq_moe_gemm_combine.argtypes = [_F, _A, _vp, _vp, _vp, _i64, _i32, _vp, _vp
 _lib.hq_moe_gemm_combine.restype = ctypes.c_int
 _lib.hq_swiglu.argtypes = [_vp, _i64, _i64, _vp, _vp]
 _lib.hq_swiglu.restype = ctypes.c_int
+_lib.hq_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+_lib.hq_set_wait_limit_ns.restype = None
 _lib.hq_status_string.argtypes = [ctypes.c_int]
 _lib.hq_status_string.restype = ctypes.c_char_p
 
@@ -238,6 +240,11 @@ def swiglu(x, out=None, stream=None):
         out = torch.empty((R, I2 // 2), dtype=torch.bfloat16, device=x.device)
     _check(_lib.hq_swiglu(_ptr(x), int(R), int(I2 // 2), _ptr(out), _stream(stream)), "hq_swiglu")
     return out
+
+
+def set_wait_limit_ns(ns):
+    """Bound (ns) of every in-kernel pipeline wait of the GEMM calls enqueued from now on; 0 restores 2 s."""
+    _lib.hq_set_wait_limit_ns(int(ns))
 
 
 def last_device_status(workspace, stream=None):

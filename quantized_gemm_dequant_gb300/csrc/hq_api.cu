@@ -6,6 +6,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "../../include/hq.h"
 #include "hq_act_quant.h"
 #include "hq_gemm_kernel.cuh"
@@ -28,6 +30,9 @@ cudaError_t launch_moe_permute(const int* counts, const int* region, int cap, in
                                int* row_off, cudaStream_t stream);
 
 namespace {
+
+// Bound of every in-kernel pipeline wait for calls enqueued from now on (hq_set_wait_limit_ns).
+std::atomic<uint64_t> g_wait_ns{DEFAULT_WAIT_NS};
 
 constexpr int64_t kMaxExperts = 512;
 constexpr int64_t kMaxRows = (int64_t)1 << 30;
@@ -379,6 +384,7 @@ hq_status_t hq_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* packe
   a.sk = p.sk;
   a.status = reinterpret_cast<int*>(ws);
   a.partials = p.sk ? reinterpret_cast<float*>(ws + p.off_partials) : nullptr;
+  a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   return cuda_status(launch_path(p, a, (cudaStream_t)stream));
 }
 
@@ -471,6 +477,7 @@ hq_status_t moe_call(const hq_format_t* fmt, const hq_act_t* A, const void* pack
   a.sk = p.sk;
   a.status = status;
   a.partials = p.sk ? reinterpret_cast<float*>(ws + p.off_partials) : nullptr;
+  a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   err = launch_path(p, a, (cudaStream_t)stream);
   if (err != cudaSuccess || !combine) return cuda_status(err);
   return cuda_status(launch_combine_round(comb, T * fmt->N, static_cast<uint16_t*>(C), (cudaStream_t)stream));
@@ -544,6 +551,8 @@ hq_status_t hq_last_device_status(void* workspace, int32_t* status_out, hq_strea
   *status_out = v;
   return HQ_OK;
 }
+
+void hq_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns ? ns : DEFAULT_WAIT_NS, std::memory_order_relaxed); }
 
 const char* hq_status_string(hq_status_t s) {
   switch (s) {

@@ -48,7 +48,8 @@ constexpr int WPROD_WARP = 8;
 constexpr int APROD_WARP = 9;
 constexpr int MMA_WARP = 10;
 constexpr int NUM_EPI_THREADS = 256;
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
+constexpr uint64_t DEFAULT_WAIT_NS = 2000000000ull;  // 2 s per pipeline wait unless the host sets another bound
+constexpr uint64_t DRAIN_WAIT_NS = 200000000ull;     // waits for this CTA's own copies and MMAs before it exits
 constexpr int ERR_TIMEOUT = 5;
 constexpr int ERR_BAD_ROUTING = 6;
 
@@ -79,6 +80,7 @@ struct GemmArgs {
   float* partials;  // Stream-K: [2 * grid][BT][128] fp32, slot 2*cta + {0 first piece, 1 later piece}
   float* comb;      // MoE combine: fp32 [T][N]; the output of routed row r is added into token r / comb_k (else null)
   int comb_k;
+  uint64_t wait_ns;  // bound of every pipeline wait (a wait that runs out records HQ_ERR_TIMEOUT)
 };
 
 template <int PATH, int BT>
@@ -415,7 +417,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
         const uint8_t* wblk = args.w + e * args.w_expert_bytes + ((int64_t)nt * args.kst) * args.w_blk;
         for (int g = pc.g0; g < pc.g1; ++g, ++blk) {
           if (blk >= npre) {
-            if (!mbar_wait(&sh.w_empty[ws], wph ^ 1, abort_flag, WAIT_LIMIT_NS)) {
+            if (!mbar_wait(&sh.w_empty[ws], wph ^ 1, abort_flag, args.wait_ns)) {
               fail(ERR_TIMEOUT);
               ok = false;
               return;
@@ -430,12 +432,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
           }
         }
       });
-      if (!ok) {
-        // aborted: let this CTA's bulk copies land before shared memory is released
-        int never = 0;
-        for (int s = 0; s < C::SW; ++s)
-          if (armed[s] > 0) mbar_wait(&sh.w_full[s], (uint32_t)((armed[s] - 1) & 1), &never, 200000000ull);
-      }
+      // Every bulk copy this CTA issued lands before its shared memory is released, also when the consumers gave
+      // up (a timeout or abort elsewhere in the CTA): wait for the latest fill of every stage used.
+      int never = 0;
+      for (int s = 0; s < C::SW; ++s)
+        if (armed[s] > 0) mbar_wait(&sh.w_full[s], (uint32_t)((armed[s] - 1) & 1), &never, DRAIN_WAIT_NS);
     }
     __syncwarp();
   } else if (active && warp == APROD_WARP) {
@@ -456,7 +457,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
           const int rbase = row0 + (args.moe ? args.row_off[e] : 0);  // first row of the box
           for (int g = pc.g0; g < pc.g1; ++g) {
             for (int j = 0; j < C::SUB; ++j) {
-              if (!mbar_wait(&sh.a_empty[as], aph ^ 1, abort_flag, WAIT_LIMIT_NS)) {
+              if (!mbar_wait(&sh.a_empty[as], aph ^ 1, abort_flag, args.wait_ns)) {
                 fail(ERR_TIMEOUT);
                 ok = false;
                 return;
@@ -475,12 +476,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
             }
           }
         });
-        if (!ok) {
-          // aborted: let this CTA's loads land before shared memory is released
-          int never = 0;
-          for (int s = 0; s < C::SA; ++s)
-            if (armed & (1u << s)) mbar_wait(&sh.a_full[s], (s < as) ? aph : (aph ^ 1), &never, 200000000ull);
-        }
+        // every load lands before shared memory is released (the latest fill of each stage used)
+        int never = 0;
+        for (int s = 0; s < C::SA; ++s)
+          if (armed & (1u << s)) mbar_wait(&sh.a_full[s], (s < as) ? aph : (aph ^ 1), &never, DRAIN_WAIT_NS);
       }
       __syncwarp();
     } else {
@@ -495,12 +494,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
         tile_rows(pc.tile, e, row0, nrows);
         // token index of every row of the tile; rows past the expert's count read zeros (row M)
         for (int i = lane; i < BT; i += 32)
-          sh.rows_tok[i] = i < nrows ? args.region[e * args.region_cap + row0 + i] / args.topk : args.M;
+          sh.rows_tok[i] = i < nrows ? args.region[(int64_t)e * args.region_cap + row0 + i] / args.topk : args.M;
         __syncwarp();
         for (int g = pc.g0; g < pc.g1; ++g) {
           for (int j = 0; j < C::SUB; ++j) {
             if (lane == 0) {
-              if (!mbar_wait(&sh.a_empty[as], aph ^ 1, abort_flag, WAIT_LIMIT_NS)) {
+              if (!mbar_wait(&sh.a_empty[as], aph ^ 1, abort_flag, args.wait_ns)) {
                 fail(ERR_TIMEOUT);
                 ok = false;
               }
@@ -528,10 +527,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
         }
         __syncwarp();  // rows_tok is rewritten for the next piece
       });
-      if (!ok && lane == 0) {
+      if (lane == 0) {  // every gather lands before shared memory is released
         int never = 0;
         for (int s = 0; s < C::SA; ++s)
-          if (armed & (1u << s)) mbar_wait(&sh.a_full[s], (s < as) ? aph : (aph ^ 1), &never, 200000000ull);
+          if (armed & (1u << s)) mbar_wait(&sh.a_full[s], (s < as) ? aph : (aph ^ 1), &never, DRAIN_WAIT_NS);
       }
       __syncwarp();
     }
@@ -544,7 +543,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
       bool ok = true;
       auto waitf = [&](uint64_t* bar, uint32_t par) {
         if (!ok) return false;
-        if (!mbar_wait(bar, par, abort_flag, WAIT_LIMIT_NS)) {
+        if (!mbar_wait(bar, par, abort_flag, args.wait_ns)) {
           fail(ERR_TIMEOUT);
           ok = false;
         }
@@ -619,12 +618,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
         umma_commit(&sh.dfull);
         ++pidx;
       });
-      if (!ok) {
-        // aborted: wait for issued MMAs before tensor memory is released
-        int never = 0;
-        umma_commit(&sh.drain);
-        mbar_wait(&sh.drain, 0, &never, 200000000ull);
-      }
+      // every issued MMA completes before tensor memory is released (also when the epilogue gave up)
+      int never = 0;
+      umma_commit(&sh.drain);
+      mbar_wait(&sh.drain, 0, &never, DRAIN_WAIT_NS);
     }
     __syncwarp();
   } else if (active && warp < 8) {
@@ -639,7 +636,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
     bool ok = true;
     auto waitf = [&](uint64_t* bar, uint32_t par) {
       if (!ok) return false;
-      if (!mbar_wait(bar, par, abort_flag, WAIT_LIMIT_NS)) {
+      if (!mbar_wait(bar, par, abort_flag, args.wait_ns)) {
         fail(ERR_TIMEOUT);
         ok = false;
       }
@@ -689,7 +686,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
             int orow = -1;
             float f = 1.0f;
             if (i < pd.nrows) {
-              orow = args.region[pd.e * args.region_cap + pd.row0 + i];
+              orow = args.region[(int64_t)pd.e * args.region_cap + pd.row0 + i];
               if (args.topk_w) f = args.topk_w[orow];
             }
             tabs[(pd.ts * 8 + warp) * HC + u * 32 + lane] = make_int2(orow, __float_as_int(f));
@@ -705,7 +702,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
         if (kTables && (args.moe || PATH == PATH_MXFP4) && i < col0 + HC && i < pd.nrows) {
           int tok;
           if (args.moe) {
-            orow = args.region[pd.e * args.region_cap + pd.row0 + i];
+            orow = args.region[(int64_t)pd.e * args.region_cap + pd.row0 + i];
             tok = orow / args.topk;
             if (args.topk_w) f = args.topk_w[orow];
           } else {

@@ -140,13 +140,13 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
         int rows_tok[BT];  // MoE indexed: token of each row of the tile; rows past the expert's count read zeros
         if (args.moe && !args.grouped)
           for (int i = 0; i < BT; ++i)
-            rows_tok[i] = i < nrows ? args.region[e * args.region_cap + row0 + i] / args.topk : args.M;
+            rows_tok[i] = i < nrows ? args.region[(int64_t)e * args.region_cap + row0 + i] / args.topk : args.M;
         const uint8_t* wblk = args.w + e * args.w_expert_bytes + ((int64_t)nt * args.kst) * args.w_blk;
         for (int g = pc.g0; g < pc.g1; ++g, ++blk) {
           uint8_t* base = smem + st * C::STAGE;
           uint8_t* act = base + C::W_REGION;
           if (blk >= npre) {
-            if (!mbar_wait(&sh.empty[st], ph ^ 1, abort_flag, WAIT_LIMIT_NS)) {
+            if (!mbar_wait(&sh.empty[st], ph ^ 1, abort_flag, args.wait_ns)) {
               fail(ERR_TIMEOUT);
               ok = false;
               return;
@@ -172,16 +172,14 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
           }
         }
       });
-      if (!ok) {
-        // aborted: let this CTA's copies land before shared memory is released (every armed stage's last
-        // phase completes once its bytes arrive)
-        int never = 0;
-        for (int s = 0; s < C::STAGES; ++s)
-          if (armed & (1u << s)) {
-            const uint32_t par = (s < st) ? ph : (ph ^ 1);  // phase of the stage's most recent fill
-            mbar_wait(&sh.full[s], par, &never, 200000000ull);
-          }
-      }
+      // every copy this CTA issued lands before its shared memory is released, also when the compute warps gave
+      // up (every armed stage's latest phase completes once its bytes arrive)
+      int never = 0;
+      for (int s = 0; s < C::STAGES; ++s)
+        if (armed & (1u << s)) {
+          const uint32_t par = (s < st) ? ph : (ph ^ 1);  // phase of the stage's most recent fill
+          mbar_wait(&sh.full[s], par, &never, DRAIN_WAIT_NS);
+        }
     }
     __syncwarp();
   } else if (active && warp < 8) {
@@ -208,7 +206,7 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
     auto epi_sync = [&]() {
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.epi_bar);
-      if (!mbar_wait(&sh.epi_bar, epi_phase, abort_flag, WAIT_LIMIT_NS)) {
+      if (!mbar_wait(&sh.epi_bar, epi_phase, abort_flag, args.wait_ns)) {
         fail(ERR_TIMEOUT);
         ok = false;
       }
@@ -240,7 +238,7 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
           float f = 1.0f;
           if (kh == 0 && col < nrows) {
             if (args.moe) {
-              orow = args.region[e * args.region_cap + row0 + col];
+              orow = args.region[(int64_t)e * args.region_cap + row0 + col];
               if (args.topk_w) f = args.topk_w[orow];
             } else {
               orow = row0 + col;
@@ -250,7 +248,7 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT>::CTAS_PER_SM) hq_gemm
           t_mul[i][u] = f;
         }
       for (int g = pc.g0; g < pc.g1; ++g) {
-        if (!mbar_wait(&sh.full[st], ph, abort_flag, WAIT_LIMIT_NS)) {
+        if (!mbar_wait(&sh.full[st], ph, abort_flag, args.wait_ns)) {
           fail(ERR_TIMEOUT);
           ok = false;
           return;

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/hq.h"
 
 namespace {
@@ -17,19 +19,21 @@ constexpr int kMaxDevices = 64;
 // Shared by every call on a device; holds the last call's contents.
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
-// Device address of g_scratch, looked up once per device (the host-side name
-// of a __device__ array is only a stand-in and must never reach a kernel).
-void* g_scratch_ptr[kMaxDevices] = {nullptr};
+// Device address of g_scratch, looked up once per device with that device
+// current (the host-side name of a __device__ array is only a stand-in and must
+// never reach a kernel).  Host threads making their first call on a device at
+// the same time may both look it up; they store the same address.
+std::atomic<void*> g_scratch_ptr[kMaxDevices];
 
 hq_status_t scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return HQ_ERR_CUDA;
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
+  void* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (!p) {
     if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return HQ_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
+    g_scratch_ptr[dev].store(p, std::memory_order_release);
   }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return HQ_OK;
 }
 

@@ -64,13 +64,15 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
 
 // Wait for phase `parity` of `bar` to complete.  Gives up (returns false) when
 // `*abort` becomes non-zero or after `limit_ns` nanoseconds of waiting (both
-// checked each time the suspended thread wakes, at least every millisecond).
+// checked each time the suspended thread wakes, at least every millisecond, or
+// every `limit_ns` when that is shorter).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  const uint32_t hint = limit_ns < 1000000ull ? (uint32_t)limit_ns : 1000000u;
   for (;;) {
-    if (mbar_try_wait_suspend(bar, parity, 1000000u)) return true;
+    if (mbar_try_wait_suspend(bar, parity, hint)) return true;
     if (*abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }

@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(RED_THREADS) splitk_reduce_kernel(const __grid
       int orow;
       float mul = mul0;
       if (args.moe) {
-        orow = args.region[e * args.region_cap + row0 + col];
+        orow = args.region[(int64_t)e * args.region_cap + row0 + col];
         if (args.topk_w) mul *= args.topk_w[orow];
         if (PATH == PATH_MXFP4) mul *= args.a_scale[orow / args.topk];
       } else {
