@@ -22,8 +22,10 @@ It also quantizes bf16 activations to the FP8 (per-token scale) and NVFP4
 operands of the W4A8 and W4A4 paths ("Selecting activation types"; section
 "activation quantization" at the end), taking every decision in IEEE binary32.
 
-Conventions (the pages are silent on them): codes are two per byte with the low
-nibble holding the even k; W is [N, K] ("out, in"); scale groups run along K.
+Conventions (the pages are silent on them): 4-bit codes are two per byte with
+the low nibble holding the even k, 2-bit codes four per byte from the lowest
+bits up, 8-bit codes one per byte; W is [N, K] ("out, in"); scale groups run
+along K.
 """
 import numpy as np
 
@@ -92,11 +94,20 @@ def unpack_nibbles(packed):
     return out
 
 
+def unpack_crumbs(packed):
+    """[..., K/4] bytes -> [..., K] 2-bit codes; bits 2i and 2i + 1 of a byte hold its k = 4b + i."""
+    p = np.asarray(packed).astype(np.uint8)
+    out = np.empty(p.shape[:-1] + (p.shape[-1] * 4,), dtype=np.uint8)
+    for i in range(4):
+        out[..., i::4] = (p >> (2 * i)) & 0x3
+    return out
+
+
 # ---------------------------------------------------------------- tensor formats
 
-WEIGHT_FORMATS = ("int4_sym", "uint4_zp", "nvfp4", "mxfp4")
-ACT_FORMATS = ("bf16", "e4m3_tok", "nvfp4")
-BLOCK = {"nvfp4": 16, "mxfp4": 32}
+WEIGHT_FORMATS = ("int4_sym", "uint4_zp", "nvfp4", "mxfp4", "int8_sym", "uint2_zp", "mxint4", "e4m3")
+ACT_FORMATS = ("bf16", "e4m3_tok", "nvfp4", "mxfp8")
+BLOCK = {"nvfp4": 16, "mxfp4": 32, "mxint4": 32, "mxfp8": 32}
 
 
 def dequant_weights(wfmt, codes, scales, zeros=None, gscale=None, group=128):
@@ -106,9 +117,28 @@ def dequant_weights(wfmt, codes, scales, zeros=None, gscale=None, group=128):
     uint4_zp : value = (q - z) * s, q and z in [0, 15], s bf16 per (n, group)
     nvfp4    : value = e2m1(q) * ue4m3(sb) * g, sb per (n, 16 along K), g fp32 per tensor
     mxfp4    : value = e2m1(q) * e8m0(sb), sb per (n, 32 along K)
+    int8_sym : value = q * s, q one byte, two's complement in [-127, 127] (the value set of the zero-exponent
+               float e0m7, "Results: quantization support"), s bf16 per (n, group)
+    uint2_zp : value = (q - z) * s, q and z in [0, 3], q four per byte (see unpack_crumbs), s bf16 per (n, group)
+    mxint4   : value = q * e8m0(sb), q two's complement nibbles in [-7, 7], sb per (n, 32 along K)
+    e4m3     : value = e4m3(q) * s, q one OCP OFP8 E4M3 byte, s bf16 per (n, group)
     """
+    if wfmt in ("int8_sym", "e4m3"):
+        q = np.asarray(codes).astype(np.uint8)
+        k = q.shape[-1]
+        s = np.repeat(decode_bf16(scales), group, axis=-1)[..., :k]
+        return (decode_int(q, 8, True) if wfmt == "int8_sym" else decode_e4m3(q)) * s
+    if wfmt == "uint2_zp":
+        q = unpack_crumbs(codes)
+        k = q.shape[-1]
+        s = np.repeat(decode_bf16(scales), group, axis=-1)[..., :k]
+        zq = np.repeat(np.asarray(zeros).astype(np.float64), group, axis=-1)[..., :k]
+        return (decode_int(q, 2, False) - zq) * s
     q = unpack_nibbles(codes)
     k = q.shape[-1]
+    if wfmt == "mxint4":
+        sb = np.repeat(decode_e8m0(scales), BLOCK[wfmt], axis=-1)[..., :k]
+        return decode_int(q, 4, True) * sb
     if wfmt == "int4_sym":
         s = decode_bf16(scales)
         return decode_int(q, 4, True) * np.repeat(s, group, axis=-1)[..., :k]
@@ -134,9 +164,14 @@ def dequant_acts(afmt, data, scale=None, gscale=None):
     bf16     : the bf16 values
     e4m3_tok : e4m3(a) * s_t, one fp32 scale per row (token)
     nvfp4    : e2m1(q) * ue4m3(sb) * g, sb per (row, 16 along K), g fp32 per tensor
+    mxfp8    : e4m3(a) * e8m0(sb), sb per (row, 32 along K) (OCP Microscaling v1.0 MXFP8 E4M3)
     """
     if afmt == "bf16":
         return decode_bf16(data)
+    if afmt == "mxfp8":
+        q = np.asarray(data).astype(np.uint8)
+        sb = np.repeat(decode_e8m0(scale), BLOCK[afmt], axis=-1)[..., : q.shape[-1]]
+        return decode_e4m3(q) * sb
     if afmt == "e4m3_tok":
         s = np.asarray(scale, dtype=np.float64).reshape(-1, 1)
         return decode_e4m3(data) * s

@@ -281,6 +281,80 @@ def pin_moe_reduces_to_dense(o, rng=None):
     assert np.array_equal(moe_p, dense[perm])
 
 
+def pack_crumbs_loop(q):
+    """Independent packer of 2-bit codes: byte b holds k = 4b + i in bits 2i and 2i + 1."""
+    q = np.asarray(q)
+    out = np.zeros(q.shape[:-1] + (q.shape[-1] // 4,), dtype=np.uint8)
+    for idx in np.ndindex(q.shape[:-1]):
+        for b in range(q.shape[-1] // 4):
+            v = 0
+            for i in range(4):
+                v |= (int(q[idx + (4 * b + i,)]) & 0x3) << (2 * i)
+            out[idx + (b,)] = v
+    return out
+
+
+def pin_crumbs(o, rng=None):
+    """2-bit code order: the oracle's unpacking inverts an independent loop packer, and a hand-made byte decodes as
+    written (0b11_10_01_00 -> k = 0, 1, 2, 3 hold 0, 1, 2, 3)."""
+    rng = rng or np.random.default_rng(11)
+    q = rng.integers(0, 4, size=(3, 40))
+    assert np.array_equal(o.unpack_crumbs(pack_crumbs_loop(q)), q)
+    assert o.unpack_crumbs(np.array([0b11100100], np.uint8)).tolist() == [0, 1, 2, 3]
+
+
+def _int_bf16(a):
+    return np.vectorize(lambda v: np.float32(v).view(np.uint32) >> 16)(a).astype(np.uint16)
+
+
+def pin_exact_more_formats(o, rng=None):
+    """INT8 (e0m7 codes), UINT2 with zero points and MXINT4 with integer activations and power-of-two scales equal
+    integer arithmetic; FP8 E4M3 weights equal torch's float8_e4m3fn decoder times a power-of-two scale; MXFP8
+    activations equal the generic minifloat decoder times their e8m0 block scale (Fraction sums)."""
+    rng = rng or np.random.default_rng(12)
+    N, K, M, G = 5, 64, 3, 32
+    a = rng.integers(-3, 4, size=(M, K))
+    ad = o.dequant_acts("bf16", _int_bf16(a))
+    sj = rng.integers(-3, 3, size=(N, K // G))
+    scales = np.vectorize(bf16_pow2)(sj).astype(np.uint16)
+    pw = 2.0 ** np.repeat(sj, G, axis=-1)
+
+    def check(w, ref):
+        assert np.array_equal(w, ref)
+        y = o.gemm(ad, w)
+        want = np.array([[sum(int(a[m, k]) * Fraction(ref[n, k]) for k in range(K)) for n in range(N)]
+                         for m in range(M)], dtype=object)
+        assert all(y[m, n] == float(want[m, n]) for m in range(M) for n in range(N))
+
+    q8 = rng.integers(-127, 128, size=(N, K))
+    check(o.dequant_weights("int8_sym", (q8 & 0xFF).astype(np.uint8), scales, group=G), q8 * pw)
+    q2 = rng.integers(0, 4, size=(N, K))
+    z2 = rng.integers(0, 4, size=(N, K // G))
+    check(o.dequant_weights("uint2_zp", pack_crumbs_loop(q2), scales, zeros=z2.astype(np.uint8), group=G),
+          (q2 - np.repeat(z2, G, axis=-1)) * pw)
+    q4 = rng.integers(-7, 8, size=(N, K))
+    je = rng.integers(-9, 5, size=(N, K // 32))
+    check(o.dequant_weights("mxint4", pack_nibbles_loop(q4 & 0xF), (je + 127).astype(np.uint8)),
+          q4 * 2.0 ** np.repeat(je, 32, axis=-1))
+    b8 = rng.integers(0, 256, size=(N, K)).astype(np.uint8)
+    b8[(b8 & 0x7F) == 0x7F] = 0x40  # no NaN codes
+    ref = torch.from_numpy(b8.copy()).view(torch.float8_e4m3fn).double().numpy() * pw
+    check(o.dequant_weights("e4m3", b8, scales, group=G), ref)
+    # MXFP8 activations (e4m3 + e8m0 per 32) against int4 weights with unit scales
+    a8 = rng.integers(0, 256, size=(M, K)).astype(np.uint8)
+    a8[(a8 & 0x7F) == 0x7F] = 0x38
+    ja = rng.integers(-5, 5, size=(M, K // 32))
+    ax = o.dequant_acts("mxfp8", a8, (ja + 127).astype(np.uint8))
+    qw = rng.integers(-7, 8, size=(N, K))
+    w = o.dequant_weights("int4_sym", pack_nibbles_loop(qw & 0xF), np.full((N, K // G), 0x3F80, np.uint16), group=G)
+    y = o.gemm(ax, w)
+    for m in range(M):
+        for n in range(N):
+            ref = sum(minifloat(a8[m, k], 4, 3, 7, fn_nan=True) * Fraction(2) ** int(ja[m, k // 32]) * int(qw[n, k])
+                      for k in range(K))
+            assert y[m, n] == float(ref)
+
+
 # ------------------------------------------------------------ pins on the activation quantizers
 
 def _bf16_bits(x):
@@ -415,5 +489,5 @@ def pin_swiglu(o):
 
 
 ALL_PINS = [pin_e4m3, pin_e8m0, pin_e2m1, pin_bf16, pin_int4, pin_e0m_equivalence, pin_exact_int4,
-            pin_exact_fp4, pin_library_special_case, pin_brute_force, pin_moe_reduces_to_dense, pin_encode_e4m3,
+            pin_exact_fp4, pin_crumbs, pin_exact_more_formats, pin_library_special_case, pin_brute_force, pin_moe_reduces_to_dense, pin_encode_e4m3,
             pin_encode_e2m1, pin_act_quant_e4m3, pin_act_quant_nvfp4, pin_moe_combine, pin_swiglu]

@@ -55,6 +55,14 @@ MUTATIONS = {
     "combine_overwrites": ("            y[i] += v", "            y[i] = v"),
     "silu_sign": ("return g / (1.0 + np.exp(-g)) * u", "return g / (1.0 + np.exp(g)) * u"),
     "gate_up_swapped": ("g, u = x[:, :half], x[:, half:]", "u, g = x[:, :half], x[:, half:]"),
+    "crumb_order_reversed": ("out[..., i::4] = (p >> (2 * i)) & 0x3", "out[..., i::4] = (p >> (6 - 2 * i)) & 0x3"),
+    "int8_as_unsigned": ("(decode_int(q, 8, True) if wfmt", "(decode_int(q, 8, False) if wfmt"),
+    "uint2_zero_point_dropped": ("return (decode_int(q, 2, False) - zq) * s", "return decode_int(q, 2, False) * s"),
+    "mxint4_block_16": ("np.repeat(decode_e8m0(scales), BLOCK[wfmt], axis=-1)[..., :k]\n        return decode_int(q, 4, True)",
+                        "np.repeat(decode_e8m0(scales), 16, axis=-1)[..., :k]\n        return decode_int(q, 4, True)"),
+    "mxint4_unsigned": ("return decode_int(q, 4, True) * sb", "return decode_int(q, 4, False) * sb"),
+    "e4m3_weight_scale_dropped": ("else decode_e4m3(q)) * s", "else decode_e4m3(q)) * (s if wfmt == 'int8_sym' else 1.0)"),
+    "mxfp8_scale_dropped": ("return decode_e4m3(q) * sb", "return decode_e4m3(q)"),
     "act_nvfp4_nibbles": ("packed = (q[:, 0::2] | (q[:, 1::2] << 4))", "packed = (q[:, 1::2] | (q[:, 0::2] << 4))"),
 }
 

@@ -12,11 +12,22 @@ public definition:
   e4m3(amax_b / (6 g)) saturated at 448, e2m1 codes of x / (sb * g);
 * MXFP4 (OCP Microscaling v1.0 section 6.3): e8m0 block-32 scale
   2**(floor(log2 amax_b) - 2), e2m1 codes of x / scale, saturating;
-* FP8 per token: s_t = absmax_t / 448, e4m3(a / s_t) saturated.
+* FP8 per token: s_t = absmax_t / 448, e4m3(a / s_t) saturated;
+* grouped INT8 (the e0m7 value set): scale = absmax / 127 in bf16, codes
+  rint(w / scale) clamped to [-127, 127], one byte each;
+* grouped UINT2 with zero point: scale = (max - min) / 3 in bf16, zero =
+  clamp(rint(-min / scale), 0, 3), code = clamp(rint(w / scale) + zero, 0, 3),
+  four codes per byte from the lowest bits up;
+* MXINT4 (e8m0 block-32 scale): 2**(floor(log2 amax_b) - 2) (4 = 2**2 is the
+  largest power of two of the integer range, as for MXFP4), codes rint(w /
+  scale) clamped to [-7, 7];
+* grouped FP8 E4M3 weights: scale = absmax / 448 in bf16, e4m3(w / scale);
+* MXFP8 (OCP Microscaling v1.0 section 6.3): e8m0 block-32 scale
+  2**(floor(log2 amax_b) - 8) (8 = E4M3's largest exponent), e4m3(x / scale).
 
 Rounding is to nearest, ties to even, everywhere.  All functions take torch
-tensors on any device and return tensors on the same device.  Codes are packed
-two per byte, low nibble = even k.
+tensors on any device and return tensors on the same device.  4-bit codes are
+packed two per byte, low nibble = even k.
 """
 import torch
 
@@ -129,3 +140,73 @@ def quant_e4m3_per_token(a):
     q = e4m3_encode(a / safe.unsqueeze(-1))
     q = torch.where(s.unsqueeze(-1) > 0, q, torch.zeros_like(q))
     return q.contiguous(), s.to(torch.float32).contiguous()
+
+
+def pack_crumbs(codes):
+    """[..., K] uint8 codes in 0..3 -> [..., K/4] bytes; bits 2i, 2i + 1 of byte b hold k = 4b + i."""
+    c = codes.to(torch.uint8)
+    return (c[..., 0::4] | (c[..., 1::4] << 2) | (c[..., 2::4] << 4) | (c[..., 3::4] << 6)).contiguous()
+
+
+def quant_int8_sym(w, group):
+    """w fp32 [..., N, K] -> (int8 codes as bytes [..., N, K], scales bf16 [..., N, K/group])."""
+    *lead, n, k = w.shape
+    wg = w.reshape(*lead, n, k // group, group)
+    s = (wg.abs().amax(dim=-1) / 127.0).to(torch.bfloat16)
+    sf = s.float().unsqueeze(-1)
+    q = torch.where(sf > 0, _rint(wg / torch.where(sf > 0, sf, torch.ones_like(sf))), torch.zeros_like(wg))
+    q = q.clamp(-127, 127).to(torch.int16)
+    return (q & 0xFF).to(torch.uint8).reshape(*lead, n, k).contiguous(), s.contiguous()
+
+
+def quant_uint2_zp(w, group):
+    """w fp32 [..., N, K] -> (packed 2-bit codes [..., N, K/4], scales bf16 [..., N, K/g], zeros uint8 [..., N, K/g])."""
+    *lead, n, k = w.shape
+    wg = w.reshape(*lead, n, k // group, group)
+    lo = wg.amin(dim=-1)
+    hi = wg.amax(dim=-1)
+    s = ((hi - lo) / 3.0).to(torch.bfloat16)
+    sf = s.float()
+    safe = torch.where(sf > 0, sf, torch.ones_like(sf))
+    z = torch.where(sf > 0, _rint(-lo / safe), torch.zeros_like(sf)).clamp(0, 3)
+    q = torch.where(sf.unsqueeze(-1) > 0, _rint(wg / safe.unsqueeze(-1)) + z.unsqueeze(-1), torch.zeros_like(wg))
+    q = q.clamp(0, 3).to(torch.uint8).reshape(*lead, n, k)
+    return pack_crumbs(q), s.contiguous(), z.to(torch.uint8).contiguous()
+
+
+def _e8m0_block_scale(amax, emax):
+    """e8m0 byte and value of 2**(floor(log2 amax) - emax) per block (127, i.e. 1, for an all-zero block)."""
+    _, ex = torch.frexp(amax)  # amax = m * 2**ex, m in [0.5, 1): floor(log2 amax) = ex - 1
+    e = (ex.to(torch.int32) - 1 - emax + 127).clamp(0, 254)
+    e = torch.where(amax > 0, e, torch.full_like(e, 127))
+    return e, torch.ldexp(torch.ones_like(amax), (e - 127).to(torch.float32))
+
+
+def quant_mxint4(w, block=32):
+    """w fp32 [..., N, K] -> (packed int4 codes [..., N, K/2], e8m0 scales uint8 [..., N, K/32])."""
+    *lead, n, k = w.shape
+    wb = w.reshape(*lead, n, k // block, block)
+    e, scale = _e8m0_block_scale(wb.abs().amax(dim=-1), 2)
+    q = _rint(wb / scale.unsqueeze(-1)).clamp(-7, 7).to(torch.int16)
+    codes = (q & 0xF).to(torch.uint8).reshape(*lead, n, k)
+    return pack_nibbles(codes), e.to(torch.uint8).contiguous()
+
+
+def quant_e4m3_grouped(w, group):
+    """w fp32 [..., N, K] -> (e4m3 bytes [..., N, K], scales bf16 [..., N, K/group] = absmax / 448)."""
+    *lead, n, k = w.shape
+    wg = w.reshape(*lead, n, k // group, group)
+    s = (wg.abs().amax(dim=-1) / E4M3_MAX).to(torch.bfloat16)
+    sf = s.float().unsqueeze(-1)
+    q = e4m3_encode(wg / torch.where(sf > 0, sf, torch.ones_like(sf)))
+    q = torch.where(sf > 0, q, torch.zeros_like(q))
+    return q.reshape(*lead, n, k).contiguous(), s.contiguous()
+
+
+def quant_mxfp8(x, block=32):
+    """x fp32 [..., R, K] -> (e4m3 bytes [..., R, K], e8m0 scales uint8 [..., R, K/32])."""
+    *lead, r, k = x.shape
+    xb = x.reshape(*lead, r, k // block, block)
+    e, scale = _e8m0_block_scale(xb.abs().amax(dim=-1), 8)
+    q = e4m3_encode(xb / scale.unsqueeze(-1)).reshape(*lead, r, k)
+    return q.contiguous(), e.to(torch.uint8).contiguous()
