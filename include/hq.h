@@ -71,7 +71,11 @@ enum {
   HQ_W_INT4_SYM = 1, /* q in [-7, 7] two's complement nibbles (the e0m3 value set), bf16 scale per group */
   HQ_W_UINT4_ZP = 2, /* q, z in [0, 15], value (q - z) * s, bf16 scale and uint4 zero per group */
   HQ_W_NVFP4 = 3,    /* e2m1 codes, ue4m3 scale per 16 K, fp32 global scale per expert */
-  HQ_W_MXFP4 = 4     /* e2m1 codes, e8m0 scale per 32 K (OCP Microscaling) */
+  HQ_W_MXFP4 = 4,    /* e2m1 codes, e8m0 scale per 32 K (OCP Microscaling) */
+  HQ_W_INT8_SYM = 5, /* q in [-127, 127] one two's complement byte each (the e0m7 value set), bf16 scale per group */
+  HQ_W_UINT2_ZP = 6, /* q, z in [0, 3], value (q - z) * s, four codes per byte, bf16 scale and zero per group */
+  HQ_W_MXINT4 = 7,   /* q in [-7, 7] two's complement nibbles, e8m0 scale per 32 K */
+  HQ_W_E4M3 = 8      /* OCP FP8 E4M3 codes, one byte each, bf16 scale per group */
 };
 /* Scale data types. */
 enum { HQ_S_BF16 = 1, HQ_S_UE4M3 = 2, HQ_S_UE8M0 = 3 };
@@ -79,7 +83,8 @@ enum { HQ_S_BF16 = 1, HQ_S_UE4M3 = 2, HQ_S_UE8M0 = 3 };
 enum {
   HQ_A_BF16 = 1,       /* bf16 [M, K] */
   HQ_A_E4M3_TOKEN = 2, /* e4m3 [M, K] bytes + fp32 scale per row (token) */
-  HQ_A_NVFP4 = 3       /* e2m1 [M, K/2] packed + ue4m3 [M, K/16] + fp32 global scale [1] */
+  HQ_A_NVFP4 = 3,      /* e2m1 [M, K/2] packed + ue4m3 [M, K/16] + fp32 global scale [1] */
+  HQ_A_MXFP8 = 4       /* e4m3 [M, K] bytes + e8m0 [M, K/32] block scales (OCP Microscaling MXFP8) */
 };
 
 /* The unified quantization description ("standard format").  Supported
@@ -87,8 +92,16 @@ enum {
  *   INT4_SYM, group 128, BF16 scales,  no zero, no global, act BF16
  *   UINT4_ZP, group 128, BF16 scales,  zero,    no global, act BF16
  *   NVFP4,    group 16,  UE4M3 scales, no zero, global,    act NVFP4
- *   MXFP4,    group 32,  UE8M0 scales, no zero, no global, act E4M3_TOKEN
- * Anything else returns HQ_ERR_UNSUPPORTED. */
+ *   MXFP4,    group 32,  UE8M0 scales, no zero, no global, act E4M3_TOKEN or MXFP8
+ *   INT8_SYM, group 128, BF16 scales,  no zero, no global, act BF16
+ *   UINT2_ZP, group 128, BF16 scales,  zero,    no global, act BF16
+ *   MXINT4,   group 32,  UE8M0 scales, no zero, no global, act BF16
+ *   E4M3,     group 128, BF16 scales,  no zero, no global, act BF16
+ * The last four are the other WnA16 widths and formats of "Results: kernel
+ * microbenchmarks" (INT2, INT8 as the zero-exponent e0m7 of "Results:
+ * quantization support", MXINT4, FP8); MXFP8 activations are the microscaled
+ * W4A8 variant of "W8A8 / W4A8 / W4A4".  Anything else returns
+ * HQ_ERR_UNSUPPORTED. */
 typedef struct {
   int32_t weight_type;      /* HQ_W_* */
   int32_t group_size;       /* K elements per scale */
@@ -118,9 +131,11 @@ HQ_API size_t hq_packed_bytes(const hq_format_t* fmt);
 /* Repack standard-format weights into the kernel layout ("Tuning and JIT
  * compilation per workload", preprocessing paragraph: validate the parameters,
  * pad N to the 128-row tile, reorder codes, scales and zeros into tile order).
- *   codes        uint8 [E][N][K/2]
+ *   codes        uint8 [E][N][K/2] (4-bit formats, low nibble = even k), [E][N][K]
+ *                (INT8_SYM, E4M3) or [E][N][K/4] (UINT2_ZP, bits 2i..2i+1 of a byte
+ *                hold its k = 4b + i)
  *   scales       [E][N][K/group] of scale_type (bf16 as 16-bit patterns, ue4m3/e8m0 bytes)
- *   zeros        uint8 [E][N][K/group], values 0..15 (UINT4_ZP), else NULL
+ *   zeros        uint8 [E][N][K/group], values 0..15 (UINT4_ZP) or 0..3 (UINT2_ZP), else NULL
  *   global_scale fp32 [E] (NVFP4), else NULL
  *   packed       hq_packed_bytes(fmt) bytes, written entirely (padding zeroed)
  * Runs one kernel on `stream`.  Bit-exact and invertible by hq_unpack_weights. */

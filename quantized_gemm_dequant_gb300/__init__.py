@@ -24,8 +24,9 @@ _lib = ctypes.CDLL(LIB_PATH)
 HQ_OK, HQ_ERR_INVALID_ARG, HQ_ERR_UNSUPPORTED, HQ_ERR_ALIGNMENT, HQ_ERR_CUDA, HQ_ERR_TIMEOUT, \
     HQ_ERR_BAD_ROUTING, HQ_ERR_WORKSPACE = range(8)
 HQ_W_INT4_SYM, HQ_W_UINT4_ZP, HQ_W_NVFP4, HQ_W_MXFP4 = 1, 2, 3, 4
+HQ_W_INT8_SYM, HQ_W_UINT2_ZP, HQ_W_MXINT4, HQ_W_E4M3 = 5, 6, 7, 8
 HQ_S_BF16, HQ_S_UE4M3, HQ_S_UE8M0 = 1, 2, 3
-HQ_A_BF16, HQ_A_E4M3_TOKEN, HQ_A_NVFP4 = 1, 2, 3
+HQ_A_BF16, HQ_A_E4M3_TOKEN, HQ_A_NVFP4, HQ_A_MXFP8 = 1, 2, 3, 4
 
 EXPORTS = ["hq_packed_bytes", "hq_pack_weights", "hq_unpack_weights", "hq_workspace_bytes", "hq_workspace_init",
            "hq_gemm", "hq_moe_gemm", "hq_last_device_status", "hq_status_string", "hq_gemm_static_scratch",
@@ -84,7 +85,12 @@ _lib.hq_status_string.restype = ctypes.c_char_p
 _WEIGHT = {"int4_sym": (HQ_W_INT4_SYM, 128, HQ_S_BF16, 0, 0, HQ_A_BF16),
            "uint4_zp": (HQ_W_UINT4_ZP, 128, HQ_S_BF16, 1, 0, HQ_A_BF16),
            "nvfp4": (HQ_W_NVFP4, 16, HQ_S_UE4M3, 0, 1, HQ_A_NVFP4),
-           "mxfp4": (HQ_W_MXFP4, 32, HQ_S_UE8M0, 0, 0, HQ_A_E4M3_TOKEN)}
+           "mxfp4": (HQ_W_MXFP4, 32, HQ_S_UE8M0, 0, 0, HQ_A_E4M3_TOKEN),
+           "int8_sym": (HQ_W_INT8_SYM, 128, HQ_S_BF16, 0, 0, HQ_A_BF16),
+           "uint2_zp": (HQ_W_UINT2_ZP, 128, HQ_S_BF16, 1, 0, HQ_A_BF16),
+           "mxint4": (HQ_W_MXINT4, 32, HQ_S_UE8M0, 0, 0, HQ_A_BF16),
+           "e4m3": (HQ_W_E4M3, 128, HQ_S_BF16, 0, 0, HQ_A_BF16)}
+_ACT_FMT = {"bf16": HQ_A_BF16, "e4m3_tok": HQ_A_E4M3_TOKEN, "nvfp4": HQ_A_NVFP4, "mxfp8": HQ_A_MXFP8}
 
 
 class HQError(RuntimeError):
@@ -258,6 +264,8 @@ def pack_inputs(inputs, device="cuda", stream=None):
     w = inputs["w"]
     E = inputs.get("E", 1)
     fmt = make_format(inputs["wfmt"], inputs["N"], inputs["K"], E)
+    if "afmt" in inputs:
+        fmt.act_type = _ACT_FMT[inputs["afmt"]]
     t = {k: v.to(device).contiguous() for k, v in w.items()}
     scales = t["scales"].view(torch.uint8) if t["scales"].dtype == torch.bfloat16 else t["scales"]
     packed = pack_weights(fmt, t["codes"], scales, t.get("zeros"), t.get("gscale"), stream=stream)

@@ -22,6 +22,7 @@ cudaError_t launch_gemm_int4(const GemmArgs& a, int bt, int grid, cudaStream_t s
 cudaError_t launch_gemm_nvfp4(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_mxfp4(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_small(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_small_fmt(int dec, const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(int path, const GemmArgs& a, int bt, int gemm_grid, int grid, cudaStream_t stream);
 cudaError_t launch_combine_round(const float* acc, int64_t n, uint16_t* c, cudaStream_t stream);
 cudaError_t launch_swiglu(const void* x, int64_t R, int64_t I, void* out, cudaStream_t stream);
@@ -35,6 +36,7 @@ namespace {
 std::atomic<uint64_t> g_wait_ns{DEFAULT_WAIT_NS};
 
 constexpr int64_t kMaxExperts = 512;
+constexpr size_t kHeaderBytes = 256;  // [0] device status, [1] epoch of the last register-decode call, [2] exit count
 constexpr int64_t kMaxRows = (int64_t)1 << 30;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -65,7 +67,26 @@ hq_status_t check_format(const hq_format_t* f) {
       break;
     case HQ_W_MXFP4:
       if (f->group_size != 32 || f->scale_type != HQ_S_UE8M0 || f->has_zero || f->has_global_scale ||
-          f->act_type != HQ_A_E4M3_TOKEN)
+          (f->act_type != HQ_A_E4M3_TOKEN && f->act_type != HQ_A_MXFP8))
+        return HQ_ERR_UNSUPPORTED;
+      if (f->K % 128) return HQ_ERR_ALIGNMENT;
+      break;
+    case HQ_W_INT8_SYM:
+    case HQ_W_E4M3:
+      if (f->group_size != 128 || f->scale_type != HQ_S_BF16 || f->has_zero || f->has_global_scale ||
+          f->act_type != HQ_A_BF16)
+        return HQ_ERR_UNSUPPORTED;
+      if (f->K % 128) return HQ_ERR_ALIGNMENT;
+      break;
+    case HQ_W_UINT2_ZP:
+      if (f->group_size != 128 || f->scale_type != HQ_S_BF16 || !f->has_zero || f->has_global_scale ||
+          f->act_type != HQ_A_BF16)
+        return HQ_ERR_UNSUPPORTED;
+      if (f->K % 128) return HQ_ERR_ALIGNMENT;
+      break;
+    case HQ_W_MXINT4:
+      if (f->group_size != 32 || f->scale_type != HQ_S_UE8M0 || f->has_zero || f->has_global_scale ||
+          f->act_type != HQ_A_BF16)
         return HQ_ERR_UNSUPPORTED;
       if (f->K % 128) return HQ_ERR_ALIGNMENT;
       break;
@@ -87,7 +108,8 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // Launch plan of one call; also fixes the workspace layout.
 struct Plan {
   int path = 0;
-  int small = 0;  // INT4 with at most 32 tokens per tile: register-decode mma.sync kernel
+  int small = 0;  // integer / FP8 weights with at most 32 tokens per tile: register-decode mma.sync kernel
+  int dec = 0;    // its decode variant
   int grouped = 0;  // MoE: routed rows copied into expert-contiguous order first (2-D TMA boxes)
   int bt = 16;
   int sk = 0;
@@ -148,7 +170,7 @@ Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int
   p.n_tiles = g.n_tiles;
   p.kst = g.k_stages;
   if (sms < 1) sms = 1;
-  size_t off = 256;  // status word
+  size_t off = kHeaderBytes;  // status word, epoch, exit count
   int64_t tiles_est = 0;  // tiles the launch is planned for (MoE: one per N tile of every expert hit)
   if (!moe) {
     p.bt = pick_bt_dense(M_or_T);
@@ -170,14 +192,16 @@ Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int
     p.sk = (est_tiles < 2 * (int64_t)sms && p.kst > 1) ? 1 : 0;
     const int64_t W = p.max_tiles * (p.sk ? p.kst : 1);
     p.grid = (int)(W < sms ? (W < 1 ? 1 : W) : sms);
-    p.off_counts = off;
-    off = align256(off + sizeof(int) * (size_t)E);
   }
   if (p.path == PATH_INT4) {
     const int force = forced_path();
-    p.small = force == 1 ? 1 : (force == 2 ? 0 : (p.bt <= 32 ? 1 : 0));
-    if (p.small && p.bt > 32) {  // forced: re-tile with 32-token tiles
-      p.bt = 32;
+    p.dec = decode_kind(f->weight_type);
+    p.small = (force == 1 || register_decode_only(f->weight_type)) ? 1 : (force == 2 ? 0 : (p.bt <= 32 ? 1 : 0));
+    // forced to the register-decode kernel: re-tile with 32-token tiles; dense calls with at most 8 rows use its
+    // 8-token tiles
+    const int small_bt = p.bt > 32 ? 32 : ((!moe && M_or_T <= 8) ? 8 : p.bt);
+    if (p.small && small_bt != p.bt) {
+      p.bt = small_bt;
       if (!moe) {
         p.m_tiles = (M_or_T + p.bt - 1) / p.bt;
         p.max_tiles = p.m_tiles * p.n_tiles;
@@ -188,9 +212,10 @@ Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int
       }
       p.sk = (p.max_tiles < 2 * (int64_t)sms && p.kst > 1) ? 1 : 0;
     }
-    if (p.small) {  // the register-decode kernel runs two CTAs per SM with 16-token tiles
-      const int64_t W = p.max_tiles * (p.sk ? p.kst : 1);
+    if (p.small) {  // the register-decode kernel runs two CTAs per SM up to 16-token tiles
       const int64_t slots = p.bt <= 16 ? 2 * (int64_t)sms : sms;
+      p.sk = (p.max_tiles < 2 * slots && p.kst > 1) ? 1 : 0;
+      const int64_t W = p.max_tiles * (p.sk ? p.kst : 1);
       p.grid = (int)(W < slots ? (W < 1 ? 1 : W) : slots);
     }
   }
@@ -203,7 +228,15 @@ Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int
     const int64_t W = p.max_tiles * (p.sk ? p.kst : 1);
     p.grid = (int)(W < sms ? (W < 1 ? 1 : W) : sms);
   }
+  // Stream-K partial sums first, right after the header: the register-decode kernel tags each of its values with
+  // the call's epoch, and the fixed place keeps other tables of other calls on the same workspace out of its slots
+  if (p.sk) {
+    p.off_partials = off;
+    off = align256(off + sizeof(float) * (size_t)2 * p.grid * p.bt * TILE_N);
+  }
   if (moe) {
+    p.off_counts = off;
+    off = align256(off + sizeof(int) * (size_t)f->num_experts);
     p.off_region = off;
     off = align256(off + sizeof(int) * (size_t)(f->num_experts * (p.region_cap > 0 ? p.region_cap : 1)));
     // Grouped when tiles are wide: tile::gather4 cannot feed 64+ routed rows per stage fast enough
@@ -221,20 +254,19 @@ Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int
       }
     }
   }
-  if (p.sk) {
-    p.off_partials = off;
-    off = align256(off + sizeof(float) * (size_t)2 * p.grid * p.bt * TILE_N);
-  }
   p.ws_bytes = off;
   return p;
 }
 
 cudaError_t launch_path(const Plan& p, const GemmArgs& a, cudaStream_t s) {
   cudaError_t e;
-  if (p.path == PATH_INT4) e = p.small ? launch_gemm_small(a, p.bt, p.grid, s) : launch_gemm_int4(a, p.bt, p.grid, s);
+  if (p.path == PATH_INT4)
+    e = !p.small ? launch_gemm_int4(a, p.bt, p.grid, s)
+                 : (p.dec == DEC_INT4 ? launch_gemm_small(a, p.bt, p.grid, s)
+                                      : launch_gemm_small_fmt(p.dec, a, p.bt, p.grid, s));
   else if (p.path == PATH_NVFP4) e = launch_gemm_nvfp4(a, p.bt, p.grid, s);
   else e = launch_gemm_mxfp4(a, p.bt, p.grid, s);
-  if (e != cudaSuccess || !p.sk) return e;
+  if (e != cudaSuccess || !p.sk || p.small) return e;  // the register-decode kernel finishes cut tiles itself
   // tiles cut between CTAs: sum their partial slots, one CTA per 32 token columns of a tile
   const int64_t items = p.max_tiles * ((p.bt + 31) / 32);
   const int64_t cap = 4 * (int64_t)p.grid;
@@ -332,7 +364,7 @@ size_t hq_workspace_bytes(const hq_format_t* fmt, int64_t M_or_T, int32_t topk) 
 int32_t hq_kernels_per_call(const hq_format_t* fmt, int64_t M_or_T, int32_t topk, int32_t moe) {
   if (check_format(fmt) != HQ_OK || M_or_T < 1 || topk < 1) return 0;
   const Plan p = make_plan(fmt, M_or_T, topk, moe != 0, num_sms());
-  int32_t n = 1 + (p.sk ? 1 : 0);  // GEMM (+ split-K reduction)
+  int32_t n = 1 + (p.sk && !p.small ? 1 : 0);  // GEMM (+ split-K reduction of the UMMA kernel)
   if (moe) n += 1 + (p.grouped ? 1 : 0);  // routing (+ row permutation)
   if (moe == 2) n += 1;                    // combine: rounding of the summed token rows
   return n;

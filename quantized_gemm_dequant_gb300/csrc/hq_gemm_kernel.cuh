@@ -77,7 +77,8 @@ struct GemmArgs {
   int m_tiles;  // dense: token tiles
   int sk;       // 1: Stream-K split over K blocks
   int* status;
-  float* partials;  // Stream-K: [2 * grid][BT][128] fp32, slot 2*cta + {0 first piece, 1 later piece}
+  float* partials;  // Stream-K: tcgen05 kernel [2 * grid][BT][128] fp32, slot 2*cta + {0 first piece, 1 later
+                    // piece}; register-decode kernel [grid][BT][128] 64-bit (fp32 value, epoch) words
   float* comb;      // MoE combine: fp32 [T][N]; the output of routed row r is added into token r / comb_k (else null)
   int comb_k;
   uint64_t wait_ns;  // bound of every pipeline wait (a wait that runs out records HQ_ERR_TIMEOUT)
@@ -738,12 +739,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
           for (int jj = 0; jj < 2; ++jj) {
             uint32_t out[16];
             const uint32_t wv[4] = {raw[jj].x, raw[jj].y, raw[jj].z, raw[jj].w};
+            // pair p of word w4 holds k = 8p + 2 w4 (+1) of the chunk: tensor-memory column 4p + w4
 #pragma unroll
             for (int w4 = 0; w4 < 4; ++w4) {
 #pragma unroll
               for (int p = 0; p < 4; ++p) {
                 const uint32_t x = lop3_and_or(wv[w4] >> (4 * p), 0x000F000Fu, 0x43004300u);
-                out[w4 * 4 + p] = bf16x2_mul(bf16x2_sub(x, zz), ss);
+                out[p * 4 + w4] = bf16x2_mul(bf16x2_sub(x, zz), ss);
               }
             }
             tmem_st_x<16>(tmem + lane_base + 256 + aslot * 64 + (2 * h + jj) * 16, out);

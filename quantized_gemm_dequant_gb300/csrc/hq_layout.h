@@ -1,5 +1,8 @@
 // Kernel-layout geometry of packed weights and the launch plan, shared by the
-// host API and the device code.
+// host API and the device code.  PATH_INT4 is the integer-decode family: every
+// format decoded to bf16 in registers or tensor memory (the 4-bit integer
+// formats also by the tcgen05 kernel, the others by the register-decode
+// kernel only).
 //
 // Packed weights are a sequence of fixed-size "stage blocks", one per
 // (expert, 128-row N tile, K stage), each holding exactly the bytes one
@@ -9,10 +12,34 @@
 //  INT4_SYM / UINT4_ZP, K stage = 128 (one quantization group):
 //    [0, 8192)      codes, 4 chunks x 128 rows x 16 bytes; chunk j of row r holds
 //                   k in [32j, 32j+32) as 4 words; nibble slot i of word w holds
-//                   k = 32j + 8w + {0,2,4,6,1,3,5,7}[i], so one mask extracts the
-//                   (even k, odd k) pair of a bf16x2.  INT4_SYM stores q + 8.
+//                   k = 32j + 8(i % 4) + 2w + i / 4, so slots p and p + 4 hold the
+//                   (even k, odd k) pair 32j + 8p + 2w (+1): one shift by 4p and one
+//                   mask extract it as a bf16x2.  Word w of a row chunk is exactly
+//                   what lane (g, t = w) of an ldmatrix of 8x8 b16 matrices receives,
+//                   and its four pairs are that lane's pairs of the m16n8k16 A
+//                   fragments of the chunk's two 16-K steps (p = 0, 1: first step,
+//                   k 2t and 2t + 8; p = 2, 3: second step).  INT4_SYM stores q + 8.
 //    [8192, 8448)   bf16 scale of each row for this group
 //    [8448, 8576)   UINT4_ZP only: zero point of each row (one byte)
+//  MXINT4, K stage = 128: codes as INT4_SYM (q + 8), then
+//    [8192, 8704)   e8m0 block-32 scales, 4 bytes per row (the stage's four 32-K
+//                   blocks in K order) at 8192 + 4r
+//  INT8_SYM / E4M3, K stage = 128:
+//    [0, 16384)     codes, 8 chunks x 128 rows x 16 bytes; chunk j of row r holds
+//                   k in [16j, 16j+16).  Word w holds the (even, odd) pairs
+//                   16j + 2w (+1) and 16j + 2w + 8 (+1): INT8 in byte order
+//                   (2w, 2w+8, 2w+1, 2w+9), so each pair sits in bits 0-7 and
+//                   16-23 after a shift by 0 or 8; E4M3 in byte order (2w, 2w+1,
+//                   2w+8, 2w+9), one pair per 16-bit half.  INT8 codes are two's
+//                   complement bytes as given.
+//    [16384, 16640) bf16 scale of each row for this group
+//  UINT2_ZP, K stage = 128:
+//    [0, 4096)      codes, 2 chunks x 128 rows x 16 bytes; chunk j of row r holds
+//                   k in [64j, 64j+64); 2-bit slot i of word w holds
+//                   k = 64j + 16(p / 2) + 8(p % 2) + 2w + i / 8 with p = i % 8: the
+//                   pair p of the word is slots (p, p + 8)
+//    [4096, 4352)   bf16 scale of each row for this group
+//    [4352, 4480)   zero point of each row (one byte)
 //  NVFP4, K stage = 256:
 //    [0, 16384)     e2m1 codes as the shared-memory image of a 128-row x 128-byte
 //                   K-major tile with the 128-byte swizzle (16-byte chunk c of row r
@@ -31,7 +58,29 @@
 
 namespace hq {
 
-enum WeightKind { WK_INT4_SYM = 1, WK_UINT4_ZP = 2, WK_NVFP4 = 3, WK_MXFP4 = 4 };
+enum WeightKind {
+  WK_INT4_SYM = 1,
+  WK_UINT4_ZP = 2,
+  WK_NVFP4 = 3,
+  WK_MXFP4 = 4,
+  WK_INT8_SYM = 5,
+  WK_UINT2_ZP = 6,
+  WK_MXINT4 = 7,
+  WK_E4M3 = 8
+};
+// Decode variants of the register-decode kernel, one per integer / e4m3 weight layout
+enum DecodeKind { DEC_INT4 = 0, DEC_MXINT4 = 1, DEC_INT8 = 2, DEC_E4M3 = 3, DEC_UINT2 = 4 };
+inline int decode_kind(int weight_type) {
+  switch (weight_type) {
+    case WK_MXINT4: return DEC_MXINT4;
+    case WK_INT8_SYM: return DEC_INT8;
+    case WK_E4M3: return DEC_E4M3;
+    case WK_UINT2_ZP: return DEC_UINT2;
+    default: return DEC_INT4;
+  }
+}
+// Formats only the register-decode kernel reads (any token count)
+inline bool register_decode_only(int weight_type) { return weight_type >= WK_INT8_SYM; }
 enum KernelPath { PATH_INT4 = 0, PATH_NVFP4 = 1, PATH_MXFP4 = 2 };
 
 constexpr int TILE_N = 128;  // weight rows per tile (the UMMA M dimension)
@@ -54,6 +103,18 @@ inline PackGeom pack_geom(int weight_type, int64_t N, int64_t K, int64_t E) {
     g.path = PATH_INT4;
     g.kstage = 128;
     g.blk_bytes = 8192 + 256 + (weight_type == WK_UINT4_ZP ? 128 : 0);
+  } else if (weight_type == WK_MXINT4) {
+    g.path = PATH_INT4;
+    g.kstage = 128;
+    g.blk_bytes = 8192 + 512;
+  } else if (weight_type == WK_INT8_SYM || weight_type == WK_E4M3) {
+    g.path = PATH_INT4;
+    g.kstage = 128;
+    g.blk_bytes = 16384 + 256;
+  } else if (weight_type == WK_UINT2_ZP) {
+    g.path = PATH_INT4;
+    g.kstage = 128;
+    g.blk_bytes = 4096 + 256 + 128;
   } else if (weight_type == WK_NVFP4) {
     g.path = PATH_NVFP4;
     g.kstage = 256;

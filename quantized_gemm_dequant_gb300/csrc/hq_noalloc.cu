@@ -51,8 +51,10 @@ hq_status_t hq_gemm_static_scratch(const hq_format_t* fmt, const hq_act_t* A, co
   void* ws = nullptr;
   const hq_status_t st = scratch_address(&ws);
   if (st != HQ_OK) return st;
-  // The status word (the scratch's 256-byte header) must start at zero.
-  if (cudaMemsetAsync(ws, 0, 256, (cudaStream_t)stream) != cudaSuccess) return HQ_ERR_CUDA;
+  // The status word (the first 4 bytes) must start at zero.  The rest of the header (the epoch of the last
+  // register-decode call and its exit count) carries over from call to call, as it does in a caller's workspace;
+  // the array starts zeroed when the library's device code is loaded.
+  if (cudaMemsetAsync(ws, 0, sizeof(int32_t), (cudaStream_t)stream) != cudaSuccess) return HQ_ERR_CUDA;
   return hq_gemm(fmt, A, packedW, bias, C, M, N, K, ws, kScratchBytes, stream);
 }
 

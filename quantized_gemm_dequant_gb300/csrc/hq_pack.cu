@@ -7,7 +7,8 @@
 
 namespace hq {
 
-__constant__ int kNibblePerm[8] = {0, 2, 4, 6, 1, 3, 5, 7};
+// 4-bit integer layout: K offset, within a 32-K row chunk, of nibble slot i of 32-bit word w (see hq_layout.h).
+__device__ __forceinline__ int int4_chunk_k(int w, int i) { return 8 * (i & 3) + 2 * w + (i >> 2); }
 
 struct PackArgs {
   int wt;
@@ -16,6 +17,15 @@ struct PackArgs {
   int blk_bytes;
   int64_t gscale_off;
 };
+
+// INT8 / E4M3 layout: K offset, within a 16-K row chunk, of byte b of word w (see hq_layout.h).
+__device__ __forceinline__ int int8_chunk_k(int w, int b) { return 2 * w + ((b & 1) ? 8 : 0) + (b >> 1); }
+__device__ __forceinline__ int e4m3_chunk_k(int w, int b) { return 2 * w + ((b & 2) ? 8 : 0) + (b & 1); }
+// UINT2 layout: K offset, within a 64-K row chunk, of 2-bit slot i of word w.
+__device__ __forceinline__ int uint2_chunk_k(int w, int i) {
+  const int p = i & 7;
+  return 16 * (p >> 1) + 8 * (p & 1) + 2 * w + (i >> 3);
+}
 
 __device__ __forceinline__ uint32_t get_nibble(const uint8_t* row, int64_t k) {
   uint8_t b = row[k >> 1];
@@ -38,30 +48,90 @@ __global__ void pack_kernel(PackArgs p, uint8_t* codes, uint8_t* scales, uint8_t
     const int64_t n = nt * TILE_N + r;
     const bool valid = n < p.N;
     uint8_t* blk = packed + ((e * p.n_tiles + nt) * p.k_stages + ks) * (int64_t)p.blk_bytes;
-    const int64_t rowc = (e * p.N + n) * (p.K / 2);  // byte offset of the row in codes
-    if (p.wt == WK_INT4_SYM || p.wt == WK_UINT4_ZP) {
+    const int64_t rowc = (e * p.N + n) * (p.K / 2);  // byte offset of the row in codes (4-bit formats)
+    if (p.wt == WK_INT8_SYM || p.wt == WK_E4M3 || p.wt == WK_UINT2_ZP) {
+      const int64_t ng = p.K / 128;
+      const bool two = p.wt == WK_UINT2_ZP;
+      if (!two) {
+        const int64_t rowb = (e * p.N + n) * p.K;
+        for (int j = 0; j < 8; ++j) {
+          uint8_t* dst = blk + (j * 128 + r) * 16;
+          for (int w = 0; w < 4; ++w)
+            for (int b = 0; b < 4; ++b) {
+              const int64_t k = ks * 128 + 16 * j + (p.wt == WK_INT8_SYM ? int8_chunk_k(w, b) : e4m3_chunk_k(w, b));
+              if (DIR == 0) dst[4 * w + b] = valid ? codes[rowb + k] : (uint8_t)0;
+              else if (valid) codes[rowb + k] = dst[4 * w + b];
+            }
+        }
+      } else {
+        const int64_t rowq = (e * p.N + n) * (p.K / 4);
+        for (int j = 0; j < 2; ++j) {
+          uint32_t* dst = reinterpret_cast<uint32_t*>(blk + (j * 128 + r) * 16);
+          for (int w = 0; w < 4; ++w) {
+            if (DIR == 0) {
+              uint32_t word = 0;
+              if (valid)
+                for (int i = 0; i < 16; ++i) {
+                  const int64_t k = ks * 128 + 64 * j + uint2_chunk_k(w, i);
+                  word |= (uint32_t)((codes[rowq + (k >> 2)] >> (2 * (k & 3))) & 3u) << (2 * i);
+                }
+              dst[w] = word;
+            } else if (valid) {
+              const uint32_t word = dst[w];
+              for (int i = 0; i < 16; ++i) {
+                const int64_t k = ks * 128 + 64 * j + uint2_chunk_k(w, i);
+                uint8_t* bp = codes + rowq + (k >> 2);
+                const int sh = 2 * (int)(k & 3);
+                *bp = (uint8_t)((*bp & ~(3u << sh)) | (((word >> (2 * i)) & 3u) << sh));
+              }
+            }
+          }
+        }
+      }
+      const int soff = two ? 4096 : 16384;
+      uint16_t* sdst = reinterpret_cast<uint16_t*>(blk + soff) + r;
+      uint16_t* ssrc = reinterpret_cast<uint16_t*>(scales) + (e * p.N + n) * ng + ks;
+      if (DIR == 0) *sdst = valid ? *ssrc : (uint16_t)0;
+      else if (valid) *ssrc = *sdst;
+      if (two) {
+        uint8_t* zdst = blk + 4352 + r;
+        uint8_t* zsrc = zeros + (e * p.N + n) * ng + ks;
+        if (DIR == 0) *zdst = valid ? (uint8_t)(*zsrc & 0x3) : (uint8_t)0;
+        else if (valid) *zsrc = *zdst;
+      }
+    } else if (p.wt == WK_INT4_SYM || p.wt == WK_UINT4_ZP || p.wt == WK_MXINT4) {
       const int G = 128;
       const int64_t ng = p.K / G;
-      const uint32_t xr = (p.wt == WK_INT4_SYM) ? 8u : 0u;
+      const uint32_t xr = (p.wt != WK_UINT4_ZP) ? 8u : 0u;
       for (int j = 0; j < 4; ++j) {
         uint32_t* dst = reinterpret_cast<uint32_t*>(blk + (j * 128 + r) * 16);
         for (int w = 0; w < 4; ++w) {
-          const int64_t k0 = ks * 128 + 32 * j + 8 * w;
+          const int64_t k0 = ks * 128 + 32 * j;
           if (DIR == 0) {
             uint32_t word = 0;
             if (valid)
-              for (int i = 0; i < 8; ++i) word |= ((get_nibble(codes + rowc, k0 + kNibblePerm[i]) ^ xr) & 0xF) << (4 * i);
+              for (int i = 0; i < 8; ++i)
+                word |= ((get_nibble(codes + rowc, k0 + int4_chunk_k(w, i)) ^ xr) & 0xF) << (4 * i);
             dst[w] = word;
           } else if (valid) {
             const uint32_t word = dst[w];
             for (int i = 0; i < 8; ++i) {
-              const int64_t k = k0 + kNibblePerm[i];
+              const int64_t k = k0 + int4_chunk_k(w, i);
               const uint32_t v = ((word >> (4 * i)) & 0xF) ^ xr;
               uint8_t* b = codes + rowc + (k >> 1);
               *b = (k & 1) ? (uint8_t)((*b & 0x0F) | (v << 4)) : (uint8_t)((*b & 0xF0) | v);
             }
           }
         }
+      }
+      if (p.wt == WK_MXINT4) {
+        uint8_t* d = blk + 8192 + 4 * r;
+        uint8_t* s = scales + (e * p.N + n) * (p.K / 32) + ks * 4;
+        for (int b = 0; b < 4; ++b) {
+          if (DIR == 0) d[b] = valid ? s[b] : (uint8_t)0;
+          else if (valid) s[b] = d[b];
+        }
+        continue;
       }
       uint16_t* sdst = reinterpret_cast<uint16_t*>(blk + 8192) + r;
       uint16_t* ssrc = reinterpret_cast<uint16_t*>(scales) + (e * p.N + n) * ng + ks;

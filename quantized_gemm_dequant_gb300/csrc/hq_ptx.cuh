@@ -47,6 +47,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of phase `parity` (mbarrier.try_wait may suspend the thread for a while before it answers).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // try_wait with a suspend-time hint: a thread whose phase is not complete is parked by the hardware until the
 // phase completes or about `hint_ns` pass, instead of re-issuing the test and taking issue slots from the warps
 // that have work.
@@ -63,18 +76,22 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
 }
 
 // Wait for phase `parity` of `bar` to complete.  Gives up (returns false) when
-// `*abort` becomes non-zero or after `limit_ns` nanoseconds of waiting (both
-// checked each time the suspended thread wakes, at least every millisecond, or
-// every `limit_ns` when that is shorter).
+// `*abort` becomes non-zero or after `limit_ns` nanoseconds of waiting.  The
+// first test does not block; later tests suspend the thread until the phase
+// completes or about min(limit_ns, 1 ms) pass.  The bound is timed with the SM
+// cycle counter at 3 cycles per ns (at least limit_ns at clocks up to 3 GHz),
+// so that even a 1 ns bound runs out when the first test finds the phase
+// incomplete.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  if (mbar_test_wait(bar, parity)) return true;
+  const long long c0 = clock64();
+  const long long lim = 3ll * (long long)limit_ns;
   const uint32_t hint = limit_ns < 1000000ull ? (uint32_t)limit_ns : 1000000u;
   for (;;) {
-    if (mbar_try_wait_suspend(bar, parity, hint)) return true;
+    if (clock64() - c0 >= lim) return false;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
+    if (mbar_try_wait_suspend(bar, parity, hint)) return true;
   }
 }
 
@@ -150,6 +167,35 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr)
                : "memory");
+}
+
+// Plain shared-memory loads by 32-bit shared address (zero-extended into 32 bits).
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+// mbarrier arrive by the threads whose `on` is non-zero (a predicated instruction: no branch).
+__device__ __forceinline__ void mbar_arrive_if(uint64_t* bar, uint32_t on) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+      "@p mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n\t}\n" ::"r"(smem_u32(bar)),
+      "r"(on)
+      : "memory");
+}
+// 64-bit relaxed gpu-scope global store and load (single-copy atomic when 8-byte aligned).
+__device__ __forceinline__ void st_relaxed_gpu_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_relaxed_gpu_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
 }
 
 // Generic-proxy writes to shared memory made visible to the async proxy (UMMA, bulk copies).

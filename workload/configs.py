@@ -12,6 +12,12 @@ Sizes and recipes (quantized GEMM microbenchmarks of the Humming announcement,
               INT4 symmetric group 128, bf16 act
   moe_mxfp4   MoE, E=256, top-8, K=7168, N=4096, T in {1,64,1024,8192},
               MXFP4 weights, FP8 e4m3 per-token activations
+  w8a16, w2a16, mxint4_a16, fp8w_a16
+              dense, K=4096, N=14336, M in {1,16,64,256}: INT8 (e0m7) g128,
+              UINT2 + zero point g128, MXINT4 (e8m0 per 32), FP8 E4M3 g128
+              weights, bf16 act
+  w4a8_mx     dense, K=7168, N=4096, M in {1,128,1024,8192}: MXFP4 weights,
+              MXFP8 activations (e4m3 + e8m0 per 32)
 
 Weights are fp32 N(0, 0.02) and activations N(0, 1) before quantization.  MoE
 routing draws k distinct experts per token from Zipf(1.1) popularities by
@@ -37,6 +43,13 @@ CONFIGS = {
                       sizes=[1, 32, 512, 4096]),
     "moe_mxfp4": dict(kind="moe", wfmt="mxfp4", afmt="e4m3_tok", E=256, topk=8, N=4096, K=7168, G=32,
                       sizes=[1, 64, 1024, 8192]),
+    # more weight formats through the same decode component (the dense W4A16 shape of the sweep above), and the
+    # microscaled W4A8 variant (MXFP4 weights x MXFP8 activations) on the NVFP4 shape
+    "w8a16": dict(kind="dense", wfmt="int8_sym", afmt="bf16", N=14336, K=4096, G=128, sizes=[1, 16, 64, 256]),
+    "w2a16": dict(kind="dense", wfmt="uint2_zp", afmt="bf16", N=14336, K=4096, G=128, sizes=[1, 16, 64, 256]),
+    "mxint4_a16": dict(kind="dense", wfmt="mxint4", afmt="bf16", N=14336, K=4096, G=32, sizes=[1, 16, 64, 256]),
+    "fp8w_a16": dict(kind="dense", wfmt="e4m3", afmt="bf16", N=14336, K=4096, G=128, sizes=[1, 16, 64, 256]),
+    "w4a8_mx": dict(kind="dense", wfmt="mxfp4", afmt="mxfp8", N=4096, K=7168, G=32, sizes=[1, 128, 1024, 8192]),
 }
 
 W_STD = 0.02
@@ -70,6 +83,18 @@ def quantize_weights(wfmt, w, G):
     if wfmt == "mxfp4":
         c, s = quant.quant_mxfp4(w)
         return dict(codes=c, scales=s)
+    if wfmt == "int8_sym":
+        c, s = quant.quant_int8_sym(w, G)
+        return dict(codes=c, scales=s)
+    if wfmt == "uint2_zp":
+        c, s, z = quant.quant_uint2_zp(w, G)
+        return dict(codes=c, scales=s, zeros=z)
+    if wfmt == "mxint4":
+        c, s = quant.quant_mxint4(w)
+        return dict(codes=c, scales=s)
+    if wfmt == "e4m3":
+        c, s = quant.quant_e4m3_grouped(w, G)
+        return dict(codes=c, scales=s)
     raise ValueError(wfmt)
 
 
@@ -82,6 +107,9 @@ def quantize_acts(afmt, a):
     if afmt == "nvfp4":
         c, s, g = quant.quant_nvfp4(a)
         return dict(data=c, scale=s, gscale=g.reshape(1))
+    if afmt == "mxfp8":
+        q, s = quant.quant_mxfp8(a)
+        return dict(data=q, scale=s)
     raise ValueError(afmt)
 
 
@@ -157,6 +185,12 @@ def dense_flops(M, N, K):
 def weight_bytes(wfmt, N, K, G, experts=1):
     """Canonical bytes of codes + scales + zeros + global scale for `experts` experts."""
     codes = N * K // 2
+    if wfmt in ("int8_sym", "e4m3"):
+        return experts * (N * K + N * (K // G) * 2)
+    if wfmt == "uint2_zp":
+        return experts * (N * K // 4 + N * (K // G) * 2 + N * (K // G) // 4)  # zeros are 2-bit values
+    if wfmt == "mxint4":
+        return experts * (codes + N * (K // 32))
     if wfmt == "int4_sym":
         sc = N * (K // G) * 2
     elif wfmt == "uint4_zp":
@@ -177,6 +211,8 @@ def act_bytes(afmt, M, K):
         return M * K + M * 4
     if afmt == "nvfp4":
         return M * K // 2 + M * K // 16 + 4
+    if afmt == "mxfp8":
+        return M * K + M * K // 32
     raise ValueError(afmt)
 
 
