@@ -201,21 +201,23 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT, DEC>::CTAS_PER_SM)
     }
   }
   pdl_trigger();
-  pdl_wait();  // no global memory a previous kernel may write is touched before this point (weights aside)
-  uint32_t epoch_prev = 0;
+  // No global memory a previous kernel may write is touched before griddepcontrol.wait (weights aside).  MoE
+  // tiles depend on the routing tables, so MoE calls wait here; dense calls set everything up first and wait only
+  // where they first touch such memory: the producer before its activation loads, the compute warps before their
+  // first epilogue, every thread before the exit count.
+  if (args.moe) {
+    pdl_wait();
+    moe_tile_prefix(args.counts, args.E, args.region_cap, BT, prefix, &sh.tile_prefix_total);
+  }
+  __syncthreads();
   if (producer) {
+    pdl_wait();
     for (int s = 0; s < npre; ++s)
 #pragma unroll
       for (int j = 0; j < 2; ++j)
         tma_load_2d(smem + s * C::STAGE + j * (BT * 128), &args.tmap_a, pre_x[s] + j * 64, pre_y[s], &sh.full[s]);
-    // the workspace epoch is needed only when a partial sum is published or collected: its load stays off the
-    // path to the first MMA (the barrier below does not wait for it)
-    epoch_prev = reinterpret_cast<volatile uint32_t*>(args.status)[1];
-  }
-  if (args.moe) moe_tile_prefix(args.counts, args.E, args.region_cap, BT, prefix, &sh.tile_prefix_total);
-  __syncthreads();
-  if (producer) {
-    sh.epoch = epoch_prev + 1u;
+    // the workspace epoch is needed only when a partial sum is published or collected
+    sh.epoch = reinterpret_cast<volatile uint32_t*>(args.status)[1] + 1u;
     mbar_arrive(&sh.epoch_bar);
   }
   const int total_tiles = args.moe ? sh.tile_prefix_total * args.n_tiles : args.m_tiles * args.n_tiles;
@@ -225,6 +227,7 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT, DEC>::CTAS_PER_SM)
   volatile int* abort_flag = &sh.abort_flag;
   auto fail = [&](int code) {
     *abort_flag = 1;
+    pdl_wait();
     atomicCAS(args.status, 0, code);
   };
   auto tile_rows = [&](int tile, int& e, int& row0, int& nrows) {
@@ -511,6 +514,7 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT, DEC>::CTAS_PER_SM)
         ph ^= st == 0 ? 1u : 0u;
       }
       // ---------------------------------------------------- K halves meet
+      pdl_wait();  // (returns at once after the first piece) the epilogue touches global memory
       float* mine = red + ((rg * 32 + lane) * 2) * (NT * 4);
       if (kh == 1) {
 #pragma unroll
@@ -654,6 +658,7 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT, DEC>::CTAS_PER_SM)
   }
 
   // ---------------------------------------------------------------- teardown
+  pdl_wait();
   __syncthreads();
   if (tid == 0) {
     // the last CTA to exit stores this call's epoch for the next call on the workspace
