@@ -36,7 +36,8 @@ from workload import configs as W  # noqa: E402
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # dense tensor-core peaks relative to bf16 (nominal 2.25 / 4.5 / 13.5 PFLOP/s)
 DTYPE_RATIO = {"bf16": 1.0, "fp8": 2.0, "fp4": 6.0}
-PATH_DTYPE = {"int4_sym": "bf16", "uint4_zp": "bf16", "nvfp4": "fp4", "mxfp4": "fp8"}
+PATH_DTYPE = {"int4_sym": "bf16", "uint4_zp": "bf16", "nvfp4": "fp4", "mxfp4": "fp8", "int8_sym": "bf16",
+              "uint2_zp": "bf16", "mxint4": "bf16", "e4m3": "bf16"}
 SPIN_CYCLES = 1_000_000  # about 0.5 ms at 2 GHz: longer than the host side of one burst of calls
 
 
@@ -216,7 +217,8 @@ def roofline_of(info, t_s, pk, dt):
 # ------------------------------------------------------------------ GPU arm
 MIN_SAMPLES = 20       # samples per size (bursts, and isolated calls)
 MIN_SAMPLES_FAST = 100  # below 10 us per call
-OTHER_CONFIGS = ["w4a16_sym", "nvfp4", "moe_w4a16", "moe_mxfp4", "moe_w4a16_down", "moe_mxfp4_down"]
+OTHER_CONFIGS = ["w4a16_sym", "nvfp4", "moe_w4a16", "moe_mxfp4", "moe_w4a16_down", "moe_mxfp4_down", "w8a16", "w2a16",
+                 "mxint4_a16", "fp8w_a16", "w4a8_mx"]
 
 
 def _burst(call, n, R, stream, counter):
@@ -434,16 +436,26 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+DECODE_KIND = {"int4_sym": 0, "uint4_zp": 0, "mxint4": 1, "int8_sym": 2, "e4m3": 3, "uint2_zp": 4}
+
+
 def kernel_name(cfg, M):
+    """The GEMM kernel instance a call of this workload with M rows (dense) or T tokens (MoE) launches, as the library's
+    launch plan picks it (tile width, register-decode or tcgen05 kernel)."""
     c = W.CONFIGS[cfg]
-    path = {"int4_sym": 0, "uint4_zp": 0, "nvfp4": 1, "mxfp4": 2}[c["wfmt"]]
+    wf = c["wfmt"]
+    path = 1 if wf == "nvfp4" else (3 if wf == "mxfp4" and c["afmt"] == "mxfp8" else (2 if wf == "mxfp4" else 0))
     if c["kind"] == "dense":
         bt = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128 if M <= 128 else 256
     else:
         avg = -(-M * c["topk"] // c["E"])
-        bt = 16 if avg <= 16 else (256 if path != 1 and avg > 128 else 128)
-    if path == 0 and bt <= 32 and os.environ.get("HQ_FORCE_PATH") != "umma":
-        return f"hq::hq_gemm_small_kernel<{bt}>"
+        bt = 16 if avg <= 16 else (256 if path not in (1, 3) and avg > 128 else 128)
+    if path == 0:
+        dec = DECODE_KIND[wf]
+        if dec != 0 or (bt <= 32 and os.environ.get("HQ_FORCE_PATH") != "umma"):
+            if c["kind"] == "dense" and M <= 8:
+                bt = 8
+            return f"hq::hq_gemm_small_kernel<{min(bt, 32)}, {dec}>"
     return f"hq::hq_gemm_kernel<{path}, {bt}, {1 if c.get('down') else 0}>"
 
 

@@ -21,6 +21,7 @@ cudaError_t launch_route(const int32_t* ids, int64_t rows, int E, int cap, int* 
 cudaError_t launch_gemm_int4(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_nvfp4(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_mxfp4(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_mxfp4a(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_small(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_small_fmt(int dec, const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(int path, const GemmArgs& a, int bt, int gemm_grid, int grid, cudaStream_t stream);
@@ -70,6 +71,8 @@ hq_status_t check_format(const hq_format_t* f) {
           (f->act_type != HQ_A_E4M3_TOKEN && f->act_type != HQ_A_MXFP8))
         return HQ_ERR_UNSUPPORTED;
       if (f->K % 128) return HQ_ERR_ALIGNMENT;
+      // MXFP8 block scales are loaded 16 bytes (512 K) at a time: rows of K/32 bytes must be 16-byte multiples
+      if (f->act_type == HQ_A_MXFP8 && f->K % 512) return HQ_ERR_ALIGNMENT;
       break;
     case HQ_W_INT8_SYM:
     case HQ_W_E4M3:
@@ -136,7 +139,7 @@ int pick_bt_moe(int path, int64_t rows, int64_t E) {
   if (E == 1) return pick_bt_dense(rows);  // one expert is a dense GEMM over the routed rows
   const int64_t avg = (rows + E - 1) / E;
   if (avg <= 16) return 16;
-  if (path != PATH_NVFP4 && avg > 128) return 256;
+  if (path != PATH_NVFP4 && path != PATH_MXFP4A && avg > 128) return 256;
   return 128;
 }
 
@@ -151,7 +154,11 @@ int forced_moe_path() {
 
 // Activation bytes per row and NVFP4 scale bytes per row.
 int64_t act_row_bytes(const hq_format_t* f) {
-  return f->act_type == HQ_A_BF16 ? 2 * f->K : (f->act_type == HQ_A_E4M3_TOKEN ? f->K : f->K / 2);
+  return f->act_type == HQ_A_BF16 ? 2 * f->K : ((f->act_type == HQ_A_E4M3_TOKEN || f->act_type == HQ_A_MXFP8) ? f->K : f->K / 2);
+}
+// Activation block-scale bytes per row (NVFP4: ue4m3 per 16; MXFP8: e8m0 per 32), else 0.
+int64_t act_scale_row_bytes(const hq_format_t* f) {
+  return f->act_type == HQ_A_NVFP4 ? f->K / 16 : (f->act_type == HQ_A_MXFP8 ? f->K / 32 : 0);
 }
 
 // HQ_FORCE_PATH=small|umma overrides the choice between the two INT4 kernels (tests compare both).
@@ -166,7 +173,7 @@ int forced_path() {
 Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int sms) {
   Plan p;
   const PackGeom g = pack_geom(f->weight_type, f->N, f->K, f->num_experts);
-  p.path = g.path;
+  p.path = (g.path == PATH_MXFP4 && f->act_type == HQ_A_MXFP8) ? PATH_MXFP4A : g.path;
   p.n_tiles = g.n_tiles;
   p.kst = g.k_stages;
   if (sms < 1) sms = 1;
@@ -183,7 +190,7 @@ Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int
   } else {
     const int64_t rows = M_or_T * topk;
     const int64_t E = f->num_experts;
-    p.bt = pick_bt_moe(g.path, rows, E);
+    p.bt = pick_bt_moe(p.path, rows, E);
     p.region_cap = M_or_T;
     const int64_t active = rows < E ? rows : E;
     p.max_tiles = p.n_tiles * (active + (rows + p.bt - 1) / p.bt);
@@ -248,9 +255,9 @@ Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int
       off = align256(off + sizeof(int) * (size_t)(f->num_experts + 1));
       p.off_gact = off;
       off = align256(off + (size_t)(rows * act_row_bytes(f)));
-      if (f->act_type == HQ_A_NVFP4) {
+      if (act_scale_row_bytes(f) > 0) {
         p.off_gsf = off;
-        off = align256(off + (size_t)(rows * (f->K / 16)));
+        off = align256(off + (size_t)(rows * act_scale_row_bytes(f)));
       }
     }
   }
@@ -265,6 +272,7 @@ cudaError_t launch_path(const Plan& p, const GemmArgs& a, cudaStream_t s) {
                  : (p.dec == DEC_INT4 ? launch_gemm_small(a, p.bt, p.grid, s)
                                       : launch_gemm_small_fmt(p.dec, a, p.bt, p.grid, s));
   else if (p.path == PATH_NVFP4) e = launch_gemm_nvfp4(a, p.bt, p.grid, s);
+  else if (p.path == PATH_MXFP4A) e = launch_gemm_mxfp4a(a, p.bt, p.grid, s);
   else e = launch_gemm_mxfp4(a, p.bt, p.grid, s);
   if (e != cudaSuccess || !p.sk || p.small) return e;  // the register-decode kernel finishes cut tiles itself
   // tiles cut between CTAs: sum their partial slots, one CTA per 32 token columns of a tile
@@ -312,6 +320,9 @@ bool act_maps(GemmArgs& a, const hq_format_t* f, const hq_act_t* A, int64_t rows
   const uint64_t K = (uint64_t)f->K;
   if (f->act_type == HQ_A_BF16) return encode_2d(&a.tmap_a, A->data, true, K, rows, 64, box_rows, true);
   if (f->act_type == HQ_A_E4M3_TOKEN) return encode_2d(&a.tmap_a, A->data, false, K, rows, 128, box_rows, true);
+  if (f->act_type == HQ_A_MXFP8)
+    return encode_2d(&a.tmap_a, A->data, false, K, rows, 128, box_rows, true) &&
+           encode_2d(&a.tmap_sf, A->scale, false, K / 32, rows, 16, box_rows, false);
   return encode_2d(&a.tmap_a, A->data, false, K / 2, rows, 128, box_rows, true) &&
          encode_2d(&a.tmap_sf, A->scale, false, K / 16, rows, 16, box_rows, false);
 }
@@ -384,7 +395,8 @@ hq_status_t hq_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* packe
   if (!A || !A->data || !packedW || !C) return HQ_ERR_INVALID_ARG;
   if (fmt->act_type == HQ_A_E4M3_TOKEN && !A->scale) return HQ_ERR_INVALID_ARG;
   if (fmt->act_type == HQ_A_NVFP4 && (!A->scale || !A->global_scale)) return HQ_ERR_INVALID_ARG;
-  if (!aligned16(A->data) || !aligned16(packedW) || (A->scale && fmt->act_type == HQ_A_NVFP4 && !aligned16(A->scale)))
+  if (fmt->act_type == HQ_A_MXFP8 && !A->scale) return HQ_ERR_INVALID_ARG;
+  if (!aligned16(A->data) || !aligned16(packedW) || (A->scale && act_scale_row_bytes(fmt) > 0 && !aligned16(A->scale)))
     return HQ_ERR_ALIGNMENT;
   const int sms = num_sms();
   if (sms < 1) return HQ_ERR_CUDA;
@@ -439,7 +451,8 @@ hq_status_t moe_call(const hq_format_t* fmt, const hq_act_t* A, const void* pack
   if (!A || !A->data || !packedW || !C || !topk_ids) return HQ_ERR_INVALID_ARG;
   if (fmt->act_type == HQ_A_E4M3_TOKEN && !A->scale) return HQ_ERR_INVALID_ARG;
   if (fmt->act_type == HQ_A_NVFP4 && (!A->scale || !A->global_scale)) return HQ_ERR_INVALID_ARG;
-  if (!aligned16(A->data) || !aligned16(packedW) || (fmt->act_type == HQ_A_NVFP4 && !aligned16(A->scale)))
+  if (fmt->act_type == HQ_A_MXFP8 && !A->scale) return HQ_ERR_INVALID_ARG;
+  if (!aligned16(A->data) || !aligned16(packedW) || (act_scale_row_bytes(fmt) > 0 && !aligned16(A->scale)))
     return HQ_ERR_ALIGNMENT;
   const int sms = num_sms();
   if (sms < 1) return HQ_ERR_CUDA;
@@ -460,7 +473,7 @@ hq_status_t moe_call(const hq_format_t* fmt, const hq_act_t* A, const void* pack
     // the GEMM reads the expert-contiguous copy with BT-row boxes
     hq_act_t G = *A;
     G.data = ws + p.off_gact;
-    if (fmt->act_type == HQ_A_NVFP4) G.scale = ws + p.off_gsf;
+    if (act_scale_row_bytes(fmt) > 0) G.scale = ws + p.off_gsf;
     if (!act_maps(a, fmt, &G, T * topk, p.bt, false)) return HQ_ERR_INVALID_ARG;
   } else if (!act_maps(a, fmt, A, a_rows, p.bt, true)) {
     return HQ_ERR_INVALID_ARG;
@@ -474,8 +487,8 @@ hq_status_t moe_call(const hq_format_t* fmt, const hq_act_t* A, const void* pack
   if (p.grouped) {
     err = launch_moe_permute(counts, region, (int)p.region_cap, (int)E, a_div, T * topk, A->data,
                              (int)act_row_bytes(fmt), ws + p.off_gact,
-                             fmt->act_type == HQ_A_NVFP4 ? A->scale : nullptr, (int)(fmt->K / 16),
-                             fmt->act_type == HQ_A_NVFP4 ? ws + p.off_gsf : nullptr,
+                             act_scale_row_bytes(fmt) > 0 ? A->scale : nullptr, (int)act_scale_row_bytes(fmt),
+                             act_scale_row_bytes(fmt) > 0 ? ws + p.off_gsf : nullptr,
                              reinterpret_cast<int*>(ws + p.off_rowoff), (cudaStream_t)stream);
     if (err != cudaSuccess) return HQ_ERR_CUDA;
   }

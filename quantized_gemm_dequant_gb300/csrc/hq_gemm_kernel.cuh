@@ -55,7 +55,7 @@ constexpr int ERR_BAD_ROUTING = 6;
 
 struct GemmArgs {
   CUtensorMap tmap_a;   // activation data: dense 2-D box of BT rows, MoE one-row boxes for gather4
-  CUtensorMap tmap_sf;  // NVFP4 activation block scales (same row structure)
+  CUtensorMap tmap_sf;  // NVFP4 / MXFP8 activation block scales (same row structure)
   const uint8_t* w;        // packed weights, all experts
   int64_t w_expert_bytes;  // bytes per expert
   int w_blk;               // bytes per packed weight block (<= Cfg::W_BLK)
@@ -86,17 +86,19 @@ struct GemmArgs {
 
 template <int PATH, int BT>
 struct Cfg {
+  static constexpr bool MX = PATH == PATH_MXFP4 || PATH == PATH_MXFP4A;  // MXFP4 weights
+  static constexpr bool AMX = PATH == PATH_MXFP4A;                        // MXFP8 activations
   static constexpr int KSTAGE = PATH == PATH_NVFP4 ? 256 : 128;  // K per weight block
   static constexpr int W_BLK = PATH == PATH_INT4 ? 8576 : (PATH == PATH_NVFP4 ? 18432 : 8704);
   static constexpr int W_REGION = ((W_BLK + 1023) / 1024) * 1024;
-  static constexpr int X_REGION = PATH == PATH_MXFP4 ? 16384 : 0;  // expanded e2m1 A tile per weight stage
+  static constexpr int X_REGION = MX ? 16384 : 0;  // expanded e2m1 A tile per weight stage
   static constexpr int SUB = PATH == PATH_INT4 ? 2 : 1;             // activation stages per weight block
   static constexpr int ACT_BYTES = BT * 128;
   static constexpr int ACT_REGION = ((ACT_BYTES + 1023) / 1024) * 1024;
   static constexpr int SF_ROWS = BT < 32 ? 32 : BT;
   // NVFP4 activation scales: dense rows are 16 bytes apart; MoE rows come in gather4 groups of four,
   // each group in its own 128-byte slot (row j at (j/4)*128 + (j%4)*16)
-  static constexpr int ASF_REGION = PATH == PATH_NVFP4 ? ((SF_ROWS * 32 + 1023) / 1024) * 1024 : 0;
+  static constexpr int ASF_REGION = (PATH == PATH_NVFP4 || AMX) ? ((SF_ROWS * 32 + 1023) / 1024) * 1024 : 0;
   static constexpr int A_STAGE = ACT_REGION + ASF_REGION;
   static constexpr int W_STAGE = W_REGION + X_REGION;
   static constexpr int RING_BUDGET = 216 * 1024;
@@ -118,7 +120,7 @@ struct Cfg {
   static_assert(SA >= 2, "activation ring too small");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
   static_assert(PATH != PATH_NVFP4 || 256 + SW * SF_STAGE_COLS <= 512, "tensor memory");
-  static_assert(PATH != PATH_MXFP4 || 256 + 4 * SW + 8 <= 512, "tensor memory");
+  static_assert(!MX || 256 + 4 * SW + (AMX ? SW * SFB_STEP : 8) <= 512, "tensor memory");
 };
 
 __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
@@ -331,11 +333,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
     for (int s = 0; s < C::SW; ++s) {
       mbar_init(&sh.w_full[s], 1);
       mbar_init(&sh.w_empty[s], PATH == PATH_INT4 ? 8 : (PATH == PATH_NVFP4 ? 4 + 1 : 8 + 1));
-      mbar_init(&sh.ready[s], PATH == PATH_MXFP4 ? 8 : 4);
+      mbar_init(&sh.ready[s], C::MX ? 8 : 4);
     }
     for (int s = 0; s < C::SA; ++s) {
       mbar_init(&sh.a_full[s], 1);
-      mbar_init(&sh.a_empty[s], PATH == PATH_NVFP4 ? 4 + 1 : 1);
+      mbar_init(&sh.a_empty[s], (PATH == PATH_NVFP4 || C::AMX) ? 4 + 1 : 1);
     }
     for (int a = 0; a < C::NA; ++a) {
       mbar_init(&sh.afull[a], 8);
@@ -361,7 +363,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
   }
   if (tid == APROD_WARP * 32) {
     prefetch_tmap(&args.tmap_a);
-    if (PATH == PATH_NVFP4) prefetch_tmap(&args.tmap_sf);
+    if (PATH == PATH_NVFP4 || C::AMX) prefetch_tmap(&args.tmap_sf);
   }
   pdl_trigger();
   pdl_wait();  // no global memory a previous kernel may write is touched before this point (weights aside)
@@ -466,9 +468,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
               uint8_t* dst = aring + as * C::A_STAGE;
               // x offset of this stage in the tensor map's element units (bf16: 64 per stage; bytes: 128)
               const int x = PATH == PATH_INT4 ? g * 128 + j * 64 : g * 128;
-              mbar_arrive_expect_tx(&sh.a_full[as], A_BOX_BYTES + (PATH == PATH_NVFP4 ? SF_BOX_BYTES : 0));
+              mbar_arrive_expect_tx(&sh.a_full[as], A_BOX_BYTES + ((PATH == PATH_NVFP4 || C::AMX) ? SF_BOX_BYTES : 0));
               tma_load_2d(dst, &args.tmap_a, x, rbase, &sh.a_full[as]);
-              if (PATH == PATH_NVFP4) tma_load_2d(dst + C::ACT_REGION, &args.tmap_sf, g * 16, rbase, &sh.a_full[as]);
+              // block scales: NVFP4 16 bytes per 256-K stage; MXFP8 the 16-byte group of four 128-K stages
+              if (PATH == PATH_NVFP4 || C::AMX)
+                tma_load_2d(dst + C::ACT_REGION, &args.tmap_sf, C::AMX ? (g >> 2) * 16 : g * 16, rbase, &sh.a_full[as]);
               armed |= 1u << as;
               if (++as == C::SA) {
                 as = 0;
@@ -509,14 +513,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
             if (!ok) return;
             uint8_t* dst = aring + as * C::A_STAGE;
             const int x = PATH == PATH_INT4 ? g * 128 + j * 64 : g * 128;
-            if (lane == 0) mbar_arrive_expect_tx(&sh.a_full[as], A_BOX_BYTES + (PATH == PATH_NVFP4 ? SF_BOX_BYTES : 0));
+            if (lane == 0)
+              mbar_arrive_expect_tx(&sh.a_full[as], A_BOX_BYTES + ((PATH == PATH_NVFP4 || C::AMX) ? SF_BOX_BYTES : 0));
             __syncwarp();
             for (int i = lane * 4; i < BT; i += 128) {
               uint8_t* d = dst + (i >> 3) * 1024 + (i & 7) * 128;
               tma_gather4(d, &args.tmap_a, x, sh.rows_tok[i], sh.rows_tok[i + 1], sh.rows_tok[i + 2],
                           sh.rows_tok[i + 3], &sh.a_full[as]);
-              if (PATH == PATH_NVFP4)
-                tma_gather4(dst + C::ACT_REGION + (i >> 2) * 128, &args.tmap_sf, g * 16, sh.rows_tok[i],
+              if (PATH == PATH_NVFP4 || C::AMX)
+                tma_gather4(dst + C::ACT_REGION + (i >> 2) * 128, &args.tmap_sf, C::AMX ? (g >> 2) * 16 : g * 16,
+                            sh.rows_tok[i],
                             sh.rows_tok[i + 1], sh.rows_tok[i + 2], sh.rows_tok[i + 3], &sh.a_full[as]);
             }
             armed |= 1u << as;
@@ -587,10 +593,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
             } else {
               const uint32_t xa = smem_u32(wring + ws * C::W_STAGE + C::W_REGION);
               const uint32_t sfa = tmem + 256 + ws * 4;
-              const uint32_t sfb = tmem + 256 + 4 * C::SW;
+              // activation block scales: unit scales written once (per-token FP8), or the stage's MXFP8 scales
+              const uint32_t sfb = tmem + 256 + 4 * C::SW + (C::AMX ? ws * C::SFB_STEP : 0);
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                const uint32_t idesc = idesc_block_scaled(128, BT, 5, 0, 1, i, 0);
+                const uint32_t idesc = idesc_block_scaled(128, BT, 5, 0, 1, i, C::AMX ? i : 0);
                 const uint64_t ad = smem_desc(xa + i * 32, 16, 1024, 2);
                 const uint64_t bd = smem_desc(act + i * 32, 16, 1024, 2);
                 umma_mxf8_ss(tmem, ad, bd, idesc, sfa, sfb, (first && i == 0) ? 0u : 1u);
@@ -675,6 +682,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
       float t_mul[TPL];
     };
     int piece_no = 0;
+    int gk = 0;  // K block of the next weight stage the mainloop role takes (MXFP8: which scale word)
     auto open_piece = [&](const Piece& pc, Pend& pd) {
       pd.pc = pc;
       tile_rows(pc.tile, pd.e, pd.row0, pd.nrows);
@@ -794,7 +802,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
             }
             tmem_wait_st();
             tc_fence_before();
-          } else if (PATH == PATH_MXFP4) {
+          } else if (C::MX) {
             if (warp < 4) {
               // weight scale factors -> tensor memory (replicated in every lane quarter)
               const uint32_t* wsf = reinterpret_cast<const uint32_t*>(wb + 8192);
@@ -802,6 +810,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
 #pragma unroll
               for (int j = 0; j < 4; ++j) v[j] = wsf[j * 32 + lane];
               tmem_st_x<4>(tmem + lane_base + 256 + ws * 4, v);
+              if (C::AMX) {
+                // MXFP8 activation scales of this stage: token j's four e8m0 bytes (one per 32 K) are word g % 4 of
+                // its 16-byte group; token j goes to lane j % 32 of column j / 32 (every lane quarter)
+                if (!waitf(&sh.a_full[as], aph)) return false;
+                const uint8_t* asf = aring + as * C::A_STAGE + C::ACT_REGION + 4 * (gk & 3);
+                uint32_t b[C::CB];
+#pragma unroll
+                for (int cc = 0; cc < C::CB; ++cc) {
+                  const int j = cc * 32 + lane;
+                  const int off = (args.moe && !args.grouped) ? (j >> 2) * 128 + (j & 3) * 16 : j * 16;
+                  b[cc] = *reinterpret_cast<const uint32_t*>(asf + off);
+                }
+                tmem_st_x<C::CB>(tmem + lane_base + 256 + 4 * C::SW + ws * C::SFB_STEP, b);
+              }
             }
             // all 8 warps: expand packed e2m1 (8 bytes per 16 K) into the padded 16-byte chunks, two chunks of a
             // row per 16-byte load
@@ -824,9 +846,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
           if (lane == 0) {
             mbar_arrive(&sh.ready[ws]);
             mbar_arrive(&sh.w_empty[ws]);
-            if (PATH == PATH_NVFP4) mbar_arrive(&sh.a_empty[as]);
+            if (PATH == PATH_NVFP4 || (C::AMX && warp < 4)) mbar_arrive(&sh.a_empty[as]);
           }
-          if (PATH == PATH_NVFP4) {
+          ++gk;
+          if (PATH == PATH_NVFP4 || C::AMX) {
             if (++as == C::SA) {
               as = 0;
               aph ^= 1;
@@ -995,6 +1018,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
       open_piece(pc, cur);
       const int nblk = pc.g1 - pc.g0;
       const int pre = nblk < PREFILL ? nblk : PREFILL;
+      gk = pc.g0;
       if (!mainloop(pre)) return;
       if (has_prev && !epilogue(prev)) return;
       if (!mainloop(nblk - pre)) return;

@@ -81,7 +81,8 @@ inline int decode_kind(int weight_type) {
 }
 // Formats only the register-decode kernel reads (any token count)
 inline bool register_decode_only(int weight_type) { return weight_type >= WK_INT8_SYM; }
-enum KernelPath { PATH_INT4 = 0, PATH_NVFP4 = 1, PATH_MXFP4 = 2 };
+// tcgen05 kernel variants; PATH_MXFP4A: MXFP4 weights with MXFP8 activations (e8m0 block scales on both operands)
+enum KernelPath { PATH_INT4 = 0, PATH_NVFP4 = 1, PATH_MXFP4 = 2, PATH_MXFP4A = 3 };
 
 constexpr int TILE_N = 128;  // weight rows per tile (the UMMA M dimension)
 

@@ -108,3 +108,58 @@ def test_exact_integer_pow2_bit_exact(lib, wfmt):
     assert np.max(np.abs(ref)) < 2 ** 20
     want = torch.from_numpy(np.asarray(ref, dtype=np.float32)).to(torch.bfloat16)
     assert torch.equal(y.cpu(), want), "not bit-exact"
+
+
+# ------------------------------------------------------------------ MXFP4 weights x MXFP8 activations (W4A8, MX)
+MX8 = dict(kind="dense", wfmt="mxfp4", afmt="mxfp8", G=32)
+
+
+@pytest.mark.parametrize("M", [1, 16, 100, 300])
+def test_mxfp8_act_dense_parity(lib, M):
+    """The microscaled W4A8 variant ("W8A8 / W4A8 / W4A4"): e8m0 block scales on both operands of the block-scaled
+    tcgen05 MMA."""
+    inp = make_dense(MX8, M, seed=M + 3, N=320, K=1024)
+    fmt, packed = lib.pack_inputs(inp, "cuda")
+    act = {k: v.cuda() for k, v in inp["a"].items()}
+    y = lib.gemm(fmt, act, packed, M)
+    torch.cuda.synchronize()
+    R.assert_parity(y, R.dense_ref(inp), f"mxfp4 x mxfp8 M={M}")
+
+
+@pytest.mark.parametrize("path", ["indexed", "grouped"])
+@pytest.mark.parametrize("T", [5, 60, 300])
+def test_mxfp8_act_moe_parity(lib, monkeypatch, path, T):
+    monkeypatch.setenv("HQ_MOE_PATH", path)
+    inp = make_moe(dict(MX8, kind="moe", topk=3), T, seed=T, E=6, N=256, K=1024, topk=3)
+    fmt, packed = lib.pack_inputs(inp, "cuda")
+    act = {k: v.cuda() for k, v in inp["a"].items()}
+    y = lib.moe_gemm(fmt, act, packed, inp["ids"].cuda(), inp["topk_w"].cuda())
+    torch.cuda.synchronize()
+    R.assert_parity(y, R.moe_ref(inp), f"moe mxfp4 x mxfp8 {path} T={T}")
+
+
+def test_mxfp8_act_exact_pow2_bit_exact(lib):
+    """e2m1 weights, e4m3 activations with small exponents and power-of-two block scales on both sides: every partial
+    sum is exact in fp32, so C equals the bf16 rounding of the exact result."""
+    gen = torch.Generator().manual_seed(13)
+    M, N, K = 24, 256, 1024
+    jw = torch.randint(-1, 2, (N, K // 32), generator=gen)
+    ja = torch.randint(-2, 2, (M, K // 32), generator=gen)
+    sgn = torch.randint(0, 2, (M, K), generator=gen) << 7
+    ex = torch.randint(6, 9, (M, K), generator=gen) << 3
+    a8 = (sgn | ex | torch.randint(0, 8, (M, K), generator=gen)).to(torch.uint8)
+    inp = dict(M=M, N=N, K=K, wfmt="mxfp4", afmt="mxfp8", G=32,
+               w=dict(codes=torch.randint(0, 256, (N, K // 2), generator=gen, dtype=torch.uint8),
+                      scales=(jw + 127).to(torch.uint8)),
+               a=dict(data=a8, scale=(ja + 127).to(torch.uint8)))
+    fmt, packed = lib.pack_inputs(inp, "cuda")
+    y = lib.gemm(fmt, {k: v.cuda() for k, v in inp["a"].items()}, packed, M)
+    torch.cuda.synchronize()
+    ref = R.dense_ref(inp)
+    assert np.max(np.abs(ref)) < 2 ** 20
+    assert torch.equal(y.cpu(), torch.from_numpy(np.asarray(ref, dtype=np.float32)).to(torch.bfloat16))
+
+
+def test_mxfp8_act_needs_k_multiple_of_512(lib):
+    fmt = lib.make_format("mxfp4", 256, 640, act_type=lib.HQ_A_MXFP8)
+    assert lib.packed_bytes(fmt) == 0
