@@ -12,6 +12,7 @@
 #include "hq_act_quant.h"
 #include "hq_gemm_kernel.cuh"
 #include "hq_layout.h"
+#include "hq_tune.h"
 
 namespace hq {
 cudaError_t launch_pack(int dir, int wt, int64_t N, int64_t K, int64_t E, const void* codes, const void* scales,
@@ -114,6 +115,7 @@ struct Plan {
   int small = 0;  // integer / FP8 weights with at most 32 tokens per tile: register-decode mma.sync kernel
   int dec = 0;    // its decode variant
   int grouped = 0;  // MoE: routed rows copied into expert-contiguous order first (2-D TMA boxes)
+  int fused = 0;    // MoE: the register-decode kernel routes the rows itself (no routing kernel)
   int bt = 16;
   int sk = 0;
   int grid = 1;
@@ -170,6 +172,30 @@ int forced_path() {
   return 0;
 }
 
+int tune_class(const hq_format_t* f, int path) {
+  if (path == PATH_NVFP4) return TC_NVFP4;
+  if (path == PATH_MXFP4A) return TC_MXFP4A;
+  if (path == PATH_MXFP4) return TC_MXFP4;
+  return register_decode_only(f->weight_type) ? TC_REGDEC : TC_INT4;
+}
+
+// Tiles of the launch for token tile bt: (upper bound, planning estimate).  MoE: the host does not know the routing,
+// so the bound assumes every routed expert's rows end in a partial tile; the estimate is one tile per expert hit.
+void plan_tiles(Plan& p, int64_t M_or_T, int32_t topk, bool moe, int64_t E, int64_t* tiles_est) {
+  if (!moe) {
+    p.m_tiles = (M_or_T + p.bt - 1) / p.bt;
+    p.max_tiles = p.m_tiles * p.n_tiles;
+    *tiles_est = p.max_tiles;
+  } else {
+    const int64_t rows = M_or_T * topk;
+    const int64_t active = rows < E ? rows : E;
+    p.max_tiles = p.n_tiles * (active + (rows + p.bt - 1) / p.bt);
+    *tiles_est = p.n_tiles * active;
+  }
+}
+
+// The built-in rule, then the tuned table's row for (format class, size bucket), then HQ_TUNE; every choice is
+// checked against what the kernels support before it is taken.
 Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int sms) {
   Plan p;
   const PackGeom g = pack_geom(f->weight_type, f->N, f->K, f->num_experts);
@@ -178,62 +204,59 @@ Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int
   p.kst = g.k_stages;
   if (sms < 1) sms = 1;
   size_t off = kHeaderBytes;  // status word, epoch, exit count
-  int64_t tiles_est = 0;  // tiles the launch is planned for (MoE: one per N tile of every expert hit)
-  if (!moe) {
-    p.bt = pick_bt_dense(M_or_T);
-    p.m_tiles = (M_or_T + p.bt - 1) / p.bt;
-    p.max_tiles = p.m_tiles * p.n_tiles;
-    tiles_est = p.max_tiles;
-    p.sk = (p.max_tiles < 2 * (int64_t)sms && p.kst > 1) ? 1 : 0;
-    const int64_t W = p.max_tiles * (p.sk ? p.kst : 1);
-    p.grid = (int)(W < sms ? (W < 1 ? 1 : W) : sms);
-  } else {
-    const int64_t rows = M_or_T * topk;
-    const int64_t E = f->num_experts;
-    p.bt = pick_bt_moe(p.path, rows, E);
-    p.region_cap = M_or_T;
-    const int64_t active = rows < E ? rows : E;
-    p.max_tiles = p.n_tiles * (active + (rows + p.bt - 1) / p.bt);
-    const int64_t est_tiles = p.n_tiles * active;
-    tiles_est = est_tiles;
-    p.sk = (est_tiles < 2 * (int64_t)sms && p.kst > 1) ? 1 : 0;
-    const int64_t W = p.max_tiles * (p.sk ? p.kst : 1);
-    p.grid = (int)(W < sms ? (W < 1 ? 1 : W) : sms);
-  }
+  const int64_t E = f->num_experts;
+  const int64_t rows = M_or_T * (moe ? topk : 1);
+  const int64_t key = moe ? (rows + E - 1) / E : M_or_T;  // size bucket key: M, or routed rows per expert
+  if (moe) p.region_cap = M_or_T;  // rows per expert list
+  // built-in rule: token tile by size; INT4 tiles of at most 32 tokens on the register-decode kernel
+  p.bt = moe ? pick_bt_moe(p.path, rows, E) : pick_bt_dense(M_or_T);
   if (p.path == PATH_INT4) {
-    const int force = forced_path();
     p.dec = decode_kind(f->weight_type);
-    p.small = (force == 1 || register_decode_only(f->weight_type)) ? 1 : (force == 2 ? 0 : (p.bt <= 32 ? 1 : 0));
-    // forced to the register-decode kernel: re-tile with 32-token tiles; dense calls with at most 8 rows use its
-    // 8-token tiles
-    const int small_bt = p.bt > 32 ? 32 : ((!moe && M_or_T <= 8) ? 8 : p.bt);
-    if (p.small && small_bt != p.bt) {
-      p.bt = small_bt;
-      if (!moe) {
-        p.m_tiles = (M_or_T + p.bt - 1) / p.bt;
-        p.max_tiles = p.m_tiles * p.n_tiles;
-      } else {
-        const int64_t rows = M_or_T * topk;
-        const int64_t active = rows < f->num_experts ? rows : f->num_experts;
-        p.max_tiles = p.n_tiles * (active + (rows + p.bt - 1) / p.bt);
-      }
-      p.sk = (p.max_tiles < 2 * (int64_t)sms && p.kst > 1) ? 1 : 0;
-    }
-    if (p.small) {  // the register-decode kernel runs two CTAs per SM up to 16-token tiles
-      const int64_t slots = p.bt <= 16 ? 2 * (int64_t)sms : sms;
-      p.sk = (p.max_tiles < 2 * slots && p.kst > 1) ? 1 : 0;
-      const int64_t W = p.max_tiles * (p.sk ? p.kst : 1);
-      p.grid = (int)(W < slots ? (W < 1 ? 1 : W) : slots);
-    }
+    p.small = (register_decode_only(f->weight_type) || p.bt <= 32) ? 1 : 0;
+    if (p.small) p.bt = p.bt > 32 ? 32 : ((!moe && M_or_T <= 8) ? 8 : p.bt);
   }
-  if (!p.small) {
+  // tuned choice
+  TuneChoice tc = tune_lookup(tune_class(f, p.path), moe, key);
+  tune_env_override(tc);
+  const int force = forced_path();
+  if (force) tc.kernel = force == 1 ? 1 : 0;
+  if (p.path == PATH_INT4 && !register_decode_only(f->weight_type) && tc.kernel >= 0 && tc.kernel != p.small) {
+    p.small = tc.kernel;
+    if (p.small && p.bt > 32) p.bt = 32;       // re-tile for the register-decode kernel
+    if (!p.small && p.bt < 16) p.bt = 16;
+  }
+  if (tc.bt > 0) {
+    const bool ok = p.small ? (tc.bt == 8 || tc.bt == 16 || tc.bt == 32)
+                            : (tc.bt == 16 || tc.bt == 32 || tc.bt == 64 || tc.bt == 128 ||
+                               (tc.bt == 256 && !(moe && (p.path == PATH_NVFP4 || p.path == PATH_MXFP4A))));
+    if (ok) p.bt = tc.bt;
+  }
+  int64_t tiles_est = 0;
+  plan_tiles(p, M_or_T, topk, moe, E, &tiles_est);
+  // persistent grid: the register-decode kernel holds two CTAs per SM up to 16-token tiles (all CTAs of a launch
+  // must be resident at once: owners of cut tiles wait for the other CTAs' partial sums)
+  const int max_per_sm = p.small && p.bt <= 16 ? 2 : 1;
+  const int per_sm = tc.slots >= 1 && tc.slots <= max_per_sm ? tc.slots : max_per_sm;
+  const int64_t slots = (int64_t)per_sm * sms;
+  if (p.small) {
+    p.sk = (p.max_tiles < 2 * slots && p.kst > 1) ? 1 : 0;
+  } else {
     // UMMA kernel: Stream-K when the tiles fill less than half a wave of SMs (the split then pays for its partial
     // sums and their reduction) or more than one wave but less than two (it evens out the second wave); one
     // partial wave runs whole tiles (measured: 112 INT4 tiles of 256 tokens 36 -> 29 us, 128 NVFP4 tiles of 256
     // tokens 33 -> 21 us).
     p.sk = (p.kst > 1 && (2 * tiles_est < sms || (tiles_est > sms && tiles_est < 2 * (int64_t)sms))) ? 1 : 0;
-    const int64_t W = p.max_tiles * (p.sk ? p.kst : 1);
-    p.grid = (int)(W < sms ? (W < 1 ? 1 : W) : sms);
+  }
+  if (tc.sk >= 0) p.sk = (tc.sk && p.kst > 1) ? 1 : 0;
+  const int64_t W = p.max_tiles * (p.sk ? p.kst : 1);
+  p.grid = (int)(W < slots ? (W < 1 ? 1 : W) : slots);
+  // MoE activations: grouped when tiles are wide (tile::gather4 cannot feed 64+ routed rows per stage fast enough)
+  if (moe) {
+    const int fm = forced_moe_path();
+    p.grouped = fm == 2 ? 1 : (fm == 1 ? 0 : (tc.grouped >= 0 ? (tc.grouped ? 1 : 0) : (p.bt >= 64 ? 1 : 0)));
+    // small MoE calls on the register-decode kernel route inside it (at most 512 routed rows: its shared-memory
+    // lists)
+    p.fused = (p.small && !p.grouped && rows <= 512 && !getenv("HQ_ROUTE_KERNEL")) ? 1 : 0;
   }
   // Stream-K partial sums first, right after the header: the register-decode kernel tags each of its values with
   // the call's epoch, and the fixed place keeps other tables of other calls on the same workspace out of its slots
@@ -246,11 +269,7 @@ Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int
     off = align256(off + sizeof(int) * (size_t)f->num_experts);
     p.off_region = off;
     off = align256(off + sizeof(int) * (size_t)(f->num_experts * (p.region_cap > 0 ? p.region_cap : 1)));
-    // Grouped when tiles are wide: tile::gather4 cannot feed 64+ routed rows per stage fast enough
-    const int fm = forced_moe_path();
-    p.grouped = fm == 2 ? 1 : (fm == 1 ? 0 : (p.bt >= 64 ? 1 : 0));
     if (p.grouped) {
-      const int64_t rows = M_or_T * topk;
       p.off_rowoff = off;
       off = align256(off + sizeof(int) * (size_t)(f->num_experts + 1));
       p.off_gact = off;
@@ -376,7 +395,7 @@ int32_t hq_kernels_per_call(const hq_format_t* fmt, int64_t M_or_T, int32_t topk
   if (check_format(fmt) != HQ_OK || M_or_T < 1 || topk < 1) return 0;
   const Plan p = make_plan(fmt, M_or_T, topk, moe != 0, num_sms());
   int32_t n = 1 + (p.sk && !p.small ? 1 : 0);  // GEMM (+ split-K reduction of the UMMA kernel)
-  if (moe) n += 1 + (p.grouped ? 1 : 0);  // routing (+ row permutation)
+  if (moe) n += (p.fused ? 0 : 1) + (p.grouped ? 1 : 0);  // routing (+ row permutation), unless fused
   if (moe == 2) n += 1;                    // combine: rounding of the summed token rows
   return n;
 }
@@ -429,6 +448,9 @@ hq_status_t hq_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* packe
   a.status = reinterpret_cast<int*>(ws);
   a.partials = p.sk ? reinterpret_cast<float*>(ws + p.off_partials) : nullptr;
   a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  // weights read once per call (one token tile): evict-first in L2, so that they do not push out the kernel code,
+  // activations and partial sums that the next call needs
+  a.w_evict_first = (p.small || p.m_tiles == 1) ? 1 : 0;
   return cuda_status(launch_path(p, a, (cudaStream_t)stream));
 }
 
@@ -481,9 +503,11 @@ hq_status_t moe_call(const hq_format_t* fmt, const hq_act_t* A, const void* pack
   float* comb = combine ? reinterpret_cast<float*>(ws + comb_offset(p)) : nullptr;
   if (combine && cudaMemsetAsync(comb, 0, sizeof(float) * (size_t)(T * fmt->N), (cudaStream_t)stream) != cudaSuccess)
     return HQ_ERR_CUDA;
-  cudaError_t err =
-      launch_route(topk_ids, T * topk, (int)E, (int)p.region_cap, counts, region, status, (cudaStream_t)stream);
-  if (err != cudaSuccess) return HQ_ERR_CUDA;
+  cudaError_t err = cudaSuccess;
+  if (!p.fused) {
+    err = launch_route(topk_ids, T * topk, (int)E, (int)p.region_cap, counts, region, status, (cudaStream_t)stream);
+    if (err != cudaSuccess) return HQ_ERR_CUDA;
+  }
   if (p.grouped) {
     err = launch_moe_permute(counts, region, (int)p.region_cap, (int)E, a_div, T * topk, A->data,
                              (int)act_row_bytes(fmt), ws + p.off_gact,
@@ -517,12 +541,15 @@ hq_status_t moe_call(const hq_format_t* fmt, const hq_act_t* A, const void* pack
   a.comb_k = topk;
   a.counts = counts;
   a.region = region;
+  a.ids = p.fused ? topk_ids : nullptr;
+  a.fused_rows = p.fused ? (int)(T * topk) : 0;
   a.region_cap = (int)p.region_cap;
   a.m_tiles = 0;
   a.sk = p.sk;
   a.status = status;
   a.partials = p.sk ? reinterpret_cast<float*>(ws + p.off_partials) : nullptr;
   a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  a.w_evict_first = p.small;  // weights streamed once per call (tiles of one expert share them only at small T)
   err = launch_path(p, a, (cudaStream_t)stream);
   if (err != cudaSuccess || !combine) return cuda_status(err);
   return cuda_status(launch_combine_round(comb, T * fmt->N, static_cast<uint16_t*>(C), (cudaStream_t)stream));

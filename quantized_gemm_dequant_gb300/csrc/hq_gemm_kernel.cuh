@@ -81,7 +81,10 @@ struct GemmArgs {
                     // piece}; register-decode kernel [grid][BT][128] 64-bit (fp32 value, epoch) words
   float* comb;      // MoE combine: fp32 [T][N]; the output of routed row r is added into token r / comb_k (else null)
   int comb_k;
+  const int32_t* ids;  // register-decode kernel, routing fused: topk ids [rows] (else null: routing tables above)
+  int fused_rows;      // that many routed rows (T * topk)
   uint64_t wait_ns;  // bound of every pipeline wait (a wait that runs out records HQ_ERR_TIMEOUT)
+  int w_evict_first;  // weight copies marked evict-first in L2 (each block read once per call)
 };
 
 template <int PATH, int BT>
@@ -356,7 +359,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
           const uint8_t* wblk = args.w + ((int64_t)(pc.tile % args.n_tiles) * args.kst) * args.w_blk;
           for (int g = pc.g0; g < pc.g1 && npre < C::SW; ++g, ++npre) {
             mbar_arrive_expect_tx(&sh.w_full[npre], (uint32_t)args.w_blk);
-            bulk_g2s(wring + npre * C::W_STAGE, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk, &sh.w_full[npre]);
+            if (args.w_evict_first)
+              bulk_g2s_hint(wring + npre * C::W_STAGE, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk,
+                            &sh.w_full[npre], l2_evict_first_policy());
+            else
+              bulk_g2s(wring + npre * C::W_STAGE, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk,
+                       &sh.w_full[npre]);
           }
         });
     }
@@ -426,7 +434,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
               return;
             }
             mbar_arrive_expect_tx(&sh.w_full[ws], (uint32_t)args.w_blk);
-            bulk_g2s(wring + ws * C::W_STAGE, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk, &sh.w_full[ws]);
+            if (args.w_evict_first)
+              bulk_g2s_hint(wring + ws * C::W_STAGE, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk,
+                            &sh.w_full[ws], l2_evict_first_policy());
+            else
+              bulk_g2s(wring + ws * C::W_STAGE, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk, &sh.w_full[ws]);
           }
           ++armed[ws];
           if (++ws == C::SW) {

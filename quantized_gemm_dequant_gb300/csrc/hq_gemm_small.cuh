@@ -28,7 +28,9 @@
 // Warp roles (288 threads; two CTAs per SM up to 16-token tiles):
 //   warps 0-7  compute: warp (rg, kh) owns rows 32rg .. 32rg+31 of the 128-row
 //              tile as two 16-row MMA tiles and K half kh of every block; the
-//              two K halves meet in shared memory at the end of each piece.
+//              two K halves meet in shared memory at the end of each piece,
+//              after which warp (rg, kh) finishes 16-row half kh (fix-up
+//              polls and epilogue on all 8 warps).
 //              MMAs on 8-token column tiles that hold no token of the tile are
 //              predicated off.
 //   warp 8     producer (one thread): per block one bulk copy of the weights
@@ -55,6 +57,7 @@ namespace hq {
 constexpr int SM_THREADS = 288;
 constexpr int SM_PROD_WARP = 8;
 constexpr int SM_MAX_STAGES = 24;
+constexpr int SM_FUSED_ROWS = 512;  // routed rows up to which a MoE call routes inside this kernel
 
 // Per decode variant: bytes of a packed block and where its scales / zero points sit.
 template <int DEC>
@@ -70,16 +73,19 @@ struct SmallCfg {
   static constexpr int ACT_BYTES = 2 * BT * 128;         // two 64-K 128-byte-swizzled atoms (1 KB aligned)
   static constexpr int W_OFF = ACT_BYTES;                // then the weight block
   static constexpr int STAGE = ((ACT_BYTES + DecCfg<DEC>::BLK + 1023) / 1024) * 1024;
-  static constexpr int RING = CTAS_PER_SM == 2 ? 100 * 1024 : 196 * 1024;
+  static constexpr int RING = CTAS_PER_SM == 2 ? 96 * 1024 : 192 * 1024;
   static constexpr int STAGES = RING / STAGE > SM_MAX_STAGES ? SM_MAX_STAGES : RING / STAGE;
   static constexpr int NT = BT / 8;                          // 8-token MMA column tiles
-  static constexpr int RED_BYTES = 4 * 32 * 2 * NT * 4 * 4;  // K-half exchange: [rg][lane][m][nt][4] floats
+  static constexpr int FIX_G = BT == 8 ? 6 : 2;  // contributors polled together (Stream-K fix-up)
+  static constexpr int RED_BYTES = 4 * 2 * 32 * NT * 4 * 4;  // K-half exchange: [rg][kh][lane][nt][4] floats
   static constexpr int OFF_SH = STAGES * STAGE;
   static constexpr int OFF_PREFIX = OFF_SH + 1024;           // MoE tile prefix: E + 1 ints (E <= 512)
-  static constexpr int OFF_RED = OFF_PREFIX + 2112;
+  static constexpr int OFF_ROUTE = OFF_PREFIX + 2112;         // fused routing: row offsets [E + 1], rows [512]
+  static constexpr int OFF_RED = OFF_ROUTE + 2112 + 4 * SM_FUSED_ROWS;
   static constexpr int SMEM_BYTES = OFF_RED + RED_BYTES + 1024 /*alignment*/;
   static_assert(CTAS_PER_SM * (SMEM_BYTES + 1024) <= 228 * 1024, "CTAs per SM");
   static_assert(STAGES >= 4, "ring");
+  static_assert(RED_BYTES >= 1024 * 4, "fused routing scratch: 512 counts + 512 ids");
 };
 
 struct SmallSmem {
@@ -155,6 +161,70 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
   return __uint_as_float(b == 0u ? 0x00400000u : (b == 255u ? 0x7FC00000u : (b << 23)));
 }
 
+// Routing of a small MoE call, built by every CTA in its own shared memory: the routed rows (t * topk + j) grouped
+// by expert in increasing row order (a stable counting sort: the same lists in every CTA, which Stream-K needs, as
+// the pieces of one tile run on different CTAs).  off[e] .. off[e + 1] index expert e's rows in `rows`; cnt[e]
+// receives the counts (cnt: 1024 ints of scratch, the ids are staged in its upper half).  An id outside [0, E) routes
+// nothing and records HQ_ERR_BAD_ROUTING.  Every thread calls it.
+__device__ __forceinline__ void fused_route(const int32_t* ids, int nrows, int E, int* cnt, int* off, int* rows,
+                                            int* status) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  bool bad = false;
+  int* ids_s = cnt + 512;  // the ids, read from global memory once
+  for (int r = tid; r < nrows; r += blockDim.x) {
+    const int e = ids[r];
+    ids_s[r] = e;
+    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+    else bad = true;
+  }
+  if (bad) atomicCAS(status, 0, ERR_BAD_ROUTING);
+  __syncthreads();
+  if (tid < 32) {  // exclusive scan of the counts (one warp), then cnt becomes each expert's insertion cursor
+    const int per = (E + 31) / 32;
+    int run = 0;
+    for (int i = 0; i < per; ++i)
+      if (lane * per + i < E) run += cnt[lane * per + i];
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int acc = incl - run;
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e < E) {
+        off[e] = acc;
+        acc += cnt[e];
+        cnt[e] = off[e];
+      }
+    }
+    if (lane == 31) off[E] = incl;
+    __syncwarp();
+    // rows in increasing order, 32 at a time: rank within the chunk among lanes of the same expert
+    for (int r0 = 0; r0 < nrows; r0 += 32) {
+      const int r = r0 + lane;
+      const int e = r < nrows ? ids_s[r] : -1;
+      const bool valid = e >= 0 && e < E;
+      const unsigned same = __match_any_sync(0xffffffffu, valid ? e : -1);
+      const int rank = __popc(same & ((1u << lane) - 1u));
+      const int base = valid ? cnt[e] : 0;
+      __syncwarp();
+      if (valid) rows[base + rank] = r;
+      if (valid && rank == __popc(same) - 1) cnt[e] = base + rank + 1;  // the group's last lane moves the cursor
+      __syncwarp();
+    }
+    // restore the counts
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e < E) cnt[e] = off[e + 1] - off[e];
+    }
+  }
+  __syncthreads();
+}
+
 template <int BT, int DEC>
 __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT, DEC>::CTAS_PER_SM)
     hq_gemm_small_kernel(const __grid_constant__ GemmArgs args) {
@@ -192,8 +262,12 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT, DEC>::CTAS_PER_SM)
           const uint8_t* wblk = args.w + ((int64_t)(pc.tile % args.n_tiles) * args.kst) * args.w_blk;
           for (int g = pc.g0; g < pc.g1 && npre < C::STAGES; ++g, ++npre) {
             mbar_arrive_expect_tx(&sh.full[npre], (uint32_t)args.w_blk + C::ACT_BYTES);
-            bulk_g2s(smem + npre * C::STAGE + C::W_OFF, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk,
-                     &sh.full[npre]);
+            if (args.w_evict_first)
+              bulk_g2s_hint(smem + npre * C::STAGE + C::W_OFF, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk,
+                            &sh.full[npre], l2_evict_first_policy());
+            else
+              bulk_g2s(smem + npre * C::STAGE + C::W_OFF, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk,
+                       &sh.full[npre]);
             pre_x[npre] = g * 128;
             pre_y[npre] = (pc.tile / args.n_tiles) * BT;
           }
@@ -205,9 +279,20 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT, DEC>::CTAS_PER_SM)
   // tiles depend on the routing tables, so MoE calls wait here; dense calls set everything up first and wait only
   // where they first touch such memory: the producer before its activation loads, the compute warps before their
   // first epilogue, every thread before the exit count.
+  // fused routing: the CTA's own copy of the per-expert row lists (counts in the red area until the prefix is
+  // taken: the exchange buffer is not in use yet)
+  int* r_off = reinterpret_cast<int*>(smem + C::OFF_ROUTE);
+  int* r_rows = r_off + 528;
+  const bool fused = args.ids != nullptr;
   if (args.moe) {
     pdl_wait();
-    moe_tile_prefix(args.counts, args.E, args.region_cap, BT, prefix, &sh.tile_prefix_total);
+    const int* counts = args.counts;
+    if (fused) {
+      int* cnt = reinterpret_cast<int*>(smem + C::OFF_RED);
+      fused_route(args.ids, args.fused_rows, args.E, cnt, r_off, r_rows, args.status);
+      counts = cnt;
+    }
+    moe_tile_prefix(counts, args.E, args.region_cap, BT, prefix, &sh.tile_prefix_total);
   }
   __syncthreads();
   if (producer) {
@@ -230,12 +315,16 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT, DEC>::CTAS_PER_SM)
     pdl_wait();
     atomicCAS(args.status, 0, code);
   };
+  // routed row (t * topk + j) number i of expert e
+  auto routed_row = [&](int e, int i) -> int {
+    return fused ? r_rows[r_off[e] + i] : args.region[(int64_t)e * args.region_cap + i];
+  };
   auto tile_rows = [&](int tile, int& e, int& row0, int& nrows) {
     const int mt = tile / args.n_tiles;
     if (args.moe) {
       int lm;
       moe_locate(prefix, args.E, mt, e, lm);
-      int cnt = args.counts[e];
+      int cnt = fused ? r_off[e + 1] - r_off[e] : args.counts[e];
       cnt = cnt > args.region_cap ? args.region_cap : cnt;
       row0 = lm * BT;
       nrows = cnt - row0 < BT ? cnt - row0 : BT;
@@ -265,7 +354,7 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT, DEC>::CTAS_PER_SM)
         int rows_tok[BT];  // MoE indexed: token of each row of the tile; rows past the expert's count read zeros
         if (args.moe && !args.grouped)
           for (int i = 0; i < BT; ++i)
-            rows_tok[i] = i < nrows ? args.region[(int64_t)e * args.region_cap + row0 + i] / args.topk : args.M;
+            rows_tok[i] = i < nrows ? routed_row(e, row0 + i) / args.topk : args.M;
         const uint8_t* wblk = args.w + e * args.w_expert_bytes + ((int64_t)nt * args.kst) * args.w_blk;
         for (int g = pc.g0; g < pc.g1; ++g, ++blk) {
           uint8_t* act = smem + st * C::STAGE;
@@ -276,7 +365,11 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT, DEC>::CTAS_PER_SM)
               return;
             }
             mbar_arrive_expect_tx(&sh.full[st], (uint32_t)args.w_blk + C::ACT_BYTES);
-            bulk_g2s(act + C::W_OFF, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk, &sh.full[st]);
+            if (args.w_evict_first)
+              bulk_g2s_hint(act + C::W_OFF, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk, &sh.full[st],
+                            l2_evict_first_policy());
+            else
+              bulk_g2s(act + C::W_OFF, wblk + (int64_t)g * args.w_blk, (uint32_t)args.w_blk, &sh.full[st]);
             if (!args.moe || args.grouped) {
 #pragma unroll
               for (int j = 0; j < 2; ++j)
@@ -385,9 +478,9 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT, DEC>::CTAS_PER_SM)
           const int col = i * 8 + 2 * t4 + u;
           int orow = -1;
           float f = 1.0f;
-          if (kh == 0 && col < nrows) {
+          if (col < nrows) {
             if (args.moe) {
-              orow = args.region[(int64_t)e * args.region_cap + row0 + col];
+              orow = routed_row(e, row0 + col);
               if (args.topk_w) f = args.topk_w[orow];
             } else {
               orow = row0 + col;
@@ -514,139 +607,142 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT, DEC>::CTAS_PER_SM)
         ph ^= st == 0 ? 1u : 0u;
       }
       // ---------------------------------------------------- K halves meet
+      // Warp (rg, kh) finishes the 16-row half m = kh of its 32 rows: it hands the other half of its K-half sums to
+      // its partner (rg, kh ^ 1) and adds the partner's share of its own half, so that the fix-up polls and the
+      // epilogue run on all 8 warps.
       pdl_wait();  // (returns at once after the first piece) the epilogue touches global memory
-      float* mine = red + ((rg * 32 + lane) * 2) * (NT * 4);
-      if (kh == 1) {
+      float own[NT][4];
+      {
+        float* give = red + (((rg * 2 + kh) * 32 + lane) * NT) * 4;  // [rg][kh][lane][nt][4]
+        const float* take = red + (((rg * 2 + (kh ^ 1)) * 32 + lane) * NT) * 4;
 #pragma unroll
-        for (int m = 0; m < 2; ++m)
+        for (int i = 0; i < NT; ++i) {
 #pragma unroll
-          for (int i = 0; i < NT; ++i)
-            if (i < nn)
-              *reinterpret_cast<float4*>(mine + (m * NT + i) * 4) =
-                  make_float4(acc[m][i][0], acc[m][i][1], acc[m][i][2], acc[m][i][3]);
-      }
-      if (!epi_sync()) return;
-      if (kh == 0) {
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-#pragma unroll
-          for (int i = 0; i < NT; ++i)
-            if (i < nn) {
-              const float4 o = *reinterpret_cast<const float4*>(mine + (m * NT + i) * 4);
-              acc[m][i][0] += o.x;
-              acc[m][i][1] += o.y;
-              acc[m][i][2] += o.z;
-              acc[m][i][3] += o.w;
-            }
-        // this lane's element (m, i, 2 rr + u) sits at row 32 rg + 16 m + 8 rr + g8, token column 8 i + 2 t4 + u
-        auto slot_at = [&](int m, int i, int rr, int u) {
-          return (8 * i + 2 * t4 + u) * TILE_N + 32 * rg + 16 * m + 8 * rr + g8;
-        };
-        if (!pc.full) {
-          if (!mbar_wait(&sh.epoch_bar, 0, abort_flag, args.wait_ns)) {
-            fail(ERR_TIMEOUT);
-            ok = false;
-          }
+          for (int j = 0; j < 4; ++j) own[i][j] = kh ? acc[1][i][j] : acc[0][i][j];
+          if (i < nn)
+            *reinterpret_cast<float4*>(give + i * 4) = kh ? make_float4(acc[0][i][0], acc[0][i][1], acc[0][i][2], acc[0][i][3])
+                                                          : make_float4(acc[1][i][0], acc[1][i][1], acc[1][i][2], acc[1][i][3]);
         }
-        const uint64_t tag = (uint64_t)sh.epoch << 32;
-        if (ok && !pc.full && pc.g0 > 0) {
-          // the tile started in an earlier CTA: leave the partial sum, tagged with the call's epoch, in this
-          // CTA's slot
-          uint64_t* part = reinterpret_cast<uint64_t*>(args.partials) + (int64_t)blockIdx.x * BT * TILE_N;
+        if (!epi_sync()) return;
 #pragma unroll
-          for (int m = 0; m < 2; ++m)
+        for (int i = 0; i < NT; ++i)
+          if (i < nn) {
+            const float4 o = *reinterpret_cast<const float4*>(take + i * 4);
+            own[i][0] += o.x;
+            own[i][1] += o.y;
+            own[i][2] += o.z;
+            own[i][3] += o.w;
+          }
+      }
+      // this lane's element (i, 2 rr + u) sits at row 32 rg + 16 kh + 8 rr + g8, token column 8 i + 2 t4 + u
+      auto slot_at = [&](int i, int rr, int u) {
+        return (8 * i + 2 * t4 + u) * TILE_N + 32 * rg + 16 * kh + 8 * rr + g8;
+      };
+      if (!pc.full) {
+        if (!mbar_wait(&sh.epoch_bar, 0, abort_flag, args.wait_ns)) {
+          fail(ERR_TIMEOUT);
+          ok = false;
+        }
+      }
+      const uint64_t tag = (uint64_t)sh.epoch << 32;
+      if (ok && !pc.full && pc.g0 > 0) {
+        // the tile started in an earlier CTA: leave the partial sum, tagged with the call's epoch, in this CTA's slot
+        uint64_t* part = reinterpret_cast<uint64_t*>(args.partials) + (int64_t)blockIdx.x * BT * TILE_N;
 #pragma unroll
-            for (int i = 0; i < NT; ++i)
-              if (i < nn)
+        for (int i = 0; i < NT; ++i)
+          if (i < nn)
 #pragma unroll
-                for (int rr = 0; rr < 2; ++rr)
+            for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
-                  for (int u = 0; u < 2; ++u)
-                    st_relaxed_gpu_u64(part + slot_at(m, i, rr, u), tag | __float_as_uint(acc[m][i][2 * rr + u]));
-        } else if (ok) {
-          if (!pc.full) {
-            // this CTA holds the tile's first block: add the partial sums of the CTAs holding the rest, each value
-            // once its tag shows this call's epoch
-            const int64_t first_it = (int64_t)pc.tile * sched.kst;
-            const int c_last = sched.cta_of(first_it + sched.kst - 1);
-            for (int c2 = (int)blockIdx.x + 1; ok && c2 <= c_last; ++c2) {
-              const uint64_t* part = reinterpret_cast<const uint64_t*>(args.partials) + (int64_t)c2 * BT * TILE_N;
-              long long t0 = 0;
-              for (int tries = 0;; ++tries) {
-                float v[2][NT][4];
+              for (int u = 0; u < 2; ++u)
+                st_relaxed_gpu_u64(part + slot_at(i, rr, u), tag | __float_as_uint(own[i][2 * rr + u]));
+      } else if (ok) {
+        if (!pc.full) {
+          // this CTA holds the tile's first block: add the partial sums of the CTAs holding the rest, each value once
+          // its tag shows this call's epoch.  Contributors are polled FIX_G at a time with all their loads in flight
+          // together (one L2 round trip per group instead of one per contributor).
+          const int64_t first_it = (int64_t)pc.tile * sched.kst;
+          const int c_last = sched.cta_of(first_it + sched.kst - 1);
+          for (int cb = (int)blockIdx.x + 1; ok && cb <= c_last; cb += C::FIX_G) {
+            const int ng = c_last - cb + 1 < C::FIX_G ? c_last - cb + 1 : C::FIX_G;
+            uint32_t done = 0;  // contributor cb + j added (bit j; warp-uniform)
+            long long t0 = 0;
+            for (int tries = 0;; ++tries) {
+              uint64_t x[C::FIX_G][NT][4];
+#pragma unroll
+              for (int j = 0; j < C::FIX_G; ++j) {
+                const bool want = j < ng && !((done >> j) & 1u);
+                const uint64_t* part =
+                    reinterpret_cast<const uint64_t*>(args.partials) + (int64_t)(cb + j) * BT * TILE_N;
+#pragma unroll
+                for (int i = 0; i < NT; ++i)
+#pragma unroll
+                  for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+                      x[j][i][2 * rr + u] = (want && i < nn) ? ld_relaxed_gpu_u64(part + slot_at(i, rr, u)) : tag;
+              }
+#pragma unroll
+              for (int j = 0; j < C::FIX_G; ++j) {
+                if (j >= ng || ((done >> j) & 1u)) continue;
                 bool mine_ok = true;
 #pragma unroll
-                for (int m = 0; m < 2; ++m)
+                for (int i = 0; i < NT; ++i)
+#pragma unroll
+                  for (int q = 0; q < 4; ++q) mine_ok = mine_ok && (x[j][i][q] >> 32) == (tag >> 32);
+                if (__all_sync(0xffffffffu, mine_ok)) {
 #pragma unroll
                   for (int i = 0; i < NT; ++i)
 #pragma unroll
-                    for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-                      for (int u = 0; u < 2; ++u) {
-                        v[m][i][2 * rr + u] = 0.0f;
-                        if (i < nn) {
-                          const uint64_t x = ld_relaxed_gpu_u64(part + slot_at(m, i, rr, u));
-                          mine_ok = mine_ok && (x >> 32) == (tag >> 32);
-                          v[m][i][2 * rr + u] = __uint_as_float((uint32_t)x);
-                        }
-                      }
-                if (__all_sync(0xffffffffu, mine_ok)) {
-#pragma unroll
-                  for (int m = 0; m < 2; ++m)
-#pragma unroll
-                    for (int i = 0; i < NT; ++i)
-#pragma unroll
-                      for (int j = 0; j < 4; ++j) acc[m][i][j] += v[m][i][j];
-                  break;
+                    for (int q = 0; q < 4; ++q) own[i][q] += __uint_as_float((uint32_t)x[j][i][q]);
+                  done |= 1u << j;
                 }
-                if (tries == 0) {
-                  t0 = clock64();
-                } else if (clock64() - t0 >= 3ll * (long long)args.wait_ns || *abort_flag) {
-                  fail(ERR_TIMEOUT);
-                  ok = false;
-                  break;
-                }
-                __nanosleep(64);
               }
+              if (done == (1u << ng) - 1u) break;
+              if (tries == 0) {
+                t0 = clock64();
+              } else if (clock64() - t0 >= 3ll * (long long)args.wait_ns || *abort_flag) {
+                fail(ERR_TIMEOUT);
+                ok = false;
+                break;
+              }
+              __nanosleep(64);
             }
           }
-          if (ok) {
-            // ---------------------------------------------------- epilogue
-            const bool pair_ok = !args.comb && (args.N & 1) == 0 && (reinterpret_cast<uintptr_t>(args.c) & 3) == 0;
-            const bool odd = g8 & 1;
+        }
+        if (ok) {
+          // ---------------------------------------------------- epilogue
+          const bool pair_ok = !args.comb && (args.N & 1) == 0 && (reinterpret_cast<uintptr_t>(args.c) & 3) == 0;
+          const bool odd = g8 & 1;
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
+          for (int rr = 0; rr < 2; ++rr) {
+            const int n = nt * TILE_N + 32 * rg + 16 * kh + 8 * rr + g8;
+            const float bias = (args.bias && n < args.N) ? bf16_to_f32(args.bias[n]) : 0.0f;
 #pragma unroll
-              for (int rr = 0; rr < 2; ++rr) {
-                const int n = nt * TILE_N + 32 * rg + 16 * m + 8 * rr + g8;
-                const float bias = (args.bias && n < args.N) ? bf16_to_f32(args.bias[n]) : 0.0f;
+            for (int i = 0; i < NT; ++i) {
+              if (i >= nn) continue;
+              const float o0 = own[i][2 * rr] * t_mul[i][0] + bias;
+              const float o1 = own[i][2 * rr + 1] * t_mul[i][1] + bias;
+              if (pair_ok) {
+                // lanes g8 and g8 ^ 1 hold rows n and n ^ 1: the even lane writes token column 2t (rows n, n + 1),
+                // the odd lane token column 2t + 1 (rows n - 1, n), one 4-byte store each
+                const float send = odd ? o0 : o1;
+                const float recv = __shfl_xor_sync(0xffffffffu, send, 4);
+                const int orow = odd ? t_row[i][1] : t_row[i][0];
+                const int n_even = n & ~1;
+                const uint32_t pk = odd ? pack_bf16x2(recv, o1) : pack_bf16x2(o0, recv);
+                if (orow >= 0 && n_even < args.N)
+                  *reinterpret_cast<uint32_t*>(args.c + (int64_t)orow * args.N + n_even) = pk;
+              } else if (n < args.N) {
+                const float o[2] = {o0, o1};
 #pragma unroll
-                for (int i = 0; i < NT; ++i) {
-                  if (i >= nn) continue;
-                  const float o0 = acc[m][i][2 * rr] * t_mul[i][0] + bias;
-                  const float o1 = acc[m][i][2 * rr + 1] * t_mul[i][1] + bias;
-                  if (pair_ok) {
-                    // lanes g8 and g8 ^ 1 hold rows n and n ^ 1: the even lane writes token column 2t (rows n,
-                    // n + 1), the odd lane token column 2t + 1 (rows n - 1, n), one 4-byte store each
-                    const float send = odd ? o0 : o1;
-                    const float recv = __shfl_xor_sync(0xffffffffu, send, 4);
-                    const int orow = odd ? t_row[i][1] : t_row[i][0];
-                    const int n_even = n & ~1;
-                    const uint32_t pk = odd ? pack_bf16x2(recv, o1) : pack_bf16x2(o0, recv);
-                    if (orow >= 0 && n_even < args.N)
-                      *reinterpret_cast<uint32_t*>(args.c + (int64_t)orow * args.N + n_even) = pk;
-                  } else if (n < args.N) {
-                    const float o[2] = {o0, o1};
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                      const int orow = t_row[i][u];
-                      if (orow < 0) continue;
-                      if (args.comb)  // MoE combine: add into the token's fp32 row
-                        red_add_f32(args.comb + (int64_t)(orow / args.comb_k) * args.N + n, o[u]);
-                      else
-                        args.c[(int64_t)orow * args.N + n] = f32_to_bf16(o[u]);
-                    }
-                  }
+                for (int u = 0; u < 2; ++u) {
+                  const int orow = t_row[i][u];
+                  if (orow < 0) continue;
+                  if (args.comb)  // MoE combine: add into the token's fp32 row
+                    red_add_f32(args.comb + (int64_t)(orow / args.comb_k) * args.N + n, o[u]);
+                  else
+                    args.c[(int64_t)orow * args.N + n] = f32_to_bf16(o[u]);
                 }
               }
             }

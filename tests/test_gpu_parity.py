@@ -361,3 +361,16 @@ def test_degenerate_groups(lib, wfmt):
     inp["w"] = W.quantize_weights(c["wfmt"], w, c["G"])
     assert float(inp["w"]["scales"].float()[:, 0].abs().max()) == 0.0
     R.assert_parity(_run_dense(lib, inp), R.dense_ref(inp), f"{wfmt} degenerate groups")
+
+
+@pytest.mark.parametrize("route", ["fused", "kernel"])
+@pytest.mark.parametrize("T", [1, 4, 60])
+def test_moe_small_routing_in_kernel_and_by_routing_kernel(lib, monkeypatch, route, T):
+    """Small MoE calls (at most 512 routed rows) route inside the register-decode kernel: every CTA builds the same
+    per-expert row lists in shared memory.  Both that and the separate routing kernel match the oracle."""
+    if route == "kernel":
+        monkeypatch.setenv("HQ_ROUTE_KERNEL", "1")
+    inp = make_moe(MOE_FORMS["int4_sym"], T, seed=T + 40, E=64, N=384, K=1024, topk=8)  # <= 16 rows per expert
+    fmt, packed = lib.pack_inputs(inp, "cuda")
+    assert lib.kernels_per_call(fmt, T, 8, moe=True) == (1 if route == "fused" else 2)
+    R.assert_parity(_run_moe(lib, inp), R.moe_ref(inp), f"moe routing {route} T={T}")
