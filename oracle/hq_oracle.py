@@ -24,8 +24,8 @@ operands of the W4A8 and W4A4 paths ("Selecting activation types"; section
 
 Conventions (the pages are silent on them): 4-bit codes are two per byte with
 the low nibble holding the even k, 2-bit codes four per byte from the lowest
-bits up, 8-bit codes one per byte; W is [N, K] ("out, in"); scale groups run
-along K.
+bits up, 1- and 3-bit codes as a little-endian bit string, 8-bit codes one per
+byte; W is [N, K] ("out, in"); scale groups run along K.
 """
 import numpy as np
 
@@ -103,9 +103,21 @@ def unpack_crumbs(packed):
     return out
 
 
+def unpack_bits(packed, bits):
+    """[..., K*bits/8] bytes -> [..., K] codes of `bits` bits from a little-endian bit string: code k occupies bits
+    k*bits .. k*bits + bits - 1 of the row, bit j of the string being bit j % 8 of byte j // 8."""
+    p = np.asarray(packed).astype(np.uint8)
+    stream = np.unpackbits(p, axis=-1, bitorder="little")
+    k = stream.shape[-1] // bits
+    stream = stream[..., : k * bits].reshape(p.shape[:-1] + (k, bits)).astype(np.int64)
+    weights = np.int64(1) << np.arange(bits, dtype=np.int64)
+    return (stream * weights).sum(axis=-1).astype(np.uint8)
+
+
 # ---------------------------------------------------------------- tensor formats
 
-WEIGHT_FORMATS = ("int4_sym", "uint4_zp", "nvfp4", "mxfp4", "int8_sym", "uint2_zp", "mxint4", "e4m3")
+WEIGHT_FORMATS = ("int4_sym", "uint4_zp", "nvfp4", "mxfp4", "int8_sym", "uint2_zp", "mxint4", "e4m3", "uint1_zp",
+                  "uint3_zp")
 ACT_FORMATS = ("bf16", "e4m3_tok", "nvfp4", "mxfp8")
 BLOCK = {"nvfp4": 16, "mxfp4": 32, "mxint4": 32, "mxfp8": 32}
 
@@ -122,7 +134,18 @@ def dequant_weights(wfmt, codes, scales, zeros=None, gscale=None, group=128):
     uint2_zp : value = (q - z) * s, q and z in [0, 3], q four per byte (see unpack_crumbs), s bf16 per (n, group)
     mxint4   : value = q * e8m0(sb), q two's complement nibbles in [-7, 7], sb per (n, 32 along K)
     e4m3     : value = e4m3(q) * s, q one OCP OFP8 E4M3 byte, s bf16 per (n, group)
+    uint1_zp : value = (q - z) * s, q and z in {0, 1}, q eight per byte (see unpack_bits), s bf16 per (n, group)
+    uint3_zp : value = (q - z) * s, q and z in [0, 7], q a 3-bit little-endian bit string (see unpack_bits), s bf16
+               per (n, group); the INT1 / INT3 widths of "Results: kernel microbenchmarks" read as the GPTQ-style
+               unsigned codes with integer zero points that the GPTQ INT3 checkpoints of "vLLM integration" hold
     """
+    if wfmt in ("uint1_zp", "uint3_zp"):
+        bits = 1 if wfmt == "uint1_zp" else 3
+        q = unpack_bits(codes, bits)
+        k = q.shape[-1]
+        s = np.repeat(decode_bf16(scales), group, axis=-1)[..., :k]
+        zq = np.repeat(np.asarray(zeros).astype(np.float64), group, axis=-1)[..., :k]
+        return (decode_int(q, bits, False) - zq) * s
     if wfmt in ("int8_sym", "e4m3"):
         q = np.asarray(codes).astype(np.uint8)
         k = q.shape[-1]

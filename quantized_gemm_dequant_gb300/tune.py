@@ -52,13 +52,14 @@ PLANS = [
 ]
 
 
-def candidates(cls, moe, M):
-    """Every valid choice for one call size (the library also re-checks each)."""
+def candidates(cls, moe, key):
+    """Every valid choice for one call (the library also re-checks each); key = M (dense) or routed rows per expert
+    (MoE)."""
     out = [dict(AUTO)]
-    umma_bts = [b for b in (16, 32, 64, 128, 256) if b < 2 * max(M, 8)]
+    umma_bts = [b for b in (16, 32, 64, 128, 256) if b < 2 * max(key, 8)]
     if moe and cls in ("nvfp4", "mxfp4a"):
         umma_bts = [b for b in umma_bts if b <= 128]
-    if cls in ("int4", "regdec") and M <= 256:
+    if cls == "regdec" or (cls == "int4" and key <= (64 if moe else 256)):
         for bt in (8, 16, 32):
             for sk in (0, 1):
                 for slots in ((1, 2) if bt <= 16 else (1,)):
@@ -154,7 +155,9 @@ def sweep(plans, quick, dev):
             run, topk = calls[M]
             t_auto, y_auto = time_choice(fmt, run, M, topk, R, AUTO, bursts, per_burst)
             rows = []
-            for c in candidates(cls, moe, M):
+            c_cfg = W.CONFIGS[cfg]
+            key = -(-M * c_cfg["topk"] // c_cfg["E"]) if moe else M
+            for c in candidates(cls, moe, key):
                 t, y = (t_auto, y_auto) if c == AUTO else time_choice(fmt, run, M, topk, R, c, bursts, per_burst)
                 ok = t is not None and close(y, y_auto)
                 rows.append(dict(choice=c, ms=t, ok=ok))

@@ -303,12 +303,44 @@ def pin_crumbs(o, rng=None):
     assert o.unpack_crumbs(np.array([0b11100100], np.uint8)).tolist() == [0, 1, 2, 3]
 
 
+def pack_bits_loop(q, bits):
+    """Independent packer of `bits`-bit codes into a little-endian bit string: bit j of code k goes to bit
+    (k * bits + j) % 8 of byte (k * bits + j) // 8."""
+    q = np.asarray(q)
+    K = q.shape[-1]
+    out = np.zeros(q.shape[:-1] + (K * bits // 8,), dtype=np.uint8)
+    for idx in np.ndindex(q.shape[:-1]):
+        for k in range(K):
+            for j in range(bits):
+                if (int(q[idx + (k,)]) >> j) & 1:
+                    pos = k * bits + j
+                    out[idx + (pos // 8,)] |= np.uint8(1 << (pos % 8))
+    return out
+
+
+def pin_bits(o, rng=None):
+    """1- and 3-bit code order: the oracle's unpacking inverts an independent loop packer; hand-made bytes decode as
+    written (0b10110001 -> k = 0..7 hold 1, 0, 0, 0, 1, 1, 0, 1; the 3-bit codes 5, 3, 6, 1, 0, 7, 2, 4 written by
+    hand, lowest bit first, fill the bytes 0b10011101, 0b10000011, 0b10001011), and 2-bit codes agree with the
+    crumb order."""
+    rng = rng or np.random.default_rng(13)
+    for bits in (1, 2, 3):
+        q = rng.integers(0, 1 << bits, size=(3, 48))
+        assert np.array_equal(o.unpack_bits(pack_bits_loop(q, bits), bits), q)
+    assert o.unpack_bits(np.array([0b10110001], np.uint8), 1).tolist() == [1, 0, 0, 0, 1, 1, 0, 1]
+    # codes 5, 3, 6, 1, 0, 7, 2, 4: bit string (LSB first) 101 110 011 100 000 111 010 001
+    packed = np.array([0b10011101, 0b10000011, 0b10001011], np.uint8)
+    assert o.unpack_bits(packed, 3).tolist() == [5, 3, 6, 1, 0, 7, 2, 4]
+    q2 = rng.integers(0, 4, size=(2, 32))
+    assert np.array_equal(o.unpack_bits(pack_crumbs_loop(q2), 2), o.unpack_crumbs(pack_crumbs_loop(q2)))
+
+
 def _int_bf16(a):
     return np.vectorize(lambda v: np.float32(v).view(np.uint32) >> 16)(a).astype(np.uint16)
 
 
 def pin_exact_more_formats(o, rng=None):
-    """INT8 (e0m7 codes), UINT2 with zero points and MXINT4 with integer activations and power-of-two scales equal
+    """INT8 (e0m7 codes), UINT1 / UINT2 / UINT3 with zero points and MXINT4 with integer activations and power-of-two scales equal
     integer arithmetic; FP8 E4M3 weights equal torch's float8_e4m3fn decoder times a power-of-two scale; MXFP8
     activations equal the generic minifloat decoder times their e8m0 block scale (Fraction sums)."""
     rng = rng or np.random.default_rng(12)
@@ -332,6 +364,11 @@ def pin_exact_more_formats(o, rng=None):
     z2 = rng.integers(0, 4, size=(N, K // G))
     check(o.dequant_weights("uint2_zp", pack_crumbs_loop(q2), scales, zeros=z2.astype(np.uint8), group=G),
           (q2 - np.repeat(z2, G, axis=-1)) * pw)
+    for bits, wf in ((1, "uint1_zp"), (3, "uint3_zp")):
+        qb = rng.integers(0, 1 << bits, size=(N, K))
+        zb = rng.integers(0, 1 << bits, size=(N, K // G))
+        check(o.dequant_weights(wf, pack_bits_loop(qb, bits), scales, zeros=zb.astype(np.uint8), group=G),
+              (qb - np.repeat(zb, G, axis=-1)) * pw)
     q4 = rng.integers(-7, 8, size=(N, K))
     je = rng.integers(-9, 5, size=(N, K // 32))
     check(o.dequant_weights("mxint4", pack_nibbles_loop(q4 & 0xF), (je + 127).astype(np.uint8)),
@@ -489,5 +526,5 @@ def pin_swiglu(o):
 
 
 ALL_PINS = [pin_e4m3, pin_e8m0, pin_e2m1, pin_bf16, pin_int4, pin_e0m_equivalence, pin_exact_int4,
-            pin_exact_fp4, pin_crumbs, pin_exact_more_formats, pin_library_special_case, pin_brute_force, pin_moe_reduces_to_dense, pin_encode_e4m3,
+            pin_exact_fp4, pin_crumbs, pin_bits, pin_exact_more_formats, pin_library_special_case, pin_brute_force, pin_moe_reduces_to_dense, pin_encode_e4m3,
             pin_encode_e2m1, pin_act_quant_e4m3, pin_act_quant_nvfp4, pin_moe_combine, pin_swiglu]

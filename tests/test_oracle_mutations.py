@@ -63,6 +63,11 @@ MUTATIONS = {
     "mxint4_unsigned": ("return decode_int(q, 4, True) * sb", "return decode_int(q, 4, False) * sb"),
     "e4m3_weight_scale_dropped": ("else decode_e4m3(q)) * s", "else decode_e4m3(q)) * (s if wfmt == 'int8_sym' else 1.0)"),
     "mxfp8_scale_dropped": ("return decode_e4m3(q) * sb", "return decode_e4m3(q)"),
+    "bit_string_msb_first": ('stream = np.unpackbits(p, axis=-1, bitorder="little")', 'stream = np.unpackbits(p, axis=-1, bitorder="big")'),
+    "bit_weights_reversed": ("weights = np.int64(1) << np.arange(bits, dtype=np.int64)",
+                             "weights = np.int64(1) << np.arange(bits, dtype=np.int64)[::-1]"),
+    "uint3_zero_point_dropped": ("return (decode_int(q, bits, False) - zq) * s", "return decode_int(q, bits, False) * s"),
+    "uint3_as_signed": ("return (decode_int(q, bits, False) - zq) * s", "return (decode_int(q, bits, True) - zq) * s"),
     "act_nvfp4_nibbles": ("packed = (q[:, 0::2] | (q[:, 1::2] << 4))", "packed = (q[:, 1::2] | (q[:, 0::2] << 4))"),
 }
 

@@ -30,10 +30,12 @@ def test_rows_merge_and_keep_order(tmp_path, monkeypatch):
 
 def test_candidates_are_valid():
     from quantized_gemm_dequant_gb300 import tune
-    for cls, _, moe, buckets in tune.PLANS:
+    for cls, cfg, moe, buckets in tune.PLANS:
         for _, sizes in buckets:
             for M in sizes:
-                for c in tune.candidates(cls, moe, M):
+                c_cfg = tune.W.CONFIGS[cfg]
+                key = -(-M * c_cfg["topk"] // c_cfg["E"]) if moe else M
+                for c in tune.candidates(cls, moe, key):
                     assert c["bt"] in (0, 8, 16, 32, 64, 128, 256)
                     if c["kernel"] == 1:
                         assert c["bt"] <= 32 and (c["slots"] <= 1 or c["bt"] <= 16)

@@ -43,3 +43,24 @@ def test_dense_and_moe_shapes():
     m = configs.make_moe("moe_mxfp4", 5, E=4, N=64, K=256)
     assert m["w"]["codes"].shape == (4, 64, 128) and m["w"]["scales"].shape == (4, 64, 8)
     assert m["a"]["data"].dtype == torch.uint8 and m["a"]["scale"].shape == (5,)
+
+
+def test_bit_string_packer_matches_the_loop_packer():
+    """The recipe's 1/2/3-bit packer writes the same bytes as the pins' independent loop packer."""
+    import numpy as np
+
+    from tests.pins import pack_bits_loop
+    from workload import quant
+    g = torch.Generator().manual_seed(3)
+    for bits in (1, 2, 3):
+        q = torch.randint(0, 1 << bits, (3, 64), generator=g, dtype=torch.uint8)
+        assert np.array_equal(quant.pack_bits(q, bits).numpy(), pack_bits_loop(q.numpy(), bits))
+    q2 = torch.randint(0, 4, (2, 32), generator=g, dtype=torch.uint8)
+    assert torch.equal(quant.pack_bits(q2, 2), quant.pack_crumbs(q2))
+
+
+def test_uint1_uint3_shapes_and_ranges():
+    for wfmt, bits in (("uint1_zp", 1), ("uint3_zp", 3)):
+        d = configs.make_dense(dict(kind="dense", wfmt=wfmt, afmt="bf16", G=128), 2, N=64, K=256)
+        assert d["w"]["codes"].shape == (64, 256 * bits // 8)
+        assert d["w"]["zeros"].shape == (64, 2) and int(d["w"]["zeros"].max()) < (1 << bits)

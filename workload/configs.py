@@ -12,10 +12,10 @@ Sizes and recipes (quantized GEMM microbenchmarks of the Humming announcement,
               INT4 symmetric group 128, bf16 act
   moe_mxfp4   MoE, E=256, top-8, K=7168, N=4096, T in {1,64,1024,8192},
               MXFP4 weights, FP8 e4m3 per-token activations
-  w8a16, w2a16, mxint4_a16, fp8w_a16
+  w8a16, w2a16, w1a16, w3a16, mxint4_a16, fp8w_a16
               dense, K=4096, N=14336, M in {1,16,64,256}: INT8 (e0m7) g128,
-              UINT2 + zero point g128, MXINT4 (e8m0 per 32), FP8 E4M3 g128
-              weights, bf16 act
+              UINT2 / UINT1 / UINT3 + zero point g128, MXINT4 (e8m0 per 32),
+              FP8 E4M3 g128 weights, bf16 act
   w4a8_mx     dense, K=7168, N=4096, M in {1,128,1024,8192}: MXFP4 weights,
               MXFP8 activations (e4m3 + e8m0 per 32)
 
@@ -48,6 +48,8 @@ CONFIGS = {
     "w8a16": dict(kind="dense", wfmt="int8_sym", afmt="bf16", N=14336, K=4096, G=128, sizes=[1, 16, 64, 256]),
     "w2a16": dict(kind="dense", wfmt="uint2_zp", afmt="bf16", N=14336, K=4096, G=128, sizes=[1, 16, 64, 256]),
     "mxint4_a16": dict(kind="dense", wfmt="mxint4", afmt="bf16", N=14336, K=4096, G=32, sizes=[1, 16, 64, 256]),
+    "w1a16": dict(kind="dense", wfmt="uint1_zp", afmt="bf16", N=14336, K=4096, G=128, sizes=[1, 16, 64, 256]),
+    "w3a16": dict(kind="dense", wfmt="uint3_zp", afmt="bf16", N=14336, K=4096, G=128, sizes=[1, 16, 64, 256]),
     "fp8w_a16": dict(kind="dense", wfmt="e4m3", afmt="bf16", N=14336, K=4096, G=128, sizes=[1, 16, 64, 256]),
     "w4a8_mx": dict(kind="dense", wfmt="mxfp4", afmt="mxfp8", N=4096, K=7168, G=32, sizes=[1, 128, 1024, 8192]),
 }
@@ -88,6 +90,9 @@ def quantize_weights(wfmt, w, G):
         return dict(codes=c, scales=s)
     if wfmt == "uint2_zp":
         c, s, z = quant.quant_uint2_zp(w, G)
+        return dict(codes=c, scales=s, zeros=z)
+    if wfmt in ("uint1_zp", "uint3_zp"):
+        c, s, z = quant.quant_uint_zp(w, G, 1 if wfmt == "uint1_zp" else 3)
         return dict(codes=c, scales=s, zeros=z)
     if wfmt == "mxint4":
         c, s = quant.quant_mxint4(w)
@@ -189,6 +194,9 @@ def weight_bytes(wfmt, N, K, G, experts=1):
         return experts * (N * K + N * (K // G) * 2)
     if wfmt == "uint2_zp":
         return experts * (N * K // 4 + N * (K // G) * 2 + N * (K // G) // 4)  # zeros are 2-bit values
+    if wfmt in ("uint1_zp", "uint3_zp"):
+        b = 1 if wfmt == "uint1_zp" else 3
+        return experts * (N * K * b // 8 + N * (K // G) * 2 + N * (K // G) * b // 8)  # zeros are b-bit values
     if wfmt == "mxint4":
         return experts * (codes + N * (K // 32))
     if wfmt == "int4_sym":

@@ -18,6 +18,8 @@ public definition:
 * grouped UINT2 with zero point: scale = (max - min) / 3 in bf16, zero =
   clamp(rint(-min / scale), 0, 3), code = clamp(rint(w / scale) + zero, 0, 3),
   four codes per byte from the lowest bits up;
+* grouped UINT1 / UINT3 with zero point (GPTQ style, bits b): the UINT2 rule
+  with 2**b - 1 levels, codes as a little-endian bit string;
 * MXINT4 (e8m0 block-32 scale): 2**(floor(log2 amax_b) - 2) (4 = 2**2 is the
   largest power of two of the integer range, as for MXFP4), codes rint(w /
   scale) clamped to [-7, 7];
@@ -146,6 +148,32 @@ def pack_crumbs(codes):
     """[..., K] uint8 codes in 0..3 -> [..., K/4] bytes; bits 2i, 2i + 1 of byte b hold k = 4b + i."""
     c = codes.to(torch.uint8)
     return (c[..., 0::4] | (c[..., 1::4] << 2) | (c[..., 2::4] << 4) | (c[..., 3::4] << 6)).contiguous()
+
+
+def pack_bits(codes, bits):
+    """[..., K] uint8 codes of `bits` bits -> [..., K * bits / 8] bytes: a little-endian bit string (bit j of code k
+    is bit (k * bits + j) % 8 of byte (k * bits + j) // 8)."""
+    c = codes.to(torch.int64)
+    *lead, k = c.shape
+    bit = ((c.unsqueeze(-1) >> torch.arange(bits, device=c.device)) & 1).reshape(*lead, k * bits // 8, 8)
+    return (bit << torch.arange(8, device=c.device)).sum(dim=-1).to(torch.uint8).contiguous()
+
+
+def quant_uint_zp(w, group, bits):
+    """w fp32 [..., N, K] -> (bit-string codes [..., N, K*bits/8], scales bf16 [..., N, K/g], zeros uint8
+    [..., N, K/g]); GPTQ-style unsigned codes with an integer zero point, 2**bits - 1 levels."""
+    lv = float((1 << bits) - 1)
+    *lead, n, k = w.shape
+    wg = w.reshape(*lead, n, k // group, group)
+    lo = wg.amin(dim=-1)
+    hi = wg.amax(dim=-1)
+    s = ((hi - lo) / lv).to(torch.bfloat16)
+    sf = s.float()
+    safe = torch.where(sf > 0, sf, torch.ones_like(sf))
+    z = torch.where(sf > 0, _rint(-lo / safe), torch.zeros_like(sf)).clamp(0, lv)
+    q = torch.where(sf.unsqueeze(-1) > 0, _rint(wg / safe.unsqueeze(-1)) + z.unsqueeze(-1), torch.zeros_like(wg))
+    q = q.clamp(0, lv).to(torch.uint8).reshape(*lead, n, k)
+    return pack_bits(q, bits), s.contiguous(), z.to(torch.uint8).contiguous()
 
 
 def quant_int8_sym(w, group):
