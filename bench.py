@@ -37,7 +37,7 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # dense tensor-core peaks relative to bf16 (nominal 2.25 / 4.5 / 13.5 PFLOP/s)
 DTYPE_RATIO = {"bf16": 1.0, "fp8": 2.0, "fp4": 6.0}
 PATH_DTYPE = {"int4_sym": "bf16", "uint4_zp": "bf16", "nvfp4": "fp4", "mxfp4": "fp8", "int8_sym": "bf16",
-              "uint2_zp": "bf16", "mxint4": "bf16", "e4m3": "bf16"}
+              "uint2_zp": "bf16", "mxint4": "bf16", "e4m3": "bf16", "uint1_zp": "bf16", "uint3_zp": "bf16"}
 SPIN_CYCLES = 1_000_000  # about 0.5 ms at 2 GHz: longer than the host side of one burst of calls
 
 
@@ -218,7 +218,7 @@ def roofline_of(info, t_s, pk, dt):
 MIN_SAMPLES = 20       # samples per size (bursts, and isolated calls)
 MIN_SAMPLES_FAST = 100  # below 10 us per call
 OTHER_CONFIGS = ["w4a16_sym", "nvfp4", "moe_w4a16", "moe_mxfp4", "moe_w4a16_down", "moe_mxfp4_down", "w8a16", "w2a16",
-                 "mxint4_a16", "fp8w_a16", "w4a8_mx"]
+                 "w1a16", "w3a16", "mxint4_a16", "fp8w_a16", "w4a8_mx"]
 
 
 def _burst(call, n, R, stream, counter):
@@ -436,7 +436,8 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-DECODE_KIND = {"int4_sym": 0, "uint4_zp": 0, "mxint4": 1, "int8_sym": 2, "e4m3": 3, "uint2_zp": 4}
+DECODE_KIND = {"int4_sym": 0, "uint4_zp": 0, "mxint4": 1, "int8_sym": 2, "e4m3": 3, "uint2_zp": 4, "uint1_zp": 5,
+               "uint3_zp": 6}
 
 
 def kernel_name(cfg, M):

@@ -75,7 +75,9 @@ enum {
   HQ_W_INT8_SYM = 5, /* q in [-127, 127] one two's complement byte each (the e0m7 value set), bf16 scale per group */
   HQ_W_UINT2_ZP = 6, /* q, z in [0, 3], value (q - z) * s, four codes per byte, bf16 scale and zero per group */
   HQ_W_MXINT4 = 7,   /* q in [-7, 7] two's complement nibbles, e8m0 scale per 32 K */
-  HQ_W_E4M3 = 8      /* OCP FP8 E4M3 codes, one byte each, bf16 scale per group */
+  HQ_W_E4M3 = 8,     /* OCP FP8 E4M3 codes, one byte each, bf16 scale per group */
+  HQ_W_UINT1_ZP = 9, /* q, z in {0, 1}, value (q - z) * s, eight codes per byte, bf16 scale and zero per group */
+  HQ_W_UINT3_ZP = 10 /* q, z in [0, 7], value (q - z) * s, a 3-bit bit string, bf16 scale and zero per group */
 };
 /* Scale data types. */
 enum { HQ_S_BF16 = 1, HQ_S_UE4M3 = 2, HQ_S_UE8M0 = 3 };
@@ -97,9 +99,12 @@ enum {
  *   UINT2_ZP, group 128, BF16 scales,  zero,    no global, act BF16
  *   MXINT4,   group 32,  UE8M0 scales, no zero, no global, act BF16
  *   E4M3,     group 128, BF16 scales,  no zero, no global, act BF16
- * The last four are the other WnA16 widths and formats of "Results: kernel
- * microbenchmarks" (INT2, INT8 as the zero-exponent e0m7 of "Results:
- * quantization support", MXINT4, FP8); MXFP8 activations are the microscaled
+ *   UINT1_ZP, group 128, BF16 scales,  zero,    no global, act BF16
+ *   UINT3_ZP, group 128, BF16 scales,  zero,    no global, act BF16
+ * The last six are the other WnA16 widths and formats of "Results: kernel
+ * microbenchmarks" (INT1, INT2, INT3 as GPTQ-style unsigned codes with integer
+ * zero points, INT8 as the zero-exponent e0m7 of "Results: quantization
+ * support", MXINT4, FP8); MXFP8 activations are the microscaled
  * W4A8 variant of "W8A8 / W4A8 / W4A4".  Anything else returns
  * HQ_ERR_UNSUPPORTED. */
 typedef struct {
@@ -132,10 +137,13 @@ HQ_API size_t hq_packed_bytes(const hq_format_t* fmt);
  * compilation per workload", preprocessing paragraph: validate the parameters,
  * pad N to the 128-row tile, reorder codes, scales and zeros into tile order).
  *   codes        uint8 [E][N][K/2] (4-bit formats, low nibble = even k), [E][N][K]
- *                (INT8_SYM, E4M3) or [E][N][K/4] (UINT2_ZP, bits 2i..2i+1 of a byte
- *                hold its k = 4b + i)
+ *                (INT8_SYM, E4M3), [E][N][K/4] (UINT2_ZP, bits 2i..2i+1 of a byte
+ *                hold its k = 4b + i) or [E][N][K*b/8] (UINT1_ZP b = 1, UINT3_ZP b = 3:
+ *                a little-endian bit string, bit j of code k at bit position k*b + j
+ *                of the row, position p being bit p % 8 of byte p / 8)
  *   scales       [E][N][K/group] of scale_type (bf16 as 16-bit patterns, ue4m3/e8m0 bytes)
- *   zeros        uint8 [E][N][K/group], values 0..15 (UINT4_ZP) or 0..3 (UINT2_ZP), else NULL
+ *   zeros        uint8 [E][N][K/group], values 0..2^b - 1 for the b-bit zero-point formats
+ *                (UINT4_ZP, UINT3_ZP, UINT2_ZP, UINT1_ZP), else NULL
  *   global_scale fp32 [E] (NVFP4), else NULL
  *   packed       hq_packed_bytes(fmt) bytes, written entirely (padding zeroed)
  * Runs one kernel on `stream`.  Bit-exact and invertible by hq_unpack_weights. */

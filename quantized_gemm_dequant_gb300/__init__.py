@@ -24,7 +24,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 HQ_OK, HQ_ERR_INVALID_ARG, HQ_ERR_UNSUPPORTED, HQ_ERR_ALIGNMENT, HQ_ERR_CUDA, HQ_ERR_TIMEOUT, \
     HQ_ERR_BAD_ROUTING, HQ_ERR_WORKSPACE = range(8)
 HQ_W_INT4_SYM, HQ_W_UINT4_ZP, HQ_W_NVFP4, HQ_W_MXFP4 = 1, 2, 3, 4
-HQ_W_INT8_SYM, HQ_W_UINT2_ZP, HQ_W_MXINT4, HQ_W_E4M3 = 5, 6, 7, 8
+HQ_W_INT8_SYM, HQ_W_UINT2_ZP, HQ_W_MXINT4, HQ_W_E4M3, HQ_W_UINT1_ZP, HQ_W_UINT3_ZP = 5, 6, 7, 8, 9, 10
 HQ_S_BF16, HQ_S_UE4M3, HQ_S_UE8M0 = 1, 2, 3
 HQ_A_BF16, HQ_A_E4M3_TOKEN, HQ_A_NVFP4, HQ_A_MXFP8 = 1, 2, 3, 4
 
@@ -89,7 +89,9 @@ _WEIGHT = {"int4_sym": (HQ_W_INT4_SYM, 128, HQ_S_BF16, 0, 0, HQ_A_BF16),
            "int8_sym": (HQ_W_INT8_SYM, 128, HQ_S_BF16, 0, 0, HQ_A_BF16),
            "uint2_zp": (HQ_W_UINT2_ZP, 128, HQ_S_BF16, 1, 0, HQ_A_BF16),
            "mxint4": (HQ_W_MXINT4, 32, HQ_S_UE8M0, 0, 0, HQ_A_BF16),
-           "e4m3": (HQ_W_E4M3, 128, HQ_S_BF16, 0, 0, HQ_A_BF16)}
+           "e4m3": (HQ_W_E4M3, 128, HQ_S_BF16, 0, 0, HQ_A_BF16),
+           "uint1_zp": (HQ_W_UINT1_ZP, 128, HQ_S_BF16, 1, 0, HQ_A_BF16),
+           "uint3_zp": (HQ_W_UINT3_ZP, 128, HQ_S_BF16, 1, 0, HQ_A_BF16)}
 _ACT_FMT = {"bf16": HQ_A_BF16, "e4m3_tok": HQ_A_E4M3_TOKEN, "nvfp4": HQ_A_NVFP4, "mxfp8": HQ_A_MXFP8}
 
 

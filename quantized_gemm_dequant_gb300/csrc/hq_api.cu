@@ -88,6 +88,13 @@ hq_status_t check_format(const hq_format_t* f) {
         return HQ_ERR_UNSUPPORTED;
       if (f->K % 128) return HQ_ERR_ALIGNMENT;
       break;
+    case HQ_W_UINT1_ZP:
+    case HQ_W_UINT3_ZP:
+      if (f->group_size != 128 || f->scale_type != HQ_S_BF16 || !f->has_zero || f->has_global_scale ||
+          f->act_type != HQ_A_BF16)
+        return HQ_ERR_UNSUPPORTED;
+      if (f->K % 128) return HQ_ERR_ALIGNMENT;
+      break;
     case HQ_W_MXINT4:
       if (f->group_size != 32 || f->scale_type != HQ_S_UE8M0 || f->has_zero || f->has_global_scale ||
           f->act_type != HQ_A_BF16)

@@ -6,7 +6,7 @@
 // m16n8k16, bf16 x bf16 -> fp32), in the spirit of the multistage copy + MMA
 // pipeline that the Humming announcement reports to beat TMA + UMMA at small
 // batch ("Tuning and JIT compilation per workload").  It is also the one
-// kernel for the formats the tcgen05 kernel does not decode (INT8, UINT2,
+// kernel for the formats the tcgen05 kernel does not decode (INT8, UINT1/2/3,
 // MXINT4, FP8 E4M3 weights): there it serves every token count, with 32-token
 // tiles beyond 16 tokens.
 //
@@ -14,8 +14,10 @@
 // code order makes one ldmatrix.x4 deliver a warp's A-fragment words: every
 // register holds (even k, odd k) pairs of one row that the lane feeds to MMA
 // steps.  A pair becomes bf16x2 exactly:
-//   4-bit / 2-bit ints  one shift, one mask-and-or (the bf16 of 128 + q) and one
+//   4/2/1-bit ints      one shift, one mask-and-or (the bf16 of 128 + q) and one
 //                       bf16x2 subtraction of 128 + z
+//   3-bit ints          two mask-and-ors (low two bits, then the top bit from
+//                       the 1-bit plane) and one subtraction
 //   8-bit ints          two mask-and-ors (128 + low 7 bits; 128, or 256 when the
 //                       sign bit is set) and one subtraction
 //   e4m3                cvt to f16x2 (exact), the f16 bits moved into bf16 fields
@@ -62,9 +64,20 @@ constexpr int SM_FUSED_ROWS = 512;  // routed rows up to which a MoE call routes
 // Per decode variant: bytes of a packed block and where its scales / zero points sit.
 template <int DEC>
 struct DecCfg {
-  static constexpr int BLK = DEC == DEC_INT4 ? 8576 : (DEC == DEC_MXINT4 ? 8704 : (DEC == DEC_UINT2 ? 4480 : 16640));
-  static constexpr int SOFF = DEC == DEC_INT8 || DEC == DEC_E4M3 ? 16384 : (DEC == DEC_UINT2 ? 4096 : 8192);
-  static constexpr int ZOFF = DEC == DEC_UINT2 ? 4352 : 8448;
+  static constexpr int BLK = DEC == DEC_INT4     ? 8576
+                             : DEC == DEC_MXINT4 ? 8704
+                             : DEC == DEC_UINT2  ? 4480
+                             : DEC == DEC_UINT1  ? 2432
+                             : DEC == DEC_UINT3  ? 6528
+                                                 : 16640;
+  static constexpr int SOFF = DEC == DEC_INT8 || DEC == DEC_E4M3 ? 16384
+                              : DEC == DEC_UINT2                 ? 4096
+                              : DEC == DEC_UINT1                 ? 2048
+                              : DEC == DEC_UINT3                 ? 6144
+                                                                 : 8192;
+  static constexpr int ZOFF = SOFF + 256;
+  static constexpr bool ZP_ALWAYS = DEC == DEC_UINT2 || DEC == DEC_UINT1 || DEC == DEC_UINT3;
+  static constexpr int PLANE1 = DEC == DEC_UINT3 ? 4096 : 0;  // the 1-bit plane (UINT1 codes, UINT3 bit 2)
 };
 
 template <int BT, int DEC>
@@ -142,6 +155,14 @@ __device__ __forceinline__ uint32_t dec_u4(uint32_t x, uint32_t zz) {
 // (q - z) of the 2-bit pair at bits (0-1, 16-17) of x
 __device__ __forceinline__ uint32_t dec_u2(uint32_t x, uint32_t zz) {
   return bf16x2_sub(lop3_and_or(x, 0x00030003u, 0x43004300u), zz);
+}
+// (q - z) of the 1-bit pair at bits (0, 16) of x
+__device__ __forceinline__ uint32_t dec_u1(uint32_t x, uint32_t zz) {
+  return bf16x2_sub(lop3_and_or(x, 0x00010001u, 0x43004300u), zz);
+}
+// (q - z) of the 3-bit pair whose low two bits sit at bits (0-1, 16-17) of lo and whose top bit at bits (2, 18) of hi
+__device__ __forceinline__ uint32_t dec_u3(uint32_t lo, uint32_t hi, uint32_t zz) {
+  return bf16x2_sub(lop3_and_or(hi, 0x00040004u, lop3_and_or(lo, 0x00030003u, 0x43004300u)), zz);
 }
 // two's complement bytes at bits 0-7 and 16-23 of x: (128 + (b & 127)) - (128 or 256 when b's sign bit is set)
 __device__ __forceinline__ uint32_t dec_i8(uint32_t x) {
@@ -407,11 +428,15 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT, DEC>::CTAS_PER_SM)
     const int g8 = lane >> 2, t4 = lane & 3;
     const uint32_t smem_s = smem_u32(smem);
     // ldmatrix row addresses (weights; relative to the stage's weight block).  lane L gives row L % 16 of the
-    // 16-row MMA tile (UINT2: row L of the warp's 32 rows) in the chunk the variant's matrices name.
+    // 16-row MMA tile (UINT1/2/3: row L of the warp's 32 rows) in the chunk the variant's matrices name.
     uint32_t w_lane;
     if (DEC == DEC_INT4 || DEC == DEC_MXINT4) w_lane = ((2 * kh + (lane >> 4)) * 128 + 32 * rg + (lane & 15)) * 16;
-    else if (DEC == DEC_UINT2) w_lane = (kh * 128 + 32 * rg + lane) * 16;
+    else if (DEC == DEC_UINT2 || DEC == DEC_UINT3) w_lane = (kh * 128 + 32 * rg + lane) * 16;
+    else if (DEC == DEC_UINT1) w_lane = (32 * rg + lane) * 16;
     else w_lane = ((4 * kh + (lane >> 4)) * 128 + 32 * rg + (lane & 15)) * 16;
+    // the 1-bit plane: rows 32 rg + lane, both K halves in one 16-byte row (UINT1 codes, UINT3 bit 2)
+    const uint32_t w_lane1 = (uint32_t)D::PLANE1 + (uint32_t)(32 * rg + lane) * 16;
+    const uint32_t kh_shift = 8u * (uint32_t)kh;  // this warp's pairs of the 1-bit plane start at bit 8 kh
     // this lane's rows g8, g8 + 8 of both 16-row tiles: scale and zero-point offsets in the block
     uint32_t s_off[2][2], z_off[2][2];
 #pragma unroll
@@ -511,13 +536,23 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT, DEC>::CTAS_PER_SM)
               sc[m][rr][0] = __uint_as_float(lds_u16(stage_s + s_off[m][rr]) << 16);
             }
             uint32_t z = 8u;  // INT4_SYM and MXINT4 store q + 8
-            if (DEC == DEC_UINT2 || (DEC == DEC_INT4 && zp)) z = lds_u8(stage_s + z_off[m][rr]);
+            if (D::ZP_ALWAYS || (DEC == DEC_INT4 && zp)) z = lds_u8(stage_s + z_off[m][rr]);
             zz[m][rr] = z * 0x00010001u + 0x43004300u;
           }
         // weight words
         uint32_t wr[2][8];
-        if (DEC == DEC_UINT2) {
+        uint32_t wb1[2][2];  // 1-bit plane, shifted to this warp's K half (UINT3: top bit moved to bit 2)
+        if (DEC == DEC_UINT1 || DEC == DEC_UINT3) {
+          ldsm_x4(stage_s + C::W_OFF + w_lane1, wb1[0][0], wb1[0][1], wb1[1][0], wb1[1][1]);
+#pragma unroll
+          for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr)
+              wb1[m][rr] = DEC == DEC_UINT3 ? (wb1[m][rr] >> kh_shift) << 2 : wb1[m][rr] >> kh_shift;
+        }
+        if (DEC == DEC_UINT2 || DEC == DEC_UINT3) {
           ldsm_x4(stage_s + C::W_OFF + w_lane, wr[0][0], wr[0][1], wr[1][0], wr[1][1]);
+        } else if (DEC == DEC_UINT1) {
         } else {
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
@@ -565,6 +600,16 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT, DEC>::CTAS_PER_SM)
               a[1] = dec_u2(wr[m][1] >> (4 * s), zz[m][1]);
               a[2] = dec_u2(wr[m][0] >> (4 * s + 2), zz[m][0]);
               a[3] = dec_u2(wr[m][1] >> (4 * s + 2), zz[m][1]);
+            } else if (DEC == DEC_UINT1) {
+              a[0] = dec_u1(wb1[m][0] >> (2 * s), zz[m][0]);
+              a[1] = dec_u1(wb1[m][1] >> (2 * s), zz[m][1]);
+              a[2] = dec_u1(wb1[m][0] >> (2 * s + 1), zz[m][0]);
+              a[3] = dec_u1(wb1[m][1] >> (2 * s + 1), zz[m][1]);
+            } else if (DEC == DEC_UINT3) {
+              a[0] = dec_u3(wr[m][0] >> (4 * s), wb1[m][0] >> (2 * s), zz[m][0]);
+              a[1] = dec_u3(wr[m][1] >> (4 * s), wb1[m][1] >> (2 * s), zz[m][1]);
+              a[2] = dec_u3(wr[m][0] >> (4 * s + 2), wb1[m][0] >> (2 * s + 1), zz[m][0]);
+              a[3] = dec_u3(wr[m][1] >> (4 * s + 2), wb1[m][1] >> (2 * s + 1), zz[m][1]);
             } else {
               const uint32_t rg8 = wr[m][4 * (s >> 1) + 2 * (s & 1)], rg88 = wr[m][4 * (s >> 1) + 2 * (s & 1) + 1];
               if (DEC == DEC_INT8) {

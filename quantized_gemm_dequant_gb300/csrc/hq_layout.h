@@ -40,6 +40,19 @@
 //                   pair p of the word is slots (p, p + 8)
 //    [4096, 4352)   bf16 scale of each row for this group
 //    [4352, 4480)   zero point of each row (one byte)
+//  UINT1_ZP, K stage = 128:
+//    [0, 2048)      codes, 1 chunk x 128 rows x 16 bytes; bit b of word w of row r
+//                   holds k = 64(p / 8) + 16((p % 8) / 2) + 8(p % 2) + 2w + b / 16 with
+//                   p = b % 16: pair p of the word is bits (p, p + 16), and after a
+//                   shift by 8 kh the pairs of K half kh sit at bits 2s (k 2w + 16s)
+//                   and 2s + 1 (k 2w + 16s + 8) of MMA step s
+//    [2048, 2304)   bf16 scale of each row for this group
+//    [2304, 2432)   zero point of each row (one byte)
+//  UINT3_ZP, K stage = 128:
+//    [0, 4096)      bits 0-1 of the codes in the UINT2 layout
+//    [4096, 6144)   bit 2 of the codes in the UINT1 layout
+//    [6144, 6400)   bf16 scale of each row for this group
+//    [6400, 6528)   zero point of each row (one byte)
 //  NVFP4, K stage = 256:
 //    [0, 16384)     e2m1 codes as the shared-memory image of a 128-row x 128-byte
 //                   K-major tile with the 128-byte swizzle (16-byte chunk c of row r
@@ -66,16 +79,20 @@ enum WeightKind {
   WK_INT8_SYM = 5,
   WK_UINT2_ZP = 6,
   WK_MXINT4 = 7,
-  WK_E4M3 = 8
+  WK_E4M3 = 8,
+  WK_UINT1_ZP = 9,
+  WK_UINT3_ZP = 10
 };
 // Decode variants of the register-decode kernel, one per integer / e4m3 weight layout
-enum DecodeKind { DEC_INT4 = 0, DEC_MXINT4 = 1, DEC_INT8 = 2, DEC_E4M3 = 3, DEC_UINT2 = 4 };
+enum DecodeKind { DEC_INT4 = 0, DEC_MXINT4 = 1, DEC_INT8 = 2, DEC_E4M3 = 3, DEC_UINT2 = 4, DEC_UINT1 = 5, DEC_UINT3 = 6 };
 inline int decode_kind(int weight_type) {
   switch (weight_type) {
     case WK_MXINT4: return DEC_MXINT4;
     case WK_INT8_SYM: return DEC_INT8;
     case WK_E4M3: return DEC_E4M3;
     case WK_UINT2_ZP: return DEC_UINT2;
+    case WK_UINT1_ZP: return DEC_UINT1;
+    case WK_UINT3_ZP: return DEC_UINT3;
     default: return DEC_INT4;
   }
 }
@@ -116,6 +133,14 @@ inline PackGeom pack_geom(int weight_type, int64_t N, int64_t K, int64_t E) {
     g.path = PATH_INT4;
     g.kstage = 128;
     g.blk_bytes = 4096 + 256 + 128;
+  } else if (weight_type == WK_UINT1_ZP) {
+    g.path = PATH_INT4;
+    g.kstage = 128;
+    g.blk_bytes = 2048 + 256 + 128;
+  } else if (weight_type == WK_UINT3_ZP) {
+    g.path = PATH_INT4;
+    g.kstage = 128;
+    g.blk_bytes = 6144 + 256 + 128;
   } else if (weight_type == WK_NVFP4) {
     g.path = PATH_NVFP4;
     g.kstage = 256;

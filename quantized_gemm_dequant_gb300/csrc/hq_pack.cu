@@ -27,6 +27,26 @@ __device__ __forceinline__ int uint2_chunk_k(int w, int i) {
   return 16 * (p >> 1) + 8 * (p & 1) + 2 * w + (i >> 3);
 }
 
+// UINT1 layout (also bit 2 of UINT3 codes): K offset, within a 128-K row, of bit b of word w.
+__device__ __forceinline__ int uint1_chunk_k(int w, int b) {
+  const int p = b & 15;
+  return 64 * (p >> 3) + 16 * ((p & 7) >> 1) + 8 * (p & 1) + 2 * w + (b >> 4);
+}
+
+// Bits [pos, pos + n) of a little-endian bit string (n <= 3: at most two bytes).
+__device__ __forceinline__ uint32_t get_bits(const uint8_t* row, int64_t pos, int n) {
+  uint32_t two = row[pos >> 3];
+  if ((int)(pos & 7) + n > 8) two |= (uint32_t)row[(pos >> 3) + 1] << 8;
+  return (two >> (pos & 7)) & ((1u << n) - 1u);
+}
+__device__ __forceinline__ void put_bits(uint8_t* row, int64_t pos, int n, uint32_t v) {
+  for (int j = 0; j < n; ++j, ++pos) {
+    uint8_t* b = row + (pos >> 3);
+    const int sh = (int)(pos & 7);
+    *b = (uint8_t)((*b & ~(1u << sh)) | (((v >> j) & 1u) << sh));
+  }
+}
+
 __device__ __forceinline__ uint32_t get_nibble(const uint8_t* row, int64_t k) {
   uint8_t b = row[k >> 1];
   return (k & 1) ? (b >> 4) : (b & 0xF);
@@ -49,7 +69,54 @@ __global__ void pack_kernel(PackArgs p, uint8_t* codes, uint8_t* scales, uint8_t
     const bool valid = n < p.N;
     uint8_t* blk = packed + ((e * p.n_tiles + nt) * p.k_stages + ks) * (int64_t)p.blk_bytes;
     const int64_t rowc = (e * p.N + n) * (p.K / 2);  // byte offset of the row in codes (4-bit formats)
-    if (p.wt == WK_INT8_SYM || p.wt == WK_E4M3 || p.wt == WK_UINT2_ZP) {
+    if (p.wt == WK_UINT1_ZP || p.wt == WK_UINT3_ZP) {
+      // bit-string codes: UINT3 low two bits as the UINT2 planes, bit 2 (UINT1: the code) as the 1-bit plane
+      const int bits = p.wt == WK_UINT1_ZP ? 1 : 3;
+      const int64_t ng = p.K / 128;
+      uint8_t* row = codes + (e * p.N + n) * (p.K * bits / 8);
+      const int lo_bytes = bits == 3 ? 4096 : 0;
+      if (bits == 3)
+        for (int j = 0; j < 2; ++j) {
+          uint32_t* dst = reinterpret_cast<uint32_t*>(blk + (j * 128 + r) * 16);
+          for (int w = 0; w < 4; ++w) {
+            uint32_t word = DIR == 0 ? 0u : dst[w];
+            for (int i = 0; i < 16; ++i) {
+              const int64_t k = ks * 128 + 64 * j + uint2_chunk_k(w, i);
+              if (DIR == 0) {
+                if (valid) word |= get_bits(row, 3 * k, 2) << (2 * i);
+              } else if (valid) {
+                put_bits(row, 3 * k, 2, word >> (2 * i));
+              }
+            }
+            if (DIR == 0) dst[w] = word;
+          }
+        }
+      {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(blk + lo_bytes + r * 16);
+        for (int w = 0; w < 4; ++w) {
+          uint32_t word = DIR == 0 ? 0u : dst[w];
+          for (int b = 0; b < 32; ++b) {
+            const int64_t k = ks * 128 + uint1_chunk_k(w, b);
+            const int64_t pos = k * bits + bits - 1;  // the code's top bit
+            if (DIR == 0) {
+              if (valid) word |= get_bits(row, pos, 1) << b;
+            } else if (valid) {
+              put_bits(row, pos, 1, word >> b);
+            }
+          }
+          if (DIR == 0) dst[w] = word;
+        }
+      }
+      const int soff = lo_bytes + 2048;
+      uint16_t* sdst = reinterpret_cast<uint16_t*>(blk + soff) + r;
+      uint16_t* ssrc = reinterpret_cast<uint16_t*>(scales) + (e * p.N + n) * ng + ks;
+      if (DIR == 0) *sdst = valid ? *ssrc : (uint16_t)0;
+      else if (valid) *ssrc = *sdst;
+      uint8_t* zdst = blk + soff + 256 + r;
+      uint8_t* zsrc = zeros + (e * p.N + n) * ng + ks;
+      if (DIR == 0) *zdst = valid ? (uint8_t)(*zsrc & ((1u << bits) - 1u)) : (uint8_t)0;
+      else if (valid) *zsrc = *zdst;
+    } else if (p.wt == WK_INT8_SYM || p.wt == WK_E4M3 || p.wt == WK_UINT2_ZP) {
       const int64_t ng = p.K / 128;
       const bool two = p.wt == WK_UINT2_ZP;
       if (!two) {

@@ -1,7 +1,7 @@
 """More weight formats through the same decode component, against the CPU oracle (GPU).
 
-INT8 (the e0m7 value set), UINT2 with zero points, MXINT4 (e8m0 block-32
-scales) and FP8 E4M3 weights, each with bf16 activations: the other WnA16
+INT8 (the e0m7 value set), UINT1 / UINT2 / UINT3 with zero points, MXINT4 (e8m0
+block-32 scales) and FP8 E4M3 weights, each with bf16 activations: the other WnA16
 widths and formats of "Results: kernel microbenchmarks" and the zero-exponent
 INT8 of "Results: quantization support".  The register-decode kernel reads
 them at every token count (32-token tiles beyond 16 tokens).  Checked here:
@@ -23,8 +23,11 @@ FORMS = {
     "uint2_zp": dict(kind="dense", wfmt="uint2_zp", afmt="bf16", G=128),
     "mxint4": dict(kind="dense", wfmt="mxint4", afmt="bf16", G=32),
     "e4m3": dict(kind="dense", wfmt="e4m3", afmt="bf16", G=128),
+    "uint1_zp": dict(kind="dense", wfmt="uint1_zp", afmt="bf16", G=128),
+    "uint3_zp": dict(kind="dense", wfmt="uint3_zp", afmt="bf16", G=128),
 }
-CODE_COLS = {"int8_sym": 1, "e4m3": 1, "uint2_zp": 4, "mxint4": 2}  # K / (code bytes per row)
+CODE_BITS = {"int8_sym": 8, "e4m3": 8, "uint2_zp": 2, "mxint4": 4, "uint1_zp": 1, "uint3_zp": 3}
+ZERO_BITS = {"uint2_zp": 2, "uint1_zp": 1, "uint3_zp": 3}
 
 
 @pytest.mark.parametrize("wfmt", list(FORMS))
@@ -32,13 +35,14 @@ def test_pack_unpack_round_trip_bit_exact(lib, wfmt):
     E, N, K = 2, 300, 512
     g = FORMS[wfmt]["G"]
     gen = torch.Generator().manual_seed(21)
-    codes = torch.randint(0, 256, (E, N, K // CODE_COLS[wfmt]), generator=gen, dtype=torch.uint8)
+    codes = torch.randint(0, 256, (E, N, K * CODE_BITS[wfmt] // 8), generator=gen, dtype=torch.uint8)
     if wfmt == "mxint4":
         scales = torch.randint(0, 256, (E, N, K // g), generator=gen, dtype=torch.uint8)
     else:
         scales = torch.randint(0, 65536, (E, N, K // g), generator=gen, dtype=torch.int32).to(torch.int16)
         scales = scales.view(torch.uint8).reshape(E, N, 2 * (K // g))
-    zeros = torch.randint(0, 4, (E, N, K // g), generator=gen, dtype=torch.uint8) if wfmt == "uint2_zp" else None
+    zeros = (torch.randint(0, 1 << ZERO_BITS[wfmt], (E, N, K // g), generator=gen, dtype=torch.uint8)
+             if wfmt in ZERO_BITS else None)
     fmt = lib.make_format(wfmt, N, K, E)
     packed = lib.pack_weights(fmt, codes.cuda(), scales.cuda(), zeros.cuda() if zeros is not None else None)
     c2 = torch.zeros_like(codes).cuda()
@@ -92,6 +96,11 @@ def test_exact_integer_pow2_bit_exact(lib, wfmt):
         q = torch.randint(0, 4, (N, K), generator=gen)
         w = dict(codes=quant.pack_crumbs(q.to(torch.uint8)), scales=pow2_bf16,
                  zeros=torch.randint(0, 4, (N, K // G), generator=gen, dtype=torch.uint8))
+    elif wfmt in ("uint1_zp", "uint3_zp"):
+        b = CODE_BITS[wfmt]
+        q = torch.randint(0, 1 << b, (N, K), generator=gen)
+        w = dict(codes=quant.pack_bits(q.to(torch.uint8), b), scales=pow2_bf16,
+                 zeros=torch.randint(0, 1 << b, (N, K // G), generator=gen, dtype=torch.uint8))
     elif wfmt == "mxint4":
         q = torch.randint(-7, 8, (N, K), generator=gen)
         w = dict(codes=quant.pack_nibbles((q & 0xF).to(torch.uint8)), scales=(j + 127).to(torch.uint8))

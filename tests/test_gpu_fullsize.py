@@ -38,8 +38,12 @@ def dense_layers(lib):
     return get
 
 
+OTHER_DENSE = ["w8a16", "w2a16", "w1a16", "w3a16", "mxint4_a16", "fp8w_a16", "w4a8_mx"]
+
+
 @pytest.mark.parametrize("cfg,M", [("w4a16_sym", 8)] + [("w4a16_asym", m) for m in CONFIGS["w4a16_asym"]["sizes"]]
-                         + [("nvfp4", m) for m in CONFIGS["nvfp4"]["sizes"]])
+                         + [("nvfp4", m) for m in CONFIGS["nvfp4"]["sizes"]]
+                         + [(c, m) for c in OTHER_DENSE for m in (CONFIGS[c]["sizes"][0], CONFIGS[c]["sizes"][-1])])
 def test_dense_full_size_sampled(lib, dense_layers, cfg, M):
     c = CONFIGS[cfg]
     fmt, packed, wdeq = dense_layers(cfg)
