@@ -118,7 +118,7 @@ def unpack_bits(packed, bits):
 
 WEIGHT_FORMATS = ("int4_sym", "uint4_zp", "nvfp4", "mxfp4", "int8_sym", "uint2_zp", "mxint4", "e4m3", "uint1_zp",
                   "uint3_zp")
-ACT_FORMATS = ("bf16", "e4m3_tok", "nvfp4", "mxfp8")
+ACT_FORMATS = ("bf16", "e4m3_tok", "nvfp4", "mxfp8", "mxfp4")
 BLOCK = {"nvfp4": 16, "mxfp4": 32, "mxint4": 32, "mxfp8": 32}
 
 
@@ -188,9 +188,15 @@ def dequant_acts(afmt, data, scale=None, gscale=None):
     e4m3_tok : e4m3(a) * s_t, one fp32 scale per row (token)
     nvfp4    : e2m1(q) * ue4m3(sb) * g, sb per (row, 16 along K), g fp32 per tensor
     mxfp8    : e4m3(a) * e8m0(sb), sb per (row, 32 along K) (OCP Microscaling v1.0 MXFP8 E4M3)
+    mxfp4    : e2m1(q) * e8m0(sb), q two per byte (low nibble = even k), sb per (row, 32 along K) (OCP
+               Microscaling v1.0 MXFP4, the W4A4 operand of "W8A8 / W4A8 / W4A4")
     """
     if afmt == "bf16":
         return decode_bf16(data)
+    if afmt == "mxfp4":
+        q = unpack_nibbles(data)
+        sb = np.repeat(decode_e8m0(scale), BLOCK[afmt], axis=-1)[..., : q.shape[-1]]
+        return decode_e2m1(q) * sb
     if afmt == "mxfp8":
         q = np.asarray(data).astype(np.uint8)
         sb = np.repeat(decode_e8m0(scale), BLOCK[afmt], axis=-1)[..., : q.shape[-1]]

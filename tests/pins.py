@@ -390,6 +390,15 @@ def pin_exact_more_formats(o, rng=None):
             ref = sum(minifloat(a8[m, k], 4, 3, 7, fn_nan=True) * Fraction(2) ** int(ja[m, k // 32]) * int(qw[n, k])
                       for k in range(K))
             assert y[m, n] == float(ref)
+    # MXFP4 activations (e2m1 nibbles, low nibble = even k, + e8m0 per 32), same check with the E2M1 minifloat
+    c4 = rng.integers(0, 16, size=(M, K))
+    ax4 = o.dequant_acts("mxfp4", pack_nibbles_loop(c4), (ja + 127).astype(np.uint8))
+    y4 = o.gemm(ax4, w)
+    for m in range(M):
+        for n in range(N):
+            ref = sum(minifloat(c4[m, k], 2, 1, 1) * Fraction(2) ** int(ja[m, k // 32]) * int(qw[n, k])
+                      for k in range(K))
+            assert y4[m, n] == float(ref)
 
 
 # ------------------------------------------------------------ pins on the activation quantizers

@@ -68,6 +68,7 @@ MUTATIONS = {
                              "weights = np.int64(1) << np.arange(bits, dtype=np.int64)[::-1]"),
     "uint3_zero_point_dropped": ("return (decode_int(q, bits, False) - zq) * s", "return decode_int(q, bits, False) * s"),
     "uint3_as_signed": ("return (decode_int(q, bits, False) - zq) * s", "return (decode_int(q, bits, True) - zq) * s"),
+    "act_mxfp4_scale_dropped": ("        return decode_e2m1(q) * sb\n    if afmt == \"mxfp8\"", "        return decode_e2m1(q)\n    if afmt == \"mxfp8\""),
     "act_nvfp4_nibbles": ("packed = (q[:, 0::2] | (q[:, 1::2] << 4))", "packed = (q[:, 1::2] | (q[:, 0::2] << 4))"),
 }
 

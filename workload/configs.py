@@ -18,6 +18,7 @@ Sizes and recipes (quantized GEMM microbenchmarks of the Humming announcement,
               FP8 E4M3 g128 weights, bf16 act
   w4a8_mx     dense, K=7168, N=4096, M in {1,128,1024,8192}: MXFP4 weights,
               MXFP8 activations (e4m3 + e8m0 per 32)
+  w4a4_mx     the same with MXFP4 activations (e2m1 + e8m0 per 32)
 
 Weights are fp32 N(0, 0.02) and activations N(0, 1) before quantization.  MoE
 routing draws k distinct experts per token from Zipf(1.1) popularities by
@@ -51,6 +52,7 @@ CONFIGS = {
     "w1a16": dict(kind="dense", wfmt="uint1_zp", afmt="bf16", N=14336, K=4096, G=128, sizes=[1, 16, 64, 256]),
     "w3a16": dict(kind="dense", wfmt="uint3_zp", afmt="bf16", N=14336, K=4096, G=128, sizes=[1, 16, 64, 256]),
     "fp8w_a16": dict(kind="dense", wfmt="e4m3", afmt="bf16", N=14336, K=4096, G=128, sizes=[1, 16, 64, 256]),
+    "w4a4_mx": dict(kind="dense", wfmt="mxfp4", afmt="mxfp4", N=4096, K=7168, G=32, sizes=[1, 128, 1024, 8192]),
     "w4a8_mx": dict(kind="dense", wfmt="mxfp4", afmt="mxfp8", N=4096, K=7168, G=32, sizes=[1, 128, 1024, 8192]),
 }
 
@@ -115,6 +117,9 @@ def quantize_acts(afmt, a):
     if afmt == "mxfp8":
         q, s = quant.quant_mxfp8(a)
         return dict(data=q, scale=s)
+    if afmt == "mxfp4":
+        c, s = quant.quant_mxfp4(a)
+        return dict(data=c, scale=s)
     raise ValueError(afmt)
 
 
@@ -221,6 +226,8 @@ def act_bytes(afmt, M, K):
         return M * K // 2 + M * K // 16 + 4
     if afmt == "mxfp8":
         return M * K + M * K // 32
+    if afmt == "mxfp4":
+        return M * K // 2 + M * K // 32
     raise ValueError(afmt)
 
 

@@ -10,8 +10,9 @@ public definition:
   clamp(rint(-min / scale), 0, 15), code = clamp(rint(w / scale) + zero, 0, 15);
 * NVFP4: fp32 tensor scale g = amax / (6 * 448), e4m3 block-16 scale
   e4m3(amax_b / (6 g)) saturated at 448, e2m1 codes of x / (sb * g);
-* MXFP4 (OCP Microscaling v1.0 section 6.3): e8m0 block-32 scale
-  2**(floor(log2 amax_b) - 2), e2m1 codes of x / scale, saturating;
+* MXFP4 (OCP Microscaling v1.0 section 6.3), weights and W4A4 activations:
+  e8m0 block-32 scale 2**(floor(log2 amax_b) - 2), e2m1 codes of x / scale,
+  saturating;
 * FP8 per token: s_t = absmax_t / 448, e4m3(a / s_t) saturated;
 * grouped INT8 (the e0m7 value set): scale = absmax / 127 in bf16, codes
   rint(w / scale) clamped to [-127, 127], one byte each;
