@@ -38,6 +38,13 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 DTYPE_RATIO = {"bf16": 1.0, "fp8": 2.0, "fp4": 6.0}
 PATH_DTYPE = {"int4_sym": "bf16", "uint4_zp": "bf16", "nvfp4": "fp4", "mxfp4": "fp8", "int8_sym": "bf16",
               "uint2_zp": "bf16", "mxint4": "bf16", "e4m3": "bf16", "uint1_zp": "bf16", "uint3_zp": "bf16"}
+
+
+def path_dtype(c):
+    """The MMA's operand type of a workload: FP4 on both sides (NVFP4, MXFP4 x MXFP4) runs at the FP4 rate."""
+    return "fp4" if c["afmt"] in ("nvfp4", "mxfp4") else PATH_DTYPE[c["wfmt"]]
+
+
 SPIN_CYCLES = 1_000_000  # about 0.5 ms at 2 GHz: longer than the host side of one burst of calls
 
 
@@ -218,7 +225,7 @@ def roofline_of(info, t_s, pk, dt):
 MIN_SAMPLES = 20       # samples per size (bursts, and isolated calls)
 MIN_SAMPLES_FAST = 100  # below 10 us per call
 OTHER_CONFIGS = ["w4a16_sym", "nvfp4", "moe_w4a16", "moe_mxfp4", "moe_w4a16_down", "moe_mxfp4_down", "w8a16", "w2a16",
-                 "w1a16", "w3a16", "mxint4_a16", "fp8w_a16", "w4a8_mx"]
+                 "w1a16", "w3a16", "mxint4_a16", "fp8w_a16", "w4a8_mx", "w4a4_mx"]
 
 
 def _burst(call, n, R, stream, counter):
@@ -305,7 +312,7 @@ def measure_other_config(cfg_name, args, pk, pk_src, stream, dev):
     """The burst + isolated samples of another workload (no timed steps): per-size records and its dominant
     kernel's roofline, as for the headline workload."""
     c = W.CONFIGS[cfg_name]
-    dt = PATH_DTYPE[c["wfmt"]]
+    dt = path_dtype(c)
     fmt, calls, R = make_calls(cfg_name, args.seed, dev)
     counter = [0]
     burst = R if args.burst is None else max(1, args.burst)
@@ -343,7 +350,7 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
     pk, pk_src = peaks()
     c = W.CONFIGS[args.config]
-    dt = PATH_DTYPE[c["wfmt"]]
+    dt = path_dtype(c)
     fmt, calls, R = make_calls(args.config, args.seed, dev)
     stream = torch.cuda.current_stream(dev)
     counter = [0]
@@ -436,28 +443,20 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-DECODE_KIND = {"int4_sym": 0, "uint4_zp": 0, "mxint4": 1, "int8_sym": 2, "e4m3": 3, "uint2_zp": 4, "uint1_zp": 5,
-               "uint3_zp": 6}
 
 
 def kernel_name(cfg, M):
-    """The GEMM kernel instance a call of this workload with M rows (dense) or T tokens (MoE) launches, as the library's
-    launch plan picks it (tile width, register-decode or tcgen05 kernel)."""
+    """The GEMM kernel instance a call of this workload with M rows (dense) or T tokens (MoE) launches, from the
+    library's own launch plan (built-in rule and tuned table)."""
+    import quantized_gemm_dequant_gb300 as hq
     c = W.CONFIGS[cfg]
-    wf = c["wfmt"]
-    path = 1 if wf == "nvfp4" else (3 if wf == "mxfp4" and c["afmt"] == "mxfp8" else (2 if wf == "mxfp4" else 0))
-    if c["kind"] == "dense":
-        bt = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128 if M <= 128 else 256
-    else:
-        avg = -(-M * c["topk"] // c["E"])
-        bt = 16 if avg <= 16 else (256 if path not in (1, 3) and avg > 128 else 128)
-    if path == 0:
-        dec = DECODE_KIND[wf]
-        if dec != 0 or (bt <= 32 and os.environ.get("HQ_FORCE_PATH") != "umma"):
-            if c["kind"] == "dense" and M <= 8:
-                bt = 8
-            return f"hq::hq_gemm_small_kernel<{min(bt, 32)}, {dec}>"
-    return f"hq::hq_gemm_kernel<{path}, {bt}, {1 if c.get('down') else 0}>"
+    fmt = hq.make_format(c["wfmt"], c["N"], c["K"], c.get("E", 1))
+    fmt.act_type = hq._ACT_FMT[c["afmt"]]
+    moe = c["kind"] != "dense"
+    p = hq.launch_plan(fmt, M, c.get("topk", 1), ("combine" if c.get("down") else True) if moe else False)
+    if p["kernel"] == "regdec":
+        return f"hq::hq_gemm_small_kernel<{p['bt']}, {p['variant']}>"
+    return f"hq::hq_gemm_kernel<{p['variant']}, {p['bt']}, {1 if c.get('down') else 0}>"
 
 
 def gpu_launches(cfg, fmt, calls):

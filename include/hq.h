@@ -86,7 +86,8 @@ enum {
   HQ_A_BF16 = 1,       /* bf16 [M, K] */
   HQ_A_E4M3_TOKEN = 2, /* e4m3 [M, K] bytes + fp32 scale per row (token) */
   HQ_A_NVFP4 = 3,      /* e2m1 [M, K/2] packed + ue4m3 [M, K/16] + fp32 global scale [1] */
-  HQ_A_MXFP8 = 4       /* e4m3 [M, K] bytes + e8m0 [M, K/32] block scales (OCP Microscaling MXFP8) */
+  HQ_A_MXFP8 = 4,      /* e4m3 [M, K] bytes + e8m0 [M, K/32] block scales (OCP Microscaling MXFP8) */
+  HQ_A_MXFP4 = 5       /* e2m1 [M, K/2] packed (low nibble = even k) + e8m0 [M, K/32] (OCP Microscaling MXFP4) */
 };
 
 /* The unified quantization description ("standard format").  Supported
@@ -94,7 +95,7 @@ enum {
  *   INT4_SYM, group 128, BF16 scales,  no zero, no global, act BF16
  *   UINT4_ZP, group 128, BF16 scales,  zero,    no global, act BF16
  *   NVFP4,    group 16,  UE4M3 scales, no zero, global,    act NVFP4
- *   MXFP4,    group 32,  UE8M0 scales, no zero, no global, act E4M3_TOKEN or MXFP8
+ *   MXFP4,    group 32,  UE8M0 scales, no zero, no global, act E4M3_TOKEN, MXFP8 or MXFP4
  *   INT8_SYM, group 128, BF16 scales,  no zero, no global, act BF16
  *   UINT2_ZP, group 128, BF16 scales,  zero,    no global, act BF16
  *   MXINT4,   group 32,  UE8M0 scales, no zero, no global, act BF16
@@ -104,9 +105,9 @@ enum {
  * The last six are the other WnA16 widths and formats of "Results: kernel
  * microbenchmarks" (INT1, INT2, INT3 as GPTQ-style unsigned codes with integer
  * zero points, INT8 as the zero-exponent e0m7 of "Results: quantization
- * support", MXINT4, FP8); MXFP8 activations are the microscaled
- * W4A8 variant of "W8A8 / W4A8 / W4A4".  Anything else returns
- * HQ_ERR_UNSUPPORTED. */
+ * support", MXINT4, FP8); MXFP8 and MXFP4 activations are the microscaled
+ * W4A8 and W4A4 variants of "W8A8 / W4A8 / W4A4" (both need K a multiple
+ * of 512).  Anything else returns HQ_ERR_UNSUPPORTED. */
 typedef struct {
   int32_t weight_type;      /* HQ_W_* */
   int32_t group_size;       /* K elements per scale */
@@ -120,7 +121,8 @@ typedef struct {
 } hq_format_t;
 
 /* Activation operand.  data: see HQ_A_*; scale: fp32 [M] for E4M3_TOKEN,
- * ue4m3 [M, K/16] for NVFP4, NULL for BF16; global_scale: fp32 [1] for NVFP4. */
+ * ue4m3 [M, K/16] for NVFP4, e8m0 [M, K/32] for MXFP8 and MXFP4, NULL for
+ * BF16; global_scale: fp32 [1] for NVFP4. */
 typedef struct {
   const void* data;
   const void* scale;
@@ -170,6 +172,14 @@ HQ_API size_t hq_workspace_bytes(const hq_format_t* fmt, int64_t M_or_T, int32_t
  * hq_moe_gemm_combine (moe = 2) with M rows / T tokens and `topk` experts each (1 for dense).  Counts this library's kernels only
  * (the routing memset of hq_moe_gemm is not a kernel); 0 for an invalid format or size.  Host-only. */
 HQ_API int32_t hq_kernels_per_call(const hq_format_t* fmt, int64_t M_or_T, int32_t topk, int32_t moe);
+
+/* The launch plan of such a call on the current device (built-in rule, tuned table, HQ_TUNE): writes
+ * plan_out[0] = GEMM kernel (0 tcgen05, 1 register-decode), plan_out[1] = its variant (tcgen05: 0 INT4, 1 NVFP4,
+ * 2 MXFP4 x FP8, 3 MXFP4 x MXFP8, 4 MXFP4 x MXFP4; register-decode: the decode kind, 0 INT4 ... 6 UINT3),
+ * plan_out[2] = token tile, plan_out[3] = 1 if K is split over CTAs (Stream-K), plan_out[4] = CTAs launched,
+ * plan_out[5] = 1 if MoE rows are copied expert-contiguous first.  Returns HQ_ERR_INVALID_ARG for an invalid
+ * format, size or null plan_out.  Host-only ("Tuning and JIT compilation per workload": the per-size choice). */
+HQ_API hq_status_t hq_launch_plan(const hq_format_t* fmt, int64_t M_or_T, int32_t topk, int32_t moe, int32_t* plan_out);
 
 /* Zero `bytes` of workspace on `stream` (cudaMemsetAsync).  Errors:
  * HQ_ERR_INVALID_ARG for a null pointer or zero size, HQ_ERR_CUDA. */

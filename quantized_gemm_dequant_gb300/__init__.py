@@ -26,11 +26,11 @@ HQ_OK, HQ_ERR_INVALID_ARG, HQ_ERR_UNSUPPORTED, HQ_ERR_ALIGNMENT, HQ_ERR_CUDA, HQ
 HQ_W_INT4_SYM, HQ_W_UINT4_ZP, HQ_W_NVFP4, HQ_W_MXFP4 = 1, 2, 3, 4
 HQ_W_INT8_SYM, HQ_W_UINT2_ZP, HQ_W_MXINT4, HQ_W_E4M3, HQ_W_UINT1_ZP, HQ_W_UINT3_ZP = 5, 6, 7, 8, 9, 10
 HQ_S_BF16, HQ_S_UE4M3, HQ_S_UE8M0 = 1, 2, 3
-HQ_A_BF16, HQ_A_E4M3_TOKEN, HQ_A_NVFP4, HQ_A_MXFP8 = 1, 2, 3, 4
+HQ_A_BF16, HQ_A_E4M3_TOKEN, HQ_A_NVFP4, HQ_A_MXFP8, HQ_A_MXFP4 = 1, 2, 3, 4, 5
 
 EXPORTS = ["hq_packed_bytes", "hq_pack_weights", "hq_unpack_weights", "hq_workspace_bytes", "hq_workspace_init",
            "hq_gemm", "hq_moe_gemm", "hq_last_device_status", "hq_status_string", "hq_gemm_static_scratch",
-           "hq_kernels_per_call", "hq_quantize_act_workspace_bytes", "hq_quantize_act",
+           "hq_kernels_per_call", "hq_launch_plan", "hq_quantize_act_workspace_bytes", "hq_quantize_act",
            "hq_moe_combine_workspace_bytes", "hq_moe_gemm_combine", "hq_swiglu", "hq_set_wait_limit_ns"]
 
 
@@ -67,6 +67,8 @@ _lib.hq_gemm_static_scratch.argtypes = [_F, _A, _vp, _vp, _vp, _i64, _i64, _i64,
 _lib.hq_gemm_static_scratch.restype = ctypes.c_int
 _lib.hq_kernels_per_call.argtypes = [_F, _i64, _i32, _i32]
 _lib.hq_kernels_per_call.restype = _i32
+_lib.hq_launch_plan.argtypes = [_F, _i64, _i32, _i32, ctypes.POINTER(ctypes.c_int32)]
+_lib.hq_launch_plan.restype = ctypes.c_int
 _lib.hq_quantize_act_workspace_bytes.argtypes = [_i32, _i64, _i64]
 _lib.hq_quantize_act_workspace_bytes.restype = _sz
 _lib.hq_quantize_act.argtypes = [_i32, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
@@ -92,7 +94,8 @@ _WEIGHT = {"int4_sym": (HQ_W_INT4_SYM, 128, HQ_S_BF16, 0, 0, HQ_A_BF16),
            "e4m3": (HQ_W_E4M3, 128, HQ_S_BF16, 0, 0, HQ_A_BF16),
            "uint1_zp": (HQ_W_UINT1_ZP, 128, HQ_S_BF16, 1, 0, HQ_A_BF16),
            "uint3_zp": (HQ_W_UINT3_ZP, 128, HQ_S_BF16, 1, 0, HQ_A_BF16)}
-_ACT_FMT = {"bf16": HQ_A_BF16, "e4m3_tok": HQ_A_E4M3_TOKEN, "nvfp4": HQ_A_NVFP4, "mxfp8": HQ_A_MXFP8}
+_ACT_FMT = {"bf16": HQ_A_BF16, "e4m3_tok": HQ_A_E4M3_TOKEN, "nvfp4": HQ_A_NVFP4, "mxfp8": HQ_A_MXFP8,
+            "mxfp4": HQ_A_MXFP4}
 
 
 class HQError(RuntimeError):
@@ -158,6 +161,16 @@ def kernels_per_call(fmt, rows, topk=1, moe=False):
     current device."""
     m = 2 if moe == "combine" else (1 if moe else 0)
     return int(_lib.hq_kernels_per_call(ctypes.byref(fmt), int(rows), int(topk), m))
+
+
+def launch_plan(fmt, rows, topk=1, moe=False):
+    """The planner's choice for such a call on the current device: dict(kernel ('umma' | 'regdec'), variant, bt, sk,
+    grid, grouped)."""
+    m = 2 if moe == "combine" else (1 if moe else 0)
+    out = (ctypes.c_int32 * 6)()
+    _check(_lib.hq_launch_plan(ctypes.byref(fmt), int(rows), int(topk), m, out), "hq_launch_plan")
+    return dict(kernel="regdec" if out[0] else "umma", variant=int(out[1]), bt=int(out[2]), sk=int(out[3]),
+                grid=int(out[4]), grouped=int(out[5]))
 
 
 def make_workspace(fmt, rows, topk=1, device="cuda", stream=None):

@@ -13,7 +13,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libhq.so")
-SOURCES = ["hq_api.cu", "hq_pack.cu", "hq_route.cu", "hq_gemm_int4.cu", "hq_gemm_nvfp4.cu", "hq_gemm_mxfp4.cu", "hq_gemm_mxfp4a.cu", "hq_gemm_small.cu", "hq_gemm_small_fmt.cu", "hq_gemm_small_bits.cu", "hq_splitk.cu", "hq_noalloc.cu", "hq_act_quant.cu", "hq_moe_combine.cu", "hq_gemm_int4_comb.cu", "hq_gemm_nvfp4_comb.cu", "hq_gemm_mxfp4_comb.cu"]
+SOURCES = ["hq_api.cu", "hq_pack.cu", "hq_route.cu", "hq_gemm_int4.cu", "hq_gemm_nvfp4.cu", "hq_gemm_mxfp4.cu", "hq_gemm_mxfp4a.cu", "hq_gemm_mxfp4x.cu", "hq_gemm_mxfp4x_comb.cu", "hq_gemm_small.cu", "hq_gemm_small_fmt.cu", "hq_gemm_small_bits.cu", "hq_splitk.cu", "hq_noalloc.cu", "hq_act_quant.cu", "hq_moe_combine.cu", "hq_gemm_int4_comb.cu", "hq_gemm_nvfp4_comb.cu", "hq_gemm_mxfp4_comb.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
 

@@ -23,6 +23,7 @@ cudaError_t launch_gemm_int4(const GemmArgs& a, int bt, int grid, cudaStream_t s
 cudaError_t launch_gemm_nvfp4(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_mxfp4(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_mxfp4a(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_mxfp4x(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_small(const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_small_fmt(int dec, const GemmArgs& a, int bt, int grid, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(int path, const GemmArgs& a, int bt, int gemm_grid, int grid, cudaStream_t stream);
@@ -69,11 +70,12 @@ hq_status_t check_format(const hq_format_t* f) {
       break;
     case HQ_W_MXFP4:
       if (f->group_size != 32 || f->scale_type != HQ_S_UE8M0 || f->has_zero || f->has_global_scale ||
-          (f->act_type != HQ_A_E4M3_TOKEN && f->act_type != HQ_A_MXFP8))
+          (f->act_type != HQ_A_E4M3_TOKEN && f->act_type != HQ_A_MXFP8 && f->act_type != HQ_A_MXFP4))
         return HQ_ERR_UNSUPPORTED;
       if (f->K % 128) return HQ_ERR_ALIGNMENT;
-      // MXFP8 block scales are loaded 16 bytes (512 K) at a time: rows of K/32 bytes must be 16-byte multiples
-      if (f->act_type == HQ_A_MXFP8 && f->K % 512) return HQ_ERR_ALIGNMENT;
+      // MXFP8 / MXFP4 block scales are loaded 16 bytes (512 K) at a time: rows of K/32 bytes must be 16-byte
+      // multiples
+      if ((f->act_type == HQ_A_MXFP8 || f->act_type == HQ_A_MXFP4) && f->K % 512) return HQ_ERR_ALIGNMENT;
       break;
     case HQ_W_INT8_SYM:
     case HQ_W_E4M3:
@@ -105,6 +107,12 @@ hq_status_t check_format(const hq_format_t* f) {
       return HQ_ERR_UNSUPPORTED;
   }
   return HQ_OK;
+}
+
+// Packed layout of a descriptor: MXFP4 weights meant for MXFP4 activations are packed like NVFP4 (packed e2m1 in
+// the MMA, scales as tensor-memory words), every other format by its weight type.
+int pack_kind(const hq_format_t* f) {
+  return (f->weight_type == HQ_W_MXFP4 && f->act_type == HQ_A_MXFP4) ? (int)WK_MXFP4_X : f->weight_type;
 }
 
 int num_sms() {
@@ -148,7 +156,7 @@ int pick_bt_moe(int path, int64_t rows, int64_t E) {
   if (E == 1) return pick_bt_dense(rows);  // one expert is a dense GEMM over the routed rows
   const int64_t avg = (rows + E - 1) / E;
   if (avg <= 16) return 16;
-  if (path != PATH_NVFP4 && path != PATH_MXFP4A && avg > 128) return 256;
+  if (path != PATH_NVFP4 && path != PATH_MXFP4A && path != PATH_MXFP4X && avg > 128) return 256;
   return 128;
 }
 
@@ -167,7 +175,7 @@ int64_t act_row_bytes(const hq_format_t* f) {
 }
 // Activation block-scale bytes per row (NVFP4: ue4m3 per 16; MXFP8: e8m0 per 32), else 0.
 int64_t act_scale_row_bytes(const hq_format_t* f) {
-  return f->act_type == HQ_A_NVFP4 ? f->K / 16 : (f->act_type == HQ_A_MXFP8 ? f->K / 32 : 0);
+  return f->act_type == HQ_A_NVFP4 ? f->K / 16 : ((f->act_type == HQ_A_MXFP8 || f->act_type == HQ_A_MXFP4) ? f->K / 32 : 0);
 }
 
 // HQ_FORCE_PATH=small|umma overrides the choice between the two INT4 kernels (tests compare both).
@@ -182,6 +190,7 @@ int forced_path() {
 int tune_class(const hq_format_t* f, int path) {
   if (path == PATH_NVFP4) return TC_NVFP4;
   if (path == PATH_MXFP4A) return TC_MXFP4A;
+  if (path == PATH_MXFP4X) return TC_MXFP4X;
   if (path == PATH_MXFP4) return TC_MXFP4;
   return register_decode_only(f->weight_type) ? TC_REGDEC : TC_INT4;
 }
@@ -205,7 +214,7 @@ void plan_tiles(Plan& p, int64_t M_or_T, int32_t topk, bool moe, int64_t E, int6
 // checked against what the kernels support before it is taken.
 Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int sms) {
   Plan p;
-  const PackGeom g = pack_geom(f->weight_type, f->N, f->K, f->num_experts);
+  const PackGeom g = pack_geom(pack_kind(f), f->N, f->K, f->num_experts);
   p.path = (g.path == PATH_MXFP4 && f->act_type == HQ_A_MXFP8) ? PATH_MXFP4A : g.path;
   p.n_tiles = g.n_tiles;
   p.kst = g.k_stages;
@@ -235,7 +244,8 @@ Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int
   if (tc.bt > 0) {
     const bool ok = p.small ? (tc.bt == 8 || tc.bt == 16 || tc.bt == 32)
                             : (tc.bt == 16 || tc.bt == 32 || tc.bt == 64 || tc.bt == 128 ||
-                               (tc.bt == 256 && !(moe && (p.path == PATH_NVFP4 || p.path == PATH_MXFP4A))));
+                               (tc.bt == 256 &&
+                                !(moe && (p.path == PATH_NVFP4 || p.path == PATH_MXFP4A || p.path == PATH_MXFP4X))));
     if (ok) p.bt = tc.bt;
   }
   int64_t tiles_est = 0;
@@ -303,6 +313,7 @@ cudaError_t launch_path(const Plan& p, const GemmArgs& a, cudaStream_t s) {
                                       : launch_gemm_small_fmt(p.dec, a, p.bt, p.grid, s));
   else if (p.path == PATH_NVFP4) e = launch_gemm_nvfp4(a, p.bt, p.grid, s);
   else if (p.path == PATH_MXFP4A) e = launch_gemm_mxfp4a(a, p.bt, p.grid, s);
+  else if (p.path == PATH_MXFP4X) e = launch_gemm_mxfp4x(a, p.bt, p.grid, s);
   else e = launch_gemm_mxfp4(a, p.bt, p.grid, s);
   if (e != cudaSuccess || !p.sk || p.small) return e;  // the register-decode kernel finishes cut tiles itself
   // tiles cut between CTAs: sum their partial slots, one CTA per 32 token columns of a tile
@@ -353,6 +364,9 @@ bool act_maps(GemmArgs& a, const hq_format_t* f, const hq_act_t* A, int64_t rows
   if (f->act_type == HQ_A_MXFP8)
     return encode_2d(&a.tmap_a, A->data, false, K, rows, 128, box_rows, true) &&
            encode_2d(&a.tmap_sf, A->scale, false, K / 32, rows, 16, box_rows, false);
+  if (f->act_type == HQ_A_MXFP4)
+    return encode_2d(&a.tmap_a, A->data, false, K / 2, rows, 128, box_rows, true) &&
+           encode_2d(&a.tmap_sf, A->scale, false, K / 32, rows, 16, box_rows, false);
   return encode_2d(&a.tmap_a, A->data, false, K / 2, rows, 128, box_rows, true) &&
          encode_2d(&a.tmap_sf, A->scale, false, K / 16, rows, 16, box_rows, false);
 }
@@ -366,7 +380,7 @@ extern "C" {
 
 size_t hq_packed_bytes(const hq_format_t* fmt) {
   if (check_format(fmt) != HQ_OK) return 0;
-  return (size_t)pack_geom(fmt->weight_type, fmt->N, fmt->K, fmt->num_experts).total_bytes;
+  return (size_t)pack_geom(pack_kind(fmt), fmt->N, fmt->K, fmt->num_experts).total_bytes;
 }
 
 hq_status_t hq_pack_weights(const hq_format_t* fmt, const uint8_t* codes, const void* scales, const uint8_t* zeros,
@@ -377,7 +391,7 @@ hq_status_t hq_pack_weights(const hq_format_t* fmt, const uint8_t* codes, const 
   if (fmt->has_zero && !zeros) return HQ_ERR_INVALID_ARG;
   if (fmt->has_global_scale && !global_scale) return HQ_ERR_INVALID_ARG;
   if (!aligned16(packed)) return HQ_ERR_ALIGNMENT;
-  return cuda_status(launch_pack(0, fmt->weight_type, fmt->N, fmt->K, fmt->num_experts, codes, scales, zeros,
+  return cuda_status(launch_pack(0, pack_kind(fmt), fmt->N, fmt->K, fmt->num_experts, codes, scales, zeros,
                                  global_scale, packed, (cudaStream_t)stream));
 }
 
@@ -388,7 +402,7 @@ hq_status_t hq_unpack_weights(const hq_format_t* fmt, const void* packed, uint8_
   if (!codes || !scales || !packed) return HQ_ERR_INVALID_ARG;
   if (fmt->has_zero && !zeros) return HQ_ERR_INVALID_ARG;
   if (!aligned16(packed)) return HQ_ERR_ALIGNMENT;
-  return cuda_status(launch_pack(1, fmt->weight_type, fmt->N, fmt->K, fmt->num_experts, codes, scales, zeros,
+  return cuda_status(launch_pack(1, pack_kind(fmt), fmt->N, fmt->K, fmt->num_experts, codes, scales, zeros,
                                  global_scale, const_cast<void*>(packed), (cudaStream_t)stream));
 }
 
@@ -411,6 +425,18 @@ int32_t hq_kernels_per_call(const hq_format_t* fmt, int64_t M_or_T, int32_t topk
   return n;
 }
 
+hq_status_t hq_launch_plan(const hq_format_t* fmt, int64_t M_or_T, int32_t topk, int32_t moe, int32_t* plan_out) {
+  if (check_format(fmt) != HQ_OK || M_or_T < 1 || topk < 1 || !plan_out) return HQ_ERR_INVALID_ARG;
+  const Plan p = make_plan(fmt, M_or_T, topk, moe != 0, num_sms());
+  plan_out[0] = p.small;
+  plan_out[1] = p.small ? p.dec : p.path;
+  plan_out[2] = p.bt;
+  plan_out[3] = p.sk;
+  plan_out[4] = p.grid;
+  plan_out[5] = p.grouped;
+  return HQ_OK;
+}
+
 hq_status_t hq_workspace_init(void* workspace, size_t bytes, hq_stream_t stream) {
   if (!workspace || bytes == 0) return HQ_ERR_INVALID_ARG;
   return cuda_status(cudaMemsetAsync(workspace, 0, bytes, (cudaStream_t)stream));
@@ -425,14 +451,14 @@ hq_status_t hq_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* packe
   if (!A || !A->data || !packedW || !C) return HQ_ERR_INVALID_ARG;
   if (fmt->act_type == HQ_A_E4M3_TOKEN && !A->scale) return HQ_ERR_INVALID_ARG;
   if (fmt->act_type == HQ_A_NVFP4 && (!A->scale || !A->global_scale)) return HQ_ERR_INVALID_ARG;
-  if (fmt->act_type == HQ_A_MXFP8 && !A->scale) return HQ_ERR_INVALID_ARG;
+  if ((fmt->act_type == HQ_A_MXFP8 || fmt->act_type == HQ_A_MXFP4) && !A->scale) return HQ_ERR_INVALID_ARG;
   if (!aligned16(A->data) || !aligned16(packedW) || (A->scale && act_scale_row_bytes(fmt) > 0 && !aligned16(A->scale)))
     return HQ_ERR_ALIGNMENT;
   const int sms = num_sms();
   if (sms < 1) return HQ_ERR_CUDA;
   const Plan p = make_plan(fmt, M, 1, false, sms);
   if (!workspace || ws_bytes < p.ws_bytes) return HQ_ERR_WORKSPACE;
-  const PackGeom g = pack_geom(fmt->weight_type, N, K, 1);
+  const PackGeom g = pack_geom(pack_kind(fmt), N, K, 1);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   GemmArgs a{};
   a.w = static_cast<const uint8_t*>(packedW);
@@ -484,7 +510,7 @@ hq_status_t moe_call(const hq_format_t* fmt, const hq_act_t* A, const void* pack
   if (!A || !A->data || !packedW || !C || !topk_ids) return HQ_ERR_INVALID_ARG;
   if (fmt->act_type == HQ_A_E4M3_TOKEN && !A->scale) return HQ_ERR_INVALID_ARG;
   if (fmt->act_type == HQ_A_NVFP4 && (!A->scale || !A->global_scale)) return HQ_ERR_INVALID_ARG;
-  if (fmt->act_type == HQ_A_MXFP8 && !A->scale) return HQ_ERR_INVALID_ARG;
+  if ((fmt->act_type == HQ_A_MXFP8 || fmt->act_type == HQ_A_MXFP4) && !A->scale) return HQ_ERR_INVALID_ARG;
   if (!aligned16(A->data) || !aligned16(packedW) || (act_scale_row_bytes(fmt) > 0 && !aligned16(A->scale)))
     return HQ_ERR_ALIGNMENT;
   const int sms = num_sms();
@@ -496,7 +522,7 @@ hq_status_t moe_call(const hq_format_t* fmt, const hq_act_t* A, const void* pack
   const int64_t a_rows = combine ? T * topk : T;  // activation rows: tokens, or routed rows for the combine
   const int a_div = combine ? 1 : topk;          // routed row -> activation row
   const int64_t E = fmt->num_experts;
-  const PackGeom g = pack_geom(fmt->weight_type, fmt->N, fmt->K, E);
+  const PackGeom g = pack_geom(pack_kind(fmt), fmt->N, fmt->K, E);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int* status = reinterpret_cast<int*>(ws);
   int* counts = reinterpret_cast<int*>(ws + p.off_counts);

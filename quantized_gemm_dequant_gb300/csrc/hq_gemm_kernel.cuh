@@ -91,8 +91,11 @@ template <int PATH, int BT>
 struct Cfg {
   static constexpr bool MX = PATH == PATH_MXFP4 || PATH == PATH_MXFP4A;  // MXFP4 weights
   static constexpr bool AMX = PATH == PATH_MXFP4A;                        // MXFP8 activations
-  static constexpr int KSTAGE = PATH == PATH_NVFP4 ? 256 : 128;  // K per weight block
-  static constexpr int W_BLK = PATH == PATH_INT4 ? 8576 : (PATH == PATH_NVFP4 ? 18432 : 8704);
+  // packed e2m1 on both operands with scale warps feeding both scale sets: NVFP4, and MXFP4 x MXFP4
+  static constexpr bool NVF = PATH == PATH_NVFP4 || PATH == PATH_MXFP4X;
+  static constexpr bool XMX = PATH == PATH_MXFP4X;  // the MX variant (e8m0 per 32, two scales per MMA step)
+  static constexpr int KSTAGE = NVF ? 256 : 128;  // K per weight block
+  static constexpr int W_BLK = PATH == PATH_INT4 ? 8576 : (NVF ? 18432 : 8704);
   static constexpr int W_REGION = ((W_BLK + 1023) / 1024) * 1024;
   static constexpr int X_REGION = MX ? 16384 : 0;  // expanded e2m1 A tile per weight stage
   static constexpr int SUB = PATH == PATH_INT4 ? 2 : 1;             // activation stages per weight block
@@ -101,17 +104,17 @@ struct Cfg {
   static constexpr int SF_ROWS = BT < 32 ? 32 : BT;
   // NVFP4 activation scales: dense rows are 16 bytes apart; MoE rows come in gather4 groups of four,
   // each group in its own 128-byte slot (row j at (j/4)*128 + (j%4)*16)
-  static constexpr int ASF_REGION = (PATH == PATH_NVFP4 || AMX) ? ((SF_ROWS * 32 + 1023) / 1024) * 1024 : 0;
+  static constexpr int ASF_REGION = (NVF || AMX) ? ((SF_ROWS * 32 + 1023) / 1024) * 1024 : 0;
   static constexpr int A_STAGE = ACT_REGION + ASF_REGION;
   static constexpr int W_STAGE = W_REGION + X_REGION;
   static constexpr int RING_BUDGET = 216 * 1024;
   static constexpr int SW = PATH == PATH_INT4 ? (BT <= 64 ? 12 : 4)
-                                              : (PATH == PATH_NVFP4 ? (BT <= 64 ? 8 : 4) : (BT <= 64 ? 6 : 3));
+                                              : (NVF ? (BT <= 64 ? 8 : 4) : (BT <= 64 ? 6 : 3));
   static constexpr int SA_FIT = (RING_BUDGET - SW * W_STAGE) / A_STAGE;
   static constexpr int SA = SA_FIT > 16 ? 16 : SA_FIT;
   static constexpr int CB = BT < 32 ? 1 : BT / 32;  // scale-factor columns per MMA step for B
   static constexpr int SFB_STEP = CB < 4 ? 4 : CB;  // column stride per MMA step (kept 4-aligned)
-  static constexpr int SF_STAGE_COLS = PATH == PATH_NVFP4 ? 16 + 4 * SFB_STEP : 4;
+  static constexpr int SF_STAGE_COLS = NVF ? 16 + 4 * SFB_STEP : 4;
   static constexpr int NA = 4;  // INT4: tensor-memory A slots of 64 columns
   static constexpr int RING_BYTES = SW * W_STAGE + SA * A_STAGE;
   // INT4 256-token tiles keep the epilogue's per-column rows and multipliers (MoE) in shared memory: two pieces x
@@ -122,7 +125,7 @@ struct Cfg {
   static constexpr int SMEM_BYTES = SMEM_RAW < 120 * 1024 ? 120 * 1024 : SMEM_RAW;
   static_assert(SA >= 2, "activation ring too small");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-  static_assert(PATH != PATH_NVFP4 || 256 + SW * SF_STAGE_COLS <= 512, "tensor memory");
+  static_assert(!NVF || 256 + SW * SF_STAGE_COLS <= 512, "tensor memory");
   static_assert(!MX || 256 + 4 * SW + (AMX ? SW * SFB_STEP : 8) <= 512, "tensor memory");
 };
 
@@ -335,12 +338,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
   if (tid == WPROD_WARP * 32) {
     for (int s = 0; s < C::SW; ++s) {
       mbar_init(&sh.w_full[s], 1);
-      mbar_init(&sh.w_empty[s], PATH == PATH_INT4 ? 8 : (PATH == PATH_NVFP4 ? 4 + 1 : 8 + 1));
+      mbar_init(&sh.w_empty[s], PATH == PATH_INT4 ? 8 : (C::NVF ? 4 + 1 : 8 + 1));
       mbar_init(&sh.ready[s], C::MX ? 8 : 4);
     }
     for (int s = 0; s < C::SA; ++s) {
       mbar_init(&sh.a_full[s], 1);
-      mbar_init(&sh.a_empty[s], (PATH == PATH_NVFP4 || C::AMX) ? 4 + 1 : 1);
+      mbar_init(&sh.a_empty[s], (C::NVF || C::AMX) ? 4 + 1 : 1);
     }
     for (int a = 0; a < C::NA; ++a) {
       mbar_init(&sh.afull[a], 8);
@@ -371,7 +374,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
   }
   if (tid == APROD_WARP * 32) {
     prefetch_tmap(&args.tmap_a);
-    if (PATH == PATH_NVFP4 || C::AMX) prefetch_tmap(&args.tmap_sf);
+    if (C::NVF || C::AMX) prefetch_tmap(&args.tmap_sf);
   }
   pdl_trigger();
   pdl_wait();  // no global memory a previous kernel may write is touched before this point (weights aside)
@@ -480,11 +483,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
               uint8_t* dst = aring + as * C::A_STAGE;
               // x offset of this stage in the tensor map's element units (bf16: 64 per stage; bytes: 128)
               const int x = PATH == PATH_INT4 ? g * 128 + j * 64 : g * 128;
-              mbar_arrive_expect_tx(&sh.a_full[as], A_BOX_BYTES + ((PATH == PATH_NVFP4 || C::AMX) ? SF_BOX_BYTES : 0));
+              mbar_arrive_expect_tx(&sh.a_full[as], A_BOX_BYTES + ((C::NVF || C::AMX) ? SF_BOX_BYTES : 0));
               tma_load_2d(dst, &args.tmap_a, x, rbase, &sh.a_full[as]);
               // block scales: NVFP4 16 bytes per 256-K stage; MXFP8 the 16-byte group of four 128-K stages
-              if (PATH == PATH_NVFP4 || C::AMX)
-                tma_load_2d(dst + C::ACT_REGION, &args.tmap_sf, C::AMX ? (g >> 2) * 16 : g * 16, rbase, &sh.a_full[as]);
+              if (C::NVF || C::AMX)
+                tma_load_2d(dst + C::ACT_REGION, &args.tmap_sf, C::AMX ? (g >> 2) * 16 : (C::XMX ? (g >> 1) * 16 : g * 16),
+                            rbase, &sh.a_full[as]);
               armed |= 1u << as;
               if (++as == C::SA) {
                 as = 0;
@@ -526,14 +530,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
             uint8_t* dst = aring + as * C::A_STAGE;
             const int x = PATH == PATH_INT4 ? g * 128 + j * 64 : g * 128;
             if (lane == 0)
-              mbar_arrive_expect_tx(&sh.a_full[as], A_BOX_BYTES + ((PATH == PATH_NVFP4 || C::AMX) ? SF_BOX_BYTES : 0));
+              mbar_arrive_expect_tx(&sh.a_full[as], A_BOX_BYTES + ((C::NVF || C::AMX) ? SF_BOX_BYTES : 0));
             __syncwarp();
             for (int i = lane * 4; i < BT; i += 128) {
               uint8_t* d = dst + (i >> 3) * 1024 + (i & 7) * 128;
               tma_gather4(d, &args.tmap_a, x, sh.rows_tok[i], sh.rows_tok[i + 1], sh.rows_tok[i + 2],
                           sh.rows_tok[i + 3], &sh.a_full[as]);
-              if (PATH == PATH_NVFP4 || C::AMX)
-                tma_gather4(dst + C::ACT_REGION + (i >> 2) * 128, &args.tmap_sf, C::AMX ? (g >> 2) * 16 : g * 16,
+              if (C::NVF || C::AMX)
+                tma_gather4(dst + C::ACT_REGION + (i >> 2) * 128, &args.tmap_sf,
+                            C::AMX ? (g >> 2) * 16 : (C::XMX ? (g >> 1) * 16 : g * 16),
                             sh.rows_tok[i],
                             sh.rows_tok[i + 1], sh.rows_tok[i + 2], sh.rows_tok[i + 3], &sh.a_full[as]);
             }
@@ -591,16 +596,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
                 const uint64_t bd = smem_desc(act + i * 32, 16, 1024, 2);
                 umma_bf16_ts(tmem, a_t + i * 8, bd, idesc, (first && i == 0) ? 0u : 1u);
               }
-            } else if (PATH == PATH_NVFP4) {
-              constexpr uint32_t idesc = idesc_block_scaled(128, BT, 1, 1, 0, 0, 0);
+            } else if (C::NVF) {
+              constexpr uint32_t idesc = idesc_block_scaled(128, BT, 1, 1, C::XMX ? 1 : 0, 0, 0);
               const uint32_t wa = smem_u32(wring + ws * C::W_STAGE);
               const uint32_t sf = tmem + 256 + ws * C::SF_STAGE_COLS;
 #pragma unroll
               for (int t = 0; t < 4; ++t) {
                 const uint64_t ad = smem_desc(wa + t * 32, 16, 1024, 2);
                 const uint64_t bd = smem_desc(act + t * 32, 16, 1024, 2);
-                umma_nvf4_ss(tmem, ad, bd, idesc, sf + 4 * t, sf + 16 + t * C::SFB_STEP,
-                             (first && t == 0) ? 0u : 1u);
+                if (C::XMX)
+                  umma_mxf4_ss(tmem, ad, bd, idesc, sf + 4 * t, sf + 16 + t * C::SFB_STEP, (first && t == 0) ? 0u : 1u);
+                else
+                  umma_nvf4_ss(tmem, ad, bd, idesc, sf + 4 * t, sf + 16 + t * C::SFB_STEP,
+                               (first && t == 0) ? 0u : 1u);
               }
             } else {
               const uint32_t xa = smem_u32(wring + ws * C::W_STAGE + C::W_REGION);
@@ -739,7 +747,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
     };
     // mainloop role for the next nblk weight blocks, in ring order
     auto mainloop = [&](int nblk) -> bool {
-      for (int k = 0; !(PATH == PATH_NVFP4 && warp >= 4) && k < nblk; ++k) {  // NVFP4 warps 4-7: epilogue only
+      for (int k = 0; !(C::NVF && warp >= 4) && k < nblk; ++k) {  // NVFP4 warps 4-7: epilogue only
         if (!waitf(&sh.w_full[ws], wph)) return false;
         uint8_t* wb = wring + ws * C::W_STAGE;
         if (PATH == PATH_INT4) {
@@ -779,7 +787,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
             aslph ^= 1;
           }
         } else {
-          if (PATH == PATH_NVFP4 && warp < 4) {
+          if (C::NVF && warp < 4) {
             // scale factors -> tensor memory (replicated in every lane quarter)
             const uint32_t sf = tmem + lane_base + 256 + ws * C::SF_STAGE_COLS;
             // lane l's 16 words (4 MMA steps x 4 row groups) are contiguous: four 16-byte loads
@@ -796,13 +804,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
             tmem_st_x<16>(sf, v);
             if (!waitf(&sh.a_full[as], aph)) return false;
             const uint8_t* asf = aring + as * C::A_STAGE + C::ACT_REGION;
-            // one 16-byte load per activation row holds its scales of all four MMA steps
+            // one 16-byte load per activation row holds its scales of all four MMA steps (MXFP4: 8 bytes, two e8m0
+            // per step, the half of a 16-byte group of two 256-K stages; each pair goes into both halves of its word)
             uint4 rq[C::CB];
 #pragma unroll
             for (int cc = 0; cc < C::CB; ++cc) {
               const int j = cc * 32 + lane;
               const int off = (args.moe && !args.grouped) ? (j >> 2) * 128 + (j & 3) * 16 : j * 16;
-              rq[cc] = *reinterpret_cast<const uint4*>(asf + off);
+              if (C::XMX) {
+                const uint2 h = *reinterpret_cast<const uint2*>(asf + off + 8 * (gk & 1));
+                rq[cc] = make_uint4((h.x & 0xFFFFu) * 0x10001u, (h.x >> 16) * 0x10001u, (h.y & 0xFFFFu) * 0x10001u,
+                                    (h.y >> 16) * 0x10001u);
+              } else {
+                rq[cc] = *reinterpret_cast<const uint4*>(asf + off);
+              }
             }
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
@@ -858,10 +873,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
           if (lane == 0) {
             mbar_arrive(&sh.ready[ws]);
             mbar_arrive(&sh.w_empty[ws]);
-            if (PATH == PATH_NVFP4 || (C::AMX && warp < 4)) mbar_arrive(&sh.a_empty[as]);
+            if (C::NVF || (C::AMX && warp < 4)) mbar_arrive(&sh.a_empty[as]);
           }
           ++gk;
-          if (PATH == PATH_NVFP4 || C::AMX) {
+          if (C::NVF || C::AMX) {
             if (++as == C::SA) {
               as = 0;
               aph ^= 1;

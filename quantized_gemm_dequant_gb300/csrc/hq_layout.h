@@ -61,6 +61,10 @@
 //                   (l*16 + t*4 + c) holds the 4 scales of MMA step t (64 K) of
 //                   row 32c + l (the 16 words of lane l are contiguous)
 //    global scales: fp32 [E] after the last expert's blocks
+//  MXFP4 with MXFP4 activations (WK_MXFP4_X), K stage = 256: codes as NVFP4, then
+//    [16384, 18432) e8m0 block-32 scales as tensor-memory words in the NVFP4 word
+//                   order: word (l*16 + t*4 + c) holds the two scales of MMA step t
+//                   (64 K) of row 32c + l as bytes (s0, s1, s0, s1)
 //  MXFP4, K stage = 128:
 //    [0, 8192)      e2m1 codes, 8 bytes (16 K) per piece, piece p = r*8 + c lands in
 //                   the low half of swizzled 16-byte chunk c of row r
@@ -81,7 +85,8 @@ enum WeightKind {
   WK_MXINT4 = 7,
   WK_E4M3 = 8,
   WK_UINT1_ZP = 9,
-  WK_UINT3_ZP = 10
+  WK_UINT3_ZP = 10,
+  WK_MXFP4_X = 11  // MXFP4 weights packed for MXFP4 activations (not an API format: chosen by the activation type)
 };
 // Decode variants of the register-decode kernel, one per integer / e4m3 weight layout
 enum DecodeKind { DEC_INT4 = 0, DEC_MXINT4 = 1, DEC_INT8 = 2, DEC_E4M3 = 3, DEC_UINT2 = 4, DEC_UINT1 = 5, DEC_UINT3 = 6 };
@@ -99,7 +104,8 @@ inline int decode_kind(int weight_type) {
 // Formats only the register-decode kernel reads (any token count)
 inline bool register_decode_only(int weight_type) { return weight_type >= WK_INT8_SYM; }
 // tcgen05 kernel variants; PATH_MXFP4A: MXFP4 weights with MXFP8 activations (e8m0 block scales on both operands)
-enum KernelPath { PATH_INT4 = 0, PATH_NVFP4 = 1, PATH_MXFP4 = 2, PATH_MXFP4A = 3 };
+// PATH_MXFP4X: MXFP4 weights with MXFP4 activations (e8m0 block scales on both operands, packed e2m1 in the MMA)
+enum KernelPath { PATH_INT4 = 0, PATH_NVFP4 = 1, PATH_MXFP4 = 2, PATH_MXFP4A = 3, PATH_MXFP4X = 4 };
 
 constexpr int TILE_N = 128;  // weight rows per tile (the UMMA M dimension)
 
@@ -141,6 +147,10 @@ inline PackGeom pack_geom(int weight_type, int64_t N, int64_t K, int64_t E) {
     g.path = PATH_INT4;
     g.kstage = 128;
     g.blk_bytes = 6144 + 256 + 128;
+  } else if (weight_type == WK_MXFP4_X) {
+    g.path = PATH_MXFP4X;
+    g.kstage = 256;
+    g.blk_bytes = 16384 + 2048;
   } else if (weight_type == WK_NVFP4) {
     g.path = PATH_NVFP4;
     g.kstage = 256;

@@ -210,7 +210,7 @@ __global__ void pack_kernel(PackArgs p, uint8_t* codes, uint8_t* scales, uint8_t
         if (DIR == 0) *zdst = valid ? (uint8_t)(*zsrc & 0xF) : (uint8_t)0;
         else if (valid) *zsrc = *zdst;
       }
-    } else if (p.wt == WK_NVFP4) {
+    } else if (p.wt == WK_NVFP4 || p.wt == WK_MXFP4_X) {
       for (int kb = 0; kb < 128; ++kb) {
         const int c = kb >> 4;
         uint8_t* d = blk + (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4) + (kb & 15);
@@ -219,6 +219,18 @@ __global__ void pack_kernel(PackArgs p, uint8_t* codes, uint8_t* scales, uint8_t
         else if (valid) *s = *d;
       }
       const int l = r & 31, cq = r >> 5;
+      if (p.wt == WK_MXFP4_X) {  // two e8m0 scales per MMA step, written twice in the word
+        const int64_t nb = p.K / 32;
+        for (int tt = 0; tt < 4; ++tt) {
+          uint8_t* d = blk + 16384 + (l * 16 + tt * 4 + cq) * 4;
+          uint8_t* s = scales + (e * p.N + n) * nb + ks * 8 + tt * 2;
+          for (int b = 0; b < 4; ++b) {
+            if (DIR == 0) d[b] = valid ? s[b & 1] : (uint8_t)0;
+            else if (valid && b < 2) s[b] = d[b];
+          }
+        }
+        continue;
+      }
       const int64_t nb = p.K / 16;
       for (int tt = 0; tt < 4; ++tt) {
         uint8_t* d = blk + 16384 + (l * 16 + tt * 4 + cq) * 4;

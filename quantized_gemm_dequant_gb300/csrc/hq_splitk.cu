@@ -141,6 +141,8 @@ cudaError_t launch_splitk_reduce(int path, const GemmArgs& a, int bt, int gemm_g
       return launch_kernel(splitk_reduce_kernel<PATH_MXFP4>, dim3(grid), dim3(RED_THREADS), 0, stream, a, bt, gemm_grid);
     case PATH_MXFP4A:
       return launch_kernel(splitk_reduce_kernel<PATH_MXFP4A>, dim3(grid), dim3(RED_THREADS), 0, stream, a, bt, gemm_grid);
+    case PATH_MXFP4X:
+      return launch_kernel(splitk_reduce_kernel<PATH_MXFP4X>, dim3(grid), dim3(RED_THREADS), 0, stream, a, bt, gemm_grid);
     default:
       return cudaErrorInvalidValue;
   }

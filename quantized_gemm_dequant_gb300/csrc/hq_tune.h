@@ -16,6 +16,7 @@ enum TuneClass {
   TC_NVFP4 = 2,   // NVFP4 x NVFP4
   TC_MXFP4 = 3,   // MXFP4 x per-token FP8
   TC_MXFP4A = 4,  // MXFP4 x MXFP8
+  TC_MXFP4X = 5,  // MXFP4 x MXFP4
 };
 
 // One choice.  -1 / 0 in a field leave it to the built-in rule.

@@ -37,6 +37,18 @@ def test_host_only_queries_work_without_a_gpu():
     assert hq.packed_bytes(hq.make_format("int4_sym", 100, 100)) == 0
     assert hq.status_string(hq.HQ_ERR_BAD_ROUTING).startswith("top-k")
     assert set(hq.EXPORTS) == set(declared())
+    # the launch plan is host logic: register-decode kernel for small M, tcgen05 for large M, formats only the
+    # register-decode kernel reads at any M, MXFP4 x MXFP4 on its own tcgen05 variant, bad arguments refused
+    assert hq.launch_plan(f, 1)["kernel"] == "regdec"
+    big = hq.launch_plan(f, 8192)
+    assert big["kernel"] == "umma" and big["variant"] == 0 and big["bt"] == 256
+    assert hq.launch_plan(hq.make_format("uint3_zp", 4096, 4096), 4096)["kernel"] == "regdec"
+    x = hq.launch_plan(hq.make_format("mxfp4", 4096, 7168, act_type=hq.HQ_A_MXFP4), 1024)
+    assert x["kernel"] == "umma" and x["variant"] == 4
+    with pytest.raises(hq.HQError):
+        hq.launch_plan(f, 0)
+    # MXFP4 weights for MXFP4 activations are packed like NVFP4 (256-K blocks of 18432 bytes)
+    assert hq.packed_bytes(hq.make_format("mxfp4", 256, 1024, act_type=hq.HQ_A_MXFP4)) == 2 * 4 * 18432
 
 
 def _lib():

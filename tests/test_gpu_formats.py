@@ -172,3 +172,71 @@ def test_mxfp8_act_exact_pow2_bit_exact(lib):
 def test_mxfp8_act_needs_k_multiple_of_512(lib):
     fmt = lib.make_format("mxfp4", 256, 640, act_type=lib.HQ_A_MXFP8)
     assert lib.packed_bytes(fmt) == 0
+
+
+# ------------------------------------------------------------------ MXFP4 weights x MXFP4 activations (W4A4, MX)
+MX4 = dict(kind="dense", wfmt="mxfp4", afmt="mxfp4", G=32)
+
+
+def test_mxfp4_act_repack_round_trip_bit_exact(lib):
+    """MXFP4 weights meant for MXFP4 activations take their own packed layout (packed e2m1 in the MMA)."""
+    E, N, K = 2, 300, 1024
+    gen = torch.Generator().manual_seed(23)
+    codes = torch.randint(0, 256, (E, N, K // 2), generator=gen, dtype=torch.uint8)
+    scales = torch.randint(0, 256, (E, N, K // 32), generator=gen, dtype=torch.uint8)
+    fmt = lib.make_format("mxfp4", N, K, E, act_type=lib.HQ_A_MXFP4)
+    packed = lib.pack_weights(fmt, codes.cuda(), scales.cuda())
+    c2 = torch.zeros_like(codes).cuda()
+    s2 = torch.zeros_like(scales).cuda()
+    lib.unpack_weights(fmt, packed, c2, s2)
+    torch.cuda.synchronize()
+    assert torch.equal(c2.cpu(), codes) and torch.equal(s2.cpu(), scales)
+
+
+@pytest.mark.parametrize("M", [1, 16, 100, 300])
+def test_mxfp4_act_dense_parity(lib, M):
+    """The microscaled W4A4 variant ("W8A8 / W4A8 / W4A4"): packed e2m1 on both operands, e8m0 block scales on both
+    (kind::mxf4nvf4, scale_vec::2X)."""
+    inp = make_dense(MX4, M, seed=M + 5, N=320, K=1024)
+    fmt, packed = lib.pack_inputs(inp, "cuda")
+    act = {k: v.cuda() for k, v in inp["a"].items()}
+    y = lib.gemm(fmt, act, packed, M)
+    torch.cuda.synchronize()
+    R.assert_parity(y, R.dense_ref(inp), f"mxfp4 x mxfp4 M={M}")
+
+
+@pytest.mark.parametrize("path", ["indexed", "grouped"])
+@pytest.mark.parametrize("T", [5, 60, 300])
+def test_mxfp4_act_moe_parity(lib, monkeypatch, path, T):
+    monkeypatch.setenv("HQ_MOE_PATH", path)
+    inp = make_moe(dict(MX4, kind="moe", topk=3), T, seed=T + 1, E=6, N=256, K=1024, topk=3)
+    fmt, packed = lib.pack_inputs(inp, "cuda")
+    act = {k: v.cuda() for k, v in inp["a"].items()}
+    y = lib.moe_gemm(fmt, act, packed, inp["ids"].cuda(), inp["topk_w"].cuda())
+    torch.cuda.synchronize()
+    R.assert_parity(y, R.moe_ref(inp), f"moe mxfp4 x mxfp4 {path} T={T}")
+
+
+def test_mxfp4_act_exact_pow2_bit_exact(lib):
+    """e2m1 on both sides with power-of-two block scales: every partial sum is exact in fp32, so C equals the bf16
+    rounding of the exact result bit for bit."""
+    gen = torch.Generator().manual_seed(17)
+    M, N, K = 24, 256, 1024
+    jw = torch.randint(-1, 2, (N, K // 32), generator=gen)
+    ja = torch.randint(-2, 2, (M, K // 32), generator=gen)
+    inp = dict(M=M, N=N, K=K, wfmt="mxfp4", afmt="mxfp4", G=32,
+               w=dict(codes=torch.randint(0, 256, (N, K // 2), generator=gen, dtype=torch.uint8),
+                      scales=(jw + 127).to(torch.uint8)),
+               a=dict(data=torch.randint(0, 256, (M, K // 2), generator=gen, dtype=torch.uint8),
+                      scale=(ja + 127).to(torch.uint8)))
+    fmt, packed = lib.pack_inputs(inp, "cuda")
+    y = lib.gemm(fmt, {k: v.cuda() for k, v in inp["a"].items()}, packed, M)
+    torch.cuda.synchronize()
+    ref = R.dense_ref(inp)
+    assert np.max(np.abs(ref)) < 2 ** 20
+    assert torch.equal(y.cpu(), torch.from_numpy(np.asarray(ref, dtype=np.float32)).to(torch.bfloat16))
+
+
+def test_mxfp4_act_needs_k_multiple_of_512(lib):
+    fmt = lib.make_format("mxfp4", 256, 640, act_type=lib.HQ_A_MXFP4)
+    assert lib.packed_bytes(fmt) == 0

@@ -38,7 +38,7 @@ def dense_layers(lib):
     return get
 
 
-OTHER_DENSE = ["w8a16", "w2a16", "w1a16", "w3a16", "mxint4_a16", "fp8w_a16", "w4a8_mx"]
+OTHER_DENSE = ["w8a16", "w2a16", "w1a16", "w3a16", "mxint4_a16", "fp8w_a16", "w4a8_mx", "w4a4_mx"]
 
 
 @pytest.mark.parametrize("cfg,M", [("w4a16_sym", 8)] + [("w4a16_asym", m) for m in CONFIGS["w4a16_asym"]["sizes"]]

@@ -15,13 +15,14 @@ FORMS = {
     "uint4_zp": dict(kind="moe", wfmt="uint4_zp", afmt="bf16", G=128),
     "nvfp4": dict(kind="moe", wfmt="nvfp4", afmt="nvfp4", G=16),
     "mxfp4": dict(kind="moe", wfmt="mxfp4", afmt="e4m3_tok", G=32),
+    "mxfp4_mx": dict(kind="moe", wfmt="mxfp4", afmt="mxfp4", G=32),  # MXFP4 x MXFP4 (K a multiple of 512)
 }
 
 
 def _down_case(wfmt, T, topk=3, E=5, N=264, K=None, seed=0):
     """Expert weights, routing and the T*topk routed activation rows (quantized to the format's activation type)."""
     c = dict(FORMS[wfmt], topk=topk)
-    K = K or (768 if wfmt == "nvfp4" else 640)
+    K = K or {"nvfp4": 768, "mxfp4_mx": 1024}.get(wfmt, 640)
     inp = W.make_moe(c, T, seed=seed, E=E, N=N, K=K, topk=topk)
     rows = W.acts_fp32(seed + 7, T * topk, K, outliers=c["afmt"] == "nvfp4")
     inp["a"] = W.quantize_acts(c["afmt"], rows)
