@@ -12,6 +12,8 @@
 // zero keeps its sign.
 //
 // Memory-bound kernels: 16-byte loads of 8 bf16, grids in multiples of the SM count, programmatic dependent launch.
+// Each division by a scale is taken as a multiplication by the scale's correctly rounded reciprocal plus one FMA
+// correction, which yields the correctly rounded quotient (div_by below), so the codes are those of IEEE division.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -60,6 +62,32 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
   return __half2float(__ushort_as_half((uint16_t)(h & 0xFFFFu)));
 }
 
+// x / y rounded to nearest even (IEEE binary32) from yi = RN(1 / y): q = RN(x * yi) is faithful, the residual
+// x - q * y is exact with one FMA, and RN(q + residual * yi) is the correctly rounded quotient (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990).  Valid
+// while the residual stays a normal number: the callers use it only when the scale is at least 2^-100 (every quotient
+// that can round to a nonzero code then has |x| >= 2^-110), and take the plain division otherwise.
+__device__ __forceinline__ float div_by(float x, float y, float yi) {
+  const float q = __fmul_rn(x, yi);
+  const float r = __fmaf_rn(-q, y, x);
+  return __fmaf_rn(r, yi, q);
+}
+constexpr float kDivMinScale = 7.8886091e-31f;  // 2^-100
+
+// largest bf16 magnitude of 8 values (4 words), as the 16-bit pattern: finite non-negative bf16 values order like
+// their bit patterns, so a SIMD unsigned max of the sign-cleared halves suffices
+__device__ __forceinline__ uint32_t bf16x8_absmax_bits(const uint4& v, uint32_t m) {
+  m = __vmaxu2(m, v.x & 0x7FFF7FFFu);
+  m = __vmaxu2(m, v.y & 0x7FFF7FFFu);
+  m = __vmaxu2(m, v.z & 0x7FFF7FFFu);
+  m = __vmaxu2(m, v.w & 0x7FFF7FFFu);
+  return m;
+}
+__device__ __forceinline__ float absmax_bits_to_f32(uint32_t m) {
+  const uint32_t h = (m & 0xFFFFu) > (m >> 16) ? (m & 0xFFFFu) : (m >> 16);
+  return __uint_as_float(h << 16);
+}
+
 __device__ __forceinline__ float block_max(float v, float* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -73,37 +101,58 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   return v;
 }
 
-// FP8 per token: one CTA per row (grid-stride over rows).  K % 8 == 0.
+// 8 bf16 -> 8 e4m3 codes of x / s
+__device__ __forceinline__ uint2 quant8_e4m3(const uint4& w, float s, float si, bool fast) {
+  float f[8];
+  bf16x8_to_f32(w, f);
+  uint32_t b[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    b[i] = fast ? cvt_e4m3x2(div_by(f[2 * i], s, si), div_by(f[2 * i + 1], s, si))
+                : cvt_e4m3x2(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
+  return make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
+}
+
+// FP8 per token: one CTA per row (grid-stride over rows).  K % 8 == 0.  Rows of at most CH * 256 chunks of 8 are
+// read once and kept in registers between the absmax and the quantization; longer rows are read twice (the second
+// read hits L1/L2).
+template <int CH>
 __global__ void __launch_bounds__(AQ_THREADS) act_quant_e4m3_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
                                                                     uint8_t* __restrict__ q, float* __restrict__ s_out) {
   __shared__ float red[AQ_THREADS / 32];
   pdl_trigger();
   pdl_wait();
   const int64_t chunks = K >> 3;
+  const bool cached = chunks <= (int64_t)CH * AQ_THREADS;
   for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
     const uint4* xr = reinterpret_cast<const uint4*>(x + row * K);
-    float m = 0.0f;
-    for (int64_t c = threadIdx.x; c < chunks; c += AQ_THREADS) {
-      float f[8];
-      bf16x8_to_f32(__ldg(xr + c), f);
+    uint4 v[CH];
+    uint32_t mb = 0;
+    if (cached) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+      for (int j = 0; j < CH; ++j) {
+        const int64_t c = threadIdx.x + (int64_t)j * AQ_THREADS;
+        v[j] = c < chunks ? __ldg(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+        mb = bf16x8_absmax_bits(v[j], mb);
+      }
+    } else {
+      for (int64_t c = threadIdx.x; c < chunks; c += AQ_THREADS) mb = bf16x8_absmax_bits(__ldg(xr + c), mb);
     }
-    const float amax = block_max(m, red);
+    const float amax = block_max(absmax_bits_to_f32(mb), red);
     const float s = __fdiv_rn(amax, 448.0f);
+    const float si = __frcp_rn(s);
+    const bool fast = s >= kDivMinScale;
     if (threadIdx.x == 0) s_out[row] = s;
     uint2* qr = reinterpret_cast<uint2*>(q + row * K);
-    for (int64_t c = threadIdx.x; c < chunks; c += AQ_THREADS) {
-      uint2 o = make_uint2(0u, 0u);
-      if (s > 0.0f) {
-        float f[8];
-        bf16x8_to_f32(__ldg(xr + c), f);  // the row was read just above: an L1/L2 hit
-        uint32_t b[4];
+    if (cached) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) b[i] = cvt_e4m3x2(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
-        o = make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
+      for (int j = 0; j < CH; ++j) {
+        const int64_t c = threadIdx.x + (int64_t)j * AQ_THREADS;
+        if (c < chunks) qr[c] = s > 0.0f ? quant8_e4m3(v[j], s, si, fast) : make_uint2(0u, 0u);
       }
-      qr[c] = o;
+    } else {
+      for (int64_t c = threadIdx.x; c < chunks; c += AQ_THREADS)
+        qr[c] = s > 0.0f ? quant8_e4m3(__ldg(xr + c), s, si, fast) : make_uint2(0u, 0u);
     }
   }
 }
@@ -115,14 +164,10 @@ __global__ void __launch_bounds__(AQ_THREADS) act_amax_kernel(const uint16_t* __
   pdl_trigger();
   pdl_wait();
   const uint4* xv = reinterpret_cast<const uint4*>(x);
-  float m = 0.0f;
-  for (int64_t c = (int64_t)blockIdx.x * AQ_THREADS + threadIdx.x; c < n8; c += (int64_t)gridDim.x * AQ_THREADS) {
-    float f[8];
-    bf16x8_to_f32(__ldg(xv + c), f);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
-  }
-  m = block_max(m, red);
+  uint32_t mb = 0;
+  for (int64_t c = (int64_t)blockIdx.x * AQ_THREADS + threadIdx.x; c < n8; c += (int64_t)gridDim.x * AQ_THREADS)
+    mb = bf16x8_absmax_bits(__ldg(xv + c), mb);
+  const float m = block_max(absmax_bits_to_f32(mb), red);
   if (threadIdx.x == 0) partial[blockIdx.x] = m;
 }
 
@@ -150,12 +195,11 @@ __global__ void __launch_bounds__(AQ_THREADS) act_quant_nvfp4_kernel(const uint1
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   uint2* qv = reinterpret_cast<uint2*>(q);
   for (int64_t b = (int64_t)blockIdx.x * AQ_THREADS + threadIdx.x; b < nblk; b += (int64_t)gridDim.x * AQ_THREADS) {
+    const uint4 w0 = __ldg(xv + 2 * b), w1 = __ldg(xv + 2 * b + 1);
     float f[16];
-    bf16x8_to_f32(__ldg(xv + 2 * b), *reinterpret_cast<float(*)[8]>(f));
-    bf16x8_to_f32(__ldg(xv + 2 * b + 1), *reinterpret_cast<float(*)[8]>(f + 8));
-    float mb = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) mb = fmaxf(mb, fabsf(f[i]));
+    bf16x8_to_f32(w0, *reinterpret_cast<float(*)[8]>(f));
+    bf16x8_to_f32(w1, *reinterpret_cast<float(*)[8]>(f + 8));
+    const float mb = absmax_bits_to_f32(bf16x8_absmax_bits(w1, bf16x8_absmax_bits(w0, 0u)));
     uint32_t sb = 0;
     float d = 0.0f;
     if (g > 0.0f) {
@@ -163,8 +207,15 @@ __global__ void __launch_bounds__(AQ_THREADS) act_quant_nvfp4_kernel(const uint1
       d = __fmul_rn(e4m3_to_f32(sb), g);
     }
     uint32_t by[8];
+    if (d >= kDivMinScale) {
+      const float di = __frcp_rn(d);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) by[i] = d > 0.0f ? cvt_e2m1x2(__fdiv_rn(f[2 * i], d), __fdiv_rn(f[2 * i + 1], d)) : 0u;
+      for (int i = 0; i < 8; ++i) by[i] = cvt_e2m1x2(div_by(f[2 * i], d, di), div_by(f[2 * i + 1], d, di));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        by[i] = d > 0.0f ? cvt_e2m1x2(__fdiv_rn(f[2 * i], d), __fdiv_rn(f[2 * i + 1], d)) : 0u;
+    }
     qv[b] = make_uint2(by[0] | (by[1] << 8) | (by[2] << 16) | (by[3] << 24),
                        by[4] | (by[5] << 8) | (by[6] << 16) | (by[7] << 24));
     sf[b] = (uint8_t)sb;
@@ -198,7 +249,7 @@ cudaError_t launch_act_quant(int fp8, const void* x, int64_t M, int64_t K, const
   const int sms = sm_count();
   if (fp8) {
     const int64_t grid = M < 8 * (int64_t)sms ? M : 8 * (int64_t)sms;
-    return launch_kernel(act_quant_e4m3_kernel, dim3((unsigned)grid), dim3(AQ_THREADS), 0, stream,
+    return launch_kernel(act_quant_e4m3_kernel<4>, dim3((unsigned)grid), dim3(AQ_THREADS), 0, stream,
                          (const uint16_t*)x, M, K, (uint8_t*)data, (float*)scale);
   }
   int nparts = 0;
