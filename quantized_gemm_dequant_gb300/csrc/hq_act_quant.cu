@@ -114,8 +114,8 @@ __device__ __forceinline__ uint2 quant8_e4m3(const uint4& w, float s, float si, 
 }
 
 // FP8 per token: one CTA per row (grid-stride over rows).  K % 8 == 0.  Rows of at most CH * 256 chunks of 8 are
-// read once and kept in registers between the absmax and the quantization; longer rows are read twice (the second
-// read hits L1/L2).
+// read once and kept in registers between the absmax and the quantization (with the CTA's next row in flight);
+// longer rows are read twice (the second read hits L1/L2).
 template <int CH>
 __global__ void __launch_bounds__(AQ_THREADS) act_quant_e4m3_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
                                                                     uint8_t* __restrict__ q, float* __restrict__ s_out) {
@@ -124,17 +124,25 @@ __global__ void __launch_bounds__(AQ_THREADS) act_quant_e4m3_kernel(const uint16
   pdl_wait();
   const int64_t chunks = K >> 3;
   const bool cached = chunks <= (int64_t)CH * AQ_THREADS;
+  // register-cached rows: the CTA's next row is loaded while the current one is reduced and quantized
+  uint4 v[CH], nv[CH];
+  auto load_row = [&](int64_t row, uint4 (&dst)[CH]) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + row * K);
+#pragma unroll
+    for (int j = 0; j < CH; ++j) {
+      const int64_t c = threadIdx.x + (int64_t)j * AQ_THREADS;
+      dst[j] = c < chunks ? __ldg(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  if (cached && (int64_t)blockIdx.x < M) load_row(blockIdx.x, v);
   for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
     const uint4* xr = reinterpret_cast<const uint4*>(x + row * K);
-    uint4 v[CH];
+    const int64_t next = row + gridDim.x;
     uint32_t mb = 0;
     if (cached) {
+      if (next < M) load_row(next, nv);
 #pragma unroll
-      for (int j = 0; j < CH; ++j) {
-        const int64_t c = threadIdx.x + (int64_t)j * AQ_THREADS;
-        v[j] = c < chunks ? __ldg(xr + c) : make_uint4(0u, 0u, 0u, 0u);
-        mb = bf16x8_absmax_bits(v[j], mb);
-      }
+      for (int j = 0; j < CH; ++j) mb = bf16x8_absmax_bits(v[j], mb);
     } else {
       for (int64_t c = threadIdx.x; c < chunks; c += AQ_THREADS) mb = bf16x8_absmax_bits(__ldg(xr + c), mb);
     }
@@ -149,6 +157,7 @@ __global__ void __launch_bounds__(AQ_THREADS) act_quant_e4m3_kernel(const uint16
       for (int j = 0; j < CH; ++j) {
         const int64_t c = threadIdx.x + (int64_t)j * AQ_THREADS;
         if (c < chunks) qr[c] = s > 0.0f ? quant8_e4m3(v[j], s, si, fast) : make_uint2(0u, 0u);
+        v[j] = nv[j];
       }
     } else {
       for (int64_t c = threadIdx.x; c < chunks; c += AQ_THREADS)

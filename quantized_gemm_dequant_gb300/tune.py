@@ -52,11 +52,12 @@ PLANS = [
 ]
 
 
-def candidates(cls, moe, key):
+def candidates(cls, moe, key, M=None):
     """Every valid choice for one call (the library also re-checks each); key = M (dense) or routed rows per expert
-    (MoE)."""
+    (MoE, whose tiles are sized by the busiest experts: every tile width up to twice the token count is tried)."""
     out = [dict(AUTO)]
-    umma_bts = [b for b in (16, 32, 64, 128, 256) if b < 2 * max(key, 8)]
+    span = M if (moe and M is not None) else key
+    umma_bts = [b for b in (16, 32, 64, 128, 256) if b < 2 * max(span, 8)]
     if moe and cls in ("nvfp4", "mxfp4a"):
         umma_bts = [b for b in umma_bts if b <= 128]
     if cls == "regdec" or (cls == "int4" and key <= (64 if moe else 256)):
@@ -157,7 +158,7 @@ def sweep(plans, quick, dev):
             rows = []
             c_cfg = W.CONFIGS[cfg]
             key = -(-M * c_cfg["topk"] // c_cfg["E"]) if moe else M
-            for c in candidates(cls, moe, key):
+            for c in candidates(cls, moe, key, M):
                 t, y = (t_auto, y_auto) if c == AUTO else time_choice(fmt, run, M, topk, R, c, bursts, per_burst)
                 ok = t is not None and close(y, y_auto)
                 rows.append(dict(choice=c, ms=t, ok=ok))

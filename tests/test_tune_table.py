@@ -35,7 +35,7 @@ def test_candidates_are_valid():
             for M in sizes:
                 c_cfg = tune.W.CONFIGS[cfg]
                 key = -(-M * c_cfg["topk"] // c_cfg["E"]) if moe else M
-                for c in tune.candidates(cls, moe, key):
+                for c in tune.candidates(cls, moe, key, M):
                     assert c["bt"] in (0, 8, 16, 32, 64, 128, 256)
                     if c["kernel"] == 1:
                         assert c["bt"] <= 32 and (c["slots"] <= 1 or c["bt"] <= 16)
