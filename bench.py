@@ -722,7 +722,8 @@ def _aq_calls(cfg, args, dev):
     afmt, K = c["afmt"], c["K"]
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     calls = []
-    for M in c["sizes"]:
+    sizes = [int(v) for v in args.sizes.split(",")] if getattr(args, "sizes", None) else c["sizes"]
+    for M in sizes:
         R = REPLICAS_OVERRIDE or int(min(12, max(2, -(-3 * l2 // (2 * M * K)))))
         x0 = W.acts_fp32(args.seed, M, K, outliers=afmt == "nvfp4", device=dev).to(torch.bfloat16)
         xs = [x0] + [x0.clone() for _ in range(R - 1)]
