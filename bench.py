@@ -334,6 +334,8 @@ def measure_other_config(cfg_name, args, pk, pk_src, stream, dev):
            "value": round(flops / t / 1e12, 3), "unit": "TFLOP/s",
            "value_note": "one call per size: total FLOPs / sum of the per-size burst medians",
            "roofline": roof, "sweep": sweep}
+    if not args.no_context:
+        out["context_cublas_bf16"] = cublas_context(cfg_name, args, calls, sweep, stream, dev)
     del calls
     torch.cuda.synchronize(dev)
     torch.cuda.empty_cache()
@@ -405,7 +407,7 @@ def run_ours(args):
     roof["launches_per_step"] = sum(1 for (M, *_r) in calls if kernel_name(args.config, M) == roof["kernel"])
 
     e2e = measure_e2e(args, calls, stream, dev) if not args.no_e2e else None
-    ctx = cublas_context(args, calls, sweep, stream, dev) if (rank == 0 and not args.no_context) else None
+    ctx = cublas_context(args.config, args, calls, sweep, stream, dev) if (rank == 0 and not args.no_context) else None
     n_launch = gpu_launches(args.config, fmt, calls) * args.steps
     del calls
     torch.cuda.synchronize(dev)
@@ -510,14 +512,17 @@ def workload_name(cfg):
             f"T in {c['sizes']}, Zipf(1.1) routing")
 
 
-def cublas_context(args, calls, sweep, stream, dev):
+def cublas_context(cfg_name, args, calls, sweep, stream, dev):
     """Context only (the pages compare W4A16 with cuBLAS at small batch): torch.matmul in bf16 on bf16 weights of the
-    same shape, timed with the same protocol (bursts of back-to-back calls over replicas larger than L2)."""
-    c = W.CONFIGS[args.config]
+    same shape, timed with the same protocol (bursts of back-to-back calls over weight replicas that together exceed
+    three L2 sizes, so that cuBLAS too reads its weights from HBM)."""
+    c = W.CONFIGS[cfg_name]
     if c["kind"] != "dense" or c["afmt"] != "bf16":
         return None
-    R = 4
-    wts = [W.weights_fp32(args.seed, 1, c["N"], c["K"], device=dev).to(torch.bfloat16) for _ in range(R)]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    R = int(min(256, max(4, -(-3 * l2 // (2 * c["N"] * c["K"])))))
+    w0 = W.weights_fp32(args.seed, 1, c["N"], c["K"], device=dev).to(torch.bfloat16)
+    wts = [w0] + [w0.clone() for _ in range(R - 1)]
     rows = []
     for (M, call, info, acts, outs, wss), ours in zip(calls, sweep):
         a = acts[0]["data"]

@@ -256,11 +256,12 @@ Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int
   const int per_sm = tc.slots >= 1 && tc.slots <= max_per_sm ? tc.slots : max_per_sm;
   const int64_t slots = (int64_t)per_sm * sms;
   if (p.small) {
-    // Stream-K when the tiles fill less than two rounds of CTA slots; but not when there are fewer blocks than
-    // slots in all (tiny weights): every CTA would hold one block and the fix-up would cost more than running whole
-    // tiles (measured: 1024 x 1024 INT4 at M = 8, 64 blocks, 6.2 -> 5.5 us)
+    // Stream-K when the tiles fill less than two rounds of CTA slots; with fewer blocks than slots in all (tiny
+    // weights) at least two blocks per CTA, so that a cut tile has few contributors to collect (measured: 1024 x 1024
+    // INT4 at M = 8, 64 blocks: one block per CTA 6.0 us, whole tiles 5.5 us, two blocks per CTA 5.2 us)
     const int64_t blocks = p.max_tiles * p.kst;
-    p.sk = (p.max_tiles < 2 * slots && p.kst > 1 && (moe || blocks > slots)) ? 1 : 0;
+    p.sk = (p.max_tiles < 2 * slots && p.kst > 1) ? 1 : 0;
+    if (!moe && p.sk && blocks <= slots && tc.cpb <= 0) tc.cpb = 2;
   } else {
     // UMMA kernel: Stream-K when the tiles fill less than half a wave of SMs (the split then pays for its partial
     // sums and their reduction) or more than one wave but less than two (it evens out the second wave); one
@@ -271,6 +272,10 @@ Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int
   if (tc.sk >= 0) p.sk = (tc.sk && p.kst > 1) ? 1 : 0;
   const int64_t W = p.max_tiles * (p.sk ? p.kst : 1);
   p.grid = (int)(W < slots ? (W < 1 ? 1 : W) : slots);
+  if (p.sk && tc.cpb > 1) {  // fewer CTAs, each with at least cpb K blocks
+    const int64_t g = (W + tc.cpb - 1) / tc.cpb;
+    if (g >= 1 && g < p.grid) p.grid = (int)g;
+  }
   // MoE activations: grouped when tiles are wide (tile::gather4 cannot feed 64+ routed rows per stage fast enough)
   if (moe) {
     const int fm = forced_moe_path();

@@ -305,8 +305,10 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT, DEC>::CTAS_PER_SM)
   int* r_off = reinterpret_cast<int*>(smem + C::OFF_ROUTE);
   int* r_rows = r_off + 528;
   const bool fused = args.ids != nullptr;
+  uint32_t epoch_prev = 0;  // producer: header word 1 (MoE calls read it before routing, hiding the load)
   if (args.moe) {
     pdl_wait();
+    if (producer) epoch_prev = reinterpret_cast<volatile uint32_t*>(args.status)[1];
     const int* counts = args.counts;
     if (fused) {
       int* cnt = reinterpret_cast<int*>(smem + C::OFF_RED);
@@ -323,7 +325,7 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT, DEC>::CTAS_PER_SM)
       for (int j = 0; j < 2; ++j)
         tma_load_2d(smem + s * C::STAGE + j * (BT * 128), &args.tmap_a, pre_x[s] + j * 64, pre_y[s], &sh.full[s]);
     // the workspace epoch is needed only when a partial sum is published or collected
-    sh.epoch = reinterpret_cast<volatile uint32_t*>(args.status)[1] + 1u;
+    sh.epoch = (args.moe ? epoch_prev : reinterpret_cast<volatile uint32_t*>(args.status)[1]) + 1u;
     mbar_arrive(&sh.epoch_bar);
   }
   const int total_tiles = args.moe ? sh.tile_prefix_total * args.n_tiles : args.m_tiles * args.n_tiles;

@@ -26,6 +26,7 @@ struct TuneChoice {
   int sk = -1;       // Stream-K split of K over CTAs: 0 off, 1 on
   int slots = 0;     // CTAs per SM in the persistent grid
   int grouped = -1;  // MoE activations: 0 indexed rows (gather), 1 expert-grouped copy
+  int cpb = 0;       // with Stream-K: at least this many K blocks per CTA (fewer, longer pieces)
 };
 
 // A table row (the table ends with a row of class -1): applies to calls of class `cls`, dense (moe 0) or MoE (moe 1), whose key (dense: M; MoE: routed
@@ -49,14 +50,14 @@ inline TuneChoice tune_lookup(int cls, bool moe, int64_t key) {
   return TuneChoice{};
 }
 
-// HQ_TUNE="kernel=1,bt=16,sk=0,slots=2,grouped=0" replaces the table's choice for every call (the sweep times each
-// candidate this way); fields left out keep the table's value.
+// HQ_TUNE="kernel=1,bt=16,sk=0,slots=2,grouped=0,cpb=2" replaces the table's choice for every call (the sweep times
+// each candidate this way); fields left out keep the table's value.
 inline void tune_env_override(TuneChoice& c) {
   const char* v = getenv("HQ_TUNE");
   if (!v) return;
-  const char* names[5] = {"kernel=", "bt=", "sk=", "slots=", "grouped="};
-  int* fields[5] = {&c.kernel, &c.bt, &c.sk, &c.slots, &c.grouped};
-  for (int i = 0; i < 5; ++i) {
+  const char* names[6] = {"kernel=", "bt=", "sk=", "slots=", "grouped=", "cpb="};
+  int* fields[6] = {&c.kernel, &c.bt, &c.sk, &c.slots, &c.grouped, &c.cpb};
+  for (int i = 0; i < 6; ++i) {
     const char* p = strstr(v, names[i]);
     if (p && (p == v || p[-1] == ',')) *fields[i] = atoi(p + strlen(names[i]));
   }

@@ -31,7 +31,7 @@ from workload import configs as W  # noqa: E402
 TABLE = os.path.join(HERE, "csrc", "hq_tune_table.h")
 RESULTS = os.path.join(HERE, "tune_results.json")
 INF = 1 << 62
-AUTO = dict(kernel=-1, bt=0, sk=-1, slots=0, grouped=-1)
+AUTO = dict(kernel=-1, bt=0, sk=-1, slots=0, grouped=-1, cpb=0)
 MARGIN = 0.97  # a tuned choice must be at least 3 % faster than the built-in rule on every size of its bucket
 CLASS_ID = {"int4": 0, "regdec": 1, "nvfp4": 2, "mxfp4": 3, "mxfp4a": 4}
 
@@ -64,12 +64,13 @@ def candidates(cls, moe, key, M=None):
         for bt in (8, 16, 32):
             for sk in (0, 1):
                 for slots in ((1, 2) if bt <= 16 else (1,)):
-                    out.append(dict(kernel=1, bt=bt, sk=sk, slots=slots, grouped=0 if moe else -1))
+                    for cpb in ((0, 2, 6) if sk else (0,)):
+                        out.append(dict(kernel=1, bt=bt, sk=sk, slots=slots, grouped=0 if moe else -1, cpb=cpb))
     if cls != "regdec":
         for bt in umma_bts:
             for sk in (0, 1):
                 for grouped in ((0, 1) if moe else (-1,)):
-                    out.append(dict(kernel=0 if cls == "int4" else -1, bt=bt, sk=sk, slots=0, grouped=grouped))
+                    out.append(dict(kernel=0 if cls == "int4" else -1, bt=bt, sk=sk, slots=0, grouped=grouped, cpb=0))
     return out
 
 
@@ -218,7 +219,8 @@ def write_table(results, device_name):
         key = "INT64_MAX" if m["key_max"] >= INF else str(m["key_max"])
         note = "built-in rule" if c == AUTO else f"at most {m['ratio']:.2f}x the built-in time"
         lines.append(f"    {{{CLASS_ID[m['cls']]}, {m['moe']}, {key}, {{{c['kernel']}, {c['bt']}, {c['sk']}, "
-                     f"{c['slots']}, {c['grouped']}}}}},  // {m['workload']} key ({m['key_lo']}, {key}]: {note}")
+                     f"{c['slots']}, {c['grouped']}, {c.get('cpb', 0)}}}}},  // {m['workload']} key ({m['key_lo']}, "
+                     f"{key}]: {note}")
     lines += ["    {-1, -1, 0, {}},", "};", "}  // namespace hq", ""]
     with open(TABLE, "w") as f:
         f.write("\n".join(lines))

@@ -14,6 +14,8 @@ DENSE = [
     ("int4_sym", 5, "kernel=1,bt=8,sk=0,slots=1"),
     ("int4_sym", 40, "kernel=1,bt=16,sk=1,slots=1"),
     ("int4_sym", 40, "kernel=1,bt=32,sk=0"),
+    ("int4_sym", 5, "kernel=1,bt=8,sk=1,cpb=3"),  # fewer, longer Stream-K pieces
+    ("uint4_zp", 200, "kernel=0,bt=64,sk=1,cpb=5"),
     ("uint4_zp", 40, "kernel=0,bt=16,sk=0"),
     ("uint4_zp", 200, "kernel=0,bt=64,sk=1"),
     ("uint4_zp", 9, "kernel=0,bt=256,sk=1"),
@@ -42,6 +44,7 @@ def test_dense_choice(lib, monkeypatch, wfmt, M, choice):
 MOE = [
     ("int4_sym", 6, "kernel=1,bt=8,sk=1,slots=1,grouped=0"),
     ("int4_sym", 40, "kernel=0,bt=32,sk=0,grouped=0"),
+    ("int4_sym", 40, "kernel=1,bt=16,sk=1,cpb=2,grouped=0"),
     ("int4_sym", 40, "kernel=0,bt=64,sk=1,grouped=1"),
     ("uint4_zp", 90, "kernel=1,bt=32,sk=0,grouped=1"),
     ("mxfp4", 40, "bt=64,sk=1,grouped=0"),

@@ -15,15 +15,17 @@ def _result(cls, moe, lo, hi, choice, ratio):
 def test_rows_merge_and_keep_order(tmp_path, monkeypatch):
     from quantized_gemm_dequant_gb300 import tune
     monkeypatch.setattr(tune, "TABLE", str(tmp_path / "t.h"))
-    a = dict(kernel=1, bt=8, sk=0, slots=2, grouped=-1)
+    a = dict(kernel=1, bt=8, sk=1, slots=2, grouped=-1, cpb=2)
     res = [_result("int4", 0, 0, 1, a, 0.8), _result("int4", 0, 1, 8, a, 0.9),
            _result("int4", 0, 8, 16, dict(tune.AUTO), 1.0), _result("int4", 0, 16, tune.INF, a, 0.95),
            _result("nvfp4", 1, 0, 4, dict(tune.AUTO), 1.0)]
     tune.write_table(res, "test device")
     text = (tmp_path / "t.h").read_text()
-    rows = re.findall(r"^\s*\{(-?\d+), (-?\d+), (\w+), \{(-?\d+), (-?\d+), (-?\d+), (-?\d+), (-?\d+)\}\}", text, re.M)
-    assert rows == [("0", "0", "8", "1", "8", "0", "2", "-1"), ("0", "0", "16", "-1", "0", "-1", "0", "-1"),
-                    ("0", "0", "INT64_MAX", "1", "8", "0", "2", "-1"), ("2", "1", "4", "-1", "0", "-1", "0", "-1")]
+    rows = re.findall(r"^\s*\{(-?\d+), (-?\d+), (\w+), \{(-?\d+), (-?\d+), (-?\d+), (-?\d+), (-?\d+), (-?\d+)\}\}",
+                      text, re.M)
+    assert rows == [("0", "0", "8", "1", "8", "1", "2", "-1", "2"), ("0", "0", "16", "-1", "0", "-1", "0", "-1", "0"),
+                    ("0", "0", "INT64_MAX", "1", "8", "1", "2", "-1", "2"),
+                    ("2", "1", "4", "-1", "0", "-1", "0", "-1", "0")]
     assert text.rstrip().endswith("}  // namespace hq")
     assert "{-1, -1, 0, {}}," in text
 
