@@ -173,10 +173,20 @@ __global__ void __launch_bounds__(AQ_THREADS) act_amax_kernel(const uint16_t* __
   pdl_trigger();
   pdl_wait();
   const uint4* xv = reinterpret_cast<const uint4*>(x);
-  uint32_t mb = 0;
-  for (int64_t c = (int64_t)blockIdx.x * AQ_THREADS + threadIdx.x; c < n8; c += (int64_t)gridDim.x * AQ_THREADS)
-    mb = bf16x8_absmax_bits(__ldg(xv + c), mb);
-  const float m = block_max(absmax_bits_to_f32(mb), red);
+  uint32_t mb[4] = {0u, 0u, 0u, 0u};  // four independent chains: four loads in flight per thread
+  const int64_t stride = (int64_t)gridDim.x * AQ_THREADS;
+  int64_t c = (int64_t)blockIdx.x * AQ_THREADS + threadIdx.x;
+  for (; c + 3 * stride < n8; c += 4 * stride) {
+    const uint4 v0 = __ldg(xv + c), v1 = __ldg(xv + c + stride), v2 = __ldg(xv + c + 2 * stride),
+                v3 = __ldg(xv + c + 3 * stride);
+    mb[0] = bf16x8_absmax_bits(v0, mb[0]);
+    mb[1] = bf16x8_absmax_bits(v1, mb[1]);
+    mb[2] = bf16x8_absmax_bits(v2, mb[2]);
+    mb[3] = bf16x8_absmax_bits(v3, mb[3]);
+  }
+  for (; c < n8; c += stride) mb[0] = bf16x8_absmax_bits(__ldg(xv + c), mb[0]);
+  const uint32_t all = __vmaxu2(__vmaxu2(mb[0], mb[1]), __vmaxu2(mb[2], mb[3]));
+  const float m = block_max(absmax_bits_to_f32(all), red);
   if (threadIdx.x == 0) partial[blockIdx.x] = m;
 }
 
@@ -203,8 +213,20 @@ __global__ void __launch_bounds__(AQ_THREADS) act_quant_nvfp4_kernel(const uint1
   const int64_t nblk = M * (K >> 4);
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   uint2* qv = reinterpret_cast<uint2*>(q);
-  for (int64_t b = (int64_t)blockIdx.x * AQ_THREADS + threadIdx.x; b < nblk; b += (int64_t)gridDim.x * AQ_THREADS) {
-    const uint4 w0 = __ldg(xv + 2 * b), w1 = __ldg(xv + 2 * b + 1);
+  // software-pipelined: the next block's two loads are in flight while this block is quantized
+  const int64_t stride = (int64_t)gridDim.x * AQ_THREADS;
+  int64_t b = (int64_t)blockIdx.x * AQ_THREADS + threadIdx.x;
+  uint4 n0 = make_uint4(0u, 0u, 0u, 0u), n1 = n0;
+  if (b < nblk) {
+    n0 = __ldg(xv + 2 * b);
+    n1 = __ldg(xv + 2 * b + 1);
+  }
+  for (; b < nblk; b += stride) {
+    const uint4 w0 = n0, w1 = n1;
+    if (b + stride < nblk) {
+      n0 = __ldg(xv + 2 * (b + stride));
+      n1 = __ldg(xv + 2 * (b + stride) + 1);
+    }
     float f[16];
     bf16x8_to_f32(w0, *reinterpret_cast<float(*)[8]>(f));
     bf16x8_to_f32(w1, *reinterpret_cast<float(*)[8]>(f + 8));
