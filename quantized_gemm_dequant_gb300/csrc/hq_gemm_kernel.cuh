@@ -903,10 +903,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
       // tile's MMAs before any global store is issued.
       constexpr int CHUNK = HC < 16 ? HC : 16;
       uint32_t v[HC];
+      // columns past the tile's last token hold padding: up to 64 columns per warp their chunks are neither read nor
+      // stored (a cut tile's partial sums are stored whole); the 128-column slices of 256-token tiles keep the
+      // straight-line code, whose registers the guards would spill
+      const int live = (HC <= 64 && pc.full) ? nrows - col0 : HC;  // warp-uniform
 #pragma unroll
       for (int cb = 0; cb < HC; cb += CHUNK) {
-        if (CHUNK == 16) tmem_ld16(tmem + lane_base + col0 + cb, *reinterpret_cast<uint32_t(*)[16]>(v + cb));
-        else tmem_ld8(tmem + lane_base + col0 + cb, *reinterpret_cast<uint32_t(*)[8]>(v + cb));
+        if (cb < live) {
+          if (CHUNK == 16) tmem_ld16(tmem + lane_base + col0 + cb, *reinterpret_cast<uint32_t(*)[16]>(v + cb));
+          else tmem_ld8(tmem + lane_base + col0 + cb, *reinterpret_cast<uint32_t(*)[8]>(v + cb));
+        }
       }
       tmem_wait_ld();
       tc_fence_before();
@@ -962,6 +968,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
         const int n4 = n & ~3;
 #pragma unroll
         for (int j = 0; j < HC; j += 4) {
+          if (j >= live) continue;
           int orw[4];
           float o[4];
 #pragma unroll
@@ -997,6 +1004,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
         const int n_even = n & ~1;
 #pragma unroll
         for (int j = 0; j < HC; j += 2) {
+          if (j >= live) continue;
           const int col = col0 + j;
           int orow0, orow1;
           float mul0, mul1;
@@ -1018,6 +1026,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
         const int n_even = n & ~1;
 #pragma unroll
         for (int j = 0; j < HC; j += 2) {
+          if (j >= live) continue;
           const int col = col0 + j;
           const uint32_t pk = pack_bf16x2(__uint_as_float(v[j]) * dense_mul + bias_v,
                                           __uint_as_float(v[j + 1]) * dense_mul + bias_v);  // lo: col, hi: col+1
@@ -1029,7 +1038,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < HC; ++j) store(col0 + j, __uint_as_float(v[j]));
+        for (int j = 0; j < HC; ++j) {
+          if (j >= live) continue;
+          store(col0 + j, __uint_as_float(v[j]));
+        }
       }
       ++pidx;
       return ok;
