@@ -103,8 +103,9 @@ struct Cfg {
   static constexpr int ACT_REGION = ((ACT_BYTES + 1023) / 1024) * 1024;
   static constexpr int SF_ROWS = BT < 32 ? 32 : BT;
   // NVFP4 activation scales: dense rows are 16 bytes apart; MoE rows come in gather4 groups of four,
-  // each group in its own 128-byte slot (row j at (j/4)*128 + (j%4)*16)
-  static constexpr int ASF_REGION = (NVF || AMX) ? ((SF_ROWS * 32 + 1023) / 1024) * 1024 : 0;
+  // each group in its own 128-byte slot (row j at (j/4)*128 + (j%4)*16).  256-token tiles of these paths are
+  // dense only: 16 bytes per row, which leaves room for a fourth activation stage.
+  static constexpr int ASF_REGION = (NVF || AMX) ? ((SF_ROWS * (BT == 256 ? 16 : 32) + 1023) / 1024) * 1024 : 0;
   static constexpr int A_STAGE = ACT_REGION + ASF_REGION;
   static constexpr int W_STAGE = W_REGION + X_REGION;
   static constexpr int RING_BUDGET = 216 * 1024;
