@@ -246,6 +246,56 @@ __device__ __forceinline__ void fused_route(const int32_t* ids, int nrows, int E
   __syncthreads();
 }
 
+// Routing of at most 32 routed rows (decode-size calls) without a histogram: warp 0 reads the ids (one per lane),
+// groups equal experts (__match_any_sync), places each row at (routed rows of smaller experts) + (its rank among the
+// rows of its expert), the order fused_route produces, and lists the distinct experts with their token tiles; then
+// every thread fills the per-expert row offsets off[0..E] and the tile prefix prefix[0..E] from those 32 entries.
+// scratch: 96 ints.  Every thread calls it (two __syncthreads).
+__device__ __forceinline__ void fused_route_small(const int32_t* ids, int nrows, int E, int bt, int region_cap,
+                                                  int* off, int* rows, int* prefix, int* total, int* scratch,
+                                                  int* status) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  int* ids_s = scratch;           // expert of routed row j, or -1
+  int* dist_e = scratch + 32;     // distinct expert held by lane j (the lowest lane of its rows), or -1
+  int* dist_t = scratch + 64;     // its token tiles
+  if (tid < 32) {
+    const int e = lane < nrows ? ids[lane] : -1;
+    const bool valid = e >= 0 && e < E;
+    if (lane < nrows && !valid) atomicCAS(status, 0, ERR_BAD_ROUTING);
+    const unsigned same = __match_any_sync(0xffffffffu, valid ? e : -1 - lane);  // invalid rows stay alone
+    const int rank = __popc(same & ((1u << lane) - 1u));
+    const int ev = valid ? e : 0x7FFFFFFF;
+    int below = 0;  // valid routed rows of smaller experts
+#pragma unroll 8
+    for (int j = 0; j < 32; ++j) below += __shfl_sync(0xffffffffu, ev, j) < ev ? 1 : 0;
+    if (valid) rows[below + rank] = lane;
+    const bool lead = valid && __ffs(same) - 1 == lane;
+    int cnt = __popc(same);
+    cnt = cnt > region_cap ? region_cap : cnt;
+    const int tiles = lead ? (cnt + bt - 1) / bt : 0;
+    ids_s[lane] = valid ? e : -1;
+    dist_e[lane] = lead ? e : -1;
+    dist_t[lane] = tiles;
+    int sum = tiles;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) *total = sum;
+  }
+  __syncthreads();
+  for (int e = tid; e <= E; e += blockDim.x) {
+    int o = 0, t = 0;
+#pragma unroll 8
+    for (int j = 0; j < 32; ++j) {
+      const int ej = ids_s[j], dj = dist_e[j];
+      o += (ej >= 0 && ej < e) ? 1 : 0;
+      t += (dj >= 0 && dj < e) ? dist_t[j] : 0;
+    }
+    off[e] = o;
+    prefix[e] = t;
+  }
+  __syncthreads();
+}
+
 template <int BT, int DEC>
 __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT, DEC>::CTAS_PER_SM)
     hq_gemm_small_kernel(const __grid_constant__ GemmArgs args) {
@@ -310,12 +360,17 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT, DEC>::CTAS_PER_SM)
     pdl_wait();
     if (producer) epoch_prev = reinterpret_cast<volatile uint32_t*>(args.status)[1];
     const int* counts = args.counts;
-    if (fused) {
-      int* cnt = reinterpret_cast<int*>(smem + C::OFF_RED);
-      fused_route(args.ids, args.fused_rows, args.E, cnt, r_off, r_rows, args.status);
-      counts = cnt;
+    if (fused && args.fused_rows <= 32) {
+      fused_route_small(args.ids, args.fused_rows, args.E, BT, args.region_cap, r_off, r_rows, prefix,
+                        &sh.tile_prefix_total, reinterpret_cast<int*>(smem + C::OFF_RED), args.status);
+    } else {
+      if (fused) {
+        int* cnt = reinterpret_cast<int*>(smem + C::OFF_RED);
+        fused_route(args.ids, args.fused_rows, args.E, cnt, r_off, r_rows, args.status);
+        counts = cnt;
+      }
+      moe_tile_prefix(counts, args.E, args.region_cap, BT, prefix, &sh.tile_prefix_total);
     }
-    moe_tile_prefix(counts, args.E, args.region_cap, BT, prefix, &sh.tile_prefix_total);
   }
   __syncthreads();
   if (producer) {
