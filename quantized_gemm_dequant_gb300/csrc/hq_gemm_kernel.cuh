@@ -585,8 +585,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
           }
           for (int j = 0; j < C::SUB; ++j) {
             if (!waitf(&sh.a_full[as], aph)) return;
+            // (the stage was written by TMA and is read by the MMA, both in the async proxy: no proxy fence; the
+            // expanded MXFP4 tiles are fenced by the warps that write them)
             tc_fence_after();
-            fence_proxy_async_smem();
             const uint32_t act = smem_u32(aring + as * C::A_STAGE);
             const bool first = (g == pc.g0 && j == 0);
             if (PATH == PATH_INT4) {
