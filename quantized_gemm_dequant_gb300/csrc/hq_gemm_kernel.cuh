@@ -97,7 +97,7 @@ struct Cfg {
   static constexpr int KSTAGE = NVF ? 256 : 128;  // K per weight block
   static constexpr int W_BLK = PATH == PATH_INT4 ? 8576 : (NVF ? 18432 : 8704);
   static constexpr int W_REGION = ((W_BLK + 1023) / 1024) * 1024;
-  static constexpr int X_REGION = MX ? 16384 : 0;  // expanded e2m1 A tile per weight stage
+  static constexpr int X_REGION = MX ? 16384 : 0;  // expanded e2m1 A tile (one slot of the X ring)
   static constexpr int SUB = PATH == PATH_INT4 ? 2 : 1;             // activation stages per weight block
   static constexpr int ACT_BYTES = BT * 128;
   static constexpr int ACT_REGION = ((ACT_BYTES + 1023) / 1024) * 1024;
@@ -107,17 +107,21 @@ struct Cfg {
   // dense only: 16 bytes per row, which leaves room for a fourth activation stage.
   static constexpr int ASF_REGION = (NVF || AMX) ? ((SF_ROWS * (BT == 256 ? 16 : 32) + 1023) / 1024) * 1024 : 0;
   static constexpr int A_STAGE = ACT_REGION + ASF_REGION;
-  static constexpr int W_STAGE = W_REGION + X_REGION;
+  static constexpr int W_STAGE = W_REGION;
   static constexpr int RING_BUDGET = 216 * 1024;
+  // MXFP4 weights: the raw blocks and their expansions live in separate rings, so that a raw stage is refilled as
+  // soon as it is expanded and the copies run SW blocks ahead while NX expanded slots wait for the MMA
+  static constexpr int NX = MX ? (BT <= 64 ? 3 : 2) : 0;
   static constexpr int SW = PATH == PATH_INT4 ? (BT <= 64 ? 12 : 4)
-                                              : (NVF ? (BT <= 64 ? 8 : 4) : (BT <= 64 ? 6 : 3));
-  static constexpr int SA_FIT = (RING_BUDGET - SW * W_STAGE) / A_STAGE;
+                                              : (NVF ? (BT <= 64 ? 8 : 4) : (BT <= 64 ? 10 : (AMX ? 4 : 6)));
+  static constexpr int XRING_BYTES = NX * X_REGION;
+  static constexpr int SA_FIT = (RING_BUDGET - SW * W_STAGE - XRING_BYTES) / A_STAGE;
   static constexpr int SA = SA_FIT > 16 ? 16 : SA_FIT;
   static constexpr int CB = BT < 32 ? 1 : BT / 32;  // scale-factor columns per MMA step for B
   static constexpr int SFB_STEP = CB < 4 ? 4 : CB;  // column stride per MMA step (kept 4-aligned)
   static constexpr int SF_STAGE_COLS = NVF ? 16 + 4 * SFB_STEP : 4;
   static constexpr int NA = 4;  // INT4: tensor-memory A slots of 64 columns
-  static constexpr int RING_BYTES = SW * W_STAGE + SA * A_STAGE;
+  static constexpr int RING_BYTES = SW * W_STAGE + SA * A_STAGE + XRING_BYTES;
   // INT4 256-token tiles keep the epilogue's per-column rows and multipliers (MoE) in shared memory: two pieces x
   // 8 warps x 128 columns x (row, multiplier); in registers they would spill next to the 128-column accumulator slice
   static constexpr int TAB_BYTES = (PATH == PATH_INT4 && BT == 256) ? 2 * 8 * (BT / 2) * 8 : 0;
@@ -127,7 +131,7 @@ struct Cfg {
   static_assert(SA >= 2, "activation ring too small");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
   static_assert(!NVF || 256 + SW * SF_STAGE_COLS <= 512, "tensor memory");
-  static_assert(!MX || 256 + 4 * SW + (AMX ? SW * SFB_STEP : 8) <= 512, "tensor memory");
+  static_assert(!MX || 256 + 4 * NX + (AMX ? NX * SFB_STEP : 8) <= 512, "tensor memory");
 };
 
 __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
@@ -250,7 +254,8 @@ struct Smem {
   using C = Cfg<PATH, BT>;
   uint64_t w_full[C::SW];
   uint64_t w_empty[C::SW];
-  uint64_t ready[C::SW];  // FP4 paths: scales in tensor memory (+ expanded A for MXFP4)
+  uint64_t ready[C::MX ? C::NX : C::SW];  // FP4 paths: scales in tensor memory (MXFP4: per X slot, with its A)
+  uint64_t x_empty[C::MX ? C::NX : 1];     // MXFP4: X slot released by the MMAs that read it
   uint64_t a_full[C::SA];
   uint64_t a_empty[C::SA];
   uint64_t afull[C::NA];  // INT4: decoded A slot written
@@ -322,6 +327,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* wring = smem;                       // SW x W_STAGE
   uint8_t* aring = smem + C::SW * C::W_STAGE;  // SA x A_STAGE
+  uint8_t* xring = aring + C::SA * C::A_STAGE;  // NX x X_REGION (MXFP4)
   Smem<PATH, BT>& sh = *reinterpret_cast<Smem<PATH, BT>*>(smem + C::RING_BYTES);
   int* prefix = reinterpret_cast<int*>(smem + C::RING_BYTES + 4096);  // MoE: E + 1 ints (E <= 512)
   const int tid = threadIdx.x;
@@ -339,8 +345,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
   if (tid == WPROD_WARP * 32) {
     for (int s = 0; s < C::SW; ++s) {
       mbar_init(&sh.w_full[s], 1);
-      mbar_init(&sh.w_empty[s], PATH == PATH_INT4 ? 8 : (C::NVF ? 4 + 1 : 8 + 1));
-      mbar_init(&sh.ready[s], C::MX ? 8 : 4);
+      mbar_init(&sh.w_empty[s], PATH == PATH_INT4 ? 8 : (C::NVF ? 4 + 1 : 8));
+      if (!C::MX) mbar_init(&sh.ready[s], 4);
+    }
+    for (int x = 0; x < C::NX; ++x) {
+      mbar_init(&sh.ready[x], 8);
+      mbar_init(&sh.x_empty[x], 1);
     }
     for (int s = 0; s < C::SA; ++s) {
       mbar_init(&sh.a_full[s], 1);
@@ -562,8 +572,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
   } else if (active && warp == MMA_WARP) {
     // ============================================================ MMA issuer
     if (lane == 0) {
-      int ws = 0, as = 0, aslot = 0;
-      uint32_t wph = 0, aph = 0, aslph = 0;
+      int ws = 0, as = 0, aslot = 0, xs = 0;
+      uint32_t wph = 0, aph = 0, aslph = 0, xph = 0;
       int pidx = 0;
       bool ok = true;
       auto waitf = [&](uint64_t* bar, uint32_t par) {
@@ -580,6 +590,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
         for (int g = pc.g0; g < pc.g1; ++g) {
           if (PATH == PATH_INT4) {
             if (!waitf(&sh.afull[aslot], aslph)) return;
+          } else if (C::MX) {
+            if (!waitf(&sh.ready[xs], xph)) return;  // expanded A and scales of this block (its raw stage is free)
           } else {
             if (!waitf(&sh.w_full[ws], wph) || !waitf(&sh.ready[ws], wph)) return;
           }
@@ -613,10 +625,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
                                (first && t == 0) ? 0u : 1u);
               }
             } else {
-              const uint32_t xa = smem_u32(wring + ws * C::W_STAGE + C::W_REGION);
-              const uint32_t sfa = tmem + 256 + ws * 4;
+              const uint32_t xa = smem_u32(xring + xs * C::X_REGION);
+              const uint32_t sfa = tmem + 256 + xs * 4;
               // activation block scales: unit scales written once (per-token FP8), or the stage's MXFP8 scales
-              const uint32_t sfb = tmem + 256 + 4 * C::SW + (C::AMX ? ws * C::SFB_STEP : 0);
+              const uint32_t sfb = tmem + 256 + 4 * C::NX + (C::AMX ? xs * C::SFB_STEP : 0);
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const uint32_t idesc = idesc_block_scaled(128, BT, 5, 0, 1, i, C::AMX ? i : 0);
@@ -636,6 +648,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
             if (++aslot == C::NA) {
               aslot = 0;
               aslph ^= 1;
+            }
+          } else if (C::MX) {
+            umma_commit(&sh.x_empty[xs]);
+            if (++xs == C::NX) {
+              xs = 0;
+              xph ^= 1;
             }
           } else {
             umma_commit(&sh.w_empty[ws]);
@@ -660,8 +678,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
     const int h = warp >> 2;      // K half (INT4) / column half (epilogue)
     const int r = q * 32 + lane;  // weight row within the tile
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    int ws = 0, as = 0, aslot = 0;
-    uint32_t wph = 0, aph = 0, aslph = 0;
+    int ws = 0, as = 0, aslot = 0, xs = 0;
+    uint32_t wph = 0, aph = 0, aslph = 0, xph = 0;
     int pidx = 0;
     bool ok = true;
     auto waitf = [&](uint64_t* bar, uint32_t par) {
@@ -677,7 +695,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
       uint32_t ones[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) ones[j] = 0x7F7F7F7Fu;
-      tmem_st_x<8>(tmem + lane_base + 256 + 4 * C::SW, ones);
+      tmem_st_x<8>(tmem + lane_base + 256 + 4 * C::NX, ones);
       tmem_wait_st();
     }
     constexpr int HC = BT / 2;
@@ -832,13 +850,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
             tmem_wait_st();
             tc_fence_before();
           } else if (C::MX) {
+            // the X slot and its scale columns: free once the MMAs of the block NX blocks back completed
+            if (!waitf(&sh.x_empty[xs], xph ^ 1)) return false;
+            tc_fence_after();
             if (warp < 4) {
               // weight scale factors -> tensor memory (replicated in every lane quarter)
               const uint32_t* wsf = reinterpret_cast<const uint32_t*>(wb + 8192);
               uint32_t v[4];
 #pragma unroll
               for (int j = 0; j < 4; ++j) v[j] = wsf[j * 32 + lane];
-              tmem_st_x<4>(tmem + lane_base + 256 + ws * 4, v);
+              tmem_st_x<4>(tmem + lane_base + 256 + xs * 4, v);
               if (C::AMX) {
                 // MXFP8 activation scales of this stage: token j's four e8m0 bytes (one per 32 K) are word g % 4 of
                 // its 16-byte group; token j goes to lane j % 32 of column j / 32 (every lane quarter)
@@ -851,12 +872,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
                   const int off = (args.moe && !args.grouped) ? (j >> 2) * 128 + (j & 3) * 16 : j * 16;
                   b[cc] = *reinterpret_cast<const uint32_t*>(asf + off);
                 }
-                tmem_st_x<C::CB>(tmem + lane_base + 256 + 4 * C::SW + ws * C::SFB_STEP, b);
+                tmem_st_x<C::CB>(tmem + lane_base + 256 + 4 * C::NX + xs * C::SFB_STEP, b);
               }
             }
             // all 8 warps: expand packed e2m1 (8 bytes per 16 K) into the padded 16-byte chunks, two chunks of a
             // row per 16-byte load
-            uint8_t* xt = wb + C::W_REGION;
+            uint8_t* xt = xring + xs * C::X_REGION;
 #pragma unroll
             for (int q = tid; q < 512; q += 256) {
               const uint4 v = *reinterpret_cast<const uint4*>(wb + q * 16);
@@ -873,9 +894,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
           }
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(&sh.ready[ws]);
+            mbar_arrive(&sh.ready[C::MX ? xs : ws]);
             mbar_arrive(&sh.w_empty[ws]);
             if (C::NVF || (C::AMX && warp < 4)) mbar_arrive(&sh.a_empty[as]);
+          }
+          if (C::MX && ++xs == C::NX) {
+            xs = 0;
+            xph ^= 1;
           }
           ++gk;
           if (C::NVF || C::AMX) {
@@ -1049,8 +1074,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
       return ok;
     };
     // A piece's epilogue runs after the first blocks of the next piece are prepared, so that the MMA finds
-    // them ready as soon as the accumulator is released (the last ring slot frees only with the accumulator).
-    constexpr int PREFILL = (PATH == PATH_INT4 ? C::NA : C::SW) - 1;
+    // them ready as soon as the accumulator is released.  No more than the slots the previous piece's MMAs free
+    // (the next ones free only after the accumulator): A slots but one (INT4), the X ring (MXFP4), weight stages
+    // but one (NVFP4).
+    constexpr int PREFILL = PATH == PATH_INT4 ? C::NA - 1 : (C::MX ? C::NX : C::SW - 1);
     Pend prev;
     bool has_prev = false;
     for_each_piece(sched, [&](const Piece& pc) {
