@@ -113,7 +113,8 @@ struct Cfg {
   // soon as it is expanded and the copies run SW blocks ahead while NX expanded slots wait for the MMA
   static constexpr int NX = MX ? (BT <= 64 ? 3 : 2) : 0;
   static constexpr int SW = PATH == PATH_INT4 ? (BT <= 64 ? 12 : 4)
-                                              : (NVF ? (BT <= 64 ? 8 : 4) : (BT <= 64 ? 10 : (AMX ? 4 : 6)));
+                                              : (NVF ? (BT <= 64 ? 8 : (BT == 128 ? 5 : 4))
+                                                     : (BT <= 64 ? 10 : (AMX ? 4 : 6)));
   static constexpr int XRING_BYTES = NX * X_REGION;
   static constexpr int SA_FIT = (RING_BUDGET - SW * W_STAGE - XRING_BYTES) / A_STAGE;
   static constexpr int SA = SA_FIT > 16 ? 16 : SA_FIT;
