@@ -364,10 +364,11 @@ def test_degenerate_groups(lib, wfmt):
 
 
 @pytest.mark.parametrize("route", ["fused", "kernel"])
-@pytest.mark.parametrize("T", [1, 4, 60])
+@pytest.mark.parametrize("T", [1, 4, 5, 60])
 def test_moe_small_routing_in_kernel_and_by_routing_kernel(lib, monkeypatch, route, T):
     """Small MoE calls (at most 512 routed rows) route inside the register-decode kernel: every CTA builds the same
-    per-expert row lists in shared memory.  Both that and the separate routing kernel match the oracle."""
+    per-expert row lists in shared memory (one warp up to 32 routed rows: T = 1, 4; a histogram beyond: T = 5, 60).
+    Both that and the separate routing kernel match the oracle."""
     if route == "kernel":
         monkeypatch.setenv("HQ_ROUTE_KERNEL", "1")
     inp = make_moe(MOE_FORMS["int4_sym"], T, seed=T + 40, E=64, N=384, K=1024, topk=8)  # <= 16 rows per expert

@@ -23,6 +23,9 @@ DENSE = [
     ("nvfp4", 100, "bt=32,sk=1"),
     ("nvfp4", 20, "bt=128,sk=0"),
     ("mxfp4", 70, "bt=16,sk=0"),
+    # MXFP4 tiles of 128 and 256 tokens (two expanded-weight slots) with Stream-K pieces of two tiles in one CTA
+    ("mxfp4", 2048, "bt=128,sk=1"),
+    ("mxfp4", 2048, "bt=256,sk=1"),
     ("int8_sym", 20, "bt=8,sk=0,slots=2"),
     ("e4m3", 3, "bt=32,sk=1"),
 ]
@@ -48,6 +51,7 @@ MOE = [
     ("int4_sym", 40, "kernel=0,bt=64,sk=1,grouped=1"),
     ("uint4_zp", 90, "kernel=1,bt=32,sk=0,grouped=1"),
     ("mxfp4", 40, "bt=64,sk=1,grouped=0"),
+    ("mxfp4", 300, "bt=128,sk=1,grouped=1"),
     ("nvfp4", 40, "bt=256,sk=0,grouped=1"),  # 256-token NVFP4 MoE tiles do not exist: the planner keeps its own
 ]
 
