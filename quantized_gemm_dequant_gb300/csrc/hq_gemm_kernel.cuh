@@ -98,8 +98,12 @@ struct Cfg {
   static constexpr int W_BLK = PATH == PATH_INT4 ? 8576 : (NVF ? 18432 : 8704);
   static constexpr int W_REGION = ((W_BLK + 1023) / 1024) * 1024;
   static constexpr int X_REGION = MX ? 16384 : 0;  // expanded e2m1 A tile (one slot of the X ring)
-  static constexpr int SUB = PATH == PATH_INT4 ? 2 : 1;             // activation stages per weight block
-  static constexpr int ACT_BYTES = BT * 128;
+  // INT4: activation stages per weight block and 64-K atoms per stage.  Tiles of at most 128 tokens take one stage
+  // of two atoms per block (one wait for the MMA thread instead of two); 256-token tiles keep two 32 KB stages, so
+  // that the ring still holds five of them.
+  static constexpr int SUB = PATH == PATH_INT4 ? (BT <= 128 ? 1 : 2) : 1;
+  static constexpr int ATOMS = PATH == PATH_INT4 ? 2 / SUB : 1;
+  static constexpr int ACT_BYTES = ATOMS * BT * 128;
   static constexpr int ACT_REGION = ((ACT_BYTES + 1023) / 1024) * 1024;
   static constexpr int SF_ROWS = BT < 32 ? 32 : BT;
   // NVFP4 activation scales: dense rows are 16 bytes apart; MoE rows come in gather4 groups of four,
@@ -471,7 +475,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
     __syncwarp();
   } else if (active && warp == APROD_WARP) {
     // ============================================================ activation producer
-    constexpr int A_BOX_BYTES = BT * 128;
+    constexpr int A_BOX_BYTES = BT * 128;  // one TMA box: BT rows x 128 bytes
     constexpr int SF_BOX_BYTES = BT * 16;
     if (!args.moe || args.grouped) {
       // 2-D boxes: one thread runs the loop (a warp-wide loop would reconverge around every wait)
@@ -493,10 +497,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
                 return;
               }
               uint8_t* dst = aring + as * C::A_STAGE;
-              // x offset of this stage in the tensor map's element units (bf16: 64 per stage; bytes: 128)
-              const int x = PATH == PATH_INT4 ? g * 128 + j * 64 : g * 128;
-              mbar_arrive_expect_tx(&sh.a_full[as], A_BOX_BYTES + ((C::NVF || C::AMX) ? SF_BOX_BYTES : 0));
-              tma_load_2d(dst, &args.tmap_a, x, rbase, &sh.a_full[as]);
+              // x offset of this stage in the tensor map's element units (bf16: 64 per atom; bytes: 128)
+              const int x = PATH == PATH_INT4 ? g * 128 + j * C::ATOMS * 64 : g * 128;
+              mbar_arrive_expect_tx(&sh.a_full[as], C::ATOMS * A_BOX_BYTES + ((C::NVF || C::AMX) ? SF_BOX_BYTES : 0));
+#pragma unroll
+              for (int t = 0; t < C::ATOMS; ++t)
+                tma_load_2d(dst + t * A_BOX_BYTES, &args.tmap_a, x + t * 64, rbase, &sh.a_full[as]);
               // block scales: NVFP4 16 bytes per 256-K stage; MXFP8 the 16-byte group of four 128-K stages
               if (C::NVF || C::AMX)
                 tma_load_2d(dst + C::ACT_REGION, &args.tmap_sf, C::AMX ? (g >> 2) * 16 : (C::XMX ? (g >> 1) * 16 : g * 16),
@@ -540,14 +546,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) return;
             uint8_t* dst = aring + as * C::A_STAGE;
-            const int x = PATH == PATH_INT4 ? g * 128 + j * 64 : g * 128;
+            const int x = PATH == PATH_INT4 ? g * 128 + j * C::ATOMS * 64 : g * 128;
             if (lane == 0)
-              mbar_arrive_expect_tx(&sh.a_full[as], A_BOX_BYTES + ((C::NVF || C::AMX) ? SF_BOX_BYTES : 0));
+              mbar_arrive_expect_tx(&sh.a_full[as], C::ATOMS * A_BOX_BYTES + ((C::NVF || C::AMX) ? SF_BOX_BYTES : 0));
             __syncwarp();
             for (int i = lane * 4; i < BT; i += 128) {
               uint8_t* d = dst + (i >> 3) * 1024 + (i & 7) * 128;
-              tma_gather4(d, &args.tmap_a, x, sh.rows_tok[i], sh.rows_tok[i + 1], sh.rows_tok[i + 2],
-                          sh.rows_tok[i + 3], &sh.a_full[as]);
+#pragma unroll
+              for (int t = 0; t < C::ATOMS; ++t)
+                tma_gather4(d + t * A_BOX_BYTES, &args.tmap_a, x + t * 64, sh.rows_tok[i], sh.rows_tok[i + 1],
+                            sh.rows_tok[i + 2], sh.rows_tok[i + 3], &sh.a_full[as]);
               if (C::NVF || C::AMX)
                 tma_gather4(dst + C::ACT_REGION + (i >> 2) * 128, &args.tmap_sf,
                             C::AMX ? (g >> 2) * 16 : (C::XMX ? (g >> 1) * 16 : g * 16),
@@ -605,11 +613,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
             const bool first = (g == pc.g0 && j == 0);
             if (PATH == PATH_INT4) {
               constexpr uint32_t idesc = idesc_bf16(128, BT);
-              const uint32_t a_t = tmem + 256 + aslot * 64 + j * 32;
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const uint64_t bd = smem_desc(act + i * 32, 16, 1024, 2);
-                umma_bf16_ts(tmem, a_t + i * 8, bd, idesc, (first && i == 0) ? 0u : 1u);
+              for (int t = 0; t < C::ATOMS; ++t) {
+                const uint32_t a_t = tmem + 256 + aslot * 64 + (j * C::ATOMS + t) * 32;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const uint64_t bd = smem_desc(act + t * (BT * 128) + i * 32, 16, 1024, 2);
+                  umma_bf16_ts(tmem, a_t + i * 8, bd, idesc, (first && t == 0 && i == 0) ? 0u : 1u);
+                }
               }
             } else if (C::NVF) {
               constexpr uint32_t idesc = idesc_block_scaled(128, BT, 1, 1, C::XMX ? 1 : 0, 0, 0);
