@@ -128,13 +128,7 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ workload
-# Down GEMMs of the two MoE workloads' layers (hidden N, intermediate K = half the Gate-up N), with the top-k
-# combine fused into the epilogue: the routed rows T*k of K in, T token rows of N out.
-DOWN_CONFIGS = {
-    "moe_w4a16_down": dict(W.CONFIGS["moe_w4a16"], N=2048, K=768, down=True),
-    "moe_mxfp4_down": dict(W.CONFIGS["moe_mxfp4"], N=7168, K=2048, down=True),
-}
-W.CONFIGS.update(DOWN_CONFIGS)
+# (the Down GEMM workloads moe_w4a16_down / moe_mxfp4_down are in workload.configs)
 REPLICAS_OVERRIDE = None  # --replicas (profiling runs keep the device footprint small)
 
 

@@ -177,8 +177,9 @@ HQ_API int32_t hq_kernels_per_call(const hq_format_t* fmt, int64_t M_or_T, int32
  * plan_out[0] = GEMM kernel (0 tcgen05, 1 register-decode), plan_out[1] = its variant (tcgen05: 0 INT4, 1 NVFP4,
  * 2 MXFP4 x FP8, 3 MXFP4 x MXFP8, 4 MXFP4 x MXFP4; register-decode: the decode kind, 0 INT4 ... 6 UINT3),
  * plan_out[2] = token tile, plan_out[3] = 1 if K is split over CTAs (Stream-K), plan_out[4] = CTAs launched,
- * plan_out[5] = 1 if MoE rows are copied expert-contiguous first.  Returns HQ_ERR_INVALID_ARG for an invalid
- * format, size or null plan_out.  Host-only ("Tuning and JIT compilation per workload": the per-size choice). */
+ * plan_out[5] = 1 if MoE rows are copied expert-contiguous first.  moe: 0 hq_gemm, 1 hq_moe_gemm, 2
+ * hq_moe_gemm_combine (each kind has its own rows in the tuned table).  Returns HQ_ERR_INVALID_ARG for an invalid
+ * format, size, kind or null plan_out.  Host-only ("Tuning and JIT compilation per workload": the per-size choice). */
 HQ_API hq_status_t hq_launch_plan(const hq_format_t* fmt, int64_t M_or_T, int32_t topk, int32_t moe, int32_t* plan_out);
 
 /* Zero `bytes` of workspace on `stream` (cudaMemsetAsync).  Errors:

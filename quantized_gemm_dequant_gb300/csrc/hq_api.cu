@@ -212,7 +212,9 @@ void plan_tiles(Plan& p, int64_t M_or_T, int32_t topk, bool moe, int64_t E, int6
 
 // The built-in rule, then the tuned table's row for (format class, size bucket), then HQ_TUNE; every choice is
 // checked against what the kernels support before it is taken.
-Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int sms) {
+// kind: 0 dense (hq_gemm), 1 MoE (hq_moe_gemm), 2 MoE with the top-k combine (hq_moe_gemm_combine)
+Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, int kind, int sms) {
+  const bool moe = kind != 0;
   Plan p;
   const PackGeom g = pack_geom(pack_kind(f), f->N, f->K, f->num_experts);
   p.path = (g.path == PATH_MXFP4 && f->act_type == HQ_A_MXFP8) ? PATH_MXFP4A : g.path;
@@ -232,7 +234,7 @@ Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, bool moe, int
     if (p.small) p.bt = p.bt > 32 ? 32 : ((!moe && M_or_T <= 8) ? 8 : p.bt);
   }
   // tuned choice
-  TuneChoice tc = tune_lookup(tune_class(f, p.path), moe, key);
+  TuneChoice tc = tune_lookup(tune_class(f, p.path), kind, key);
   tune_env_override(tc);
   const int force = forced_path();
   if (force) tc.kernel = force == 1 ? 1 : 0;
@@ -414,16 +416,16 @@ hq_status_t hq_unpack_weights(const hq_format_t* fmt, const void* packed, uint8_
 size_t hq_workspace_bytes(const hq_format_t* fmt, int64_t M_or_T, int32_t topk) {
   if (check_format(fmt) != HQ_OK || M_or_T < 0 || topk < 1) return 0;
   const int sms = num_sms();
-  if (fmt->num_experts > 1 || topk > 1) return make_plan(fmt, M_or_T, topk, true, sms).ws_bytes;
+  if (fmt->num_experts > 1 || topk > 1) return make_plan(fmt, M_or_T, topk, 1, sms).ws_bytes;
   // one expert with top-1 serves both hq_gemm and hq_moe_gemm: cover both plans
-  const size_t d = make_plan(fmt, M_or_T, 1, false, sms).ws_bytes;
-  const size_t m = make_plan(fmt, M_or_T, 1, true, sms).ws_bytes;
+  const size_t d = make_plan(fmt, M_or_T, 1, 0, sms).ws_bytes;
+  const size_t m = make_plan(fmt, M_or_T, 1, 1, sms).ws_bytes;
   return d > m ? d : m;
 }
 
 int32_t hq_kernels_per_call(const hq_format_t* fmt, int64_t M_or_T, int32_t topk, int32_t moe) {
-  if (check_format(fmt) != HQ_OK || M_or_T < 1 || topk < 1) return 0;
-  const Plan p = make_plan(fmt, M_or_T, topk, moe != 0, num_sms());
+  if (check_format(fmt) != HQ_OK || M_or_T < 1 || topk < 1 || moe < 0 || moe > 2) return 0;
+  const Plan p = make_plan(fmt, M_or_T, topk, moe, num_sms());
   int32_t n = 1 + (p.sk && !p.small ? 1 : 0);  // GEMM (+ split-K reduction of the UMMA kernel)
   if (moe) n += (p.fused ? 0 : 1) + (p.grouped ? 1 : 0);  // routing (+ row permutation), unless fused
   if (moe == 2) n += 1;                    // combine: rounding of the summed token rows
@@ -431,8 +433,8 @@ int32_t hq_kernels_per_call(const hq_format_t* fmt, int64_t M_or_T, int32_t topk
 }
 
 hq_status_t hq_launch_plan(const hq_format_t* fmt, int64_t M_or_T, int32_t topk, int32_t moe, int32_t* plan_out) {
-  if (check_format(fmt) != HQ_OK || M_or_T < 1 || topk < 1 || !plan_out) return HQ_ERR_INVALID_ARG;
-  const Plan p = make_plan(fmt, M_or_T, topk, moe != 0, num_sms());
+  if (check_format(fmt) != HQ_OK || M_or_T < 1 || topk < 1 || moe < 0 || moe > 2 || !plan_out) return HQ_ERR_INVALID_ARG;
+  const Plan p = make_plan(fmt, M_or_T, topk, moe, num_sms());
   plan_out[0] = p.small;
   plan_out[1] = p.small ? p.dec : p.path;
   plan_out[2] = p.bt;
@@ -461,7 +463,7 @@ hq_status_t hq_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* packe
     return HQ_ERR_ALIGNMENT;
   const int sms = num_sms();
   if (sms < 1) return HQ_ERR_CUDA;
-  const Plan p = make_plan(fmt, M, 1, false, sms);
+  const Plan p = make_plan(fmt, M, 1, 0, sms);
   if (!workspace || ws_bytes < p.ws_bytes) return HQ_ERR_WORKSPACE;
   const PackGeom g = pack_geom(pack_kind(fmt), N, K, 1);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -520,7 +522,7 @@ hq_status_t moe_call(const hq_format_t* fmt, const hq_act_t* A, const void* pack
     return HQ_ERR_ALIGNMENT;
   const int sms = num_sms();
   if (sms < 1) return HQ_ERR_CUDA;
-  const Plan p = make_plan(fmt, T, topk, true, sms);
+  const Plan p = make_plan(fmt, T, topk, combine ? 2 : 1, sms);
   if (combine && fmt->N % 4) return HQ_ERR_ALIGNMENT;
   const size_t need = combine ? comb_offset(p) + sizeof(float) * (size_t)(T * fmt->N) : p.ws_bytes;
   if (!workspace || ws_bytes < need) return HQ_ERR_WORKSPACE;
@@ -615,7 +617,7 @@ hq_status_t hq_moe_gemm_combine(const hq_format_t* fmt, const hq_act_t* A, const
 
 size_t hq_moe_combine_workspace_bytes(const hq_format_t* fmt, int64_t T, int32_t topk) {
   if (check_format(fmt) != HQ_OK || T < 0 || topk < 1) return 0;
-  const Plan p = make_plan(fmt, T, topk, true, num_sms());
+  const Plan p = make_plan(fmt, T, topk, 2, num_sms());
   return comb_offset(p) + sizeof(float) * (size_t)(T * fmt->N);
 }
 

@@ -29,8 +29,9 @@ struct TuneChoice {
   int cpb = 0;       // with Stream-K: at least this many K blocks per CTA (fewer, longer pieces)
 };
 
-// A table row (the table ends with a row of class -1): applies to calls of class `cls`, dense (moe 0) or MoE (moe 1), whose key (dense: M; MoE: routed
-// rows per expert, rounded up) is at most key_max and above the previous matching row's key_max.
+// A table row (the table ends with a row of class -1): applies to calls of class `cls` and kind `moe` (0 dense, 1 MoE,
+// 2 MoE with the top-k combine: the Down GEMM, whose short K and reducing epilogue favour other tiles) whose key
+// (dense: M; MoE: routed rows per expert, rounded up) is at most key_max and above the previous matching row's key_max.
 struct TuneRow {
   int cls;
   int moe;
@@ -44,9 +45,9 @@ struct TuneRow {
 
 namespace hq {
 
-inline TuneChoice tune_lookup(int cls, bool moe, int64_t key) {
+inline TuneChoice tune_lookup(int cls, int kind, int64_t key) {
   for (const TuneRow& r : kTuneRows)
-    if (r.cls == cls && r.moe == (moe ? 1 : 0) && key <= r.key_max) return r.c;
+    if (r.cls == cls && r.moe == kind && key <= r.key_max) return r.c;
   return TuneChoice{};
 }
 

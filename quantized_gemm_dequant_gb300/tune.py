@@ -35,8 +35,8 @@ AUTO = dict(kernel=-1, bt=0, sk=-1, slots=0, grouped=-1, cpb=0)
 MARGIN = 0.97  # a tuned choice must be at least 3 % faster than the built-in rule on every size of its bucket
 CLASS_ID = {"int4": 0, "regdec": 1, "nvfp4": 2, "mxfp4": 3, "mxfp4a": 4}
 
-# (class, workload config, dense/moe, buckets: [(key upper bound, sizes measured)]); MoE keys are routed rows per
-# expert, rounded up (E=128 top-8: key = T/16; E=256 top-8: key = T/32)
+# (class, workload config, kind (0 dense, 1 MoE, 2 MoE Down GEMM with the top-k combine), buckets: [(key upper bound,
+# sizes measured)]); MoE keys are routed rows per expert, rounded up (E=128 top-8: key = T/16; E=256 top-8: key = T/32)
 PLANS = [
     ("int4", "w4a16_asym", 0, [(1, [1]), (8, [4, 8]), (16, [16]), (32, [24, 32]), (64, [48, 64]), (128, [96, 128]),
                                (256, [256]), (512, [512]), (1024, [1024]), (2048, [2048]), (4096, [4096]),
@@ -46,7 +46,11 @@ PLANS = [
     ("regdec", "w8a16", 0, [(1, [1]), (8, [8]), (16, [16]), (32, [32]), (64, [64]), (INF, [256])]),
     ("nvfp4", "nvfp4", 0, [(1, [1]), (16, [16]), (64, [64]), (128, [128]), (256, [256]), (512, [512]),
                            (1024, [1024]), (2048, [2048]), (4096, [4096]), (INF, [8192])]),
+    ("int4", "moe_w4a16_down", 2, [(1, [1, 16]), (2, [32]), (4, [64]), (8, [128]), (16, [256]), (32, [512]),
+                                   (64, [1024]), (128, [2048]), (256, [4096]), (INF, [8192])]),
     ("mxfp4", "moe_mxfp4", 1, [(1, [1, 32]), (2, [64]), (8, [256]), (32, [1024]), (128, [4096]), (INF, [8192])]),
+    ("mxfp4", "moe_mxfp4_down", 2, [(1, [1, 32]), (2, [64]), (8, [256]), (32, [1024]), (128, [4096]),
+                                    (INF, [8192])]),
     ("mxfp4a", "w4a8_mx", 0, [(1, [1]), (128, [128]), (256, [256]), (1024, [1024]), (4096, [4096]),
                               (INF, [8192])]),
 ]
@@ -101,6 +105,14 @@ def make_sized_calls(cfg_name, sizes, dev, seed=0):
             def run(r, ws, a=a, outs=outs, M=M):
                 hq.gemm(fmt, a, packs[r], M, out=outs[r], workspace=ws)
                 return outs[r]
+        elif c.get("down"):  # Down GEMM + combine: the T * topk routed rows in, the T token rows out
+            a = W.quantize_acts(c["afmt"], W.acts_fp32(seed, M * c["topk"], c["K"], device=dev))
+            ids, tw = W.zipf_route(seed, M, c["E"], c["topk"], device=dev)
+            outs = [torch.empty((M, c["N"]), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+
+            def run(r, ws, a=a, ids=ids, tw=tw, outs=outs):
+                hq.moe_gemm_combine(fmt, a, packs[r], ids, tw, out=outs[r], workspace=ws)
+                return outs[r]
         else:
             a = W.quantize_acts(c["afmt"], W.acts_fp32(seed, M, c["K"], device=dev))
             ids, tw = W.zipf_route(seed, M, c["E"], c["topk"], device=dev)
@@ -109,14 +121,15 @@ def make_sized_calls(cfg_name, sizes, dev, seed=0):
             def run(r, ws, a=a, ids=ids, tw=tw, outs=outs):
                 hq.moe_gemm(fmt, a, packs[r], ids, tw, out=outs[r], workspace=ws)
                 return outs[r]
-        res[M] = (run, c["topk"] if c["kind"] == "moe" else 1)
+        res[M] = (run, c["topk"] if c["kind"] == "moe" else 1, bool(c.get("down")))
     return fmt, res, R
 
 
-def time_choice(fmt, run, M, topk, R, choice, bursts, per_burst):
+def time_choice(fmt, run, M, topk, R, choice, bursts, per_burst, down=False):
     os.environ["HQ_TUNE"] = env_of(choice)
     try:
-        wss = [hq.make_workspace(fmt, M, topk) for _ in range(R)]
+        mk = hq.make_combine_workspace if down else hq.make_workspace
+        wss = [mk(fmt, M, topk) for _ in range(R)]
         for r in range(R):
             run(r, wss[r])
         torch.cuda.synchronize()
@@ -154,13 +167,13 @@ def sweep(plans, quick, dev):
         fmt, calls, R = make_sized_calls(cfg, sizes, dev)
         meas = {}
         for M in sizes:
-            run, topk = calls[M]
-            t_auto, y_auto = time_choice(fmt, run, M, topk, R, AUTO, bursts, per_burst)
+            run, topk, down = calls[M]
+            t_auto, y_auto = time_choice(fmt, run, M, topk, R, AUTO, bursts, per_burst, down)
             rows = []
             c_cfg = W.CONFIGS[cfg]
             key = -(-M * c_cfg["topk"] // c_cfg["E"]) if moe else M
             for c in candidates(cls, moe, key, M):
-                t, y = (t_auto, y_auto) if c == AUTO else time_choice(fmt, run, M, topk, R, c, bursts, per_burst)
+                t, y = (t_auto, y_auto) if c == AUTO else time_choice(fmt, run, M, topk, R, c, bursts, per_burst, down)
                 ok = t is not None and close(y, y_auto)
                 rows.append(dict(choice=c, ms=t, ok=ok))
             meas[M] = dict(auto_ms=t_auto, rows=rows)

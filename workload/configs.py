@@ -55,6 +55,10 @@ CONFIGS = {
     "w4a4_mx": dict(kind="dense", wfmt="mxfp4", afmt="mxfp4", N=4096, K=7168, G=32, sizes=[1, 128, 1024, 8192]),
     "w4a8_mx": dict(kind="dense", wfmt="mxfp4", afmt="mxfp8", N=4096, K=7168, G=32, sizes=[1, 128, 1024, 8192]),
 }
+# Down GEMMs of the two MoE workloads' layers (hidden N, intermediate K = half the Gate-up N), with the top-k combine
+# fused into the epilogue: the routed rows T*k of K in, T token rows of N out.
+CONFIGS["moe_w4a16_down"] = dict(CONFIGS["moe_w4a16"], N=2048, K=768, down=True)
+CONFIGS["moe_mxfp4_down"] = dict(CONFIGS["moe_mxfp4"], N=7168, K=2048, down=True)
 
 W_STD = 0.02
 
