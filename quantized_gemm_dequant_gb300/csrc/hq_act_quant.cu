@@ -45,14 +45,26 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float a, float b) {
   return d;
 }
 
-// two floats -> one byte of two e2m1 codes (low nibble = a), round to nearest even, saturating; zeros become +0
-__device__ __forceinline__ uint32_t cvt_e2m1x2(float a, float b) {
-  uint16_t d;
-  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}" : "=h"(d) : "f"(b), "f"(a));
-  uint32_t r = d & 0xFFu;
-  if ((r & 0x07u) == 0) r &= 0xF0u;
-  if ((r & 0x70u) == 0) r &= 0x0Fu;
-  return r;
+// eight floats -> one word of eight e2m1 codes (code i in nibble i), round to nearest even, saturating; the sign
+// of a zero code is kept here (see e2m1x8_clear_neg_zero)
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float (&v)[8]) {
+  uint32_t d;
+  asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n\t"
+      "mov.b32 %0, {t0, t1, t2, t3};\n\t}"
+      : "=r"(d)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return d;
+}
+
+// -0 codes -> +0, eight at once: a nibble's magnitude m (bits 0-2) is at most 7, so m + 7 sets the nibble's bit 3
+// exactly when m != 0 and never carries into the next nibble; that bit then keeps or clears the sign
+__device__ __forceinline__ uint32_t e2m1x8_clear_neg_zero(uint32_t w) {
+  const uint32_t s = (w & 0x77777777u) + 0x77777777u;
+  return w & (s | 0x77777777u);
 }
 
 // e4m3 byte (non-negative, finite) -> float, exact
@@ -190,7 +202,33 @@ __global__ void __launch_bounds__(AQ_THREADS) act_amax_kernel(const uint16_t* __
   if (threadIdx.x == 0) partial[blockIdx.x] = m;
 }
 
-// NVFP4 quantization: one 16-element block per thread and step.  K % 16 == 0.
+// 16 values of one block whose scale is d -> 16 e2m1 codes of x / d (d = 0: zero codes)
+__device__ __forceinline__ uint2 quant16_e2m1(const uint4& w0, const uint4& w1, float d) {
+  float f0[8], f1[8], v0[8], v1[8];
+  bf16x8_to_f32(w0, f0);
+  bf16x8_to_f32(w1, f1);
+  if (d >= kDivMinScale) {
+    const float di = __frcp_rn(d);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v0[i] = div_by(f0[i], d, di);
+      v1[i] = div_by(f1[i], d, di);
+    }
+  } else if (d > 0.0f) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v0[i] = __fdiv_rn(f0[i], d);
+      v1[i] = __fdiv_rn(f1[i], d);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v0[i] = v1[i] = 0.0f;
+  }
+  return make_uint2(e2m1x8_clear_neg_zero(cvt_e2m1x8(v0)), e2m1x8_clear_neg_zero(cvt_e2m1x8(v1)));
+}
+
+// NVFP4 quantization: one 16-element block per thread and step, a persistent grid (the CTAs the SMs hold at once).
+// K % 16 == 0.
 __global__ void __launch_bounds__(AQ_THREADS) act_quant_nvfp4_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
                                                                      const float* __restrict__ amax_in,
                                                                      const float* __restrict__ partial, int nparts,
@@ -210,6 +248,10 @@ __global__ void __launch_bounds__(AQ_THREADS) act_quant_nvfp4_kernel(const uint1
   const float g = __fdiv_rn(amax, 2688.0f);  // 6 * 448
   if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
   const float six_g = __fmul_rn(6.0f, g);
+  // amax_b / (6 g) through the reciprocal (div_by): a quotient that rounds to a nonzero e4m3 code is above 2^-10, so
+  // with 6 g >= 2^-93 its residual is a multiple of 2^-149 and exact; smaller quotients give the zero code either way
+  const float six_gi = __frcp_rn(six_g);
+  const bool sb_fast = six_g >= 0x1p-93f;
   const int64_t nblk = M * (K >> 4);
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   uint2* qv = reinterpret_cast<uint2*>(q);
@@ -227,28 +269,14 @@ __global__ void __launch_bounds__(AQ_THREADS) act_quant_nvfp4_kernel(const uint1
       n0 = __ldg(xv + 2 * (b + stride));
       n1 = __ldg(xv + 2 * (b + stride) + 1);
     }
-    float f[16];
-    bf16x8_to_f32(w0, *reinterpret_cast<float(*)[8]>(f));
-    bf16x8_to_f32(w1, *reinterpret_cast<float(*)[8]>(f + 8));
     const float mb = absmax_bits_to_f32(bf16x8_absmax_bits(w1, bf16x8_absmax_bits(w0, 0u)));
     uint32_t sb = 0;
     float d = 0.0f;
     if (g > 0.0f) {
-      sb = cvt_e4m3x2(__fdiv_rn(mb, six_g), 0.0f) & 0xFFu;
+      sb = cvt_e4m3x2(sb_fast ? div_by(mb, six_g, six_gi) : __fdiv_rn(mb, six_g), 0.0f) & 0xFFu;
       d = __fmul_rn(e4m3_to_f32(sb), g);
     }
-    uint32_t by[8];
-    if (d >= kDivMinScale) {
-      const float di = __frcp_rn(d);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) by[i] = cvt_e2m1x2(div_by(f[2 * i], d, di), div_by(f[2 * i + 1], d, di));
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        by[i] = d > 0.0f ? cvt_e2m1x2(__fdiv_rn(f[2 * i], d), __fdiv_rn(f[2 * i + 1], d)) : 0u;
-    }
-    qv[b] = make_uint2(by[0] | (by[1] << 8) | (by[2] << 16) | (by[3] << 24),
-                       by[4] | (by[5] << 8) | (by[6] << 16) | (by[7] << 24));
+    qv[b] = quant16_e2m1(w0, w1, d);
     sf[b] = (uint8_t)sb;
   }
 }
@@ -264,13 +292,24 @@ int sm_count() {
   return n;
 }
 
+// CTAs of a kernel that all SMs hold at once (its resident capacity)
+template <typename Kernel>
+int64_t resident_ctas(Kernel kernel) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, AQ_THREADS, 0) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  return (int64_t)per_sm * sm_count();
+}
+
 }  // namespace
 
-// CTAs of the NVFP4 amax pass: one float of workspace each, at most ACT_AMAX_MAX_PARTS.
+// CTAs of the NVFP4 amax pass: one float of workspace each, at most ACT_AMAX_MAX_PARTS; no more than the SMs hold
+// at once, so that every CTA reads its share in one wave.
 int act_amax_grid(int64_t M, int64_t K) {
+  static const int64_t resident = resident_ctas(act_amax_kernel);
   const int64_t n8 = M * (K >> 3);
   const int64_t want = (n8 + AQ_THREADS * 8 - 1) / (AQ_THREADS * 8);  // about 8 chunks per thread
-  int64_t cap = 4 * (int64_t)sm_count();
+  int64_t cap = resident;
   if (cap > ACT_AMAX_MAX_PARTS) cap = ACT_AMAX_MAX_PARTS;
   return (int)(want < 1 ? 1 : (want < cap ? want : cap));
 }
@@ -291,9 +330,10 @@ cudaError_t launch_act_quant(int fp8, const void* x, int64_t M, int64_t K, const
                                   (const uint16_t*)x, M * (K >> 3), partial);
     if (e != cudaSuccess) return e;
   }
+  static const int64_t resident = resident_ctas(act_quant_nvfp4_kernel);
   const int64_t nblk = M * (K >> 4);
   int64_t grid = (nblk + AQ_THREADS - 1) / AQ_THREADS;
-  if (grid > 8 * (int64_t)sms) grid = 8 * (int64_t)sms;
+  if (grid > resident) grid = resident;
   if (grid < 1) grid = 1;
   return launch_kernel(act_quant_nvfp4_kernel, dim3((unsigned)grid), dim3(AQ_THREADS), 0, stream, (const uint16_t*)x, M,
                        K, global_amax, (const float*)partial, nparts, (uint8_t*)data, (uint8_t*)scale, gscale);

@@ -66,6 +66,28 @@ def test_nvfp4_bit_exact(lib, M, K, seed, calibrated):
     assert _f32bits(out["gscale"])[0] == np.float32(g).view(np.uint32)
 
 
+@pytest.mark.parametrize("e", [-80, -88, -92, -96, -104, -118])
+@pytest.mark.parametrize("calibrated", [False, True])
+def test_nvfp4_tiny_scales_bit_exact(lib, e, calibrated):
+    """Tensors whose global scale g = amax / 2688 lies near or below 2^-100: the block-scale and code divisions leave
+    the reciprocal shortcut for IEEE division there, and the codes must not change at the switch.  Rows span 2^-30
+    of magnitude, so the blocks' quotients cover the e4m3 and e2m1 rounding boundaries down to zero codes."""
+    M, K = 48, 1024
+    x = W.acts_fp32(7, M, K, outliers=True, device="cuda")
+    x = x * torch.exp2(e - torch.arange(M, device="cuda", dtype=torch.float32).remainder(31)).unsqueeze(1)
+    x = x.to(torch.bfloat16).contiguous()
+    xb = _bits(x)
+    amax = None
+    if calibrated:
+        amax = np.float32(np.abs((xb.astype(np.uint32) << 16).view(np.float32)).max() / 3)
+    out = lib.quantize_act("nvfp4", x, global_amax=None if amax is None else torch.tensor([amax], device="cuda"))
+    torch.cuda.synchronize()
+    q, sb, g = oracle.quantize_act_nvfp4(xb, global_amax=amax)
+    assert np.array_equal(out["scale"].cpu().numpy(), sb)
+    assert np.array_equal(out["data"].cpu().numpy(), q)
+    assert _f32bits(out["gscale"])[0] == np.float32(g).view(np.uint32)
+
+
 def test_zero_tensor_and_empty_rows(lib):
     x = torch.zeros((7, 64), dtype=torch.bfloat16, device="cuda")
     o8 = lib.quantize_act("e4m3_tok", x)
