@@ -750,7 +750,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
               orow = args.region[(int64_t)pd.e * args.region_cap + pd.row0 + i];
               if (args.topk_w) f = args.topk_w[orow];
             }
-            tabs[(pd.ts * 8 + warp) * HC + u * 32 + lane] = make_int2(orow, __float_as_int(f));
+            // combine instances keep the routed row's token (its output row) instead of the routed row
+            const int key = (COMB && orow >= 0) ? orow / args.comb_k : orow;
+            tabs[(pd.ts * 8 + warp) * HC + u * 32 + lane] = make_int2(key, __float_as_int(f));
           }
         }
         return;
@@ -773,7 +775,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
           if (PATH == PATH_MXFP4) f *= args.a_scale[tok];
           if (PATH == PATH_NVFP4) f *= args.a_scale[0] * args.w_gscale[pd.e];
         }
-        pd.t_row[u] = orow;
+        pd.t_row[u] = (COMB && orow >= 0) ? orow / args.comb_k : orow;  // combine: the token
         pd.t_mul[u] = f;
       }
     };
@@ -999,41 +1001,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
 #pragma unroll
         for (int j = 0; j < HC; ++j) part[(col0 + j) * TILE_N + r] = __uint_as_float(v[j]);
       } else if (COMB) {
-        // MoE combine: the routed row's values (x top-k weight) are added into its token's fp32 row.  N % 4 == 0: a
-        // quad of lanes (4 adjacent output features) transposes its 4 x 4 values of 4 token columns in two shuffle
-        // rounds, so that each lane adds 4 adjacent outputs of one token with one 16-byte reduction.
+        // MoE combine: the routed row's values (x top-k weight) are added into its token's fp32 row; the table holds
+        // the token of each column.  N % 4 == 0: a quad of lanes (4 adjacent output features) transposes its 4 x 4
+        // accumulators of 4 token columns in two shuffle rounds; then lane b0 + 2 b1 of the quad holds the 4
+        // features of column j + b0 + 2 b1, looks up that column's token and top-k weight itself, and adds the 4
+        // outputs with one 16-byte reduction.
         const bool quad = (args.N & 3) == 0;
-        const int b0 = lane & 1, b1 = (lane >> 1) & 1;
+        const int b0 = lane & 1, b1 = (lane >> 1) & 1, tc = b0 + 2 * b1;
         const int n4 = n & ~3;
+        float bq[4];  // bias of the quad's 4 features
+#pragma unroll
+        for (int i = 0; i < 4; ++i) bq[i] = __shfl_sync(0xffffffffu, bias_v, (lane & ~3) + i);
 #pragma unroll
         for (int j = 0; j < HC; j += 4) {
           if (j >= live) continue;
-          int orw[4];
-          float o[4];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float mul;
-            lookup(col0 + j + c, orw[c], mul);
-            o[c] = __uint_as_float(v[j + c]) * mul + bias_v;
-          }
           if (quad) {
+            const float o0 = __uint_as_float(v[j]), o1 = __uint_as_float(v[j + 1]), o2 = __uint_as_float(v[j + 2]),
+                        o3 = __uint_as_float(v[j + 3]);
             // round 1 (lane ^ 1): tokens b0 and b0 + 2, rows 2 b1 and 2 b1 + 1 of the quad
-            const float r1a = __shfl_xor_sync(0xffffffffu, b0 ? o[0] : o[1], 1);
-            const float r1b = __shfl_xor_sync(0xffffffffu, b0 ? o[2] : o[3], 1);
-            const float ta0 = b0 ? r1a : o[0], ta1 = b0 ? o[1] : r1a;  // token b0
-            const float tb0 = b0 ? r1b : o[2], tb1 = b0 ? o[3] : r1b;  // token b0 + 2
+            const float r1a = __shfl_xor_sync(0xffffffffu, b0 ? o0 : o1, 1);
+            const float r1b = __shfl_xor_sync(0xffffffffu, b0 ? o2 : o3, 1);
+            const float ta0 = b0 ? r1a : o0, ta1 = b0 ? o1 : r1a;  // token b0
+            const float tb0 = b0 ? r1b : o2, tb1 = b0 ? o3 : r1b;  // token b0 + 2
             // round 2 (lane ^ 2): token b0 + 2 b1, rows 0..3 of the quad
             const float s0 = __shfl_xor_sync(0xffffffffu, b1 ? ta0 : tb0, 2);
             const float s1 = __shfl_xor_sync(0xffffffffu, b1 ? ta1 : tb1, 2);
-            const int tc = b0 + 2 * b1;
-            const int orow = tc == 0 ? orw[0] : (tc == 1 ? orw[1] : (tc == 2 ? orw[2] : orw[3]));
-            if (orow >= 0 && n4 < args.N)
-              red_add_v4_f32(args.comb + (int64_t)(orow / args.comb_k) * args.N + n4, b1 ? s0 : ta0, b1 ? s1 : ta1,
-                             b1 ? tb0 : s0, b1 ? tb1 : s1);
-          } else if (n < args.N) {
+            const float x0 = b1 ? s0 : ta0, x1 = b1 ? s1 : ta1, x2 = b1 ? tb0 : s0, x3 = b1 ? tb1 : s1;
+            int tok;
+            float mul;
+            lookup(col0 + j + tc, tok, mul);  // j % 4 == 0: the lanes' columns share one 32-column table slot
+            if (tok >= 0 && n4 < args.N)
+              red_add_v4_f32(args.comb + (int64_t)tok * args.N + n4, x0 * mul + bq[0], x1 * mul + bq[1],
+                             x2 * mul + bq[2], x3 * mul + bq[3]);
+          } else {
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-              if (orw[c] >= 0) red_add_f32(args.comb + (int64_t)(orw[c] / args.comb_k) * args.N + n, o[c]);
+            for (int c = 0; c < 4; ++c) {
+              int tok;
+              float mul;
+              lookup(col0 + j + c, tok, mul);  // all lanes: the lookup shuffles
+              if (tok >= 0 && n < args.N)
+                red_add_f32(args.comb + (int64_t)tok * args.N + n, __uint_as_float(v[j + c]) * mul + bias_v);
+            }
           }
         }
       } else if (use_table && pair_ok) {
