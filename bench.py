@@ -45,7 +45,8 @@ def path_dtype(c):
     return "fp4" if c["afmt"] in ("nvfp4", "mxfp4") else PATH_DTYPE[c["wfmt"]]
 
 
-SPIN_CYCLES = 1_000_000  # about 0.5 ms at 2 GHz: longer than the host side of one burst of calls
+SPIN_CYCLES = 2_000_000  # about 1 ms at 2 GHz: longer than the host side of one burst of calls (at most 12 calls,
+#                           each with the binding's argument checks and the library's launch)
 
 
 def peaks():
