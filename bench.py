@@ -467,8 +467,25 @@ def gpu_launches(cfg, fmt, calls):
     return sum(hq.kernels_per_call(fmt, M, c.get("topk", 1), moe) for (M, *_rest) in calls)
 
 
+def product_source(text):
+    """A CUDA source as the product build compiles it: each block from a line `#if HQ_DEBUG_BOUNDS` to its matching
+    `#endif` (the index checks of the debug build, libhq_debug.so) is left out, lines and all."""
+    out, depth = [], 0
+    for line in text.splitlines(keepends=True):
+        s = line.strip()
+        if depth:
+            depth += 1 if s.startswith("#if") else (-1 if s.startswith("#endif") else 0)
+            continue
+        if s == "#if HQ_DEBUG_BOUNDS":
+            depth = 1
+            continue
+        out.append(line)
+    return "".join(out)
+
+
 def kernel_source_hash():
-    """sha256 over the CUDA sources: DRAM counters recorded for another version of them are stale."""
+    """sha256 over the CUDA sources of the product build: DRAM counters recorded for another version of them are
+    stale.  The debug build's check blocks are not part of the kernels those counters describe."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "quantized_gemm_dequant_gb300", "csrc")
@@ -476,7 +493,7 @@ def kernel_source_hash():
         if f.endswith((".cu", ".cuh", ".h")):
             h.update(f.encode())
             with open(os.path.join(d, f), "rb") as fh:
-                h.update(fh.read())
+                h.update(product_source(fh.read().decode("utf-8")).encode("utf-8"))
     return h.hexdigest()[:16]
 
 

@@ -63,7 +63,9 @@ typedef enum {
   HQ_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch error, no device) */
   HQ_ERR_TIMEOUT = 5,     /* device: a pipeline wait exceeded its time limit; the output is undefined */
   HQ_ERR_BAD_ROUTING = 6, /* device: a top-k expert id outside [0, E) or repeated within a token */
-  HQ_ERR_WORKSPACE = 7    /* workspace missing or smaller than hq_workspace_bytes() */
+  HQ_ERR_WORKSPACE = 7,   /* workspace missing or smaller than hq_workspace_bytes() */
+  HQ_ERR_BOUNDS = 8       /* device, debug build (libhq_debug.so) only: an index outside its buffer was caught
+                             before a store or partial-sum access, which was skipped; the output is undefined */
 } hq_status_t;
 
 /* Weight numeric formats (the "standard format" parameters). */

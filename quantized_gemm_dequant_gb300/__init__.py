@@ -4,7 +4,9 @@ Argument marshalling only: every step of the computation runs in the library's
 CUDA kernels.  torch provides device memory and the current stream.  Importing
 this package fails loudly if libhq.so has not been built (run
 `python -c "import __graft_entry__ as g; g.build()"` or
-`python quantized_gemm_dequant_gb300/build.py`).
+`python quantized_gemm_dequant_gb300/build.py`).  With HQ_LIBRARY=debug in the
+environment it loads libhq_debug.so instead: the same kernels with device-side
+index checks that report HQ_ERR_BOUNDS through the workspace status.
 """
 import ctypes
 import os
@@ -12,17 +14,18 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libhq.so")
+DEBUG = os.environ.get("HQ_LIBRARY", "") == "debug"
+LIB_PATH = os.path.join(_HERE, "libhq_debug.so" if DEBUG else "libhq.so")
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError(f"libhq.so not found at {LIB_PATH}: build the CUDA library first "
-                      "(quantized_gemm_dequant_gb300/build.py)")
+    raise ImportError(f"{os.path.basename(LIB_PATH)} not found at {LIB_PATH}: build the CUDA library first "
+                      "(quantized_gemm_dequant_gb300/build.py" + (" --debug)" if DEBUG else ")"))
 
 _lib = ctypes.CDLL(LIB_PATH)
 
 # ----------------------------------------------------------------- C types
 HQ_OK, HQ_ERR_INVALID_ARG, HQ_ERR_UNSUPPORTED, HQ_ERR_ALIGNMENT, HQ_ERR_CUDA, HQ_ERR_TIMEOUT, \
-    HQ_ERR_BAD_ROUTING, HQ_ERR_WORKSPACE = range(8)
+    HQ_ERR_BAD_ROUTING, HQ_ERR_WORKSPACE, HQ_ERR_BOUNDS = range(9)
 HQ_W_INT4_SYM, HQ_W_UINT4_ZP, HQ_W_NVFP4, HQ_W_MXFP4 = 1, 2, 3, 4
 HQ_W_INT8_SYM, HQ_W_UINT2_ZP, HQ_W_MXINT4, HQ_W_E4M3, HQ_W_UINT1_ZP, HQ_W_UINT3_ZP = 5, 6, 7, 8, 9, 10
 HQ_S_BF16, HQ_S_UE4M3, HQ_S_UE8M0 = 1, 2, 3

@@ -311,6 +311,19 @@ Plan make_plan(const hq_format_t* f, int64_t M_or_T, int32_t topk, int kind, int
   p.ws_bytes = off;
   return p;
 }
+#if HQ_DEBUG_BOUNDS
+
+// Debug build: the extents the device-side index checks compare against.  HQ_DEBUG_ROW_LIMIT (for tests) lowers the
+// output rows a call may write below the rows that exist, so that a check can be made to catch an index without any
+// access outside the buffers.
+void dbg_extents(GemmArgs& a, const Plan& p, int64_t c_rows, int64_t comb_rows) {
+  const char* v = getenv("HQ_DEBUG_ROW_LIMIT");
+  const int64_t lim = v ? atoll(v) : c_rows;
+  a.dbg_c_rows = (int)(c_rows < lim ? c_rows : lim);
+  a.dbg_comb_rows = (int)(comb_rows < lim ? comb_rows : lim);
+  a.dbg_part_elems = p.sk ? (int64_t)(p.small ? 1 : 2) * p.grid * p.bt * TILE_N : 0;
+}
+#endif
 
 cudaError_t launch_path(const Plan& p, const GemmArgs& a, cudaStream_t s) {
   cudaError_t e;
@@ -495,6 +508,9 @@ hq_status_t hq_gemm(const hq_format_t* fmt, const hq_act_t* A, const void* packe
   // weights read once per call (one token tile): evict-first in L2, so that they do not push out the kernel code,
   // activations and partial sums that the next call needs
   a.w_evict_first = (p.small || p.m_tiles == 1) ? 1 : 0;
+#if HQ_DEBUG_BOUNDS
+  dbg_extents(a, p, M, 0);
+#endif
   return cuda_status(launch_path(p, a, (cudaStream_t)stream));
 }
 
@@ -594,6 +610,9 @@ hq_status_t moe_call(const hq_format_t* fmt, const hq_act_t* A, const void* pack
   a.partials = p.sk ? reinterpret_cast<float*>(ws + p.off_partials) : nullptr;
   a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   a.w_evict_first = p.small;  // weights streamed once per call (tiles of one expert share them only at small T)
+#if HQ_DEBUG_BOUNDS
+  dbg_extents(a, p, T * topk, combine ? T : 0);
+#endif
   err = launch_path(p, a, (cudaStream_t)stream);
   if (err != cudaSuccess || !combine) return cuda_status(err);
   return cuda_status(launch_combine_round(comb, T * fmt->N, static_cast<uint16_t*>(C), (cudaStream_t)stream));
@@ -680,6 +699,9 @@ const char* hq_status_string(hq_status_t s) {
     case HQ_ERR_TIMEOUT: return "device pipeline wait timed out";
     case HQ_ERR_BAD_ROUTING: return "top-k expert id out of range or rows per expert over capacity";
     case HQ_ERR_WORKSPACE: return "workspace missing or too small";
+#if HQ_DEBUG_BOUNDS
+    case HQ_ERR_BOUNDS: return "device index outside its buffer (debug build: the access was skipped)";
+#endif
     default: return "unknown status";
   }
 }

@@ -52,6 +52,24 @@ constexpr uint64_t DEFAULT_WAIT_NS = 2000000000ull;  // 2 s per pipeline wait un
 constexpr uint64_t DRAIN_WAIT_NS = 200000000ull;     // waits for this CTA's own copies and MMAs before it exits
 constexpr int ERR_TIMEOUT = 5;
 constexpr int ERR_BAD_ROUTING = 6;
+#if HQ_DEBUG_BOUNDS
+// Debug build (libhq_debug.so) only: device-side index checks before global stores and partial-sum accesses.  An
+// index outside its buffer records HQ_ERR_BOUNDS in the status word (the first error of a call wins) and the access
+// is skipped; nothing traps, so the context stays usable and the host reads the status.
+constexpr int ERR_BOUNDS = 8;
+// `row` if it is a skipped row (< 0) or inside [0, rows); otherwise records the error and returns -1 (skip).
+__device__ __forceinline__ int dbg_row(int row, int rows, int* status) {
+  if (row < rows) return row;
+  atomicCAS(status, 0, ERR_BOUNDS);
+  return -1;
+}
+// true if a span ending at element `end` fits a buffer of `cap` elements; otherwise records the error.
+__device__ __forceinline__ bool dbg_span(int64_t end, int64_t cap, int* status) {
+  if (end <= cap) return true;
+  atomicCAS(status, 0, ERR_BOUNDS);
+  return false;
+}
+#endif
 
 struct GemmArgs {
   CUtensorMap tmap_a;   // activation data: dense 2-D box of BT rows, MoE one-row boxes for gather4
@@ -85,6 +103,11 @@ struct GemmArgs {
   int fused_rows;      // that many routed rows (T * topk)
   uint64_t wait_ns;  // bound of every pipeline wait (a wait that runs out records HQ_ERR_TIMEOUT)
   int w_evict_first;  // weight copies marked evict-first in L2 (each block read once per call)
+#if HQ_DEBUG_BOUNDS
+  int dbg_c_rows;          // output rows a kernel may write: dense M, MoE T * topk routed rows (also for the combine)
+  int dbg_comb_rows;       // MoE combine: token rows of the fp32 sums (T)
+  int64_t dbg_part_elems;  // Stream-K partial-sum buffer, in fp32 values (tcgen05) or 64-bit words (register decode)
+#endif
 };
 
 template <int PATH, int BT>
@@ -994,9 +1017,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
         int orow;
         float mul;
         lookup(col, orow, mul);
+#if HQ_DEBUG_BOUNDS
+        orow = dbg_row(orow, args.dbg_c_rows, args.status);
+#endif
         if (orow >= 0 && n < args.N) args.c[(int64_t)orow * args.N + n] = f32_to_bf16(acc * mul + bias_v);
       };
       const bool pair_ok = (args.N & 1) == 0 && (reinterpret_cast<uintptr_t>(args.c) & 3) == 0;
+#if HQ_DEBUG_BOUNDS
+      if (!pc.full && !dbg_span((int64_t)(pc.slot + 1) * BT * TILE_N, args.dbg_part_elems, args.status)) {
+        ++pidx;
+        return ok;
+      }
+#endif
       if (!pc.full) {
 #pragma unroll
         for (int j = 0; j < HC; ++j) part[(col0 + j) * TILE_N + r] = __uint_as_float(v[j]);
@@ -1030,6 +1062,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
             int tok;
             float mul;
             lookup(col0 + j + tc, tok, mul);  // j % 4 == 0: the lanes' columns share one 32-column table slot
+#if HQ_DEBUG_BOUNDS
+            tok = dbg_row(tok, args.dbg_comb_rows, args.status);
+#endif
             if (tok >= 0 && n4 < args.N)
               red_add_v4_f32(args.comb + (int64_t)tok * args.N + n4, x0 * mul + bq[0], x1 * mul + bq[1],
                              x2 * mul + bq[2], x3 * mul + bq[3]);
@@ -1039,6 +1074,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
               int tok;
               float mul;
               lookup(col0 + j + c, tok, mul);  // all lanes: the lookup shuffles
+#if HQ_DEBUG_BOUNDS
+              tok = dbg_row(tok, args.dbg_comb_rows, args.status);
+#endif
               if (tok >= 0 && n < args.N)
                 red_add_f32(args.comb + (int64_t)tok * args.N + n, __uint_as_float(v[j + c]) * mul + bias_v);
             }
@@ -1057,6 +1095,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
           float mul0, mul1;
           lookup(col, orow0, mul0);
           lookup(col + 1, orow1, mul1);
+#if HQ_DEBUG_BOUNDS
+          orow0 = dbg_row(orow0, args.dbg_c_rows, args.status);
+          orow1 = dbg_row(orow1, args.dbg_c_rows, args.status);
+#endif
           const uint32_t pk = pack_bf16x2(__uint_as_float(v[j]) * mul0 + bias_v,
                                           __uint_as_float(v[j + 1]) * mul1 + bias_v);  // lo: col, hi: col+1
           const uint32_t recv = __shfl_xor_sync(0xffffffffu, odd ? (pk & 0xFFFFu) : (pk >> 16), 1);
@@ -1080,6 +1122,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hq_gemm_kernel(const __grid_co
           const uint32_t recv = __shfl_xor_sync(0xffffffffu, odd ? (pk & 0xFFFFu) : (pk >> 16), 1);
           const uint32_t out = odd ? (recv | (pk & 0xFFFF0000u)) : ((pk & 0xFFFFu) | (recv << 16));
           const int tok = col + (odd ? 1 : 0);
+#if HQ_DEBUG_BOUNDS
+          if (tok < nrows && dbg_row(row0 + tok, args.dbg_c_rows, args.status) < 0) continue;
+#endif
           if (tok < nrows && n_even < args.N)
             *reinterpret_cast<uint32_t*>(args.c + (int64_t)(row0 + tok) * args.N + n_even) = out;
         }

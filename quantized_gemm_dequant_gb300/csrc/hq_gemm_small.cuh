@@ -747,6 +747,10 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT, DEC>::CTAS_PER_SM)
         }
       }
       const uint64_t tag = (uint64_t)sh.epoch << 32;
+#if HQ_DEBUG_BOUNDS
+      if (ok && !pc.full && !dbg_span(((int64_t)blockIdx.x + 1) * BT * TILE_N, args.dbg_part_elems, args.status))
+        ok = false;
+#endif
       if (ok && !pc.full && pc.g0 > 0) {
         // the tile started in an earlier CTA: leave the partial sum, tagged with the call's epoch, in this CTA's slot
         uint64_t* part = reinterpret_cast<uint64_t*>(args.partials) + (int64_t)blockIdx.x * BT * TILE_N;
@@ -823,6 +827,10 @@ __global__ void __launch_bounds__(SM_THREADS, SmallCfg<BT, DEC>::CTAS_PER_SM)
 #pragma unroll
             for (int i = 0; i < NT; ++i) {
               if (i >= nn) continue;
+#if HQ_DEBUG_BOUNDS
+              t_row[i][0] = dbg_row(t_row[i][0], args.dbg_c_rows, args.status);
+              t_row[i][1] = dbg_row(t_row[i][1], args.dbg_c_rows, args.status);
+#endif
               const float o0 = own[i][2 * rr] * t_mul[i][0] + bias;
               const float o1 = own[i][2 * rr + 1] * t_mul[i][1] + bias;
               if (pair_ok) {

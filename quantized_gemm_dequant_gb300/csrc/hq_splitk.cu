@@ -71,6 +71,12 @@ __global__ void __launch_bounds__(RED_THREADS) splitk_reduce_kernel(const __grid
         const int c = c4 + k;
         const int slot = (c == c_first && s.start(c) < first_it) ? 2 * c + 1 : 2 * c;
         const float* base = args.partials + ((int64_t)slot * bt) * TILE_N + r4;
+#if HQ_DEBUG_BOUNDS
+        if (c <= c_last && !dbg_span(((int64_t)slot + 1) * bt * TILE_N, args.dbg_part_elems, args.status)) {
+          for (int u = 0; u < RED_COLS / 8; ++u) v[k][u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          continue;
+        }
+#endif
 #pragma unroll
         for (int u = 0; u < RED_COLS / 8; ++u) {
           const int col = col0 + cq + 8 * u;
@@ -106,6 +112,9 @@ __global__ void __launch_bounds__(RED_THREADS) splitk_reduce_kernel(const __grid
         orow = row0 + col;
         if (PATH == PATH_MXFP4) mul *= args.a_scale[orow];
       }
+#if HQ_DEBUG_BOUNDS
+      if (dbg_row(orow, args.dbg_c_rows, args.status) < 0) continue;
+#endif
       const float o[4] = {acc[u].x * mul + bias4[0], acc[u].y * mul + bias4[1], acc[u].z * mul + bias4[2],
                           acc[u].w * mul + bias4[3]};
       if (args.comb) {  // MoE combine: add into the token's fp32 row
