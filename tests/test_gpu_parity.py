@@ -375,3 +375,18 @@ def test_moe_small_routing_in_kernel_and_by_routing_kernel(lib, monkeypatch, rou
     fmt, packed = lib.pack_inputs(inp, "cuda")
     assert lib.kernels_per_call(fmt, T, 8, moe=True) == (1 if route == "fused" else 2)
     R.assert_parity(_run_moe(lib, inp), R.moe_ref(inp), f"moe routing {route} T={T}")
+
+
+def test_int4_tcgen05_rounding_witness(lib):
+    """The tcgen05 INT4 path feeds the MMA bf16((q - z) * s): one rounding per weight, shared by every weight of a
+    group with the same code.  On this workload-recipe input (MoE INT4, T = 200, E = 8, K = 640, seed 4) that
+    rounding takes one element to 1.087 of the general element-wise bound (a CPU emulation of the arithmetic gives
+    the same value bit for bit; exact weights give 0.315).  The path is held here to the rigorous bound of its own
+    arithmetic, 2^-9 sum_k |a_k w_k| + 2^-8 |y_ref| (+ fp32 accumulation), which any decode error (a wrong code,
+    zero point or scale, of the size of the weight itself) would break."""
+    from tests import debug_bounds_cases as D
+
+    c = D.moe_case("witness", "int4_sym", 200, 8, 256, 640)
+    assert c["plan"]["kernel"] == "umma" and c["bound"] == "bf16-decode", c["plan"]
+    assert c["status"] == lib.HQ_OK, lib.status_string(c["status"])
+    assert c["ratio"] <= 1.0, f"{c['ratio']:.3f} of the bf16-decode bound"
