@@ -222,6 +222,8 @@ def pack_weights(fmt, codes, scales, zeros=None, global_scale=None, out=None, st
     nb = packed_bytes(fmt)
     if nb == 0:
         raise HQError(HQ_ERR_UNSUPPORTED, "hq_packed_bytes")
+    if codes is None or scales is None:
+        raise HQArgError("hq_pack_weights", "codes and scales are required")
     args = _standard(fmt, codes, scales, zeros, global_scale, "hq_pack_weights").add(out, "out", nb)
     p = args.ptrs()
     if out is None:

@@ -126,6 +126,7 @@ def test_pack_checks():
     _raises(lambda: hq.pack_weights(fmt, codes, scales[:, :, :1], zeros), "scales")
     _raises(lambda: hq.pack_weights(fmt, codes, scales, zeros[:1]), "zeros", "bytes")
     _raises(lambda: hq.pack_weights(fmt, codes, scales, zeros), "device memory")
+    _raises(lambda: hq.pack_weights(fmt, None, scales, zeros), "required")
     nv = _fmt("nvfp4", E=2)
     _raises(lambda: hq.pack_weights(nv, torch.zeros(2, N, K // 2, dtype=torch.uint8),
                                     torch.zeros(2, N, K // 16, dtype=torch.uint8), None,
